@@ -1,0 +1,77 @@
+"""ctypes loader of libspecverify.so (the C ABI declared in include/specverify.h).
+
+The library is built in place by ``build.py``; importing the binding without it raises,
+so nothing can silently run without the CUDA path.
+"""
+import ctypes
+import os
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_DIR, "libspecverify.so")
+
+c_int = ctypes.c_int
+c_i32p = ctypes.c_void_p      # device pointers are passed as plain addresses
+c_size = ctypes.c_size_t
+c_vp = ctypes.c_void_p
+
+SPEC_OK = 0
+SPEC_E_INVAL = -1
+SPEC_E_NOMEM = -2
+SPEC_E_RANGE = -3
+SPEC_E_STATE = -4
+SPEC_E_TIMEOUT = -5
+SPEC_E_CUDA = -6
+SPEC_E_DRAFT = -7
+SPEC_TOPK_MAX = 32
+
+STATUS_NAMES = {0: "SPEC_OK", -1: "SPEC_E_INVAL", -2: "SPEC_E_NOMEM", -3: "SPEC_E_RANGE",
+                -4: "SPEC_E_STATE", -5: "SPEC_E_TIMEOUT", -6: "SPEC_E_CUDA", -7: "SPEC_E_DRAFT"}
+
+
+class SpecSampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "spec_last_error": (ctypes.c_char_p, []),
+    "spec_version": (ctypes.c_char_p, []),
+    "spec_verify_logits_workspace_bytes": (c_size, [c_int, c_int, c_int]),
+    "spec_verify_logits": (c_int, [c_int, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                   ctypes.POINTER(SpecSampling), c_vp, c_vp, c_vp, c_vp, c_vp,
+                                   c_vp, c_size, c_vp]),
+    "spec_sample_logits_workspace_bytes": (c_size, [c_int, c_int]),
+    "spec_sample_logits": (c_int, [c_int, c_int, c_vp, c_vp, ctypes.POINTER(SpecSampling), c_vp,
+                                   c_vp, c_size, c_vp]),
+}
+
+_lib = None
+
+
+def load():
+    """Load the shared library once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                          "(python speculative_decoding_verify_token_gb300/build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def check(code):
+    if code != SPEC_OK:
+        raise SpecError(code, load().spec_last_error().decode())
+    return code

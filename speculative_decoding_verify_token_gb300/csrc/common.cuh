@@ -1,0 +1,152 @@
+// Shared device helpers of the specverify library (sm_103a).
+//
+// * mbarrier / bulk-copy (TMA engine) wrappers in inline PTX;
+// * bounded waits: every spin on an mbarrier gives up after a wall-clock budget read from
+//   %globaltimer, so that a wait that can never complete turns into an error status
+//   instead of a hung GPU;
+// * warp-wide sorted lists: 32 (value, id) entries, one per lane, lane 0 best, ordered by
+//   value descending and then id ascending (the lower token id wins a tie).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int SENT_ID = 0x7fffffff;
+// Wall-clock budget of one bounded wait (nanoseconds).
+constexpr unsigned long long WAIT_BUDGET_NS = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false when the
+// budget ran out (the caller records an error and stops using the barrier).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > WAIT_BUDGET_NS) return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared on the TMA engine, completion counted on `bar`.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+
+// ---- warp-wide sorted (value, id) lists -------------------------------------------------
+
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+    return (a > b) || (a == b && ia < ib);
+}
+
+// Bitonic sort of one entry per lane into descending order (lane 0 best).
+__device__ __forceinline__ void warp_sort_desc(float& v, int& id, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, v, stride);
+            const int oi = __shfl_xor_sync(FULL, id, stride);
+            const bool desc_block = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            const bool take = (lower == desc_block) ? better(ov, oi, v, id) : better(v, id, ov, oi);
+            if (take) { v = ov; id = oi; }
+        }
+    }
+}
+
+// Merge a descending list (cv, cid) into the running descending list (v, id): the result
+// is the best 32 of the 64 entries, still descending.
+__device__ __forceinline__ void warp_merge_desc(float& v, int& id, float cv, int cid, int lane) {
+    const float rv = __shfl_sync(FULL, cv, 31 - lane);
+    const int ri = __shfl_sync(FULL, cid, 31 - lane);
+    if (better(rv, ri, v, id)) { v = rv; id = ri; }          // bitonic now
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const float ov = __shfl_xor_sync(FULL, v, stride);
+        const int oi = __shfl_xor_sync(FULL, id, stride);
+        const bool lower = (lane & stride) == 0;
+        const bool take = lower ? better(ov, oi, v, id) : better(v, id, ov, oi);
+        if (take) { v = ov; id = oi; }
+    }
+}
+
+// Ascending sort by integer key, carrying a float payload.
+__device__ __forceinline__ void warp_sort_asc_key(int& key, float& val, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int ok = __shfl_xor_sync(FULL, key, stride);
+            const float ov = __shfl_xor_sync(FULL, val, stride);
+            const bool asc_block = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            const bool take = (lower == asc_block) ? (ok < key) : (ok > key);
+            if (take) { key = ok; val = ov; }
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(FULL, x, o));
+    return x;
+}
+
+}  // namespace sv

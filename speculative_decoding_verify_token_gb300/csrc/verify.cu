@@ -1,0 +1,714 @@
+// Fused verify kernel: one streaming pass over the target (and draft) logits rows of a
+// speculative-decoding verify step, then per-row truncation and per-sequence acceptance.
+//
+// What it computes follows "Qwen3.5 and Qwen3.6 MTP head reaches 1.4x on Apple Silicon
+// after three fixes" ("The verify was wrong under sampling": accept with probability
+// min(1, p/q), resample from max(0, p - q) renormalised; "Truncation has to match on both
+// sides": top-k 20 / top-p 0.95 on p and q alike) and, at temperature 0, the greedy rule
+// of "What is Speculative Decoding and How Does a Draft Model Work?" ("#2": keep drafts
+// while they equal the target's choice, replace the first mismatch).
+//
+// GB300 design:
+//  * persistent grid of one 8-warp CTA per SM; every warp is an independent streaming
+//    engine with its own 3-stage ring of 8 KB shared-memory buffers filled by 1-D bulk
+//    copies on the TMA engine (one elected lane issues, mbarrier completion), so each SM
+//    keeps up to 192 KB of HBM reads in flight;
+//  * work items are (row, chunk) pieces of the logits rows, handed out by a global atomic
+//    counter so the warps stay balanced whatever B, K and V are;
+//  * each warp keeps an exact running top-k of its item as a warp-wide sorted list (one
+//    entry per lane); a stage costs one compare per float4 against the running k-th value
+//    and only rare candidates go through a bitonic sort + merge;
+//  * the last warp to finish a row (atomic arrival count, no spin-wait) merges the chunk
+//    lists and builds the row's truncated distribution; the last row of a sequence runs
+//    the acceptance scan and the final inverse-CDF draw on one warp.
+#include <cstdio>
+#include <cstring>
+#include <cmath>
+#include <algorithm>
+
+#include "common.cuh"
+#include "host_util.h"
+
+namespace sv {
+
+constexpr int VT_WARPS = 8;
+constexpr int VT_THREADS = VT_WARPS * 32;
+constexpr int VT_STAGES = 3;
+constexpr int VT_STAGE_ELEMS = 2048;                // 8 KB of fp32 per stage
+constexpr int VT_STAGE_BYTES = VT_STAGE_ELEMS * 4;
+constexpr int VT_SMEM = VT_WARPS * VT_STAGES * VT_STAGE_BYTES;
+constexpr int LISTN = 32;
+constexpr int VT_TARGET_ITEMS = 4096;
+constexpr int VT_MAX_CHUNKS = 128;
+constexpr int VT_MAX_K = 64;
+
+enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
+
+struct VerifyParams {
+    const float* target;        // [B][K+1][V] (verify) or [R][V] (sample)
+    const float* draft;         // [B][K][V] or nullptr
+    const int* draft_tokens;    // [B][K]
+    const int* draft_len;       // [B] or nullptr
+    const float* u;             // [B][K+1] (verify) or [R] (sample)
+    int B, K, V;
+    float temperature;
+    int top_k;                  // effective k (1 when greedy)
+    float top_p;
+    int mode;
+    int n_target_rows;          // B*(K+1) (verify) or R (sample)
+    int n_rows;                 // + B*K draft rows when draft logits are given
+    int chunks;                 // chunks per row
+    int chunk_elems;            // body elements per chunk (multiple of VT_STAGE_ELEMS)
+    int n_items;                // n_rows * chunks
+    int* accepted_len;
+    int* next_token;
+    int* out_ids;
+    float* out_probs;
+    int* seq_status;
+    int* out_tokens;
+    // workspace
+    int* work;                  // [1] item counter
+    int* row_cnt;               // [n_rows]
+    int* seq_cnt;               // [B]
+    float* cl_v;                // [n_rows][chunks][LISTN]
+    int* cl_id;
+    int* rd_n;                  // [n_rows]
+    int* rd_id;                 // [n_rows][LISTN]
+    float* rd_p;
+};
+
+struct RowInfo {
+    const float* ptr;
+    int seq;        // sequence (verify) or row index (sample)
+    int pos;        // position within the sequence's rows
+    bool is_draft;
+};
+
+__device__ __forceinline__ int draft_count(const VerifyParams& p, int b) {
+    if (p.draft_len == nullptr) return p.K;
+    int k = p.draft_len[b];
+    return k < 0 ? 0 : (k > p.K ? p.K : k);
+}
+
+__device__ __forceinline__ RowInfo row_info(const VerifyParams& p, int r) {
+    RowInfo ri;
+    if (p.mode == MODE_SAMPLE) {
+        ri.ptr = p.target + (size_t)r * p.V; ri.seq = r; ri.pos = 0; ri.is_draft = false;
+    } else if (r < p.n_target_rows) {
+        ri.ptr = p.target + (size_t)r * p.V; ri.seq = r / (p.K + 1); ri.pos = r % (p.K + 1); ri.is_draft = false;
+    } else {
+        const int rr = r - p.n_target_rows;
+        ri.ptr = p.draft + (size_t)rr * p.V; ri.seq = rr / p.K; ri.pos = rr % p.K; ri.is_draft = true;
+    }
+    return ri;
+}
+
+__device__ __forceinline__ bool row_needed(const VerifyParams& p, const RowInfo& ri) {
+    if (p.mode == MODE_SAMPLE) return true;
+    const int kb = draft_count(p, ri.seq);
+    return ri.is_draft ? (ri.pos < kb) : (ri.pos <= kb);
+}
+
+// Row layout: [0, head) scalar, [head, head + body) 16-byte aligned body, then a scalar tail.
+__device__ __forceinline__ void row_split(const float* ptr, int V, int& head, int& body) {
+    const int mis = (int)((reinterpret_cast<uintptr_t>(ptr) >> 2) & 3);
+    head = (4 - mis) & 3;
+    if (head > V) head = V;
+    body = ((V - head) / 4) * 4;
+}
+
+struct StageDesc {
+    int item;
+    int start;     // row-relative element index of the first element in the buffer
+    int count;     // elements (multiple of 4, may be 0)
+    int flags;     // 1 = first stage of the item, 2 = last stage of the item
+};
+
+struct ProdState {
+    int item;
+    int pos, end;
+    bool first;
+    const float* ptr;
+};
+
+// Lane 0 only: describe the next stage of this warp's stream; false when no work is left.
+__device__ bool next_stage(const VerifyParams& p, ProdState& ps, StageDesc& d) {
+    while (ps.item < 0) {
+        const int it = atomicAdd(p.work, 1);
+        if (it >= p.n_items) return false;
+        const int row = it / p.chunks, c = it % p.chunks;
+        const RowInfo ri = row_info(p, row);
+        if (!row_needed(p, ri)) continue;
+        int head, body;
+        row_split(ri.ptr, p.V, head, body);
+        const int s = c * p.chunk_elems;
+        const int e = min(body, s + p.chunk_elems);
+        ps.item = it;
+        ps.pos = head + min(s, body);
+        ps.end = head + max(e, min(s, body));
+        ps.first = true;
+        ps.ptr = ri.ptr;
+    }
+    const int n = min(VT_STAGE_ELEMS, ps.end - ps.pos);
+    d.item = ps.item;
+    d.start = ps.pos;
+    d.count = n;
+    d.flags = (ps.first ? 1 : 0) | (ps.pos + n >= ps.end ? 2 : 0);
+    ps.first = false;
+    ps.pos += n;
+    if (d.flags & 2) ps.item = -1;
+    return true;
+}
+
+__device__ __forceinline__ void issue_stage(const ProdState& ps, const StageDesc& d, uint32_t buf,
+                                            uint32_t bar, uint64_t pol) {
+    if (d.count > 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)d.count * 4u);
+        bulk_g2s(buf, ps.ptr + d.start, (uint32_t)d.count * 4u, bar, pol);
+    } else {
+        mbar_arrive(bar);
+    }
+}
+
+__device__ __forceinline__ float pick4(const float4& x, int c) {
+    float r = x.x;
+    r = (c == 1) ? x.y : r;
+    r = (c == 2) ? x.z : r;
+    r = (c == 3) ? x.w : r;
+    return r;
+}
+
+// One round: every lane offers at most one candidate; sort them and merge into the list.
+__device__ __forceinline__ void offer_round(float& lv, int& lid, bool has, float cv, int cid, int lane) {
+    if (!has) { cv = -INFINITY; cid = SENT_ID; }
+    warp_sort_desc(cv, cid, lane);
+    warp_merge_desc(lv, lid, cv, cid, lane);
+}
+
+// Truncated distribution of a merged row list (lane j = j-th best), written to rd_*.
+__device__ void build_row_dist(const VerifyParams& p, int row, float lv, int lid, int lane) {
+    const int k = p.top_k;
+    int n;
+    int oid;
+    float op;
+    if (p.temperature == 0.0f) {
+        n = 1;
+        oid = lane == 0 ? lid : -1;
+        op = lane == 0 ? 1.0f : 0.0f;
+    } else {
+        const bool valid = lane < k && lid != SENT_ID;
+        const float v0 = __shfl_sync(FULL, lv, 0);
+        const float e = valid ? expf((lv - v0) / p.temperature) : 0.0f;
+        const float S = warp_sum(e);
+        const float pr = e / S;
+        // exclusive prefix sum of pr in ranking order
+        float incl = pr;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const float before = incl - pr;
+        const bool kept = valid && (lane == 0 || p.top_p >= 1.0f || before < p.top_p);
+        n = __popc(__ballot_sync(FULL, kept));
+        const float S2 = warp_sum(kept ? e : 0.0f);
+        oid = kept ? lid : -1;
+        op = kept ? e / S2 : 0.0f;
+    }
+    p.rd_id[(size_t)row * LISTN + lane] = oid;
+    p.rd_p[(size_t)row * LISTN + lane] = op;
+    if (lane == 0) p.rd_n[row] = n;
+}
+
+// Inverse CDF over ascending token id: (key, w) per lane, key = SENT_ID for empty lanes.
+// Returns the chosen token; sorts (key, w) ascending in place.
+__device__ int inverse_cdf_draw(int& key, float& w, float u, int lane, float& Z) {
+    warp_sort_asc_key(key, w, lane);
+    Z = warp_sum(key != SENT_ID ? w : 0.0f);
+    float cum = key != SENT_ID ? w : 0.0f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(FULL, cum, o);
+        if (lane >= o) cum += t;
+    }
+    const float target = u * Z;
+    const unsigned sel = __ballot_sync(FULL, key != SENT_ID && cum > target);
+    const unsigned valid = __ballot_sync(FULL, key != SENT_ID);
+    int src;
+    if (sel) src = __ffs(sel) - 1;
+    else src = valid ? 31 - __clz(valid) : 0;
+    return __shfl_sync(FULL, key, src);
+}
+
+__device__ __forceinline__ int trow(const VerifyParams& p, int b, int i) { return b * (p.K + 1) + i; }
+__device__ __forceinline__ int drow(const VerifyParams& p, int b, int i) { return p.n_target_rows + b * p.K + i; }
+
+// Acceptance scan of one sequence on one warp.
+__device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
+    const int kb = draft_count(p, b);
+    const float* ub = p.u + (size_t)b * (p.K + 1);
+    int a = 0, next = -1, status = SPEC_OK;
+    int okey = SENT_ID;
+    float ow = 0.0f, oZ = 1.0f;
+    if (p.temperature == 0.0f) {
+        while (a < kb && p.draft_tokens[(size_t)b * p.K + a] == __ldcg(p.rd_id + (size_t)trow(p, b, a) * LISTN)) ++a;
+        next = __ldcg(p.rd_id + (size_t)trow(p, b, a) * LISTN);
+        okey = lane == 0 ? next : SENT_ID;
+        ow = lane == 0 ? 1.0f : 0.0f;
+    } else {
+        const bool has_q = p.draft != nullptr;
+        bool reject = false;
+        a = kb;
+        int d = -1;
+        for (int i = 0; i < kb; ++i) {
+            d = p.draft_tokens[(size_t)b * p.K + i];
+            const int pid = __ldcg(p.rd_id + (size_t)trow(p, b, i) * LISTN + lane);
+            const float pp = __ldcg(p.rd_p + (size_t)trow(p, b, i) * LISTN + lane);
+            const float pd = warp_max(pid == d ? pp : 0.0f);
+            float qd = 1.0f;
+            if (has_q) {
+                const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, i) * LISTN + lane);
+                const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, i) * LISTN + lane);
+                qd = warp_max(qid == d ? qp : 0.0f);
+            }
+            if (qd == 0.0f) { status = SPEC_E_DRAFT; a = i; break; }
+            const float ratio = pd / qd;
+            if (!(ub[i] < ratio)) { a = i; reject = true; break; }
+        }
+        if (status == SPEC_OK) {
+            const int prow = trow(p, b, a);
+            const int pid = __ldcg(p.rd_id + (size_t)prow * LISTN + lane);
+            const float pp = __ldcg(p.rd_p + (size_t)prow * LISTN + lane);
+            float w = pid >= 0 ? pp : 0.0f;
+            if (reject) {
+                float qx = 0.0f;
+                if (has_q) {
+                    const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, a) * LISTN + lane);
+                    const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, a) * LISTN + lane);
+                    for (int t = 0; t < LISTN; ++t) {
+                        const int tid = __shfl_sync(FULL, qid, t);
+                        const float tp = __shfl_sync(FULL, qp, t);
+                        if (tid >= 0 && tid == pid) qx = tp;
+                    }
+                } else {
+                    qx = (pid == d) ? 1.0f : 0.0f;
+                }
+                float r = pid >= 0 ? fmaxf(pp - qx, 0.0f) : 0.0f;
+                if (warp_sum(r) == 0.0f) r = w;      // residual empty: fall back to P
+                w = r;
+            }
+            okey = (pid >= 0 && w > 0.0f) ? pid : SENT_ID;
+            ow = okey != SENT_ID ? w : 0.0f;
+            next = inverse_cdf_draw(okey, ow, ub[p.K], lane, oZ);
+        }
+    }
+    if (p.out_ids != nullptr) {
+        const bool v = okey != SENT_ID && status == SPEC_OK;
+        p.out_ids[(size_t)b * SPEC_TOPK_MAX + lane] = v ? okey : -1;
+        p.out_probs[(size_t)b * SPEC_TOPK_MAX + lane] = v ? ow / oZ : 0.0f;
+    }
+    if (lane == 0) {
+        p.accepted_len[b] = a;
+        p.next_token[b] = status == SPEC_OK ? next : -1;
+        if (p.seq_status) p.seq_status[b] = status;
+    }
+}
+
+// The last chunk of a row: merge the chunk lists, build the distribution, then either
+// sample (sample mode) or arrive on the sequence.
+__device__ void finish_row(const VerifyParams& p, int row, int lane) {
+    float lv = -INFINITY;
+    int lid = SENT_ID;
+    const size_t base = (size_t)row * p.chunks * LISTN;
+    constexpr int BATCH = 8;
+    for (int c0 = 0; c0 < p.chunks; c0 += BATCH) {
+        float bv[BATCH];
+        int bi[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int c = c0 + j;
+            if (c < p.chunks) {
+                bv[j] = __ldcg(p.cl_v + base + (size_t)c * LISTN + lane);
+                bi[j] = __ldcg(p.cl_id + base + (size_t)c * LISTN + lane);
+            } else {
+                bv[j] = -INFINITY; bi[j] = SENT_ID;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j)
+            if (c0 + j < p.chunks) warp_merge_desc(lv, lid, bv[j], bi[j], lane);
+    }
+    build_row_dist(p, row, lv, lid, lane);
+
+    if (p.mode == MODE_SAMPLE) {
+        int key = __ldcg(p.rd_id + (size_t)row * LISTN + lane);
+        float w = __ldcg(p.rd_p + (size_t)row * LISTN + lane);
+        if (key < 0) { key = SENT_ID; w = 0.0f; }
+        float Z;
+        const int tok = inverse_cdf_draw(key, w, p.u[row], lane, Z);
+        if (lane == 0) p.out_tokens[row] = tok;
+        return;
+    }
+    const RowInfo ri = row_info(p, row);
+    const int b = ri.seq;
+    const int kb = draft_count(p, b);
+    const int expected = (kb + 1) + (p.draft != nullptr && p.temperature != 0.0f ? kb : 0);
+    __threadfence();
+    __syncwarp();
+    int prev = 0;
+    if (lane == 0) prev = atomicAdd(p.seq_cnt + b, 1);
+    prev = __shfl_sync(FULL, prev, 0);
+    if (prev == expected - 1) {
+        __threadfence();
+        finish_sequence(p, b, lane);
+    }
+}
+
+__device__ void record_timeout(const VerifyParams& p, int item) {
+    const int row = item / p.chunks;
+    const RowInfo ri = row_info(p, row);
+    if (p.mode == MODE_SAMPLE) {
+        p.out_tokens[row] = -1;
+    } else if (p.seq_status) {
+        p.seq_status[ri.seq] = SPEC_E_TIMEOUT;
+    }
+}
+
+__global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[VT_WARPS][VT_STAGES];
+    __shared__ StageDesc descs[VT_WARPS][VT_STAGES];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    float* ring = reinterpret_cast<float*>(smem) + (size_t)warp * VT_STAGES * VT_STAGE_ELEMS;
+    const uint32_t ring_u32 = smem_u32(ring);
+    uint32_t bar_u32[VT_STAGES];
+#pragma unroll
+    for (int s = 0; s < VT_STAGES; ++s) bar_u32[s] = smem_u32(&bars[warp][s]);
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < VT_STAGES; ++s) mbar_init(bar_u32[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    const int k = p.top_k;
+    const uint64_t pol = policy_evict_first();
+    ProdState ps;
+    ps.item = -1; ps.pos = ps.end = 0; ps.first = false; ps.ptr = nullptr;
+
+    int inflight = 0;
+    if (lane == 0) {
+        for (int s = 0; s < VT_STAGES; ++s) {
+            StageDesc d;
+            if (!next_stage(p, ps, d)) break;
+            descs[warp][s] = d;
+            issue_stage(ps, d, ring_u32 + s * VT_STAGE_BYTES, bar_u32[s], pol);
+            ++inflight;
+        }
+    }
+    inflight = __shfl_sync(FULL, inflight, 0);
+    __syncwarp();
+
+    uint32_t phase = 0;
+    float lv = -INFINITY, lb = -INFINITY;
+    int lid = SENT_ID;
+    int slot = 0;
+    while (inflight > 0) {
+        const bool ok = mbar_wait(bar_u32[slot], (phase >> slot) & 1u);
+        if (!__all_sync(FULL, ok)) {
+            // The copy never completed: report, drain the other buffers (bounded), stop.
+            if (lane == 0) record_timeout(p, descs[warp][slot].item);
+            for (int s = 1; s < inflight; ++s) {
+                const int sl = (slot + s) % VT_STAGES;
+                mbar_wait(bar_u32[sl], (phase >> sl) & 1u);
+            }
+            return;
+        }
+        phase ^= 1u << slot;
+        const StageDesc d = descs[warp][slot];
+        const float4* buf = reinterpret_cast<const float4*>(ring + slot * VT_STAGE_ELEMS);
+        const int n4 = d.count >> 2;
+
+        if (d.flags & 1) {
+            // New item: reset the list; lower bound = k-th largest lane maximum of this stage.
+            lv = -INFINITY; lid = SENT_ID;
+            float m = -INFINITY;
+#pragma unroll 4
+            for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+                const int idx = lane + 32 * j;
+                if (idx < n4) {
+                    const float4 x = buf[idx];
+                    m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+                }
+            }
+            int dummy = lane;
+            warp_sort_desc(m, dummy, lane);
+            lb = __shfl_sync(FULL, m, k - 1);
+        }
+        float thr_v = __shfl_sync(FULL, lv, k - 1);
+        int thr_id = __shfl_sync(FULL, lid, k - 1);
+        float cut = fmaxf(lb, thr_v);
+#pragma unroll 4
+        for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+            const int idx = lane + 32 * j;
+            const bool valid = idx < n4;
+            float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (valid) x = buf[idx];
+            const float m = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+            if (__any_sync(FULL, valid && m >= cut)) {
+                const int id0 = d.start + 4 * idx;
+                unsigned pend = 0;
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float xc = pick4(x, c);
+                        if (xc >= lb && better(xc, id0 + c, thr_v, thr_id)) pend |= 1u << c;
+                    }
+                }
+                while (__any_sync(FULL, pend != 0)) {
+                    const bool has = pend != 0;
+                    const int c = has ? __ffs(pend) - 1 : 0;
+                    pend &= pend - 1;
+                    offer_round(lv, lid, has, pick4(x, c), id0 + c, lane);
+                    thr_v = __shfl_sync(FULL, lv, k - 1);
+                    thr_id = __shfl_sync(FULL, lid, k - 1);
+                    cut = fmaxf(lb, thr_v);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        if ((pend >> cc) & 1u) {
+                            const float xc = pick4(x, cc);
+                            if (!better(xc, id0 + cc, thr_v, thr_id)) pend &= ~(1u << cc);
+                        }
+                    }
+                }
+            }
+        }
+
+        if (d.flags & 2) {
+            // End of the item: scalar head / tail of the row, publish the chunk list.
+            const int row = d.item / p.chunks, c = d.item % p.chunks;
+            const RowInfo ri = row_info(p, row);
+            int head, body;
+            row_split(ri.ptr, p.V, head, body);
+            const int tail0 = head + body, tail = p.V - tail0;
+            if (c == 0 && head > 0) {
+                const bool has = lane < head;
+                offer_round(lv, lid, has, has ? ri.ptr[lane] : 0.0f, lane, lane);
+            }
+            if (c == p.chunks - 1 && tail > 0) {
+                const bool has = lane < tail;
+                offer_round(lv, lid, has, has ? ri.ptr[tail0 + lane] : 0.0f, tail0 + lane, lane);
+            }
+            const size_t o = ((size_t)row * p.chunks + c) * LISTN + lane;
+            p.cl_v[o] = lv;
+            p.cl_id[o] = lid;
+            __threadfence();
+            __syncwarp();
+            int prev = 0;
+            if (lane == 0) prev = atomicAdd(p.row_cnt + row, 1);
+            prev = __shfl_sync(FULL, prev, 0);
+            if (prev == p.chunks - 1) {
+                __threadfence();
+                finish_row(p, row, lane);
+            }
+        }
+
+        __syncwarp();
+        int more = 0;
+        if (lane == 0) {
+            StageDesc nd;
+            if (next_stage(p, ps, nd)) {
+                descs[warp][slot] = nd;
+                issue_stage(ps, nd, ring_u32 + slot * VT_STAGE_BYTES, bar_u32[slot], pol);
+                more = 1;
+            }
+        }
+        more = __shfl_sync(FULL, more, 0);
+        inflight += more - 1;
+        slot = (slot + 1 == VT_STAGES) ? 0 : slot + 1;
+        __syncwarp();
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+struct Plan {
+    int n_rows, chunks, chunk_elems;
+    size_t off_work, off_row, off_seq, off_clv, off_clid, off_rdn, off_rdid, off_rdp, total, counters_bytes;
+};
+
+static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static Plan make_plan(int n_rows_max, int n_seq, int V) {
+    Plan pl{};
+    pl.n_rows = n_rows_max;
+    const int per_row = std::max(1, (VT_TARGET_ITEMS + n_rows_max - 1) / n_rows_max);
+    long long ch = ((long long)V + per_row - 1) / per_row;
+    ch = ((ch + VT_STAGE_ELEMS - 1) / VT_STAGE_ELEMS) * VT_STAGE_ELEMS;
+    if (ch < VT_STAGE_ELEMS) ch = VT_STAGE_ELEMS;
+    long long chunks = ((long long)V + ch - 1) / ch;
+    if (chunks > VT_MAX_CHUNKS) {
+        chunks = VT_MAX_CHUNKS;
+        ch = (((long long)V + chunks - 1) / chunks + VT_STAGE_ELEMS - 1) / VT_STAGE_ELEMS * VT_STAGE_ELEMS;
+        chunks = ((long long)V + ch - 1) / ch;
+    }
+    pl.chunks = (int)chunks;
+    pl.chunk_elems = (int)ch;
+    size_t o = 0;
+    pl.off_work = o; o += 4;
+    pl.off_row = o; o += (size_t)n_rows_max * 4;
+    pl.off_seq = o; o += (size_t)n_seq * 4;
+    pl.counters_bytes = o;
+    o = align256(o);
+    const size_t lists = (size_t)n_rows_max * pl.chunks * LISTN;
+    pl.off_clv = o; o = align256(o + lists * 4);
+    pl.off_clid = o; o = align256(o + lists * 4);
+    pl.off_rdn = o; o = align256(o + (size_t)n_rows_max * 4);
+    pl.off_rdid = o; o = align256(o + (size_t)n_rows_max * LISTN * 4);
+    pl.off_rdp = o; o = align256(o + (size_t)n_rows_max * LISTN * 4);
+    pl.total = o;
+    return pl;
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return n;
+}
+
+static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream_t st) {
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    prm.work = reinterpret_cast<int*>(w + pl.off_work);
+    prm.row_cnt = reinterpret_cast<int*>(w + pl.off_row);
+    prm.seq_cnt = reinterpret_cast<int*>(w + pl.off_seq);
+    prm.cl_v = reinterpret_cast<float*>(w + pl.off_clv);
+    prm.cl_id = reinterpret_cast<int*>(w + pl.off_clid);
+    prm.rd_n = reinterpret_cast<int*>(w + pl.off_rdn);
+    prm.rd_id = reinterpret_cast<int*>(w + pl.off_rdid);
+    prm.rd_p = reinterpret_cast<float*>(w + pl.off_rdp);
+    prm.chunks = pl.chunks;
+    prm.chunk_elems = pl.chunk_elems;
+    prm.n_items = prm.n_rows * pl.chunks;
+
+    static bool attr_done = false;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, VT_SMEM) != cudaSuccess)
+            return set_error(SPEC_E_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
+        attr_done = true;
+    }
+    cudaError_t e = cudaMemsetAsync(ws, 0, pl.counters_bytes, st);
+    if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    const int nsm = sm_count();
+    if (nsm <= 0) return set_error(SPEC_E_CUDA, "no CUDA device");
+    const int grid = std::max(1, std::min(nsm, (prm.n_items + VT_WARPS - 1) / VT_WARPS));
+    verify_kernel<<<grid, VT_THREADS, VT_SMEM, st>>>(prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "verify_kernel launch: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+static int check_sampling(const spec_sampling* s, int V, int& k_eff) {
+    if (s == nullptr) return set_error(SPEC_E_INVAL, "sampling is NULL");
+    if (!(s->temperature >= 0.0f) || std::isinf(s->temperature))
+        return set_error(SPEC_E_INVAL, "temperature must be finite and >= 0");
+    if (s->temperature == 0.0f) { k_eff = 1; return SPEC_OK; }
+    if (s->top_k < 1 || s->top_k > SPEC_TOPK_MAX)
+        return set_error(SPEC_E_INVAL, "top_k must be in [1, %d] when temperature > 0", SPEC_TOPK_MAX);
+    if (!(s->top_p >= 0.0f)) return set_error(SPEC_E_INVAL, "top_p must be >= 0");
+    k_eff = std::min(s->top_k, V);
+    return SPEC_OK;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t spec_verify_logits_workspace_bytes(int B, int K, int V) {
+    if (B < 1 || K < 0 || V < 2 || K > VT_MAX_K) return 0;
+    return make_plan(B * (2 * K + 1), B, V).total;
+}
+
+extern "C" int spec_verify_logits(int B, int K, int V, const float* target_logits, const float* draft_logits,
+                                  const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
+                                  const spec_sampling* sampling, int32_t* accepted_len, int32_t* next_token,
+                                  int32_t* out_ids, float* out_probs, int32_t* seq_status, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    clear_error();
+    if (B < 1 || K < 0 || V < 2) return set_error(SPEC_E_INVAL, "bad sizes B=%d K=%d V=%d", B, K, V);
+    if (K > VT_MAX_K) return set_error(SPEC_E_INVAL, "K=%d above the maximum %d", K, VT_MAX_K);
+    if ((long long)B * (2 * K + 1) * (long long)V >= (1LL << 40))
+        return set_error(SPEC_E_RANGE, "logits too large");
+    int k_eff = 1;
+    int rc = check_sampling(sampling, V, k_eff);
+    if (rc != SPEC_OK) return rc;
+    if (!target_logits || !uniforms || !accepted_len || !next_token || !workspace)
+        return set_error(SPEC_E_INVAL, "NULL required pointer");
+    if (K > 0 && !draft_tokens) return set_error(SPEC_E_INVAL, "draft_tokens is NULL");
+    if ((out_ids == nullptr) != (out_probs == nullptr))
+        return set_error(SPEC_E_INVAL, "out_ids and out_probs must both be given or both be NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return set_error(SPEC_E_INVAL, "workspace not 256-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(target_logits) & 3) || (reinterpret_cast<uintptr_t>(draft_logits) & 3))
+        return set_error(SPEC_E_INVAL, "logits must be 4-byte aligned");
+    const Plan pl = make_plan(B * (2 * K + 1), B, V);
+    if (workspace_bytes < pl.total)
+        return set_error(SPEC_E_NOMEM, "workspace %zu bytes < required %zu", workspace_bytes, pl.total);
+
+    VerifyParams prm{};
+    prm.target = target_logits;
+    const bool sampling_mode = sampling->temperature != 0.0f;
+    prm.draft = (sampling_mode && K > 0) ? draft_logits : nullptr;
+    prm.draft_tokens = draft_tokens;
+    prm.draft_len = draft_len;
+    prm.u = uniforms;
+    prm.B = B; prm.K = K; prm.V = V;
+    prm.temperature = sampling->temperature;
+    prm.top_k = k_eff;
+    prm.top_p = sampling->top_p;
+    prm.mode = MODE_VERIFY;
+    prm.n_target_rows = B * (K + 1);
+    prm.n_rows = prm.n_target_rows + (prm.draft ? B * K : 0);
+    prm.accepted_len = accepted_len;
+    prm.next_token = next_token;
+    prm.out_ids = out_ids;
+    prm.out_probs = out_probs;
+    prm.seq_status = seq_status;
+    prm.out_tokens = nullptr;
+    return launch_verify(prm, pl, workspace, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t spec_sample_logits_workspace_bytes(int R, int V) {
+    if (R < 1 || V < 2) return 0;
+    return make_plan(R, R, V).total;
+}
+
+extern "C" int spec_sample_logits(int R, int V, const float* logits, const float* uniforms,
+                                  const spec_sampling* sampling, int32_t* out_tokens, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    clear_error();
+    if (R < 1 || V < 2) return set_error(SPEC_E_INVAL, "bad sizes R=%d V=%d", R, V);
+    int k_eff = 1;
+    int rc = check_sampling(sampling, V, k_eff);
+    if (rc != SPEC_OK) return rc;
+    if (!logits || !uniforms || !out_tokens || !workspace) return set_error(SPEC_E_INVAL, "NULL required pointer");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return set_error(SPEC_E_INVAL, "workspace not 256-byte aligned");
+    if (reinterpret_cast<uintptr_t>(logits) & 3) return set_error(SPEC_E_INVAL, "logits must be 4-byte aligned");
+    const Plan pl = make_plan(R, R, V);
+    if (workspace_bytes < pl.total)
+        return set_error(SPEC_E_NOMEM, "workspace %zu bytes < required %zu", workspace_bytes, pl.total);
+    VerifyParams prm{};
+    prm.target = logits;
+    prm.u = uniforms;
+    prm.B = R; prm.K = 0; prm.V = V;
+    prm.temperature = sampling->temperature;
+    prm.top_k = k_eff;
+    prm.top_p = sampling->top_p;
+    prm.mode = MODE_SAMPLE;
+    prm.n_target_rows = R;
+    prm.n_rows = R;
+    prm.out_tokens = out_tokens;
+    return launch_verify(prm, pl, workspace, static_cast<cudaStream_t>(stream));
+}
