@@ -115,6 +115,106 @@ int spec_sample_logits(int R, int V, const float* logits, const float* uniforms,
                        const spec_sampling* sampling /* host */, int32_t* out_tokens,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+
+/* ------------------------------------------------------------------------------------
+ * Model context: the target decoder's verify pass, its paged KV cache and the trim.
+ *
+ * The decoder is the plain dense Llama/Qwen-style reading (the pages name the model
+ * families but print no architecture): x = E[tok]; per layer h = RMSNorm(x),
+ * q, k, v = h Wq^T, h Wk^T, h Wv^T, rotate-half RoPE on q and k at absolute positions,
+ * causal GQA softmax attention (scale 1/sqrt(head_dim)), x += attn Wo^T,
+ * x += (silu(RMSNorm(x) Wg^T) * (RMSNorm(x) Wu^T)) Wd^T; logits = RMSNorm(x) Wlm^T.
+ * No biases, untied lm_head.  The residual stream is fp32; dtype sets the storage of
+ * weights, GEMM inputs and the KV cache.
+ *
+ * KV cache ([SD-Apple] "Why this needed a patch"): paged, page_tokens = 16 tokens per
+ * page, one block table per sequence slot, pages shared by all layers.  The sequence
+ * lengths live on the device; a trim is an O(1) length update on the device (the pages
+ * past the new length stay reserved and are reclaimed lazily by spec_seq_len /
+ * spec_seq_reset).  Convention: before spec_verify the cache holds every committed token
+ * of the sequence except the pending one (last_tokens[b]); the pass appends K+1 entries
+ * (pending + drafts); keeping a+1 of them commits the pending token and the a accepted
+ * drafts, and next_token[b] becomes the new pending token.
+ * ---------------------------------------------------------------------------------- */
+#define SPEC_F32  0
+#define SPEC_BF16 1
+#define SPEC_PAGE_TOKENS 16
+
+typedef struct {
+    int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+    float rope_theta, rms_eps;
+    int32_t dtype;                 /* SPEC_F32 or SPEC_BF16 */
+} spec_model_cfg;
+
+typedef struct {
+    int32_t max_batch;             /* sequence slots [0, max_batch) */
+    int32_t max_ctx;               /* tokens per sequence, pending ones included */
+    int32_t max_k;                 /* drafts per verify pass, <= 64 */
+    int32_t num_pages;             /* KV pool pages; 0 = max_batch * ceil(max_ctx / 16) */
+    int32_t prefill_chunk;         /* tokens per prefill pass; 0 = 128 */
+} spec_ctx_limits;
+
+typedef struct spec_ctx spec_ctx;
+
+/* Create a context bound to `stream` (cudaStream_t as void*): allocates the KV pool,
+ * activations and workspaces on the current device.  SPEC_E_INVAL on a bad shape
+ * (head_dim must be even and <= 256, d_model / ffn_dim / heads*head_dim multiples of 8,
+ * n_q_heads a multiple of n_kv_heads), SPEC_E_NOMEM when an allocation fails. */
+int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* limits, void* stream, spec_ctx** out);
+
+/* Borrow the weights: never copied, the caller keeps them alive ([MTP-fixes] "Duplicate
+ * weights in unified memory": a second resident copy is what to avoid).  names[i] is
+ * one of "embed" [V][d], "final_norm" [d], "lm_head" [V][d], and per layer l
+ * "layers.<l>.attn_norm" [d], ".wq" [hq*hd][d], ".wk" [hkv*hd][d], ".wv" [hkv*hd][d],
+ * ".wo" [d][hq*hd], ".ffn_norm" [d], ".wg" [F][d], ".wu" [F][d], ".wd" [d][F];
+ * dev_ptrs[i] a row-major device array of the model dtype, 16-byte aligned.  Missing
+ * names are SPEC_E_STATE at the first forward. */
+int spec_load_weights(spec_ctx* ctx, const char* const* names, const void* const* dev_ptrs, int n);
+
+/* Ingest tokens[0..n) (device int32) of sequence slot seq_id after what it already holds
+ * (chunks of prefill_chunk tokens, the same kernels as the verify pass).  When
+ * out_last_logits (device fp32 [V]) is given it receives the logits after the last token.
+ * Note the KV convention above: to start a generation, prefill the prompt without its
+ * last token and pass that token as the pending one. */
+int spec_prefill(spec_ctx* ctx, int seq_id, const int32_t* tokens, int n, float* out_last_logits);
+
+/* The verify pass ([SD-Apple] "How speculative decoding works"; [Draft] "#2"):
+ * one batched target forward over [last_tokens[b], draft_tokens[b][0..K)] for the B
+ * sequence slots seq_ids[0..B) (HOST array), then the fused verify of
+ * spec_verify_logits on the resulting logits (draft_logits [B][K][V] fp32 gives q;
+ * NULL = deterministic drafts), then, when auto_trim != 0, the trim to len + a + 1.
+ * With auto_trim == 0 the K+1 entries stay and spec_kv_trim does the trim later.
+ * Outputs as spec_verify_logits; out_logits (device fp32 [B][K+1][V], may be NULL)
+ * receives the target logits.  Draft ids outside [0, V) are embedded as token 0 and can
+ * never be accepted.  SPEC_E_RANGE when a sequence would exceed max_ctx, SPEC_E_NOMEM
+ * when the page pool is exhausted. */
+int spec_verify(spec_ctx* ctx, int B, const int32_t* seq_ids, int K,
+                const int32_t* last_tokens, const int32_t* draft_tokens, const int32_t* draft_len,
+                const float* draft_logits, const float* uniforms, const spec_sampling* sampling,
+                int32_t* accepted_len, int32_t* next_token, int32_t* out_ids, float* out_probs,
+                int32_t* seq_status, float* out_logits, int auto_trim);
+
+/* Single-token decode of B slots: spec_verify with K = 0 (the token is appended and the
+ * next one is drawn from its logits with uniforms[b]).  The comparator of the verify pass. */
+int spec_decode(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* tokens,
+                const spec_sampling* sampling, const float* uniforms, int32_t* next_token,
+                float* out_logits);
+
+/* Trim after a verify pass run with auto_trim == 0: keep accepted_len[b] + 1 of the
+ * K + 1 entries it appended (device O(1) length update). */
+int spec_kv_trim(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len);
+
+/* Exact length of a slot (synchronises the context stream; reclaims pages past it). */
+int spec_seq_len(spec_ctx* ctx, int seq_id, int32_t* out_len);
+
+/* Empty a slot and return its pages to the pool. */
+int spec_seq_reset(spec_ctx* ctx, int seq_id);
+
+/* Number of kernels the context launched since creation (for launch accounting). */
+long long spec_kernel_launches(const spec_ctx* ctx);
+
+void spec_destroy(spec_ctx* ctx);
+
 #ifdef __cplusplus
 }
 #endif

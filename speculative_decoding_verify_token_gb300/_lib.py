@@ -38,6 +38,21 @@ class SpecError(RuntimeError):
         self.code = code
 
 
+class SpecModelCfg(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("dtype", ctypes.c_int32)]
+
+
+class SpecCtxLimits(ctypes.Structure):
+    _fields_ = [("max_batch", ctypes.c_int32), ("max_ctx", ctypes.c_int32), ("max_k", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("prefill_chunk", ctypes.c_int32)]
+
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "spec_last_error": (ctypes.c_char_p, []),
@@ -49,6 +64,19 @@ SIGNATURES = {
     "spec_sample_logits_workspace_bytes": (c_size, [c_int, c_int]),
     "spec_sample_logits": (c_int, [c_int, c_int, c_vp, c_vp, ctypes.POINTER(SpecSampling), c_vp,
                                    c_vp, c_size, c_vp]),
+    "spec_create": (c_int, [ctypes.POINTER(SpecModelCfg), ctypes.POINTER(SpecCtxLimits), c_vp,
+                            ctypes.POINTER(c_vp)]),
+    "spec_load_weights": (c_int, [c_vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(c_vp), c_int]),
+    "spec_prefill": (c_int, [c_vp, c_int, c_vp, c_int, c_vp]),
+    "spec_verify": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp, c_vp, c_vp, c_vp, c_vp,
+                            ctypes.POINTER(SpecSampling), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int]),
+    "spec_decode": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_vp, ctypes.POINTER(SpecSampling), c_vp,
+                            c_vp, c_vp]),
+    "spec_kv_trim": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp]),
+    "spec_seq_len": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32)]),
+    "spec_seq_reset": (c_int, [c_vp, c_int]),
+    "spec_kernel_launches": (ctypes.c_longlong, [c_vp]),
+    "spec_destroy": (None, [c_vp]),
 }
 
 _lib = None

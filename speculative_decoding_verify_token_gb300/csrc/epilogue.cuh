@@ -1,0 +1,105 @@
+// GEMM epilogues of the decoder layers, shared by the SIMT and the tcgen05 GEMMs.
+//
+// A GEMM computes acc[m][n] = sum_k X[m][k] W[n][k]; the epilogue consumes the two
+// outputs of a row pair (n0, n1) of one token m:
+//  * EPI_QKV    : the pair is (j, j + hd/2) of one head of the stacked [q; k; v] rows;
+//                 rotate-half RoPE at the token's absolute position for q and k, then q
+//                 goes to the Q buffer and k, v into the token's paged-KV slot;
+//  * EPI_SWIGLU : the pair is (gate f, up f) -> H[m][f] = silu(gate) * up;
+//  * EPI_RESID  : the pair is (2p, 2p + 1) -> X[m][n] += acc (fp32 residual stream);
+//  * EPI_STORE  : the pair is (2p, 2p + 1) -> out[m][n] = acc (fp32 logits).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace sv {
+
+enum EpiKind { EPI_QKV = 0, EPI_SWIGLU = 1, EPI_RESID = 2, EPI_STORE = 3 };
+
+struct EpiArgs {
+    int kind;
+    int M;
+    // QKV
+    void* q_out;                // [M][hq*hd]
+    void* k_layer;              // [P][hkv][16][hd] of this layer
+    void* v_layer;
+    const int* block_table;     // [slots][max_pages]
+    int max_pages;
+    const int* tok_seq;         // [M] slot of token m
+    const int* tok_pos;         // [M] absolute position of token m
+    const float2* rope;         // [max_pos][hd/2] (cos, sin)
+    int hq, hkv, hd;
+    // SWIGLU
+    void* h_out;                // [M][F]
+    int F;
+    // RESID / STORE
+    float* x;                   // [M][ldx]
+    int ldx;
+};
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Row pair of pair index p for the QKV layout: head slot hs in [0, hq + 2 hkv), j < hd/2.
+__device__ __forceinline__ void qkv_pair_rows(int p, int hd, int& hs, int& j) {
+    const int half = hd >> 1;
+    hs = p / half;
+    j = p - hs * half;
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_pair(const EpiArgs& e, int m, int p, float a0, float a1) {
+    switch (e.kind) {
+    case EPI_QKV: {
+        int hs, j;
+        qkv_pair_rows(p, e.hd, hs, j);
+        const int half = e.hd >> 1;
+        const int pos = e.tok_pos[m];
+        if (hs < e.hq + e.hkv) {
+            const float2 cs = e.rope[(size_t)pos * half + j];
+            const float r0 = a0 * cs.x - a1 * cs.y;
+            const float r1 = a1 * cs.x + a0 * cs.y;
+            a0 = r0; a1 = r1;
+        }
+        if (hs < e.hq) {
+            T* q = static_cast<T*>(e.q_out) + (size_t)m * e.hq * e.hd + (size_t)hs * e.hd;
+            q[j] = from_f32<T>(a0);
+            q[j + half] = from_f32<T>(a1);
+        } else {
+            const bool is_k = hs < e.hq + e.hkv;
+            const int kvh = is_k ? hs - e.hq : hs - e.hq - e.hkv;
+            const int page = e.block_table[(size_t)e.tok_seq[m] * e.max_pages + (pos >> 4)];
+            T* base = static_cast<T*>(is_k ? e.k_layer : e.v_layer) +
+                      (((size_t)page * e.hkv + kvh) * 16 + (pos & 15)) * e.hd;
+            base[j] = from_f32<T>(a0);
+            base[j + half] = from_f32<T>(a1);
+        }
+        break;
+    }
+    case EPI_SWIGLU:
+        static_cast<T*>(e.h_out)[(size_t)m * e.F + p] = from_f32<T>(silu_f(a0) * a1);
+        break;
+    case EPI_RESID: {
+        float* x = e.x + (size_t)m * e.ldx + 2 * p;
+        x[0] += a0;
+        x[1] += a1;
+        break;
+    }
+    default: {
+        float* x = e.x + (size_t)m * e.ldx + 2 * p;
+        x[0] = a0;
+        x[1] = a1;
+        break;
+    }
+    }
+}
+
+}  // namespace sv

@@ -1,0 +1,122 @@
+// The model context of the C ABI (spec_ctx) and the launchers of the decoder kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "specverify.h"
+
+namespace sv {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+constexpr int ATT_CHUNK = 64;          // keys per attention split (absolute positions)
+
+struct LayerWeights {
+    const void *attn_norm = nullptr, *wq = nullptr, *wk = nullptr, *wv = nullptr, *wo = nullptr;
+    const void *ffn_norm = nullptr, *wg = nullptr, *wu = nullptr, *wd = nullptr;
+};
+
+struct ModelWeights {
+    const void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+    std::vector<LayerWeights> layers;
+};
+
+struct AttnArgs {
+    const void* q;            // [M][hq][hd]
+    void* o;                  // [M][hq][hd]
+    const void* k_layer;      // [P][hkv][16][hd]
+    const void* v_layer;
+    const int* block_table;
+    int max_pages;
+    const int* seq_ids;       // [B] device
+    const int* seq_len;       // [slots] device, length before this pass
+    int T, hq, hkv, hd;
+    float scale;
+    int n_chunks;             // chunk capacity of the partial buffers
+    float* part_o;            // [B][hkv][n_chunks][T*G][hd]
+    float2* part_ml;          // [B][hkv][n_chunks][T*G]
+};
+
+struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
+
+// The five GEMMs of the decoder pass.
+enum GemmId { GEMM_QKV = 0, GEMM_O = 1, GEMM_GU = 2, GEMM_DOWN = 3, GEMM_LM = 4 };
+constexpr int SLOT_RING = 64;   // pinned staging entries for slot-id uploads
+
+struct Ctx {
+    spec_model_cfg cfg{};
+    spec_ctx_limits lim{};
+    cudaStream_t stream = nullptr;
+    int esize = 4;
+    int device = 0;
+    int num_sms = 0;
+    ModelWeights w;
+    bool weights_ready = false;
+    long long launches = 0;
+
+    // paged KV
+    int num_pages = 0, max_pages = 0;
+    void* k_pool = nullptr;    // [L][P][hkv][16][hd]
+    void* v_pool = nullptr;
+    size_t layer_pool_elems = 0;
+    int* d_block_table = nullptr;   // [slots][max_pages]
+    int* h_block_table = nullptr;   // pinned mirror
+    int* d_seq_len = nullptr;       // [slots]
+    std::vector<int> free_pages;
+    std::vector<int> n_pages;       // pages held per slot
+    std::vector<int> len_hi;        // upper bound of each slot's device length
+    float2* d_rope = nullptr;       // [max_ctx][hd/2]
+
+    // activations
+    int Mmax = 0;
+    float* X = nullptr;             // [Mmax][d]
+    void* Xn = nullptr;             // [Mmax][d]
+    void* Q = nullptr;              // [Mmax][hq*hd]
+    void* O = nullptr;              // [Mmax][hq*hd]
+    void* H = nullptr;              // [Mmax][F]
+    float* logits = nullptr;        // [Mmax][V]
+    int* d_tokens = nullptr;        // [Mmax]
+    int* d_tok_seq = nullptr;
+    int* d_tok_pos = nullptr;
+    int* d_seq_ids = nullptr;       // [max_batch]
+    int* h_seq_ids = nullptr;       // pinned staging ring [SLOT_RING][max_batch]
+    cudaEvent_t ring_ev[SLOT_RING] = {};
+    bool ring_used[SLOT_RING] = {};
+    int ring_pos = 0;
+    int n_chunks = 0;
+    float* part_o = nullptr;
+    float2* part_ml = nullptr;
+    // verify
+    void* vws = nullptr;
+    size_t vws_bytes = 0;
+    int* d_status_scratch = nullptr;
+    // tensor-core GEMM
+    TcGemm* tc = nullptr;
+    bool use_tc = false;
+    std::vector<void*> allocs;
+};
+
+// kernels
+void launch_embed(const Ctx& c, int M, int T, cudaStream_t st);
+void launch_rmsnorm(const Ctx& c, const float* X, const void* g, void* Xn, int M, cudaStream_t st);
+void launch_rope_table(float2* table, int max_pos, int hd, double theta, cudaStream_t st);
+void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens, int B, cudaStream_t st);
+void launch_advance_len(const int* seq_ids, int* seq_len, int B, int mode, int add, const int* accepted, int K,
+                        cudaStream_t st);
+struct EpiArgs;
+void launch_gemm_simt(const Ctx& c, const void* wa, const void* wb, const void* wc, int K, int n_pairs,
+                      const void* X, const EpiArgs& e, cudaStream_t st);
+int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, cudaStream_t st);
+int attention_set_smem_limits(int hd);
+
+// tcgen05 GEMM (bf16 models)
+int tc_create(Ctx& c);                       // plans + tensor maps, after weights are loaded
+void tc_destroy(Ctx& c);
+// returns kernels launched, or a negative SPEC_E_* code
+int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, const EpiArgs& e, cudaStream_t st);
+
+}  // namespace sv
+
+struct spec_ctx : public sv::Ctx {};

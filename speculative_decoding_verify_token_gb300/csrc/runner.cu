@@ -1,0 +1,484 @@
+// Model context of the C ABI: the paged KV cache manager, the decoder pass and the
+// verify / decode / prefill / trim entry points.
+//
+// One pass over B sequences x T tokens (token m = b*T + t):
+//   embed -> per layer [RMSNorm -> QKV GEMM (+RoPE, +KV append) -> attention ->
+//   O GEMM (+residual) -> RMSNorm -> gate/up GEMM (+SwiGLU) -> down GEMM (+residual)]
+//   -> final RMSNorm -> lm_head GEMM (fp32 logits) -> fused verify -> length update.
+// The verify pass is the pages' "one batched forward pass" of the target over the pending
+// token and the K drafts ("Speculative Decoding on Apple Silicon...", "How speculative
+// decoding works"); the trim is the slice of a plain KV cache ("Why this needed a patch
+// to mlx_lm at all"), here an O(1) device-side length update.
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include <cuda_bf16.h>
+
+#include "epilogue.cuh"
+#include "host_util.h"
+#include "model.h"
+
+namespace sv {
+
+// fused verify entry shared with verify.cu (no workspace allocation, context workspace)
+int verify_into(int B, int K, int V, const float* target, const float* draft, const int* draft_tokens,
+                const int* draft_len, const float* u, const spec_sampling* s, int* accepted, int* next, int* out_ids,
+                float* out_probs, int* status, void* ws, size_t ws_bytes, cudaStream_t st);
+
+static int cuda_fail(const char* what, cudaError_t e) {
+    return set_error(SPEC_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+template <typename P>
+static int dalloc(Ctx& c, P** p, size_t bytes, bool zero = false) {
+    void* q = nullptr;
+    if (bytes == 0) bytes = 256;
+    cudaError_t e = cudaMalloc(&q, bytes);
+    if (e != cudaSuccess) return set_error(SPEC_E_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+    c.allocs.push_back(q);
+    if (zero) {
+        e = cudaMemset(q, 0, bytes);
+        if (e != cudaSuccess) return cuda_fail("cudaMemset", e);
+    }
+    *p = static_cast<P*>(q);
+    return SPEC_OK;
+}
+
+static void free_all(Ctx& c) {
+    tc_destroy(c);
+    for (int i = 0; i < SLOT_RING; ++i)
+        if (c.ring_ev[i]) cudaEventDestroy(c.ring_ev[i]);
+    for (void* p : c.allocs) cudaFree(p);
+    c.allocs.clear();
+    if (c.h_block_table) cudaFreeHost(c.h_block_table);
+    if (c.h_seq_ids) cudaFreeHost(c.h_seq_ids);
+    c.h_block_table = nullptr;
+    c.h_seq_ids = nullptr;
+}
+
+// ---- page management ------------------------------------------------------------------
+
+static int reclaim(Ctx& c) {
+    cudaError_t e = cudaStreamSynchronize(c.stream);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    std::vector<int> len(c.lim.max_batch);
+    e = cudaMemcpy(len.data(), c.d_seq_len, sizeof(int) * len.size(), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("cudaMemcpy", e);
+    for (int s = 0; s < c.lim.max_batch; ++s) {
+        c.len_hi[s] = len[s];
+        const int keep = (len[s] + SPEC_PAGE_TOKENS - 1) / SPEC_PAGE_TOKENS;
+        while (c.n_pages[s] > keep) {
+            --c.n_pages[s];
+            c.free_pages.push_back(c.h_block_table[(size_t)s * c.max_pages + c.n_pages[s]]);
+        }
+    }
+    return SPEC_OK;
+}
+
+// Make sure the slots have pages for positions < len_hi + T; copies new table entries.
+static int ensure_pages(Ctx& c, const int* slots, int B, int T) {
+    for (int pass = 0; pass < 2; ++pass) {
+        int need_total = 0;
+        bool range_ok = true;
+        for (int b = 0; b < B; ++b) {
+            const int s = slots[b];
+            const int need_len = c.len_hi[s] + T;
+            if (need_len > c.lim.max_ctx) range_ok = false;
+            const int need = (need_len + SPEC_PAGE_TOKENS - 1) / SPEC_PAGE_TOKENS;
+            need_total += std::max(0, need - c.n_pages[s]);
+        }
+        if ((!range_ok || need_total > (int)c.free_pages.size()) && pass == 0) {
+            int rc = reclaim(c);
+            if (rc != SPEC_OK) return rc;
+            continue;
+        }
+        if (!range_ok) return set_error(SPEC_E_RANGE, "a sequence would exceed max_ctx=%d", c.lim.max_ctx);
+        if (need_total > (int)c.free_pages.size())
+            return set_error(SPEC_E_NOMEM, "KV page pool exhausted (%d free, %d needed)", (int)c.free_pages.size(),
+                             need_total);
+        for (int b = 0; b < B; ++b) {
+            const int s = slots[b];
+            const int need = (c.len_hi[s] + T + SPEC_PAGE_TOKENS - 1) / SPEC_PAGE_TOKENS;
+            const int first = c.n_pages[s];
+            while (c.n_pages[s] < need) {
+                c.h_block_table[(size_t)s * c.max_pages + c.n_pages[s]] = c.free_pages.back();
+                c.free_pages.pop_back();
+                ++c.n_pages[s];
+            }
+            if (c.n_pages[s] > first) {
+                const size_t off = (size_t)s * c.max_pages + first;
+                cudaError_t e = cudaMemcpyAsync(c.d_block_table + off, c.h_block_table + off,
+                                                sizeof(int) * (c.n_pages[s] - first), cudaMemcpyHostToDevice, c.stream);
+                if (e != cudaSuccess) return cuda_fail("block table copy", e);
+            }
+        }
+        return SPEC_OK;
+    }
+    return SPEC_OK;
+}
+
+static int check_slots(const Ctx& c, const int* slots, int B) {
+    if (B < 1 || B > c.lim.max_batch) return set_error(SPEC_E_INVAL, "B=%d outside [1, %d]", B, c.lim.max_batch);
+    if (!slots) return set_error(SPEC_E_INVAL, "seq_ids is NULL");
+    std::vector<char> seen(c.lim.max_batch, 0);
+    for (int b = 0; b < B; ++b) {
+        if (slots[b] < 0 || slots[b] >= c.lim.max_batch)
+            return set_error(SPEC_E_INVAL, "seq_id %d outside [0, %d)", slots[b], c.lim.max_batch);
+        if (seen[slots[b]]) return set_error(SPEC_E_INVAL, "seq_id %d repeated", slots[b]);
+        seen[slots[b]] = 1;
+    }
+    return SPEC_OK;
+}
+
+// Copy slot ids to the device through an entry of a pinned staging ring; an entry is
+// rewritten only after the event recorded behind its previous copy has completed.
+static int upload_slots(Ctx& c, const int* slots, int B) {
+    const int i = c.ring_pos;
+    c.ring_pos = (c.ring_pos + 1) % SLOT_RING;
+    cudaError_t e;
+    if (c.ring_used[i]) {
+        e = cudaEventSynchronize(c.ring_ev[i]);
+        if (e != cudaSuccess) return cuda_fail("cudaEventSynchronize", e);
+    }
+    int* h = c.h_seq_ids + (size_t)i * c.lim.max_batch;
+    std::memcpy(h, slots, sizeof(int) * B);
+    e = cudaMemcpyAsync(c.d_seq_ids, h, sizeof(int) * B, cudaMemcpyHostToDevice, c.stream);
+    if (e != cudaSuccess) return cuda_fail("seq id copy", e);
+    e = cudaEventRecord(c.ring_ev[i], c.stream);
+    if (e != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+    c.ring_used[i] = true;
+    return SPEC_OK;
+}
+
+// ---- the decoder pass ---------------------------------------------------------------------
+
+static inline void* layer_pool(const Ctx& c, void* pool, int l) {
+    return static_cast<uint8_t*>(pool) + (size_t)l * c.layer_pool_elems * c.esize;
+}
+
+static int gemm(Ctx& c, int gid, int layer, const void* wa, const void* wb, const void* wc, int K, int n_pairs,
+                const void* X, const EpiArgs& e) {
+    if (c.use_tc) {
+        const int n = tc_gemm(c, gid, layer, X, e.M, e, c.stream);
+        if (n < 0) return n;
+        c.launches += n;
+        return SPEC_OK;
+    }
+    launch_gemm_simt(c, wa, wb, wc, K, n_pairs, X, e, c.stream);
+    c.launches += 1;
+    return SPEC_OK;
+}
+
+// Forward of B x T tokens already in d_tokens for the slots in d_seq_ids.  logits_out gets
+// every row ([B*T][V]) or, when last_only, the last row only ([V]); nullptr = no lm_head.
+static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bool last_only) {
+    const spec_model_cfg& m = c.cfg;
+    const int M = B * T;
+    const int d = m.d_model, hd = m.head_dim, hq = m.n_q_heads, hkv = m.n_kv_heads, F = m.ffn_dim;
+    cudaStream_t st = c.stream;
+    launch_embed(c, M, T, st);
+    c.launches += 1;
+    int max_after = 0;
+    for (int b = 0; b < B; ++b) max_after = std::max(max_after, c.len_hi[slots[b]] + T);
+
+    EpiArgs eq{};
+    eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
+    eq.tok_seq = c.d_tok_seq; eq.tok_pos = c.d_tok_pos; eq.rope = c.d_rope; eq.hq = hq; eq.hkv = hkv; eq.hd = hd;
+    EpiArgs er{};
+    er.kind = EPI_RESID; er.M = M; er.x = c.X; er.ldx = d;
+    EpiArgs es{};
+    es.kind = EPI_SWIGLU; es.M = M; es.h_out = c.H; es.F = F;
+    AttnArgs aa{};
+    aa.q = c.Q; aa.o = c.O; aa.block_table = c.d_block_table; aa.max_pages = c.max_pages; aa.seq_ids = c.d_seq_ids;
+    aa.seq_len = c.d_seq_len; aa.T = T; aa.hq = hq; aa.hkv = hkv; aa.hd = hd; aa.scale = 1.0f / sqrtf((float)hd);
+    aa.n_chunks = c.n_chunks; aa.part_o = c.part_o; aa.part_ml = c.part_ml;
+
+    int rc;
+    for (int l = 0; l < m.n_layers; ++l) {
+        const LayerWeights& L = c.w.layers[l];
+        launch_rmsnorm(c, c.X, L.attn_norm, c.Xn, M, st);
+        c.launches += 1;
+        eq.k_layer = layer_pool(c, c.k_pool, l);
+        eq.v_layer = layer_pool(c, c.v_pool, l);
+        if ((rc = gemm(c, GEMM_QKV, l, L.wq, L.wk, L.wv, d, (hq + 2 * hkv) * hd / 2, c.Xn, eq)) != SPEC_OK) return rc;
+        aa.k_layer = eq.k_layer;
+        aa.v_layer = eq.v_layer;
+        c.launches += launch_attention(c, aa, B, max_after, st);
+        if ((rc = gemm(c, GEMM_O, l, L.wo, nullptr, nullptr, hq * hd, d / 2, c.O, er)) != SPEC_OK) return rc;
+        launch_rmsnorm(c, c.X, L.ffn_norm, c.Xn, M, st);
+        c.launches += 1;
+        if ((rc = gemm(c, GEMM_GU, l, L.wg, L.wu, nullptr, d, F, c.Xn, es)) != SPEC_OK) return rc;
+        if ((rc = gemm(c, GEMM_DOWN, l, L.wd, nullptr, nullptr, F, d / 2, c.H, er)) != SPEC_OK) return rc;
+    }
+    if (logits_out != nullptr) {
+        const int rows = last_only ? 1 : M;
+        const size_t off = last_only ? (size_t)(M - 1) : 0;
+        launch_rmsnorm(c, c.X + off * d, c.w.final_norm, static_cast<uint8_t*>(c.Xn) + off * d * c.esize, rows, st);
+        c.launches += 1;
+        EpiArgs el{};
+        el.kind = EPI_STORE; el.M = rows; el.x = logits_out; el.ldx = m.vocab;
+        if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2,
+                       static_cast<uint8_t*>(c.Xn) + off * d * c.esize, el)) != SPEC_OK)
+            return rc;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("decoder pass launch", e);
+    return SPEC_OK;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* limits, void* stream, spec_ctx** out) {
+    clear_error();
+    if (!cfg || !limits || !out) return set_error(SPEC_E_INVAL, "NULL argument");
+    const spec_model_cfg& m = *cfg;
+    if (m.n_layers < 1 || m.d_model < 8 || m.d_model % 8 || m.n_q_heads < 1 || m.n_kv_heads < 1 ||
+        m.n_q_heads % m.n_kv_heads || m.head_dim < 2 || m.head_dim % 2 || m.head_dim > 256 ||
+        (m.n_q_heads * m.head_dim) % 8 || m.ffn_dim < 8 || m.ffn_dim % 8 || m.vocab < 2 || m.vocab % 2 ||
+        !(m.rope_theta > 0.0f) || !(m.rms_eps >= 0.0f) || (m.dtype != SPEC_F32 && m.dtype != SPEC_BF16))
+        return set_error(SPEC_E_INVAL, "bad model shape");
+    spec_ctx_limits lim = *limits;
+    if (lim.max_batch < 1 || lim.max_ctx < 2 || lim.max_k < 0 || lim.max_k > 64)
+        return set_error(SPEC_E_INVAL, "bad limits");
+    if (lim.prefill_chunk <= 0) lim.prefill_chunk = 128;
+    lim.prefill_chunk = std::min(lim.prefill_chunk, 256);
+    const int max_pages = (lim.max_ctx + SPEC_PAGE_TOKENS - 1) / SPEC_PAGE_TOKENS;
+    if (lim.num_pages <= 0) lim.num_pages = lim.max_batch * max_pages;
+
+    spec_ctx* c = new spec_ctx();
+    c->cfg = m;
+    c->lim = lim;
+    c->stream = static_cast<cudaStream_t>(stream);
+    c->esize = m.dtype == SPEC_BF16 ? 2 : 4;
+    cudaGetDevice(&c->device);
+    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    c->num_pages = lim.num_pages;
+    c->max_pages = max_pages;
+    c->w.layers.resize(m.n_layers);
+    c->Mmax = std::max(lim.max_batch * (lim.max_k + 1), lim.prefill_chunk);
+    c->n_chunks = (lim.max_ctx + ATT_CHUNK - 1) / ATT_CHUNK;
+    const size_t qd = (size_t)m.n_q_heads * m.head_dim;
+    c->layer_pool_elems = (size_t)lim.num_pages * m.n_kv_heads * SPEC_PAGE_TOKENS * m.head_dim;
+    int rc = SPEC_OK;
+    auto ok = [&](int r) { rc = r; return r == SPEC_OK; };
+    if (!(ok(dalloc(*c, &c->k_pool, c->layer_pool_elems * m.n_layers * c->esize, true)) &&
+          ok(dalloc(*c, &c->v_pool, c->layer_pool_elems * m.n_layers * c->esize, true)) &&
+          ok(dalloc(*c, &c->d_block_table, sizeof(int) * (size_t)lim.max_batch * max_pages, true)) &&
+          ok(dalloc(*c, &c->d_seq_len, sizeof(int) * lim.max_batch, true)) &&
+          ok(dalloc(*c, &c->d_rope, sizeof(float2) * (size_t)lim.max_ctx * (m.head_dim / 2))) &&
+          ok(dalloc(*c, &c->X, sizeof(float) * (size_t)c->Mmax * m.d_model, true)) &&
+          ok(dalloc(*c, &c->Xn, (size_t)c->esize * c->Mmax * m.d_model, true)) &&
+          ok(dalloc(*c, &c->Q, (size_t)c->esize * c->Mmax * qd, true)) &&
+          ok(dalloc(*c, &c->O, (size_t)c->esize * c->Mmax * qd, true)) &&
+          ok(dalloc(*c, &c->H, (size_t)c->esize * c->Mmax * m.ffn_dim, true)) &&
+          ok(dalloc(*c, &c->logits, sizeof(float) * (size_t)c->Mmax * m.vocab)) &&
+          ok(dalloc(*c, &c->d_tokens, sizeof(int) * c->Mmax, true)) &&
+          ok(dalloc(*c, &c->d_tok_seq, sizeof(int) * c->Mmax, true)) &&
+          ok(dalloc(*c, &c->d_tok_pos, sizeof(int) * c->Mmax, true)) &&
+          ok(dalloc(*c, &c->d_seq_ids, sizeof(int) * lim.max_batch, true)) &&
+          ok(dalloc(*c, &c->part_o, sizeof(float) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks * m.head_dim)) &&
+          ok(dalloc(*c, &c->part_ml, sizeof(float2) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks)) &&
+          ok(dalloc(*c, &c->d_status_scratch, sizeof(int) * lim.max_batch)))) {
+        free_all(*c);
+        delete c;
+        return rc;
+    }
+    c->vws_bytes = 0;
+    for (int b = 1; b <= lim.max_batch; ++b)
+        for (int k = 0; k <= lim.max_k; ++k)
+            c->vws_bytes = std::max(c->vws_bytes, spec_verify_logits_workspace_bytes(b, k, m.vocab));
+    if (!ok(dalloc(*c, &c->vws, c->vws_bytes))) {
+        free_all(*c);
+        delete c;
+        return rc;
+    }
+    if (cudaMallocHost(reinterpret_cast<void**>(&c->h_block_table), sizeof(int) * (size_t)lim.max_batch * max_pages) !=
+            cudaSuccess ||
+        cudaMallocHost(reinterpret_cast<void**>(&c->h_seq_ids), sizeof(int) * SLOT_RING * lim.max_batch) !=
+            cudaSuccess) {
+        free_all(*c);
+        delete c;
+        return set_error(SPEC_E_NOMEM, "cudaMallocHost failed");
+    }
+    std::memset(c->h_block_table, 0, sizeof(int) * (size_t)lim.max_batch * max_pages);
+    for (int i = 0; i < SLOT_RING; ++i) {
+        if (cudaEventCreateWithFlags(&c->ring_ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            free_all(*c);
+            delete c;
+            return set_error(SPEC_E_CUDA, "cudaEventCreate failed");
+        }
+    }
+    c->free_pages.resize(lim.num_pages);
+    for (int i = 0; i < lim.num_pages; ++i) c->free_pages[i] = lim.num_pages - 1 - i;
+    c->n_pages.assign(lim.max_batch, 0);
+    c->len_hi.assign(lim.max_batch, 0);
+    launch_rope_table(c->d_rope, lim.max_ctx, m.head_dim, (double)m.rope_theta, c->stream);
+    if (attention_set_smem_limits(m.head_dim) != 0) {
+        free_all(*c);
+        delete c;
+        return set_error(SPEC_E_CUDA, "attention shared-memory attribute");
+    }
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        free_all(*c);
+        delete c;
+        return cuda_fail("spec_create", e);
+    }
+    *out = c;
+    return SPEC_OK;
+}
+
+extern "C" int spec_load_weights(spec_ctx* c, const char* const* names, const void* const* ptrs, int n) {
+    clear_error();
+    if (!c || (n > 0 && (!names || !ptrs))) return set_error(SPEC_E_INVAL, "NULL argument");
+    for (int i = 0; i < n; ++i) {
+        if (!names[i] || !ptrs[i]) return set_error(SPEC_E_INVAL, "NULL name or pointer at %d", i);
+        if (reinterpret_cast<uintptr_t>(ptrs[i]) & 15) return set_error(SPEC_E_INVAL, "%s not 16-byte aligned", names[i]);
+        const std::string s(names[i]);
+        if (s == "embed") { c->w.embed = ptrs[i]; continue; }
+        if (s == "final_norm") { c->w.final_norm = ptrs[i]; continue; }
+        if (s == "lm_head") { c->w.lm_head = ptrs[i]; continue; }
+        int l = -1;
+        char field[32] = {0};
+        if (std::sscanf(s.c_str(), "layers.%d.%31s", &l, field) != 2 || l < 0 || l >= c->cfg.n_layers)
+            return set_error(SPEC_E_INVAL, "unknown weight name '%s'", names[i]);
+        LayerWeights& L = c->w.layers[l];
+        const std::string f(field);
+        if (f == "attn_norm") L.attn_norm = ptrs[i];
+        else if (f == "wq") L.wq = ptrs[i];
+        else if (f == "wk") L.wk = ptrs[i];
+        else if (f == "wv") L.wv = ptrs[i];
+        else if (f == "wo") L.wo = ptrs[i];
+        else if (f == "ffn_norm") L.ffn_norm = ptrs[i];
+        else if (f == "wg") L.wg = ptrs[i];
+        else if (f == "wu") L.wu = ptrs[i];
+        else if (f == "wd") L.wd = ptrs[i];
+        else return set_error(SPEC_E_INVAL, "unknown weight name '%s'", names[i]);
+    }
+    bool all = c->w.embed && c->w.final_norm && c->w.lm_head;
+    for (const LayerWeights& L : c->w.layers)
+        all = all && L.attn_norm && L.wq && L.wk && L.wv && L.wo && L.ffn_norm && L.wg && L.wu && L.wd;
+    c->weights_ready = all;
+    if (all && c->cfg.dtype == SPEC_BF16) {
+        const int rc = tc_create(*c);
+        if (rc != SPEC_OK) return rc;
+    }
+    return SPEC_OK;
+}
+
+static int common_checks(spec_ctx* c) {
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    if (!c->weights_ready) return set_error(SPEC_E_STATE, "weights not (fully) loaded");
+    return SPEC_OK;
+}
+
+extern "C" int spec_prefill(spec_ctx* c, int seq_id, const int32_t* tokens, int n, float* out_last_logits) {
+    clear_error();
+    int rc = common_checks(c);
+    if (rc != SPEC_OK) return rc;
+    if (seq_id < 0 || seq_id >= c->lim.max_batch) return set_error(SPEC_E_INVAL, "bad seq_id");
+    if (n < 1 || !tokens) return set_error(SPEC_E_INVAL, "bad tokens");
+    if ((rc = upload_slots(*c, &seq_id, 1)) != SPEC_OK) return rc;
+    for (int p0 = 0; p0 < n; p0 += c->lim.prefill_chunk) {
+        const int T = std::min(c->lim.prefill_chunk, n - p0);
+        if ((rc = ensure_pages(*c, &seq_id, 1, T)) != SPEC_OK) return rc;
+        cudaError_t e = cudaMemcpyAsync(c->d_tokens, tokens + p0, sizeof(int) * T, cudaMemcpyDeviceToDevice, c->stream);
+        if (e != cudaSuccess) return cuda_fail("token copy", e);
+        const bool last = p0 + T == n;
+        if ((rc = forward(*c, &seq_id, 1, T, last ? out_last_logits : nullptr, true)) != SPEC_OK) return rc;
+        launch_advance_len(c->d_seq_ids, c->d_seq_len, 1, 0, T, nullptr, 0, c->stream);
+        c->launches += 1;
+        c->len_hi[seq_id] += T;
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_prefill", e);
+}
+
+extern "C" int spec_verify(spec_ctx* c, int B, const int32_t* seq_ids, int K, const int32_t* last_tokens,
+                           const int32_t* draft_tokens, const int32_t* draft_len, const float* draft_logits,
+                           const float* uniforms, const spec_sampling* sampling, int32_t* accepted_len,
+                           int32_t* next_token, int32_t* out_ids, float* out_probs, int32_t* seq_status,
+                           float* out_logits, int auto_trim) {
+    clear_error();
+    int rc = common_checks(c);
+    if (rc != SPEC_OK) return rc;
+    if ((rc = check_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    if (K < 0 || K > c->lim.max_k) return set_error(SPEC_E_INVAL, "K=%d outside [0, %d]", K, c->lim.max_k);
+    if (!last_tokens || (K > 0 && !draft_tokens) || !uniforms || !sampling || !accepted_len || !next_token)
+        return set_error(SPEC_E_INVAL, "NULL required pointer");
+    if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    if ((rc = ensure_pages(*c, seq_ids, B, K + 1)) != SPEC_OK) return rc;
+    launch_verify_tokens(last_tokens, draft_tokens, K, c->d_tokens, B, c->stream);
+    c->launches += 1;
+    float* logits = out_logits ? out_logits : c->logits;
+    if ((rc = forward(*c, seq_ids, B, K + 1, logits, false)) != SPEC_OK) return rc;
+    rc = verify_into(B, K, c->cfg.vocab, logits, draft_logits, draft_tokens, draft_len, uniforms, sampling,
+                     accepted_len, next_token, out_ids, out_probs, seq_status, c->vws, c->vws_bytes, c->stream);
+    if (rc != SPEC_OK) return rc;
+    c->launches += 1;
+    if (auto_trim) launch_advance_len(c->d_seq_ids, c->d_seq_len, B, 1, 0, accepted_len, K, c->stream);
+    else launch_advance_len(c->d_seq_ids, c->d_seq_len, B, 0, K + 1, nullptr, K, c->stream);
+    c->launches += 1;
+    for (int b = 0; b < B; ++b) c->len_hi[seq_ids[b]] += K + 1;
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_verify", e);
+}
+
+extern "C" int spec_decode(spec_ctx* c, int B, const int32_t* seq_ids, const int32_t* tokens,
+                           const spec_sampling* sampling, const float* uniforms, int32_t* next_token,
+                           float* out_logits) {
+    int rc = common_checks(c);
+    if (rc != SPEC_OK) return rc;
+    if (B < 1 || B > c->lim.max_batch) return set_error(SPEC_E_INVAL, "bad B");
+    return spec_verify(c, B, seq_ids, 0, tokens, nullptr, nullptr, nullptr, uniforms, sampling,
+                       c->d_status_scratch, next_token, nullptr, nullptr, nullptr, out_logits, 1);
+}
+
+extern "C" int spec_kv_trim(spec_ctx* c, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    int rc = check_slots(*c, seq_ids, B);
+    if (rc != SPEC_OK) return rc;
+    if (K < 0 || K > c->lim.max_k || !accepted_len) return set_error(SPEC_E_INVAL, "bad K or accepted_len");
+    if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    launch_advance_len(c->d_seq_ids, c->d_seq_len, B, 2, 0, accepted_len, K, c->stream);
+    c->launches += 1;
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_kv_trim", e);
+}
+
+extern "C" int spec_seq_len(spec_ctx* c, int seq_id, int32_t* out_len) {
+    clear_error();
+    if (!c || !out_len || seq_id < 0 || seq_id >= c->lim.max_batch) return set_error(SPEC_E_INVAL, "bad argument");
+    const int rc = reclaim(*c);
+    if (rc != SPEC_OK) return rc;
+    *out_len = c->len_hi[seq_id];
+    return SPEC_OK;
+}
+
+extern "C" int spec_seq_reset(spec_ctx* c, int seq_id) {
+    clear_error();
+    if (!c || seq_id < 0 || seq_id >= c->lim.max_batch) return set_error(SPEC_E_INVAL, "bad argument");
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    e = cudaMemset(c->d_seq_len + seq_id, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail("cudaMemset", e);
+    while (c->n_pages[seq_id] > 0) {
+        --c->n_pages[seq_id];
+        c->free_pages.push_back(c->h_block_table[(size_t)seq_id * c->max_pages + c->n_pages[seq_id]]);
+    }
+    c->len_hi[seq_id] = 0;
+    return SPEC_OK;
+}
+
+extern "C" long long spec_kernel_launches(const spec_ctx* c) { return c ? c->launches : 0; }
+
+extern "C" void spec_destroy(spec_ctx* c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->stream);
+    free_all(*c);
+    delete c;
+}

@@ -41,6 +41,7 @@ constexpr int LISTN = 32;
 constexpr int VT_TARGET_ITEMS = 4096;
 constexpr int VT_MAX_CHUNKS = 128;
 constexpr int VT_MAX_K = 64;
+constexpr int VT_CAND_CAP = 128;          // per-warp candidate buffer (entries)
 
 enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
 
@@ -70,6 +71,7 @@ struct VerifyParams {
     int* work;                  // [1] item counter
     int* row_cnt;               // [n_rows]
     int* seq_cnt;               // [B]
+    unsigned* row_bound;        // [n_rows] order-preserving key of a lower bound of the row's k-th best
     float* cl_v;                // [n_rows][chunks][LISTN]
     int* cl_id;
     int* rd_n;                  // [n_rows]
@@ -183,6 +185,48 @@ __device__ __forceinline__ void offer_round(float& lv, int& lid, bool has, float
     if (!has) { cv = -INFINITY; cid = SENT_ID; }
     warp_sort_desc(cv, cid, lane);
     warp_merge_desc(lv, lid, cv, cid, lane);
+}
+
+// Order-preserving map of floats to unsigned ints (for atomicMax); 0 means "no bound".
+__device__ __forceinline__ unsigned float_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(unsigned k) {
+    if (k == 0u) return -INFINITY;
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Maximum of the lane's float4s of a stage buffer (4 independent chains; NaN ignored).
+__device__ __forceinline__ float stage_lane_max(const float4* buf, int n4, int lane) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    if (n4 == VT_STAGE_ELEMS / 4) {
+#pragma unroll
+        for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+            const float4 x = buf[lane + 32 * j];
+            m0 = fmaxf(m0, x.x); m1 = fmaxf(m1, x.y); m2 = fmaxf(m2, x.z); m3 = fmaxf(m3, x.w);
+        }
+    } else {
+        for (int idx = lane; idx < n4; idx += 32) {
+            const float4 x = buf[idx];
+            m0 = fmaxf(m0, x.x); m1 = fmaxf(m1, x.y); m2 = fmaxf(m2, x.z); m3 = fmaxf(m3, x.w);
+        }
+    }
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// Sort + merge the warp's buffered candidates into its running list, 32 at a time.
+__device__ __forceinline__ void flush_candidates(float& lv, int& lid, const float* cv, const int* ci, int n,
+                                                 int lane) {
+    __syncwarp();
+    for (int base = 0; base < n; base += 32) {
+        const bool has = base + lane < n;
+        float v = has ? cv[base + lane] : -INFINITY;
+        int id = has ? ci[base + lane] : SENT_ID;
+        warp_sort_desc(v, id, lane);
+        warp_merge_desc(lv, lid, v, id, lane);
+    }
+    __syncwarp();
 }
 
 // Truncated distribution of a merged row list (lane j = j-th best), written to rd_*.
@@ -378,6 +422,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[VT_WARPS][VT_STAGES];
     __shared__ StageDesc descs[VT_WARPS][VT_STAGES];
+    __shared__ float cand_v[VT_WARPS][VT_CAND_CAP];
+    __shared__ int cand_id[VT_WARPS][VT_CAND_CAP];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -413,9 +459,12 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
     __syncwarp();
 
     uint32_t phase = 0;
-    float lv = -INFINITY, lb = -INFINITY;
+    float lv = -INFINITY, lb = -INFINITY, published = -INFINITY;
     int lid = SENT_ID;
     int slot = 0;
+    int ccount = 0;
+    float* cbuf_v = cand_v[warp];
+    int* cbuf_id = cand_id[warp];
     while (inflight > 0) {
         const bool ok = mbar_wait(bar_u32[slot], (phase >> slot) & 1u);
         if (!__all_sync(FULL, ok)) {
@@ -432,58 +481,77 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
         const float4* buf = reinterpret_cast<const float4*>(ring + slot * VT_STAGE_ELEMS);
         const int n4 = d.count >> 2;
 
+        const int row_now = d.item / p.chunks;
+        unsigned* rb_ptr = p.row_bound + row_now;
         if (d.flags & 1) {
-            // New item: reset the list; lower bound = k-th largest lane maximum of this stage.
+            // New item: reset the list; lower bound = k-th largest lane maximum of this stage
+            // (k distinct elements reach it, so the chunk's -- and the row's -- k-th best does).
             lv = -INFINITY; lid = SENT_ID;
-            float m = -INFINITY;
-#pragma unroll 4
-            for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
-                const int idx = lane + 32 * j;
-                if (idx < n4) {
-                    const float4 x = buf[idx];
-                    m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
-                }
-            }
+            published = -INFINITY;
+            float m = stage_lane_max(buf, n4, lane);
             int dummy = lane;
             warp_sort_desc(m, dummy, lane);
             lb = __shfl_sync(FULL, m, k - 1);
+            if (lane == 0 && lb > -INFINITY) atomicMax(rb_ptr, float_key(lb));
+            published = lb;
         }
+        // Row-wide bound published by the other chunks of the row (any chunk's k-th best is
+        // a lower bound of the row's k-th best, so filtering by it is exact).
+        lb = fmaxf(lb, key_float(*reinterpret_cast<volatile unsigned*>(rb_ptr)));
         float thr_v = __shfl_sync(FULL, lv, k - 1);
         int thr_id = __shfl_sync(FULL, lid, k - 1);
-        float cut = fmaxf(lb, thr_v);
+        const float cut = fmaxf(lb, thr_v);
+        // Pass 1: the lane's maximum over its 64 values (4 independent chains).
+        const float mx = stage_lane_max(buf, n4, lane);
+        if (__any_sync(FULL, mx >= cut)) {
+            // Pass 2 (rare): exact (value, id) test of the lanes whose maximum reached the cut.
+            unsigned long long pend = 0;
+            if (mx >= cut) {
 #pragma unroll 4
-        for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
-            const int idx = lane + 32 * j;
-            const bool valid = idx < n4;
-            float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (valid) x = buf[idx];
-            const float m = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-            if (__any_sync(FULL, valid && m >= cut)) {
-                const int id0 = d.start + 4 * idx;
-                unsigned pend = 0;
-                if (valid) {
+                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+                    const int idx = lane + 32 * j;
+                    if (idx < n4) {
+                        const float4 x = buf[idx];
+                        const int id0 = d.start + 4 * idx;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float xc = pick4(x, c);
-                        if (xc >= lb && better(xc, id0 + c, thr_v, thr_id)) pend |= 1u << c;
-                    }
-                }
-                while (__any_sync(FULL, pend != 0)) {
-                    const bool has = pend != 0;
-                    const int c = has ? __ffs(pend) - 1 : 0;
-                    pend &= pend - 1;
-                    offer_round(lv, lid, has, pick4(x, c), id0 + c, lane);
-                    thr_v = __shfl_sync(FULL, lv, k - 1);
-                    thr_id = __shfl_sync(FULL, lid, k - 1);
-                    cut = fmaxf(lb, thr_v);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        if ((pend >> cc) & 1u) {
-                            const float xc = pick4(x, cc);
-                            if (!better(xc, id0 + cc, thr_v, thr_id)) pend &= ~(1u << cc);
+                        for (int c = 0; c < 4; ++c) {
+                            const float xc = pick4(x, c);
+                            if (xc >= lb && better(xc, id0 + c, thr_v, thr_id)) pend |= 1ull << (4 * j + c);
                         }
                     }
                 }
+            }
+            // Compact candidates into the warp's buffer, one per lane per round.
+            const float* sb = ring + slot * VT_STAGE_ELEMS;
+            while (true) {
+                const bool has = pend != 0;
+                const unsigned bal = __ballot_sync(FULL, has);
+                if (bal == 0) break;
+                if (has) {
+                    const int bit = __ffsll(pend) - 1;
+                    pend &= pend - 1;
+                    const int e = 4 * (lane + 32 * (bit >> 2)) + (bit & 3);
+                    const int pos = ccount + __popc(bal & ((1u << lane) - 1u));
+                    cbuf_v[pos] = sb[e];
+                    cbuf_id[pos] = d.start + e;
+                }
+                ccount += __popc(bal);
+                if (ccount > VT_CAND_CAP - 32) {
+                    flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
+                    ccount = 0;
+                }
+            }
+        }
+        if (ccount >= 16 || (ccount > 0 && __shfl_sync(FULL, lid, k - 1) == SENT_ID)) {
+            flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
+            ccount = 0;
+        }
+        {
+            const float kth = __shfl_sync(FULL, lv, k - 1);
+            if (kth > published) {
+                if (lane == 0) atomicMax(rb_ptr, float_key(kth));
+                published = kth;
+                lb = fmaxf(lb, kth);
             }
         }
 
@@ -494,6 +562,10 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
             int head, body;
             row_split(ri.ptr, p.V, head, body);
             const int tail0 = head + body, tail = p.V - tail0;
+            if (ccount > 0) {
+                flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
+                ccount = 0;
+            }
             if (c == 0 && head > 0) {
                 const bool has = lane < head;
                 offer_round(lv, lid, has, has ? ri.ptr[lane] : 0.0f, lane, lane);
@@ -537,7 +609,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
 
 struct Plan {
     int n_rows, chunks, chunk_elems;
-    size_t off_work, off_row, off_seq, off_clv, off_clid, off_rdn, off_rdid, off_rdp, total, counters_bytes;
+    size_t off_work, off_row, off_seq, off_rb, off_clv, off_clid, off_rdn, off_rdid, off_rdp, total, counters_bytes;
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -561,6 +633,7 @@ static Plan make_plan(int n_rows_max, int n_seq, int V) {
     pl.off_work = o; o += 4;
     pl.off_row = o; o += (size_t)n_rows_max * 4;
     pl.off_seq = o; o += (size_t)n_seq * 4;
+    pl.off_rb = o; o += (size_t)n_rows_max * 4;
     pl.counters_bytes = o;
     o = align256(o);
     const size_t lists = (size_t)n_rows_max * pl.chunks * LISTN;
@@ -585,6 +658,7 @@ static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream
     prm.work = reinterpret_cast<int*>(w + pl.off_work);
     prm.row_cnt = reinterpret_cast<int*>(w + pl.off_row);
     prm.seq_cnt = reinterpret_cast<int*>(w + pl.off_seq);
+    prm.row_bound = reinterpret_cast<unsigned*>(w + pl.off_rb);
     prm.cl_v = reinterpret_cast<float*>(w + pl.off_clv);
     prm.cl_id = reinterpret_cast<int*>(w + pl.off_clid);
     prm.rd_n = reinterpret_cast<int*>(w + pl.off_rdn);
@@ -623,21 +697,12 @@ static int check_sampling(const spec_sampling* s, int V, int& k_eff) {
     return SPEC_OK;
 }
 
-}  // namespace sv
 
-using namespace sv;
-
-extern "C" size_t spec_verify_logits_workspace_bytes(int B, int K, int V) {
-    if (B < 1 || K < 0 || V < 2 || K > VT_MAX_K) return 0;
-    return make_plan(B * (2 * K + 1), B, V).total;
-}
-
-extern "C" int spec_verify_logits(int B, int K, int V, const float* target_logits, const float* draft_logits,
-                                  const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
-                                  const spec_sampling* sampling, int32_t* accepted_len, int32_t* next_token,
-                                  int32_t* out_ids, float* out_probs, int32_t* seq_status, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
-    clear_error();
+// Validation + launch of the fused verify (used by spec_verify_logits and spec_verify).
+int verify_into(int B, int K, int V, const float* target_logits, const float* draft_logits,
+                const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
+                const spec_sampling* sampling, int32_t* accepted_len, int32_t* next_token, int32_t* out_ids,
+                float* out_probs, int32_t* seq_status, void* workspace, size_t workspace_bytes, cudaStream_t st) {
     if (B < 1 || K < 0 || V < 2) return set_error(SPEC_E_INVAL, "bad sizes B=%d K=%d V=%d", B, K, V);
     if (K > VT_MAX_K) return set_error(SPEC_E_INVAL, "K=%d above the maximum %d", K, VT_MAX_K);
     if ((long long)B * (2 * K + 1) * (long long)V >= (1LL << 40))
@@ -677,7 +742,27 @@ extern "C" int spec_verify_logits(int B, int K, int V, const float* target_logit
     prm.out_probs = out_probs;
     prm.seq_status = seq_status;
     prm.out_tokens = nullptr;
-    return launch_verify(prm, pl, workspace, static_cast<cudaStream_t>(stream));
+    return launch_verify(prm, pl, workspace, st);
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t spec_verify_logits_workspace_bytes(int B, int K, int V) {
+    if (B < 1 || K < 0 || V < 2 || K > VT_MAX_K) return 0;
+    return make_plan(B * (2 * K + 1), B, V).total;
+}
+
+extern "C" int spec_verify_logits(int B, int K, int V, const float* target_logits, const float* draft_logits,
+                                  const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
+                                  const spec_sampling* sampling, int32_t* accepted_len, int32_t* next_token,
+                                  int32_t* out_ids, float* out_probs, int32_t* seq_status, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    clear_error();
+    return verify_into(B, K, V, target_logits, draft_logits, draft_tokens, draft_len, uniforms, sampling,
+                       accepted_len, next_token, out_ids, out_probs, seq_status, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t spec_sample_logits_workspace_bytes(int R, int V) {
