@@ -1,12 +1,541 @@
-// tcgen05 GEMM (bf16 models): placeholder until the tensor-core path lands.
-#include "model.h"
+// Skinny bf16 GEMM of the verify pass on the 5th-generation tensor cores (tcgen05).
+//
+// Y[m][n] = sum_k X[m][k] W[n][k] with M = B*(K+1) tokens (<= 256) and weight matrices of
+// 6-150 k rows: the work is streaming the weights through HBM ("most of that pass is spent
+// moving weights through memory", "Speculative Decoding on Apple Silicon...", section
+// "How speculative decoding works").  Design:
+//  * swap-AB: a 128-row weight tile is the A operand, the tokens are the N dimension
+//    (16..256); the fp32 accumulator [128 x N] lives in tensor memory;
+//  * operands arrive by TMA (cp.async.bulk.tensor, 128-byte swizzle) into an mbarrier ring
+//    of up to 8 stages of 64 k-elements; weights are loaded evict-first, activations
+//    evict-last (every CTA re-reads them);
+//  * warp roles: warp 0 = TMA producer, warp 1 = tcgen05.mma issuer (one thread) and TMEM
+//    owner, warps 2-5 = epilogue (tcgen05.ld of the 4 lane quarters);
+//  * persistent stream-K: the (tile, k-block) space is cut into one contiguous range per
+//    CTA; a tile shared by several CTAs is finished by the last one to arrive (atomic
+//    ticket, no spin-wait), which adds the partial sums in CTA order.  The split depends
+//    only on the weight shape and the SM count, so a token's outputs are bit-identical for
+//    every M (a decode step and a verify pass agree exactly);
+//  * fused epilogues (RoPE + paged KV append, SwiGLU, residual add, fp32 logits) shared
+//    with the CUDA-core GEMM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <algorithm>
+
+#include "common.cuh"
+#include "epilogue.cuh"
 #include "host_util.h"
+#include "model.h"
 
 namespace sv {
-int tc_create(Ctx& c) { c.use_tc = false; return SPEC_OK; }
-void tc_destroy(Ctx& c) { (void)c; }
-int tc_gemm(Ctx& c, int, int, const void*, int, const EpiArgs&, cudaStream_t) {
-    (void)c;
-    return set_error(SPEC_E_STATE, "tensor-core GEMM not available");
+
+constexpr int TC_THREADS = 192;
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;       // 16 KB
+constexpr int TC_MAX_NTOK = 256;
+constexpr int TC_MAX_STAGES = 8;
+constexpr int TC_CW = 16;                           // epilogue column chunk
+constexpr int TC_XPITCH = TC_CW + 1;
+constexpr int TC_XBYTES = TC_BM * TC_XPITCH * 4;
+constexpr int TC_SMEM_MAX = 226 * 1024;   // dynamic bytes (static barriers stay below the 227 KB cap)
+
+struct TcParams {
+    CUtensorMap wmap[3];
+    CUtensorMap xmap;
+    int gid;
+    int n_tiles, KB;
+    int ntok, M, x_row0;
+    int stages, stage_bytes;
+    int hq, hkv;
+    float* partial;          // [grid][2][128][ntok]
+    int* tile_cnt;           // [n_tiles], zero between launches
+    int* err;
+    EpiArgs e;
+};
+
+// ---- PTX wrappers --------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol) : "memory");
 }
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 1 if any of the 128 epilogue threads passes pred != 0 (and a barrier among them).
+__device__ __forceinline__ int epi_any(int pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(pred) : "memory");
+    return r;
+}
+
+// ---- tile geometry --------------------------------------------------------------------------
+
+__device__ __forceinline__ void tile_rows(const TcParams& p, int tile, const CUtensorMap*& m0, int& r0,
+                                          const CUtensorMap*& m1, int& r1) {
+    if (p.gid == GEMM_QKV) {
+        int t = tile, w = 0;
+        if (t >= p.hq) { t -= p.hq; w = 1; if (t >= p.hkv) { t -= p.hkv; w = 2; } }
+        m0 = m1 = &p.wmap[w];
+        r0 = t * TC_BM;
+        r1 = r0 + 64;
+    } else if (p.gid == GEMM_GU) {
+        m0 = &p.wmap[0];
+        m1 = &p.wmap[1];
+        r0 = r1 = tile * 64;
+    } else {
+        m0 = m1 = &p.wmap[0];
+        r0 = tile * TC_BM;
+        r1 = r0 + 64;
+    }
+}
+
+__device__ __forceinline__ long long range_start(long long T, int G, int c) { return (long long)c * T / G; }
+
+// CTA whose k-block range contains k-block x.
+__device__ __forceinline__ int owner_cta(long long T, int G, long long x) {
+    int c = (int)(((x + 1) * G + T - 1) / T) - 1;
+    while (c > 0 && range_start(T, G, c) > x) --c;
+    while (c + 1 < G && range_start(T, G, c + 1) <= x) ++c;
+    return c;
+}
+
+// Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
+__device__ __forceinline__ void epi_chunk(const TcParams& p, const float* xs, int tile, int c0, int etid) {
+    const int i = etid & 63;
+    const int half = etid >> 6;
+    const bool adjacent = (p.gid == GEMM_O || p.gid == GEMM_DOWN || p.gid == GEMM_LM);
+    const int r0 = adjacent ? 2 * i : i;
+    const int r1 = adjacent ? 2 * i + 1 : i + 64;
+    const int pidx = tile * 64 + i;
+    for (int cc = half; cc < TC_CW; cc += 2) {
+        const int m = c0 + cc;
+        if (m >= p.M) break;
+        epi_pair<__nv_bfloat16>(p.e, m, pidx, xs[r0 * TC_XPITCH + cc], xs[r1 * TC_XPITCH + cc]);
+    }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[TC_MAX_STAGES], empty_bar[TC_MAX_STAGES];
+    __shared__ __align__(8) uint64_t accf[2], acce[2], done_bar;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int last_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    float* xs = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)) + p.stages * p.stage_bytes);
+    const int G = gridDim.x, cta = blockIdx.x;
+    const long long T = (long long)p.n_tiles * p.KB;
+    const long long s0 = range_start(T, G, cta), s1 = range_start(T, G, cta + 1);
+    const int S = p.stages;
+    const uint32_t ncols = (uint32_t)max(32, 1 << (32 - __clz(2 * p.ntok - 1)));
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accf[b]), 1);
+            mbar_init(smem_u32(&acce[b]), 128);
+        }
+        mbar_init(smem_u32(&done_bar), 1);
+        fence_barrier_init();
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&p.wmap[0])) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&tmem_sh)), "r"(ncols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pw = policy_evict_first();
+            const uint64_t px = policy_evict_last();
+            const uint32_t tx = (uint32_t)(TC_A_BYTES + p.ntok * TC_BK * 2);
+            long long i = 0;
+            for (long long g = s0; g < s1; ++g, ++i) {
+                const int tile = (int)(g / p.KB), kb = (int)(g % p.KB);
+                const int s = (int)(i % S);
+                if (!mbar_wait(smem_u32(&empty_bar[s]), (uint32_t)(((i / S) & 1) ^ 1))) {
+                    atomicExch(p.err, SPEC_E_TIMEOUT);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full_bar[s]);
+                mbar_arrive_expect_tx(fb, tx);
+                const uint32_t a_dst = base + (uint32_t)s * p.stage_bytes;
+                const CUtensorMap *m0, *m1;
+                int r0, r1;
+                tile_rows(p, tile, m0, r0, m1, r1);
+                tma_load_2d(a_dst, m0, kb * TC_BK, r0, fb, pw);
+                tma_load_2d(a_dst + TC_A_BYTES / 2, m1, kb * TC_BK, r1, fb, pw);
+                const uint32_t b_dst = a_dst + TC_A_BYTES;
+                for (int t = 0; t < p.ntok / 16; ++t)
+                    tma_load_2d(b_dst + t * 2048, &p.xmap, kb * TC_BK, p.x_row0 + t * 16, fb, px);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(p.ntok);
+            long long i = 0;
+            int si = 0;
+            bool ok = true;
+            long long g = s0;
+            while (ok && g < s1) {
+                const int tile = (int)(g / p.KB);
+                const long long seg_end = min(s1, (long long)(tile + 1) * p.KB);
+                const int buf = si & 1;
+                if (!mbar_wait(smem_u32(&acce[buf]), (uint32_t)(((si >> 1) & 1) ^ 1))) {
+                    atomicExch(p.err, SPEC_E_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * p.ntok);
+                const long long seg_start = g;
+                for (; g < seg_end; ++g, ++i) {
+                    const int s = (int)(i % S);
+                    if (!mbar_wait(smem_u32(&full_bar[s]), (uint32_t)((i / S) & 1))) {
+                        atomicExch(p.err, SPEC_E_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = base + (uint32_t)s * p.stage_bytes;
+                    const uint32_t b_addr = a_addr + TC_A_BYTES;
+                    const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128(b_addr);
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / 16; ++kk)
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                 (g != seg_start || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&empty_bar[s]));
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&accf[buf]));
+                ++si;
+            }
+            // make sure no MMA is still writing tensor memory before it is freed
+            mma_commit(smem_u32(&done_bar));
+            mbar_wait(smem_u32(&done_bar), 0);
+        }
+    } else {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int etid = threadIdx.x - 64;
+        int si = 0;
+        long long g = s0;
+        while (g < s1) {
+            const int tile = (int)(g / p.KB);
+            const long long tile_k0 = (long long)tile * p.KB;
+            const long long seg_end = min(s1, tile_k0 + p.KB);
+            const bool full_tile = (g == tile_k0) && (seg_end == tile_k0 + p.KB);
+            const int buf = si & 1;
+            const bool okw = mbar_wait(smem_u32(&accf[buf]), (uint32_t)((si >> 1) & 1));
+            if (epi_any(okw ? 0 : 1)) {
+                if (etid == 0) atomicExch(p.err, SPEC_E_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.ntok);
+            if (full_tile) {
+                for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    if (c0 + TC_CW >= p.ntok) {
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&acce[buf]));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = v[j];
+                    epi_bar();
+                    epi_chunk(p, xs, tile, c0, etid);
+                    epi_bar();
+                }
+            } else {
+                const int which = (s0 >= tile_k0) ? 0 : 1;
+                float* dst = p.partial + (((size_t)cta * 2 + which) * TC_BM + row) * p.ntok;
+                for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&acce[buf]));
+                const int c_lo = owner_cta(T, G, tile_k0);
+                const int c_hi = owner_cta(T, G, tile_k0 + p.KB - 1);
+                __threadfence();
+                epi_bar();
+                if (etid == 0) {
+                    const int prev = atomicAdd(p.tile_cnt + tile, 1);
+                    last_flag = (prev == c_hi - c_lo) ? 1 : 0;
+                }
+                epi_bar();
+                if (last_flag) {
+                    __threadfence();
+                    for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
+                        float acc[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
+                            const int wc = (range_start(T, G, cc) >= tile_k0) ? 0 : 1;
+                            const float* src = p.partial + (((size_t)cc * 2 + wc) * TC_BM + row) * p.ntok + c0;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4) {
+                                const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src + j));
+                                acc[j] += t4.x; acc[j + 1] += t4.y; acc[j + 2] += t4.z; acc[j + 3] += t4.w;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = acc[j];
+                        epi_bar();
+                        epi_chunk(p, xs, tile, c0, etid);
+                        epi_bar();
+                    }
+                    if (etid == 0) p.tile_cnt[tile] = 0;
+                }
+            }
+            g = seg_end;
+            ++si;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(ncols) : "memory");
+}
+
+// ---- host side ------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct TcLayerMaps {
+    CUtensorMap q, k, v, o, g, u, d;
+};
+
+struct TcGemm {
+    std::vector<TcLayerMaps> layers;
+    CUtensorMap lm;
+    CUtensorMap xn, xo, xh;
+    float* partial = nullptr;
+    int* tile_cnt = nullptr;
+    int* err = nullptr;
+    int grid = 0;
+};
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// bf16 row-major [rows][cols], box = 64 columns (128 B, the swizzle span) x box_rows rows.
+static int make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return set_error(SPEC_E_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(SPEC_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return SPEC_OK;
+}
+
+bool tc_supported(const Ctx& c) {
+    const spec_model_cfg& m = c.cfg;
+    return m.dtype == SPEC_BF16 && m.head_dim == 128 && m.d_model % 128 == 0 && m.vocab % 128 == 0 &&
+           m.ffn_dim % 64 == 0 && (m.n_q_heads * m.head_dim) % 64 == 0 && c.Mmax <= TC_MAX_NTOK && encode_fn();
+}
+
+int tc_create(Ctx& c) {
+    c.use_tc = false;
+    if (!tc_supported(c)) return SPEC_OK;
+    const spec_model_cfg& m = c.cfg;
+    TcGemm* t = new TcGemm();
+    const uint64_t d = m.d_model, qd = (uint64_t)m.n_q_heads * m.head_dim, kvd = (uint64_t)m.n_kv_heads * m.head_dim,
+                   F = m.ffn_dim, V = m.vocab;
+    int rc = SPEC_OK;
+    t->layers.resize(m.n_layers);
+    for (int l = 0; l < m.n_layers && rc == SPEC_OK; ++l) {
+        const LayerWeights& L = c.w.layers[l];
+        TcLayerMaps& M = t->layers[l];
+        if ((rc = make_map(&M.q, L.wq, qd, d, 64)) || (rc = make_map(&M.k, L.wk, kvd, d, 64)) ||
+            (rc = make_map(&M.v, L.wv, kvd, d, 64)) || (rc = make_map(&M.o, L.wo, d, qd, 64)) ||
+            (rc = make_map(&M.g, L.wg, F, d, 64)) || (rc = make_map(&M.u, L.wu, F, d, 64)) ||
+            (rc = make_map(&M.d, L.wd, d, F, 64)))
+            break;
+    }
+    if (rc == SPEC_OK) rc = make_map(&t->lm, c.w.lm_head, V, d, 64);
+    if (rc == SPEC_OK) rc = make_map(&t->xn, c.Xn, c.Mmax, d, 16);
+    if (rc == SPEC_OK) rc = make_map(&t->xo, c.O, c.Mmax, qd, 16);
+    if (rc == SPEC_OK) rc = make_map(&t->xh, c.H, c.Mmax, F, 16);
+    t->grid = c.num_sms;
+    const int max_tiles = (int)std::max<uint64_t>({V / 128, F / 64, d / 128, qd / 128 + 2 * kvd / 128});
+    if (rc == SPEC_OK) {
+        void *a = nullptr, *b = nullptr, *e = nullptr;
+        if (cudaMalloc(&a, sizeof(float) * (size_t)t->grid * 2 * TC_BM * TC_MAX_NTOK) != cudaSuccess ||
+            cudaMalloc(&b, sizeof(int) * (size_t)max_tiles) != cudaSuccess ||
+            cudaMalloc(&e, sizeof(int)) != cudaSuccess) {
+            rc = set_error(SPEC_E_NOMEM, "tensor-core GEMM workspace allocation failed");
+        } else {
+            cudaMemset(b, 0, sizeof(int) * (size_t)max_tiles);
+            cudaMemset(e, 0, sizeof(int));
+        }
+        t->partial = static_cast<float*>(a);
+        t->tile_cnt = static_cast<int*>(b);
+        t->err = static_cast<int*>(e);
+    }
+    if (rc == SPEC_OK &&
+        cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX) != cudaSuccess)
+        rc = set_error(SPEC_E_CUDA, "cudaFuncSetAttribute(tc_gemm_kernel)");
+    if (rc != SPEC_OK) {
+        if (t->partial) cudaFree(t->partial);
+        if (t->tile_cnt) cudaFree(t->tile_cnt);
+        if (t->err) cudaFree(t->err);
+        delete t;
+        return rc;
+    }
+    c.tc = t;
+    c.use_tc = true;
+    return SPEC_OK;
+}
+
+void tc_destroy(Ctx& c) {
+    if (!c.tc) return;
+    cudaFree(c.tc->partial);
+    cudaFree(c.tc->tile_cnt);
+    cudaFree(c.tc->err);
+    delete c.tc;
+    c.tc = nullptr;
+    c.use_tc = false;
+}
+
+int tc_error_word(Ctx& c, int* out) {
+    if (!c.tc) { *out = 0; return SPEC_OK; }
+    return cudaMemcpy(out, c.tc->err, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess ? SPEC_OK : SPEC_E_CUDA;
+}
+
+int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, cudaStream_t st) {
+    TcGemm* t = c.tc;
+    const spec_model_cfg& m = c.cfg;
+    if (M < 1 || M > TC_MAX_NTOK) return set_error(SPEC_E_RANGE, "GEMM with M=%d tokens (max %d)", M, TC_MAX_NTOK);
+    TcParams p{};
+    const int d = m.d_model, qd = m.n_q_heads * m.head_dim, F = m.ffn_dim;
+    int Kdim = d;
+    const CUtensorMap* xm = &t->xn;
+    const uint8_t* xbase = static_cast<const uint8_t*>(c.Xn);
+    switch (gid) {
+    case GEMM_QKV:
+        p.wmap[0] = t->layers[layer].q; p.wmap[1] = t->layers[layer].k; p.wmap[2] = t->layers[layer].v;
+        p.n_tiles = m.n_q_heads + 2 * m.n_kv_heads;
+        break;
+    case GEMM_O:
+        p.wmap[0] = t->layers[layer].o; p.n_tiles = d / TC_BM; Kdim = qd; xm = &t->xo;
+        xbase = static_cast<const uint8_t*>(c.O);
+        break;
+    case GEMM_GU:
+        p.wmap[0] = t->layers[layer].g; p.wmap[1] = t->layers[layer].u; p.n_tiles = F / 64;
+        break;
+    case GEMM_DOWN:
+        p.wmap[0] = t->layers[layer].d; p.n_tiles = d / TC_BM; Kdim = F; xm = &t->xh;
+        xbase = static_cast<const uint8_t*>(c.H);
+        break;
+    default:
+        p.wmap[0] = t->lm; p.n_tiles = m.vocab / TC_BM;
+        break;
+    }
+    const size_t off = static_cast<const uint8_t*>(X) - xbase;
+    p.x_row0 = (int)(off / ((size_t)Kdim * 2));
+    p.xmap = *xm;
+    p.gid = gid;
+    p.KB = Kdim / TC_BK;
+    p.ntok = (M + 15) & ~15;
+    p.M = M;
+    p.stage_bytes = TC_A_BYTES + p.ntok * TC_BK * 2;
+    p.stages = std::min(TC_MAX_STAGES, (TC_SMEM_MAX - 1024 - TC_XBYTES - 256) / p.stage_bytes);
+    p.hq = m.n_q_heads;
+    p.hkv = m.n_kv_heads;
+    p.partial = t->partial;
+    p.tile_cnt = t->tile_cnt;
+    p.err = t->err;
+    p.e = e;
+    const long long T = (long long)p.n_tiles * p.KB;
+    const int grid = (int)std::min<long long>(t->grid, T);
+    const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + TC_XBYTES;
+    tc_gemm_kernel<<<grid, TC_THREADS, smem, st>>>(p);
+    return 1;
+}
+
 }  // namespace sv

@@ -116,6 +116,8 @@ int tc_create(Ctx& c);                       // plans + tensor maps, after weigh
 void tc_destroy(Ctx& c);
 // returns kernels launched, or a negative SPEC_E_* code
 int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, const EpiArgs& e, cudaStream_t st);
+bool tc_supported(const Ctx& c);
+int tc_error_word(Ctx& c, int* out);          // device error word of the tensor-core GEMM (synchronous)
 
 }  // namespace sv
 

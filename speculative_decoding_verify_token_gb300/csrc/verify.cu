@@ -41,7 +41,7 @@ constexpr int LISTN = 32;
 constexpr int VT_TARGET_ITEMS = 4096;
 constexpr int VT_MAX_CHUNKS = 128;
 constexpr int VT_MAX_K = 64;
-constexpr int VT_CAND_CAP = 128;          // per-warp candidate buffer (entries)
+constexpr int VT_CAND_CAP = 256;          // per-warp candidate buffer (entries)
 
 enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
 
@@ -131,13 +131,15 @@ struct ProdState {
     int pos, end;
     bool first;
     const float* ptr;
+    int pref;      // next work item index, fetched one item ahead so the atomic's latency hides
 };
 
 // Lane 0 only: describe the next stage of this warp's stream; false when no work is left.
 __device__ bool next_stage(const VerifyParams& p, ProdState& ps, StageDesc& d) {
     while (ps.item < 0) {
-        const int it = atomicAdd(p.work, 1);
+        const int it = ps.pref;
         if (it >= p.n_items) return false;
+        ps.pref = atomicAdd(p.work, 1);
         const int row = it / p.chunks, c = it % p.chunks;
         const RowInfo ri = row_info(p, row);
         if (!row_needed(p, ri)) continue;
@@ -227,6 +229,38 @@ __device__ __forceinline__ void flush_candidates(float& lv, int& lid, const floa
         warp_merge_desc(lv, lid, v, id, lane);
     }
     __syncwarp();
+}
+
+// Exact path for a stage whose candidates overflowed the buffer (e.g. many equal values):
+// lanes offer one element per round, tested exactly against the running k-th entry.
+__device__ __noinline__ void exact_rounds(const float4 (&x)[VT_STAGE_ELEMS / 128], int start, float lb, float& lv,
+                                          int& lid, float* cv, int* ci, int& ccount, int k, int lane) {
+    for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+        for (int c = 0; c < 4; ++c) {
+            const float thr_v = __shfl_sync(FULL, lv, k - 1);
+            const int thr_id = __shfl_sync(FULL, lid, k - 1);
+            float4 xj = x[0];
+#pragma unroll
+            for (int q = 1; q < VT_STAGE_ELEMS / 128; ++q)
+                if (q == j) xj = x[q];
+            const float xc = pick4(xj, c);
+            const int id = start + 4 * (lane + 32 * j) + c;
+            const bool has = xc >= lb && better(xc, id, thr_v, thr_id);
+            const unsigned bal = __ballot_sync(FULL, has);
+            if (bal == 0) continue;
+            if (ccount + 32 > VT_CAND_CAP) {
+                flush_candidates(lv, lid, cv, ci, ccount, lane);
+                ccount = 0;
+            }
+            if (has) {
+                const int pos = ccount + __popc(bal & ((1u << lane) - 1u));
+                cv[pos] = xc;
+                ci[pos] = id;
+            }
+            ccount += __popc(bal);
+            __syncwarp();
+        }
+    }
 }
 
 // Truncated distribution of a merged row list (lane j = j-th best), written to rd_*.
@@ -424,6 +458,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
     __shared__ StageDesc descs[VT_WARPS][VT_STAGES];
     __shared__ float cand_v[VT_WARPS][VT_CAND_CAP];
     __shared__ int cand_id[VT_WARPS][VT_CAND_CAP];
+    __shared__ int ccnt_s[VT_WARPS];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -437,13 +472,15 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
 #pragma unroll
         for (int s = 0; s < VT_STAGES; ++s) mbar_init(bar_u32[s], 1);
         fence_barrier_init();
+        ccnt_s[warp] = 0;
     }
     __syncwarp();
 
     const int k = p.top_k;
     const uint64_t pol = policy_evict_first();
     ProdState ps;
-    ps.item = -1; ps.pos = ps.end = 0; ps.first = false; ps.ptr = nullptr;
+    ps.item = -1; ps.pos = ps.end = 0; ps.first = false; ps.ptr = nullptr; ps.pref = 0;
+    if (lane == 0) ps.pref = atomicAdd(p.work, 1);
 
     int inflight = 0;
     if (lane == 0) {
@@ -478,17 +515,49 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
         }
         phase ^= 1u << slot;
         const StageDesc d = descs[warp][slot];
-        const float4* buf = reinterpret_cast<const float4*>(ring + slot * VT_STAGE_ELEMS);
-        const int n4 = d.count >> 2;
-
         const int row_now = d.item / p.chunks;
         unsigned* rb_ptr = p.row_bound + row_now;
+        const unsigned rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
+        // Copy the stage to registers, then hand the buffer straight back to the TMA engine.
+        float4 x[VT_STAGE_ELEMS / 128];
+        const int n4 = d.count >> 2;
+        {
+            const float4* buf = reinterpret_cast<const float4*>(ring + slot * VT_STAGE_ELEMS);
+            if (n4 == VT_STAGE_ELEMS / 4) {
+#pragma unroll
+                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) x[j] = buf[lane + 32 * j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+                    const int idx = lane + 32 * j;
+                    x[j] = idx < n4 ? buf[idx] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+            }
+        }
+        __syncwarp();
+        int more = 0;
+        if (lane == 0) {
+            StageDesc nd;
+            if (next_stage(p, ps, nd)) {
+                descs[warp][slot] = nd;
+                issue_stage(ps, nd, ring_u32 + slot * VT_STAGE_BYTES, bar_u32[slot], pol);
+                more = 1;
+            }
+        }
+        more = __shfl_sync(FULL, more, 0);
+
+        // Lane maximum (4 independent chains; padding is -inf, NaN is ignored).
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+            m0 = fmaxf(m0, x[j].x); m1 = fmaxf(m1, x[j].y); m2 = fmaxf(m2, x[j].z); m3 = fmaxf(m3, x[j].w);
+        }
+        const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
         if (d.flags & 1) {
             // New item: reset the list; lower bound = k-th largest lane maximum of this stage
             // (k distinct elements reach it, so the chunk's -- and the row's -- k-th best does).
             lv = -INFINITY; lid = SENT_ID;
-            published = -INFINITY;
-            float m = stage_lane_max(buf, n4, lane);
+            float m = mx;
             int dummy = lane;
             warp_sort_desc(m, dummy, lane);
             lb = __shfl_sync(FULL, m, k - 1);
@@ -497,54 +566,46 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
         }
         // Row-wide bound published by the other chunks of the row (any chunk's k-th best is
         // a lower bound of the row's k-th best, so filtering by it is exact).
-        lb = fmaxf(lb, key_float(*reinterpret_cast<volatile unsigned*>(rb_ptr)));
+        lb = fmaxf(lb, key_float(rb_key));
         float thr_v = __shfl_sync(FULL, lv, k - 1);
         int thr_id = __shfl_sync(FULL, lid, k - 1);
-        const float cut = fmaxf(lb, thr_v);
-        // Pass 1: the lane's maximum over its 64 values (4 independent chains).
-        const float mx = stage_lane_max(buf, n4, lane);
+        float cut = fmaxf(lb, thr_v);
         if (__any_sync(FULL, mx >= cut)) {
-            // Pass 2 (rare): exact (value, id) test of the lanes whose maximum reached the cut.
-            unsigned long long pend = 0;
+            // Candidates: values reaching the cut (a value test only; an entry equal to the
+            // k-th value with a larger id is a harmless extra for the exact merge).  Lanes
+            // append with a shared-memory atomic; an overflow falls back to exact rounds.
+            const int pre = ccount;
             if (mx >= cut) {
-#pragma unroll 4
-                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
-                    const int idx = lane + 32 * j;
-                    if (idx < n4) {
-                        const float4 x = buf[idx];
-                        const int id0 = d.start + 4 * idx;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float xc = pick4(x, c);
-                            if (xc >= lb && better(xc, id0 + c, thr_v, thr_id)) pend |= 1ull << (4 * j + c);
+                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float xc = pick4(x[j], c);
+                        if (xc >= cut) {
+                            const int pos = atomicAdd(&ccnt_s[warp], 1);
+                            if (pos < VT_CAND_CAP) {
+                                cbuf_v[pos] = xc;
+                                cbuf_id[pos] = d.start + 4 * (lane + 32 * j) + c;
+                            }
                         }
                     }
                 }
             }
-            // Compact candidates into the warp's buffer, one per lane per round.
-            const float* sb = ring + slot * VT_STAGE_ELEMS;
-            while (true) {
-                const bool has = pend != 0;
-                const unsigned bal = __ballot_sync(FULL, has);
-                if (bal == 0) break;
-                if (has) {
-                    const int bit = __ffsll(pend) - 1;
-                    pend &= pend - 1;
-                    const int e = 4 * (lane + 32 * (bit >> 2)) + (bit & 3);
-                    const int pos = ccount + __popc(bal & ((1u << lane) - 1u));
-                    cbuf_v[pos] = sb[e];
-                    cbuf_id[pos] = d.start + e;
-                }
-                ccount += __popc(bal);
-                if (ccount > VT_CAND_CAP - 32) {
-                    flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
-                    ccount = 0;
-                }
+            __syncwarp();
+            ccount = *reinterpret_cast<volatile int*>(&ccnt_s[warp]);
+            if (ccount > VT_CAND_CAP) {
+                ccount = pre;
+                exact_rounds(x, d.start, lb, lv, lid, cbuf_v, cbuf_id, ccount, k, lane);
             }
+            __syncwarp();
+            if (lane == 0) ccnt_s[warp] = ccount;
+            __syncwarp();
         }
-        if (ccount >= 16 || (ccount > 0 && __shfl_sync(FULL, lid, k - 1) == SENT_ID)) {
+        if (ccount >= 32 || (ccount > 0 && __shfl_sync(FULL, lid, k - 1) == SENT_ID)) {
             flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
             ccount = 0;
+            if (lane == 0) ccnt_s[warp] = 0;
+            __syncwarp();
         }
         {
             const float kth = __shfl_sync(FULL, lv, k - 1);
@@ -565,6 +626,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
             if (ccount > 0) {
                 flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
                 ccount = 0;
+                if (lane == 0) ccnt_s[warp] = 0;
+                __syncwarp();
             }
             if (c == 0 && head > 0) {
                 const bool has = lane < head;
@@ -588,17 +651,6 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
             }
         }
 
-        __syncwarp();
-        int more = 0;
-        if (lane == 0) {
-            StageDesc nd;
-            if (next_stage(p, ps, nd)) {
-                descs[warp][slot] = nd;
-                issue_stage(ps, nd, ring_u32 + slot * VT_STAGE_BYTES, bar_u32[slot], pol);
-                more = 1;
-            }
-        }
-        more = __shfl_sync(FULL, more, 0);
         inflight += more - 1;
         slot = (slot + 1 == VT_STAGES) ? 0 : slot + 1;
         __syncwarp();

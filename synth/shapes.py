@@ -45,6 +45,7 @@ class ModelShape:
 
 TINY_TARGET = ModelShape("tiny-target", 2, 256, 4, 2, 64, 768, 1024, dtype="f32")
 TINY_DRAFT = ModelShape("tiny-draft", 1, 128, 2, 1, 64, 384, 1024, dtype="f32")
+SMALL_BF16 = ModelShape("small-bf16", 2, 512, 4, 2, 128, 1536, 4096)
 QWEN_8B = ModelShape("dense-8b", 36, 4096, 32, 8, 128, 12288, 151936)
 QWEN_27B = ModelShape("dense-27b", 64, 5120, 40, 8, 128, 17408, 151936)
 DRAFT_0P8B = ModelShape("draft-0.8b", 28, 1024, 16, 8, 128, 3072, 151936)
