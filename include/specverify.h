@@ -210,6 +210,19 @@ int spec_seq_len(spec_ctx* ctx, int seq_id, int32_t* out_len);
 /* Empty a slot and return its pages to the pool. */
 int spec_seq_reset(spec_ctx* ctx, int seq_id);
 
+/* Per-kernel-class timing of the context's passes with CUDA events recorded on its
+ * stream around each launch (off by default; meant for a measurement pass).  Classes:
+ * 0 QKV GEMM, 1 O GEMM, 2 gate/up GEMM, 3 down GEMM, 4 lm_head GEMM, 5 attention,
+ * 6 fused verify, 7 other small kernels. */
+#define SPEC_PROF_CLASSES 8
+int spec_profile(spec_ctx* ctx, int enable);
+
+/* Synchronise the context stream and return, per class, the summed event time (ms), the
+ * number of launches and the algorithmic bytes those launches move (weights for the
+ * GEMMs, KV pages read + written for attention, logits for the verify), accumulated since
+ * the previous read; then reset.  Arrays of SPEC_PROF_CLASSES entries (host). */
+int spec_profile_read(spec_ctx* ctx, double* ms, long long* launches, double* bytes);
+
 /* Number of kernels the context launched since creation (for launch accounting). */
 long long spec_kernel_launches(const spec_ctx* ctx);
 

@@ -107,7 +107,8 @@ class Decoder:
 
             def get(name, _w=weights, _c=cache):
                 if name not in _c:
-                    _c[name] = to_f64(_w[name])
+                    v = _w[name]
+                    _c[name] = v if hasattr(v, "__getitem__") and not hasattr(v, "shape") else to_f64(v)
                 return _c[name]
             self.w = get
         else:

@@ -50,6 +50,9 @@ class SpecCtxLimits(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("prefill_chunk", ctypes.c_int32)]
 
 
+SPEC_PROF_CLASSES = 8
+PROF_CLASS_NAMES = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head", "attention",
+                    "verify", "other"]
 SPEC_F32 = 0
 SPEC_BF16 = 1
 
@@ -76,6 +79,9 @@ SIGNATURES = {
     "spec_seq_len": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32)]),
     "spec_seq_reset": (c_int, [c_vp, c_int]),
     "spec_kernel_launches": (ctypes.c_longlong, [c_vp]),
+    "spec_profile": (c_int, [c_vp, c_int]),
+    "spec_profile_read": (c_int, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong),
+                                  ctypes.POINTER(ctypes.c_double)]),
     "spec_destroy": (None, [c_vp]),
 }
 

@@ -92,6 +92,11 @@ struct Ctx {
     void* vws = nullptr;
     size_t vws_bytes = 0;
     int* d_status_scratch = nullptr;
+    // profiling (events around each launch of a class)
+    bool prof_on = false;
+    struct ProfRec { int cls; cudaEvent_t a, b; double bytes; };
+    std::vector<ProfRec> prof_recs;
+    std::vector<cudaEvent_t> prof_pool;
     // tensor-core GEMM
     TcGemm* tc = nullptr;
     bool use_tc = false;

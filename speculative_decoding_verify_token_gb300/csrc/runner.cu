@@ -47,6 +47,10 @@ static int dalloc(Ctx& c, P** p, size_t bytes, bool zero = false) {
 
 static void free_all(Ctx& c) {
     tc_destroy(c);
+    for (auto& r : c.prof_recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+    for (auto e : c.prof_pool) cudaEventDestroy(e);
+    c.prof_recs.clear();
+    c.prof_pool.clear();
     for (int i = 0; i < SLOT_RING; ++i)
         if (c.ring_ev[i]) cudaEventDestroy(c.ring_ev[i]);
     for (void* p : c.allocs) cudaFree(p);
@@ -153,12 +157,58 @@ static int upload_slots(Ctx& c, const int* slots, int B) {
 
 // ---- the decoder pass ---------------------------------------------------------------------
 
+static cudaEvent_t prof_event(Ctx& c) {
+    if (!c.prof_pool.empty()) {
+        cudaEvent_t e = c.prof_pool.back();
+        c.prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Scoped timing of one launch (or a group of launches) of class `cls`.
+struct ProfScope {
+    Ctx& c;
+    int cls;
+    double bytes;
+    cudaEvent_t a = nullptr;
+    ProfScope(Ctx& c_, int cls_, double bytes_) : c(c_), cls(cls_), bytes(bytes_) {
+        if (c.prof_on) {
+            a = prof_event(c);
+            cudaEventRecord(a, c.stream);
+        }
+    }
+    ~ProfScope() {
+        if (a) {
+            cudaEvent_t b = prof_event(c);
+            cudaEventRecord(b, c.stream);
+            c.prof_recs.push_back({cls, a, b, bytes});
+        }
+    }
+};
+
+static double gemm_weight_bytes(const Ctx& c, int gid) {
+    const spec_model_cfg& m = c.cfg;
+    const double d = m.d_model, qd = (double)m.n_q_heads * m.head_dim, kvd = (double)m.n_kv_heads * m.head_dim;
+    const double F = m.ffn_dim, V = m.vocab, es = c.esize;
+    switch (gid) {
+    case GEMM_QKV: return (qd + 2 * kvd) * d * es;
+    case GEMM_O: return d * qd * es;
+    case GEMM_GU: return 2 * F * d * es;
+    case GEMM_DOWN: return d * F * es;
+    default: return V * d * es;
+    }
+}
+
 static inline void* layer_pool(const Ctx& c, void* pool, int l) {
     return static_cast<uint8_t*>(pool) + (size_t)l * c.layer_pool_elems * c.esize;
 }
 
 static int gemm(Ctx& c, int gid, int layer, const void* wa, const void* wb, const void* wc, int K, int n_pairs,
                 const void* X, const EpiArgs& e) {
+    ProfScope ps(c, gid, gemm_weight_bytes(c, gid));
     if (c.use_tc) {
         const int n = tc_gemm(c, gid, layer, X, e.M, e, c.stream);
         if (n < 0) return n;
@@ -180,7 +230,11 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     launch_embed(c, M, T, st);
     c.launches += 1;
     int max_after = 0;
-    for (int b = 0; b < B; ++b) max_after = std::max(max_after, c.len_hi[slots[b]] + T);
+    double kv_bytes = 0.0;    // keys + values read per layer (upper bound of the lengths) + written
+    for (int b = 0; b < B; ++b) {
+        max_after = std::max(max_after, c.len_hi[slots[b]] + T);
+        kv_bytes += (double)(c.len_hi[slots[b]] + 2 * T) * 2.0 * hkv * hd * c.esize;
+    }
 
     EpiArgs eq{};
     eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
@@ -204,7 +258,10 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         if ((rc = gemm(c, GEMM_QKV, l, L.wq, L.wk, L.wv, d, (hq + 2 * hkv) * hd / 2, c.Xn, eq)) != SPEC_OK) return rc;
         aa.k_layer = eq.k_layer;
         aa.v_layer = eq.v_layer;
-        c.launches += launch_attention(c, aa, B, max_after, st);
+        {
+            ProfScope ps(c, 5, kv_bytes);
+            c.launches += launch_attention(c, aa, B, max_after, st);
+        }
         if ((rc = gemm(c, GEMM_O, l, L.wo, nullptr, nullptr, hq * hd, d / 2, c.O, er)) != SPEC_OK) return rc;
         launch_rmsnorm(c, c.X, L.ffn_norm, c.Xn, M, st);
         c.launches += 1;
@@ -415,8 +472,12 @@ extern "C" int spec_verify(spec_ctx* c, int B, const int32_t* seq_ids, int K, co
     c->launches += 1;
     float* logits = out_logits ? out_logits : c->logits;
     if ((rc = forward(*c, seq_ids, B, K + 1, logits, false)) != SPEC_OK) return rc;
+    {
+    ProfScope psv(*c, 6, (double)B * (K + 1) * c->cfg.vocab * 4.0 +
+                             (draft_logits && sampling->temperature > 0 ? (double)B * K * c->cfg.vocab * 4.0 : 0.0));
     rc = verify_into(B, K, c->cfg.vocab, logits, draft_logits, draft_tokens, draft_len, uniforms, sampling,
                      accepted_len, next_token, out_ids, out_probs, seq_status, c->vws, c->vws_bytes, c->stream);
+    }
     if (rc != SPEC_OK) return rc;
     c->launches += 1;
     if (auto_trim) launch_advance_len(c->d_seq_ids, c->d_seq_len, B, 1, 0, accepted_len, K, c->stream);
@@ -475,6 +536,32 @@ extern "C" int spec_seq_reset(spec_ctx* c, int seq_id) {
 }
 
 extern "C" long long spec_kernel_launches(const spec_ctx* c) { return c ? c->launches : 0; }
+
+extern "C" int spec_profile(spec_ctx* c, int enable) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    c->prof_on = enable != 0;
+    return SPEC_OK;
+}
+
+extern "C" int spec_profile_read(spec_ctx* c, double* ms, long long* launches, double* bytes) {
+    clear_error();
+    if (!c || !ms || !launches || !bytes) return set_error(SPEC_E_INVAL, "NULL argument");
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    for (int i = 0; i < SPEC_PROF_CLASSES; ++i) { ms[i] = 0.0; launches[i] = 0; bytes[i] = 0.0; }
+    for (const auto& r : c->prof_recs) {
+        float t = 0.0f;
+        cudaEventElapsedTime(&t, r.a, r.b);
+        ms[r.cls] += t;
+        launches[r.cls] += 1;
+        bytes[r.cls] += r.bytes;
+        c->prof_pool.push_back(r.a);
+        c->prof_pool.push_back(r.b);
+    }
+    c->prof_recs.clear();
+    return SPEC_OK;
+}
 
 extern "C" void spec_destroy(spec_ctx* c) {
     if (!c) return;

@@ -121,3 +121,15 @@ class SpecModel:
 
     def launches(self):
         return int(self.lib.spec_kernel_launches(self.h))
+
+    def profile(self, enable=True):
+        _lib.check(self.lib.spec_profile(self.h, 1 if enable else 0))
+
+    def profile_read(self):
+        n = _lib.SPEC_PROF_CLASSES
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_longlong * n)()
+        by = (ctypes.c_double * n)()
+        _lib.check(self.lib.spec_profile_read(self.h, ms, cnt, by))
+        return {name: {"ms": ms[i], "launches": cnt[i], "bytes": by[i]}
+                for i, name in enumerate(_lib.PROF_CLASS_NAMES)}
