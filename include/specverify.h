@@ -158,7 +158,7 @@ typedef struct spec_ctx spec_ctx;
 
 /* Create a context bound to `stream` (cudaStream_t as void*): allocates the KV pool,
  * activations and workspaces on the current device.  SPEC_E_INVAL on a bad shape
- * (head_dim must be even and <= 256, d_model / ffn_dim / heads*head_dim multiples of 8,
+ * (head_dim a multiple of 32 and <= 256, d_model / ffn_dim / heads*head_dim multiples of 8,
  * n_q_heads a multiple of n_kv_heads), SPEC_E_NOMEM when an allocation fails. */
 int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* limits, void* stream, spec_ctx** out);
 
@@ -209,6 +209,14 @@ int spec_seq_len(spec_ctx* ctx, int seq_id, int32_t* out_len);
 
 /* Empty a slot and return its pages to the pool. */
 int spec_seq_reset(spec_ctx* ctx, int seq_id);
+
+/* Execution options (both on by default): SPEC_OPT_GRAPHS replays the decoder pass of a
+ * (B, K) shape from a CUDA graph captured on first use; SPEC_OPT_PDL lets each GEMM start
+ * (barrier set-up, first weight tiles) while the previous kernel finishes.  Neither
+ * changes any result bit. */
+#define SPEC_OPT_GRAPHS 1
+#define SPEC_OPT_PDL    2
+int spec_set_option(spec_ctx* ctx, int option, int value);
 
 /* Per-kernel-class timing of the context's passes with CUDA events recorded on its
  * stream around each launch (off by default; meant for a measurement pass).  Classes:

@@ -50,6 +50,8 @@ class SpecCtxLimits(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("prefill_chunk", ctypes.c_int32)]
 
 
+SPEC_OPT_GRAPHS = 1
+SPEC_OPT_PDL = 2
 SPEC_PROF_CLASSES = 8
 PROF_CLASS_NAMES = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head", "attention",
                     "verify", "other"]
@@ -80,6 +82,7 @@ SIGNATURES = {
     "spec_seq_reset": (c_int, [c_vp, c_int]),
     "spec_kernel_launches": (ctypes.c_longlong, [c_vp]),
     "spec_profile": (c_int, [c_vp, c_int]),
+    "spec_set_option": (c_int, [c_vp, c_int, c_int]),
     "spec_profile_read": (c_int, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong),
                                   ctypes.POINTER(ctypes.c_double)]),
     "spec_destroy": (None, [c_vp]),

@@ -1,157 +1,236 @@
 // Paged causal GQA attention of a decoder pass over T new tokens per sequence.
 //
 // For each (sequence, kv head) the T*G query rows (T positions x G = hq/hkv query heads)
-// share one pass over the sequence's KV pages.  The keys are split into chunks of 64
-// absolute positions; chunk c of a row holds partial (max, sum, unnormalised output) over
-// the keys in [64c, 64c + 64) that the row may see (key position <= row position).  The
-// combine walks a row's chunks 0..pos/64 in order.  Every row is computed on its own with
-// a fixed order of operations, so a token gets the same bits whether it is decoded alone
-// (T = 1) or verified together with K drafts (T = K + 1).
+// share one pass over the sequence's KV pages.  The keys are split at fixed absolute
+// positions (SPLIT keys, a multiple of the 16-token page); one CTA per (split, kv head,
+// sequence) loads all pages of its split with 1-D bulk copies on the TMA engine (each
+// page-head block is a contiguous 16 x head_dim run) and computes, per visible row, the
+// split's max, sum and unnormalised output.  The last CTA of a (sequence, kv head) to
+// finish (atomic arrival count, no spin-wait) combines a row's splits 0..pos/SPLIT in
+// order.  Every row is computed on its own in a fixed order of operations that depends
+// only on its absolute position, so a token gets the same bits whether it is decoded
+// alone (T = 1) or verified together with K drafts (T = K + 1).
 #include <cuda_bf16.h>
 #include <cmath>
 
+#include "common.cuh"
 #include "epilogue.cuh"
 #include "model.h"
 
 namespace sv {
 
-constexpr int ATT_RT = 32;
+constexpr int ATT_THREADS = 256;
+constexpr int ATT_RT = 32;                     // query rows per tile
+constexpr int ATT_KV_SMEM = 128 * 1024;        // K + V bytes of one split
+
+int attention_split_keys(int hd, int esize) {
+    int s = ATT_KV_SMEM / (2 * hd * esize);
+    s = (s / 16) * 16;
+    return s > 256 ? 256 : s;
+}
 
 template <typename T>
-__global__ void __launch_bounds__(256) attn_partial_kernel(const AttnArgs a) {
-    extern __shared__ float sm[];
-    const int hd = a.hd, hdp = hd + 1;
-    float* Ks = sm;                                   // [64][hd+1]
-    float* Vs = Ks + ATT_CHUNK * hdp;                 // [64][hd]
-    float* Qs = Vs + ATT_CHUNK * hd;                  // [RT][hd+1]
-    float* Ss = Qs + ATT_RT * hdp;                    // [RT][65]
+struct Vec16;   // 16 bytes of T as floats
+template <>
+struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* v) {
+        const uint4 x = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+template <>
+struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void load(const float* p, float* v) {
+        const float4 x = *reinterpret_cast<const float4*>(p);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    }
+};
 
-    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+template <typename T>
+__global__ void __launch_bounds__(ATT_THREADS, 1) attn_split_kernel(const AttnArgs a) {
+    extern __shared__ __align__(128) uint8_t sm_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int last_flag;
+    const int hd = a.hd, split = a.split_keys;
+    T* Ks = reinterpret_cast<T*>(sm_raw);                               // [split][hd]
+    T* Vs = Ks + (size_t)split * hd;                                    // [split][hd]
+    float* Qs = reinterpret_cast<float*>(Vs + (size_t)split * hd);      // [RT][hd]
+    float* Ss = Qs + (size_t)ATT_RT * hd;                               // [RT][split]
+
+    pdl_launch_dependents();
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int slot = a.seq_ids[b];
     const int L0 = a.seq_len[slot];
     const int Ltot = L0 + a.T;
-    const int k0 = c * ATT_CHUNK;
+    const int k0 = s * split;
     if (k0 >= Ltot) return;
-    const int nk = min(ATT_CHUNK, Ltot - k0);
+    const int nk = min(split, Ltot - k0);
     const int G = a.hq / a.hkv;
     const int R = a.T * G;
-    const T* kp = static_cast<const T*>(a.k_layer);
-    const T* vp = static_cast<const T*>(a.v_layer);
-    for (int i = threadIdx.x; i < nk * hd; i += blockDim.x) {
-        const int key = i / hd, dd = i - key * hd;
-        const int pos = k0 + key;
-        const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
-        const size_t off = (((size_t)page * a.hkv + g) * 16 + (pos & 15)) * hd + dd;
-        Ks[key * hdp + dd] = to_f32<T>(kp[off]);
-        Vs[key * hd + dd] = to_f32<T>(vp[off]);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar_u = smem_u32(&bar);
+
+    // ---- load the split's K and V pages (bulk copies, one mbarrier phase) ----
+    const int npages = (nk + 15) >> 4;
+    const uint32_t page_bytes = (uint32_t)(16 * hd * sizeof(T));
+    if (threadIdx.x == 0) {
+        mbar_init(bar_u, 1);
+        fence_barrier_init();
+        mbar_arrive_expect_tx(bar_u, 2u * page_bytes * (uint32_t)npages);
+        const uint64_t pol = policy_evict_first();
+        const T* kp = static_cast<const T*>(a.k_layer);
+        const T* vp = static_cast<const T*>(a.v_layer);
+        for (int pg = 0; pg < npages; ++pg) {
+            const int page = a.block_table[(size_t)slot * a.max_pages + ((k0 >> 4) + pg)];
+            const size_t off = ((size_t)page * a.hkv + g) * 16 * hd;
+            bulk_g2s(smem_u32(Ks + (size_t)pg * 16 * hd), kp + off, page_bytes, bar_u, pol);
+            bulk_g2s(smem_u32(Vs + (size_t)pg * 16 * hd), vp + off, page_bytes, bar_u, pol);
+        }
     }
     const int t_first = max(0, k0 - L0);
     const T* Q = static_cast<const T*>(a.q);
-    const size_t cbase = (((size_t)b * a.hkv + g) * a.n_chunks + c) * R;
+    const size_t pbase = (((size_t)b * a.hkv + g) * a.n_chunks + s) * R;
+    const int chunks16 = hd * (int)sizeof(T) / 16;          // 16-byte chunks per K row
+    constexpr int VN = Vec16<T>::N;
+    const int dpl = hd / 32;                                 // output dims per lane
+    __syncthreads();
+    bool ok = true;
     for (int rt = t_first * G; rt < R; rt += ATT_RT) {
         const int nr = min(ATT_RT, R - rt);
         __syncthreads();
-        for (int i = threadIdx.x; i < nr * hd; i += blockDim.x) {
+        for (int i = threadIdx.x; i < nr * hd; i += ATT_THREADS) {
             const int ri = i / hd, dd = i - ri * hd;
             const int r = rt + ri, t = r / G, hh = r - t * G;
             const size_t m = (size_t)b * a.T + t;
-            Qs[ri * hdp + dd] = to_f32<T>(Q[(m * a.hq + (size_t)g * G + hh) * hd + dd]);
+            Qs[ri * hd + dd] = to_f32<T>(Q[(m * a.hq + (size_t)g * G + hh) * hd + dd]);
         }
+        if (rt == t_first * G) ok = mbar_wait(bar_u, 0);     // the pages must have landed
         __syncthreads();
-        for (int i = threadIdx.x; i < nr * ATT_CHUNK; i += blockDim.x) {
-            const int ri = i / ATT_CHUNK, key = i - ri * ATT_CHUNK;
-            const int pos = L0 + (rt + ri) / G;
-            float s = -INFINITY;
-            if (key < nk && k0 + key <= pos) {
-                const float* q = Qs + ri * hdp;
-                const float* kk = Ks + key * hdp;
-                float acc = 0.0f;
-                for (int dd = 0; dd < hd; ++dd) acc = fmaf(q[dd], kk[dd], acc);
-                s = acc * a.scale;
-            }
-            Ss[ri * (ATT_CHUNK + 1) + key] = s;
-        }
-        __syncthreads();
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int ri = warp; ri < nr; ri += blockDim.x >> 5) {
-            float* srow = Ss + ri * (ATT_CHUNK + 1);
-            const float s0 = srow[lane], s1 = srow[lane + 32];
-            float mx = fmaxf(s0, s1);
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, o));
-            const float p0 = s0 == -INFINITY ? 0.0f : expf(s0 - mx);
-            const float p1 = s1 == -INFINITY ? 0.0f : expf(s1 - mx);
-            srow[lane] = p0;
-            srow[lane + 32] = p1;
-            float l = p0 + p1;
-            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(FULL_MASK, l, o);
-            if (lane == 0) a.part_ml[cbase + rt + ri] = make_float2(mx, l);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nr * hd; i += blockDim.x) {
-            const int ri = i / hd, dd = i - ri * hd;
+        if (!__syncthreads_and(ok)) break;
+        // scores: warp per row, lane per key (keys lane + 32 i); each lane walks the
+        // 16-byte chunks of its key row in a rotated order (conflict-free banks).
+        for (int ri = warp; ri < nr; ri += ATT_THREADS / 32) {
             const int pos = L0 + (rt + ri) / G;
             const int lim = min(nk, pos - k0 + 1);
-            const float* prow = Ss + ri * (ATT_CHUNK + 1);
-            float acc = 0.0f;
-            for (int key = 0; key < lim; ++key) acc = fmaf(prow[key], Vs[key * hd + dd], acc);
-            a.part_o[(cbase + rt + ri) * hd + dd] = acc;
+            const float* q = Qs + ri * hd;
+            float* srow = Ss + (size_t)ri * split;
+            for (int j = lane; j < split; j += 32) {
+                float acc = -INFINITY;
+                if (j < lim) {
+                    acc = 0.0f;
+                    const T* krow = Ks + (size_t)j * hd;
+                    for (int c = 0; c < chunks16; ++c) {
+                        const int cc = (c + lane) % chunks16;
+                        float kv[VN];
+                        Vec16<T>::load(krow + cc * VN, kv);
+#pragma unroll
+                        for (int e = 0; e < VN; ++e) acc = fmaf(q[cc * VN + e], kv[e], acc);
+                    }
+                    acc *= a.scale;
+                }
+                srow[j] = acc;
+            }
+            __syncwarp();
+            float mx = -INFINITY;
+            for (int j = lane; j < lim; j += 32) mx = fmaxf(mx, srow[j]);
+            mx = warp_max(mx);
+            float l = 0.0f;
+            for (int j = lane; j < lim; j += 32) {
+                const float p = expf(srow[j] - mx);
+                srow[j] = p;
+                l += p;
+            }
+            l = warp_sum(l);
+            __syncwarp();
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = 0.0f;
+            for (int j = 0; j < lim; ++j) {
+                const float p = srow[j];
+                const T* vrow = Vs + (size_t)j * hd + lane * dpl;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e < dpl) o[e] = fmaf(p, to_f32<T>(vrow[e]), o[e]);
+            }
+            float* dst = a.part_o + (pbase + rt + ri) * hd + lane * dpl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (e < dpl) dst[e] = o[e];
+            if (lane == 0) a.part_ml[pbase + rt + ri] = make_float2(mx, l);
         }
     }
-}
-
-template <typename T>
-__global__ void attn_combine_kernel(const AttnArgs a) {
-    const int r = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int G = a.hq / a.hkv;
-    const int R = a.T * G;
-    if (r >= R) return;
-    const int slot = a.seq_ids[b];
-    const int t = r / G, hh = r - t * G;
-    const int pos = a.seq_len[slot] + t;
-    const int nc = pos / ATT_CHUNK + 1;
-    const size_t base = ((size_t)b * a.hkv + g) * a.n_chunks;
-    float mt = -INFINITY;
-    for (int c = 0; c < nc; ++c) mt = fmaxf(mt, a.part_ml[(base + c) * R + r].x);
+    if (!ok) {
+        // The copy never completed: give it one more bounded wait, leave the outputs of this
+        // head unwritten and return.
+        mbar_wait(bar_u, 0);
+        return;
+    }
+    // ---- arrival; the last split of this (sequence, kv head) combines ----
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int nsplit = (Ltot + split - 1) / split;
+        const int prev = atomicAdd(a.att_cnt + b * a.hkv + g, 1);
+        last_flag = prev == nsplit - 1;
+        if (last_flag) a.att_cnt[b * a.hkv + g] = 0;
+    }
+    __syncthreads();
+    if (!last_flag) return;
+    __threadfence();
+    const size_t cbase = ((size_t)b * a.hkv + g) * a.n_chunks;
     T* O = static_cast<T*>(a.o);
-    const size_t m = (size_t)b * a.T + t;
-    for (int dd = threadIdx.x; dd < a.hd; dd += blockDim.x) {
-        float o = 0.0f, l = 0.0f;
-        for (int c = 0; c < nc; ++c) {
-            const float2 ml = a.part_ml[(base + c) * R + r];
+    for (int r = warp; r < R; r += ATT_THREADS / 32) {
+        const int t = r / G, hh = r - t * G;
+        const int pos = L0 + t;
+        const int ns = pos / split + 1;
+        float mt = -INFINITY;
+        for (int c = 0; c < ns; ++c) mt = fmaxf(mt, __ldcg(&a.part_ml[(cbase + c) * R + r].x));
+        float o[8], l = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = 0.0f;
+        for (int c = 0; c < ns; ++c) {
+            const float2 ml = __ldcg(&a.part_ml[(cbase + c) * R + r]);
             const float w = expf(ml.x - mt);
-            o = fmaf(w, a.part_o[((base + c) * R + r) * a.hd + dd], o);
+            const float* src = a.part_o + ((cbase + c) * R + r) * hd + lane * dpl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (e < dpl) o[e] = fmaf(w, __ldcg(src + e), o[e]);
             l = fmaf(w, ml.y, l);
         }
-        O[(m * a.hq + (size_t)g * G + hh) * a.hd + dd] = from_f32<T>(o / l);
+        const size_t m = (size_t)b * a.T + t;
+        T* dst = O + (m * a.hq + (size_t)g * G + hh) * hd + lane * dpl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e < dpl) dst[e] = from_f32<T>(o[e] / l);
     }
 }
 
-size_t attn_partial_smem(int hd) {
-    return sizeof(float) * ((size_t)ATT_CHUNK * (hd + 1) + (size_t)ATT_CHUNK * hd + (size_t)ATT_RT * (hd + 1) +
-                            (size_t)ATT_RT * (ATT_CHUNK + 1));
+size_t attn_smem(int hd, int esize) {
+    const int split = attention_split_keys(hd, esize);
+    return (size_t)2 * split * hd * esize + sizeof(float) * ((size_t)ATT_RT * hd + (size_t)ATT_RT * split);
 }
 
 int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, cudaStream_t st) {
-    const int chunks = (max_len_after + ATT_CHUNK - 1) / ATT_CHUNK;
-    const size_t smem = attn_partial_smem(a.hd);
-    const dim3 g1(chunks, a.hkv, B);
-    const dim3 g2(a.T * (a.hq / a.hkv), a.hkv, B);
-    if (c.cfg.dtype == SPEC_BF16) {
-        attn_partial_kernel<__nv_bfloat16><<<g1, 256, smem, st>>>(a);
-        attn_combine_kernel<__nv_bfloat16><<<g2, 128, 0, st>>>(a);
-    } else {
-        attn_partial_kernel<float><<<g1, 256, smem, st>>>(a);
-        attn_combine_kernel<float><<<g2, 128, 0, st>>>(a);
-    }
-    return 2;
+    const int nsplit = (max_len_after + a.split_keys - 1) / a.split_keys;
+    const size_t smem = attn_smem(a.hd, c.esize);
+    const dim3 grid(nsplit, a.hkv, B);
+    if (c.cfg.dtype == SPEC_BF16) attn_split_kernel<__nv_bfloat16><<<grid, ATT_THREADS, smem, st>>>(a);
+    else attn_split_kernel<float><<<grid, ATT_THREADS, smem, st>>>(a);
+    return 1;
 }
 
 int attention_set_smem_limits(int hd) {
-    const int smem = (int)attn_partial_smem(hd);
-    if (cudaFuncSetAttribute(attn_partial_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_partial_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(attn_split_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_smem(hd, 2)) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_split_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_smem(hd, 4)) != cudaSuccess)
         return -1;
     return 0;
 }

@@ -83,6 +83,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start its prologue, and
+// wait for the previous kernel's completion (and memory) before touching its outputs.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- warp-wide sorted (value, id) lists -------------------------------------------------
 
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {

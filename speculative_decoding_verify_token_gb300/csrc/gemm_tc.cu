@@ -204,14 +204,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_sh;
+    pdl_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pw = policy_evict_first();
             const uint64_t px = policy_evict_last();
             const uint32_t tx = (uint32_t)(TC_A_BYTES + p.ntok * TC_BK * 2);
-            long long i = 0;
-            for (long long g = s0; g < s1; ++g, ++i) {
+            // The first ring's worth of weight tiles does not depend on the previous kernel:
+            // issue it before waiting for that kernel, then the activations.
+            const long long pre = min((long long)S, s1 - s0);
+            for (long long i = 0; i < pre; ++i) {
+                const long long g = s0 + i;
+                const int tile = (int)(g / p.KB), kb = (int)(g % p.KB);
+                const uint32_t fb = smem_u32(&full_bar[i]);
+                mbar_arrive_expect_tx(fb, tx);
+                const uint32_t a_dst = base + (uint32_t)i * p.stage_bytes;
+                const CUtensorMap *m0, *m1;
+                int r0, r1;
+                tile_rows(p, tile, m0, r0, m1, r1);
+                tma_load_2d(a_dst, m0, kb * TC_BK, r0, fb, pw);
+                tma_load_2d(a_dst + TC_A_BYTES / 2, m1, kb * TC_BK, r1, fb, pw);
+            }
+            pdl_wait();
+            for (long long i = 0; i < pre; ++i) {
+                const int kb = (int)((s0 + i) % p.KB);
+                const uint32_t b_dst = base + (uint32_t)i * p.stage_bytes + TC_A_BYTES;
+                for (int t = 0; t < p.ntok / 16; ++t)
+                    tma_load_2d(b_dst + t * 2048, &p.xmap, kb * TC_BK, p.x_row0 + t * 16, smem_u32(&full_bar[i]), px);
+            }
+            long long i = pre;
+            for (long long g = s0 + pre; g < s1; ++g, ++i) {
                 const int tile = (int)(g / p.KB), kb = (int)(g % p.KB);
                 const int s = (int)(i % S);
                 if (!mbar_wait(smem_u32(&empty_bar[s]), (uint32_t)(((i / S) & 1) ^ 1))) {
@@ -275,6 +298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             mbar_wait(smem_u32(&done_bar), 0);
         }
     } else {
+        pdl_wait();     // outputs of the previous kernel may still be read by it until then
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const int etid = threadIdx.x - 64;
@@ -534,7 +558,18 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, 
     const long long T = (long long)p.n_tiles * p.KB;
     const int grid = (int)std::min<long long>(t->grid, T);
     const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + TC_XBYTES;
-    tc_gemm_kernel<<<grid, TC_THREADS, smem, st>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = c.use_pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, p);
+    if (err != cudaSuccess) return set_error(SPEC_E_CUDA, "tc_gemm_kernel launch: %s", cudaGetErrorString(err));
     return 1;
 }
 

@@ -11,7 +11,6 @@
 namespace sv {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
-constexpr int ATT_CHUNK = 64;          // keys per attention split (absolute positions)
 
 struct LayerWeights {
     const void *attn_norm = nullptr, *wq = nullptr, *wk = nullptr, *wv = nullptr, *wo = nullptr;
@@ -34,9 +33,11 @@ struct AttnArgs {
     const int* seq_len;       // [slots] device, length before this pass
     int T, hq, hkv, hd;
     float scale;
-    int n_chunks;             // chunk capacity of the partial buffers
+    int n_chunks;             // split capacity of the partial buffers
+    int split_keys;           // keys per split (multiple of 16, fixed per context)
     float* part_o;            // [B][hkv][n_chunks][T*G][hd]
     float2* part_ml;          // [B][hkv][n_chunks][T*G]
+    int* att_cnt;             // [slots * hkv] arrival counters, zero between passes
 };
 
 struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
@@ -88,6 +89,8 @@ struct Ctx {
     int n_chunks = 0;
     float* part_o = nullptr;
     float2* part_ml = nullptr;
+    int* att_cnt = nullptr;
+    int split_keys = 0;
     // verify
     void* vws = nullptr;
     size_t vws_bytes = 0;
@@ -97,6 +100,11 @@ struct Ctx {
     struct ProfRec { int cls; cudaEvent_t a, b; double bytes; };
     std::vector<ProfRec> prof_recs;
     std::vector<cudaEvent_t> prof_pool;
+    // CUDA graphs of the decoder pass per (B, T); programmatic dependent launch
+    bool use_graphs = true;
+    bool use_pdl = true;
+    struct GraphEntry { int B, T; cudaGraphExec_t exec; long long kernels; };
+    std::vector<GraphEntry> graphs;
     // tensor-core GEMM
     TcGemm* tc = nullptr;
     bool use_tc = false;
@@ -115,6 +123,7 @@ void launch_gemm_simt(const Ctx& c, const void* wa, const void* wb, const void* 
                       const void* X, const EpiArgs& e, cudaStream_t st);
 int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, cudaStream_t st);
 int attention_set_smem_limits(int hd);
+int attention_split_keys(int hd, int esize);
 
 // tcgen05 GEMM (bf16 models)
 int tc_create(Ctx& c);                       // plans + tensor maps, after weights are loaded

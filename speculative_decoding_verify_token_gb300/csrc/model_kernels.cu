@@ -2,6 +2,7 @@
 // RMSNorm, the RoPE table, the verify-pass token layout and the O(1) KV length updates.
 #include <cuda_bf16.h>
 
+#include "common.cuh"
 #include "epilogue.cuh"
 #include "model.h"
 
@@ -14,6 +15,7 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
                              const int* __restrict__ seq_len, int T_per_seq, const T* __restrict__ E,
                              float* __restrict__ X, int* __restrict__ tok_seq, int* __restrict__ tok_pos, int d,
                              int V) {
+    pdl_launch_dependents();
     const int m = blockIdx.x;
     const int b = m / T_per_seq;
     const int t = m - b * T_per_seq;
@@ -32,6 +34,7 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
 template <typename T>
 __global__ void rmsnorm_kernel(const float* __restrict__ X, const T* __restrict__ g, T* __restrict__ Xn, int d,
                                float eps) {
+    pdl_launch_dependents();
     const int m = blockIdx.x;
     const float* x = X + (size_t)m * d;
     float ss = 0.0f;

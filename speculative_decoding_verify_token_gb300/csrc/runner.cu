@@ -45,7 +45,13 @@ static int dalloc(Ctx& c, P** p, size_t bytes, bool zero = false) {
     return SPEC_OK;
 }
 
+static void drop_graphs(Ctx& c) {
+    for (auto& g : c.graphs) cudaGraphExecDestroy(g.exec);
+    c.graphs.clear();
+}
+
 static void free_all(Ctx& c) {
+    drop_graphs(c);
     tc_destroy(c);
     for (auto& r : c.prof_recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
     for (auto e : c.prof_pool) cudaEventDestroy(e);
@@ -222,7 +228,8 @@ static int gemm(Ctx& c, int gid, int layer, const void* wa, const void* wb, cons
 
 // Forward of B x T tokens already in d_tokens for the slots in d_seq_ids.  logits_out gets
 // every row ([B*T][V]) or, when last_only, the last row only ([V]); nullptr = no lm_head.
-static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bool last_only) {
+static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bool last_only,
+                   bool graph_mode = false) {
     const spec_model_cfg& m = c.cfg;
     const int M = B * T;
     const int d = m.d_model, hd = m.head_dim, hq = m.n_q_heads, hkv = m.n_kv_heads, F = m.ffn_dim;
@@ -235,6 +242,7 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         max_after = std::max(max_after, c.len_hi[slots[b]] + T);
         kv_bytes += (double)(c.len_hi[slots[b]] + 2 * T) * 2.0 * hkv * hd * c.esize;
     }
+    if (graph_mode) max_after = c.lim.max_ctx;   // the graph is replayed at any length
 
     EpiArgs eq{};
     eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
@@ -247,6 +255,7 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     aa.q = c.Q; aa.o = c.O; aa.block_table = c.d_block_table; aa.max_pages = c.max_pages; aa.seq_ids = c.d_seq_ids;
     aa.seq_len = c.d_seq_len; aa.T = T; aa.hq = hq; aa.hkv = hkv; aa.hd = hd; aa.scale = 1.0f / sqrtf((float)hd);
     aa.n_chunks = c.n_chunks; aa.part_o = c.part_o; aa.part_ml = c.part_ml;
+    aa.split_keys = c.split_keys; aa.att_cnt = c.att_cnt;
 
     int rc;
     for (int l = 0; l < m.n_layers; ++l) {
@@ -284,6 +293,39 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     return SPEC_OK;
 }
 
+// The decoder pass of B x T tokens through a CUDA graph captured once per (B, T) (logits
+// to the internal buffer).  Falls back to eager launches while profiling.
+static int forward_graph(Ctx& c, const int* slots, int B, int T) {
+    GraphEntryLookup:
+    for (auto& g : c.graphs) {
+        if (g.B == B && g.T == T) {
+            cudaError_t e = cudaGraphLaunch(g.exec, c.stream);
+            if (e != cudaSuccess) return cuda_fail("cudaGraphLaunch", e);
+            c.launches += g.kernels;
+            return SPEC_OK;
+        }
+    }
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(c.stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamBeginCapture", e);
+    const long long l0 = c.launches;
+    const int rc = forward(c, slots, B, T, c.logits, false, true);
+    const long long n = c.launches - l0;
+    c.launches = l0;
+    e = cudaStreamEndCapture(c.stream, &graph);
+    if (rc != SPEC_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    if (e != cudaSuccess) return cuda_fail("cudaStreamEndCapture", e);
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail("cudaGraphInstantiate", e);
+    c.graphs.push_back({B, T, exec, n});
+    goto GraphEntryLookup;
+}
+
 }  // namespace sv
 
 using namespace sv;
@@ -293,7 +335,7 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
     if (!cfg || !limits || !out) return set_error(SPEC_E_INVAL, "NULL argument");
     const spec_model_cfg& m = *cfg;
     if (m.n_layers < 1 || m.d_model < 8 || m.d_model % 8 || m.n_q_heads < 1 || m.n_kv_heads < 1 ||
-        m.n_q_heads % m.n_kv_heads || m.head_dim < 2 || m.head_dim % 2 || m.head_dim > 256 ||
+        m.n_q_heads % m.n_kv_heads || m.head_dim < 32 || m.head_dim % 32 || m.head_dim > 256 ||
         (m.n_q_heads * m.head_dim) % 8 || m.ffn_dim < 8 || m.ffn_dim % 8 || m.vocab < 2 || m.vocab % 2 ||
         !(m.rope_theta > 0.0f) || !(m.rms_eps >= 0.0f) || (m.dtype != SPEC_F32 && m.dtype != SPEC_BF16))
         return set_error(SPEC_E_INVAL, "bad model shape");
@@ -316,7 +358,8 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
     c->max_pages = max_pages;
     c->w.layers.resize(m.n_layers);
     c->Mmax = std::max(lim.max_batch * (lim.max_k + 1), lim.prefill_chunk);
-    c->n_chunks = (lim.max_ctx + ATT_CHUNK - 1) / ATT_CHUNK;
+    c->split_keys = attention_split_keys(m.head_dim, c->esize);
+    c->n_chunks = (lim.max_ctx + c->split_keys - 1) / c->split_keys;
     const size_t qd = (size_t)m.n_q_heads * m.head_dim;
     c->layer_pool_elems = (size_t)lim.num_pages * m.n_kv_heads * SPEC_PAGE_TOKENS * m.head_dim;
     int rc = SPEC_OK;
@@ -338,6 +381,7 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
           ok(dalloc(*c, &c->d_seq_ids, sizeof(int) * lim.max_batch, true)) &&
           ok(dalloc(*c, &c->part_o, sizeof(float) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks * m.head_dim)) &&
           ok(dalloc(*c, &c->part_ml, sizeof(float2) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks)) &&
+          ok(dalloc(*c, &c->att_cnt, sizeof(int) * (size_t)lim.max_batch * m.n_kv_heads, true)) &&
           ok(dalloc(*c, &c->d_status_scratch, sizeof(int) * lim.max_batch)))) {
         free_all(*c);
         delete c;
@@ -471,7 +515,17 @@ extern "C" int spec_verify(spec_ctx* c, int B, const int32_t* seq_ids, int K, co
     launch_verify_tokens(last_tokens, draft_tokens, K, c->d_tokens, B, c->stream);
     c->launches += 1;
     float* logits = out_logits ? out_logits : c->logits;
-    if ((rc = forward(*c, seq_ids, B, K + 1, logits, false)) != SPEC_OK) return rc;
+    if (c->use_graphs && !c->prof_on) {
+        logits = c->logits;
+        if ((rc = forward_graph(*c, seq_ids, B, K + 1)) != SPEC_OK) return rc;
+        if (out_logits) {
+            cudaError_t e = cudaMemcpyAsync(out_logits, c->logits, sizeof(float) * (size_t)B * (K + 1) * c->cfg.vocab,
+                                            cudaMemcpyDeviceToDevice, c->stream);
+            if (e != cudaSuccess) return cuda_fail("logits copy", e);
+        }
+    } else if ((rc = forward(*c, seq_ids, B, K + 1, logits, false)) != SPEC_OK) {
+        return rc;
+    }
     {
     ProfScope psv(*c, 6, (double)B * (K + 1) * c->cfg.vocab * 4.0 +
                              (draft_logits && sampling->temperature > 0 ? (double)B * K * c->cfg.vocab * 4.0 : 0.0));
@@ -536,6 +590,20 @@ extern "C" int spec_seq_reset(spec_ctx* c, int seq_id) {
 }
 
 extern "C" long long spec_kernel_launches(const spec_ctx* c) { return c ? c->launches : 0; }
+
+extern "C" int spec_set_option(spec_ctx* c, int option, int value) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    if (option == SPEC_OPT_GRAPHS) {
+        c->use_graphs = value != 0;
+    } else if (option == SPEC_OPT_PDL) {
+        c->use_pdl = value != 0;
+        drop_graphs(*c);
+    } else {
+        return set_error(SPEC_E_INVAL, "unknown option %d", option);
+    }
+    return SPEC_OK;
+}
 
 extern "C" int spec_profile(spec_ctx* c, int enable) {
     clear_error();

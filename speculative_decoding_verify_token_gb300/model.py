@@ -122,6 +122,9 @@ class SpecModel:
     def launches(self):
         return int(self.lib.spec_kernel_launches(self.h))
 
+    def set_option(self, option, value):
+        _lib.check(self.lib.spec_set_option(self.h, int(option), int(value)))
+
     def profile(self, enable=True):
         _lib.check(self.lib.spec_profile(self.h, 1 if enable else 0))
 
