@@ -52,6 +52,8 @@ static void drop_graphs(Ctx& c) {
 
 static void free_all(Ctx& c) {
     drop_graphs(c);
+    if (c.cap_stream) cudaStreamDestroy(c.cap_stream);
+    c.cap_stream = nullptr;
     tc_destroy(c);
     for (auto& r : c.prof_recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
     for (auto e : c.prof_pool) cudaEventDestroy(e);
@@ -305,14 +307,22 @@ static int forward_graph(Ctx& c, const int* slots, int B, int T) {
             return SPEC_OK;
         }
     }
+    // capture on the context's private stream (the caller's may be the legacy stream, which
+    // cannot be captured); the graph is launched on the caller's stream
     cudaGraph_t graph = nullptr;
+    cudaStream_t saved = c.stream;
+    c.stream = c.cap_stream;
     cudaError_t e = cudaStreamBeginCapture(c.stream, cudaStreamCaptureModeThreadLocal);
-    if (e != cudaSuccess) return cuda_fail("cudaStreamBeginCapture", e);
+    if (e != cudaSuccess) {
+        c.stream = saved;
+        return cuda_fail("cudaStreamBeginCapture", e);
+    }
     const long long l0 = c.launches;
     const int rc = forward(c, slots, B, T, c.logits, false, true);
     const long long n = c.launches - l0;
     c.launches = l0;
     e = cudaStreamEndCapture(c.stream, &graph);
+    c.stream = saved;
     if (rc != SPEC_OK) {
         if (graph) cudaGraphDestroy(graph);
         return rc;
@@ -416,6 +426,11 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
     for (int i = 0; i < lim.num_pages; ++i) c->free_pages[i] = lim.num_pages - 1 - i;
     c->n_pages.assign(lim.max_batch, 0);
     c->len_hi.assign(lim.max_batch, 0);
+    if (cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        free_all(*c);
+        delete c;
+        return set_error(SPEC_E_CUDA, "cudaStreamCreate failed");
+    }
     launch_rope_table(c->d_rope, lim.max_ctx, m.head_dim, (double)m.rope_theta, c->stream);
     if (attention_set_smem_limits(m.head_dim) != 0) {
         free_all(*c);

@@ -9,15 +9,17 @@
 // while they equal the target's choice, replace the first mismatch).
 //
 // GB300 design:
-//  * persistent grid of one 8-warp CTA per SM; every warp is an independent streaming
-//    engine with its own 3-stage ring of 8 KB shared-memory buffers filled by 1-D bulk
-//    copies on the TMA engine (one elected lane issues, mbarrier completion), so each SM
-//    keeps up to 192 KB of HBM reads in flight;
-//  * work items are (row, chunk) pieces of the logits rows, handed out by a global atomic
-//    counter so the warps stay balanced whatever B, K and V are;
+//  * persistent grid of 3 CTAs x 8 warps per SM; every warp streams one (row, chunk) work
+//    item at a time with coalesced 16-byte streaming loads, 8 in flight per lane (about
+//    100 KB of HBM reads in flight per SM), handed out by a global atomic counter so the
+//    warps stay balanced whatever B, K and V are (the index of the next item is fetched
+//    one item ahead);
 //  * each warp keeps an exact running top-k of its item as a warp-wide sorted list (one
-//    entry per lane); a stage costs one compare per float4 against the running k-th value
-//    and only rare candidates go through a bitonic sort + merge;
+//    entry per lane); the common path per 1024 elements is a lane maximum and one vote
+//    against the running cut, which is the larger of the list's k-th value and a lower
+//    bound of the row's k-th value shared by all chunks of the row (atomicMax on an
+//    order-preserving integer key); the rare candidates go to a shared-memory buffer and
+//    through a bitonic sort + merge 32 at a time;
 //  * the last warp to finish a row (atomic arrival count, no spin-wait) merges the chunk
 //    lists and builds the row's truncated distribution; the last row of a sequence runs
 //    the acceptance scan and the final inverse-CDF draw on one warp.
@@ -33,10 +35,9 @@ namespace sv {
 
 constexpr int VT_WARPS = 8;
 constexpr int VT_THREADS = VT_WARPS * 32;
-constexpr int VT_STAGES = 3;
-constexpr int VT_STAGE_ELEMS = 2048;                // 8 KB of fp32 per stage
-constexpr int VT_STAGE_BYTES = VT_STAGE_ELEMS * 4;
-constexpr int VT_SMEM = VT_WARPS * VT_STAGES * VT_STAGE_BYTES;
+constexpr int VT_BLOCKS_PER_SM = 3;
+constexpr int VS_UNROLL = 8;                         // 16-byte loads in flight per lane
+constexpr int VT_CHUNK_QUANTUM = 1024;               // chunk sizes are multiples of this
 constexpr int LISTN = 32;
 constexpr int VT_TARGET_ITEMS = 4096;
 constexpr int VT_MAX_CHUNKS = 128;
@@ -59,7 +60,7 @@ struct VerifyParams {
     int n_target_rows;          // B*(K+1) (verify) or R (sample)
     int n_rows;                 // + B*K draft rows when draft logits are given
     int chunks;                 // chunks per row
-    int chunk_elems;            // body elements per chunk (multiple of VT_STAGE_ELEMS)
+    int chunk_elems;            // body elements per chunk (multiple of VT_CHUNK_QUANTUM)
     int n_items;                // n_rows * chunks
     int* accepted_len;
     int* next_token;
@@ -119,61 +120,6 @@ __device__ __forceinline__ void row_split(const float* ptr, int V, int& head, in
     body = ((V - head) / 4) * 4;
 }
 
-struct StageDesc {
-    int item;
-    int start;     // row-relative element index of the first element in the buffer
-    int count;     // elements (multiple of 4, may be 0)
-    int flags;     // 1 = first stage of the item, 2 = last stage of the item
-};
-
-struct ProdState {
-    int item;
-    int pos, end;
-    bool first;
-    const float* ptr;
-    int pref;      // next work item index, fetched one item ahead so the atomic's latency hides
-};
-
-// Lane 0 only: describe the next stage of this warp's stream; false when no work is left.
-__device__ bool next_stage(const VerifyParams& p, ProdState& ps, StageDesc& d) {
-    while (ps.item < 0) {
-        const int it = ps.pref;
-        if (it >= p.n_items) return false;
-        ps.pref = atomicAdd(p.work, 1);
-        const int row = it / p.chunks, c = it % p.chunks;
-        const RowInfo ri = row_info(p, row);
-        if (!row_needed(p, ri)) continue;
-        int head, body;
-        row_split(ri.ptr, p.V, head, body);
-        const int s = c * p.chunk_elems;
-        const int e = min(body, s + p.chunk_elems);
-        ps.item = it;
-        ps.pos = head + min(s, body);
-        ps.end = head + max(e, min(s, body));
-        ps.first = true;
-        ps.ptr = ri.ptr;
-    }
-    const int n = min(VT_STAGE_ELEMS, ps.end - ps.pos);
-    d.item = ps.item;
-    d.start = ps.pos;
-    d.count = n;
-    d.flags = (ps.first ? 1 : 0) | (ps.pos + n >= ps.end ? 2 : 0);
-    ps.first = false;
-    ps.pos += n;
-    if (d.flags & 2) ps.item = -1;
-    return true;
-}
-
-__device__ __forceinline__ void issue_stage(const ProdState& ps, const StageDesc& d, uint32_t buf,
-                                            uint32_t bar, uint64_t pol) {
-    if (d.count > 0) {
-        mbar_arrive_expect_tx(bar, (uint32_t)d.count * 4u);
-        bulk_g2s(buf, ps.ptr + d.start, (uint32_t)d.count * 4u, bar, pol);
-    } else {
-        mbar_arrive(bar);
-    }
-}
-
 __device__ __forceinline__ float pick4(const float4& x, int c) {
     float r = x.x;
     r = (c == 1) ? x.y : r;
@@ -199,24 +145,6 @@ __device__ __forceinline__ float key_float(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Maximum of the lane's float4s of a stage buffer (4 independent chains; NaN ignored).
-__device__ __forceinline__ float stage_lane_max(const float4* buf, int n4, int lane) {
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-    if (n4 == VT_STAGE_ELEMS / 4) {
-#pragma unroll
-        for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
-            const float4 x = buf[lane + 32 * j];
-            m0 = fmaxf(m0, x.x); m1 = fmaxf(m1, x.y); m2 = fmaxf(m2, x.z); m3 = fmaxf(m3, x.w);
-        }
-    } else {
-        for (int idx = lane; idx < n4; idx += 32) {
-            const float4 x = buf[idx];
-            m0 = fmaxf(m0, x.x); m1 = fmaxf(m1, x.y); m2 = fmaxf(m2, x.z); m3 = fmaxf(m3, x.w);
-        }
-    }
-    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-}
-
 // Sort + merge the warp's buffered candidates into its running list, 32 at a time.
 __device__ __forceinline__ void flush_candidates(float& lv, int& lid, const float* cv, const int* ci, int n,
                                                  int lane) {
@@ -233,15 +161,15 @@ __device__ __forceinline__ void flush_candidates(float& lv, int& lid, const floa
 
 // Exact path for a stage whose candidates overflowed the buffer (e.g. many equal values):
 // lanes offer one element per round, tested exactly against the running k-th entry.
-__device__ __noinline__ void exact_rounds(const float4 (&x)[VT_STAGE_ELEMS / 128], int start, float lb, float& lv,
+__device__ __noinline__ void exact_rounds(const float4 (&x)[VS_UNROLL], int start, float lb, float& lv,
                                           int& lid, float* cv, int* ci, int& ccount, int k, int lane) {
-    for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+    for (int j = 0; j < VS_UNROLL; ++j) {
         for (int c = 0; c < 4; ++c) {
             const float thr_v = __shfl_sync(FULL, lv, k - 1);
             const int thr_id = __shfl_sync(FULL, lid, k - 1);
             float4 xj = x[0];
 #pragma unroll
-            for (int q = 1; q < VT_STAGE_ELEMS / 128; ++q)
+            for (int q = 1; q < VS_UNROLL; ++q)
                 if (q == j) xj = x[q];
             const float xc = pick4(xj, c);
             const int id = start + 4 * (lane + 32 * j) + c;
@@ -442,172 +370,112 @@ __device__ void finish_row(const VerifyParams& p, int row, int lane) {
     }
 }
 
-__device__ void record_timeout(const VerifyParams& p, int item) {
-    const int row = item / p.chunks;
-    const RowInfo ri = row_info(p, row);
-    if (p.mode == MODE_SAMPLE) {
-        p.out_tokens[row] = -1;
-    } else if (p.seq_status) {
-        p.seq_status[ri.seq] = SPEC_E_TIMEOUT;
-    }
-}
 
-__global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[VT_WARPS][VT_STAGES];
-    __shared__ StageDesc descs[VT_WARPS][VT_STAGES];
+// One warp streams one (row, chunk) work item at a time: coalesced 16-byte streaming loads,
+// VS_UNROLL of them in flight per lane, several CTAs per SM so that enough warps hide the
+// HBM latency.  Per iteration of 1024 elements the common path is the lane maximum and one
+// vote against the running cut; only lanes whose maximum reaches it look at elements.
+__global__ void __launch_bounds__(VT_THREADS, VT_BLOCKS_PER_SM) verify_kernel(const VerifyParams p) {
     __shared__ float cand_v[VT_WARPS][VT_CAND_CAP];
     __shared__ int cand_id[VT_WARPS][VT_CAND_CAP];
     __shared__ int ccnt_s[VT_WARPS];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    float* ring = reinterpret_cast<float*>(smem) + (size_t)warp * VT_STAGES * VT_STAGE_ELEMS;
-    const uint32_t ring_u32 = smem_u32(ring);
-    uint32_t bar_u32[VT_STAGES];
-#pragma unroll
-    for (int s = 0; s < VT_STAGES; ++s) bar_u32[s] = smem_u32(&bars[warp][s]);
-
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < VT_STAGES; ++s) mbar_init(bar_u32[s], 1);
-        fence_barrier_init();
-        ccnt_s[warp] = 0;
-    }
-    __syncwarp();
-
-    const int k = p.top_k;
-    const uint64_t pol = policy_evict_first();
-    ProdState ps;
-    ps.item = -1; ps.pos = ps.end = 0; ps.first = false; ps.ptr = nullptr; ps.pref = 0;
-    if (lane == 0) ps.pref = atomicAdd(p.work, 1);
-
-    int inflight = 0;
-    if (lane == 0) {
-        for (int s = 0; s < VT_STAGES; ++s) {
-            StageDesc d;
-            if (!next_stage(p, ps, d)) break;
-            descs[warp][s] = d;
-            issue_stage(ps, d, ring_u32 + s * VT_STAGE_BYTES, bar_u32[s], pol);
-            ++inflight;
-        }
-    }
-    inflight = __shfl_sync(FULL, inflight, 0);
-    __syncwarp();
-
-    uint32_t phase = 0;
-    float lv = -INFINITY, lb = -INFINITY, published = -INFINITY;
-    int lid = SENT_ID;
-    int slot = 0;
-    int ccount = 0;
     float* cbuf_v = cand_v[warp];
     int* cbuf_id = cand_id[warp];
-    while (inflight > 0) {
-        const bool ok = mbar_wait(bar_u32[slot], (phase >> slot) & 1u);
-        if (!__all_sync(FULL, ok)) {
-            // The copy never completed: report, drain the other buffers (bounded), stop.
-            if (lane == 0) record_timeout(p, descs[warp][slot].item);
-            for (int s = 1; s < inflight; ++s) {
-                const int sl = (slot + s) % VT_STAGES;
-                mbar_wait(bar_u32[sl], (phase >> sl) & 1u);
-            }
-            return;
-        }
-        phase ^= 1u << slot;
-        const StageDesc d = descs[warp][slot];
-        const int row_now = d.item / p.chunks;
-        unsigned* rb_ptr = p.row_bound + row_now;
-        const unsigned rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
-        // Copy the stage to registers, then hand the buffer straight back to the TMA engine.
-        float4 x[VT_STAGE_ELEMS / 128];
-        const int n4 = d.count >> 2;
-        {
-            const float4* buf = reinterpret_cast<const float4*>(ring + slot * VT_STAGE_ELEMS);
-            if (n4 == VT_STAGE_ELEMS / 4) {
-#pragma unroll
-                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) x[j] = buf[lane + 32 * j];
-            } else {
-#pragma unroll
-                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
-                    const int idx = lane + 32 * j;
-                    x[j] = idx < n4 ? buf[idx] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                }
-            }
-        }
-        __syncwarp();
-        int more = 0;
-        if (lane == 0) {
-            StageDesc nd;
-            if (next_stage(p, ps, nd)) {
-                descs[warp][slot] = nd;
-                issue_stage(ps, nd, ring_u32 + slot * VT_STAGE_BYTES, bar_u32[slot], pol);
-                more = 1;
-            }
-        }
-        more = __shfl_sync(FULL, more, 0);
+    if (lane == 0) ccnt_s[warp] = 0;
+    __syncwarp();
+    const int k = p.top_k;
+    int pref = 0;
+    if (lane == 0) pref = atomicAdd(p.work, 1);
 
-        // Lane maximum (4 independent chains; padding is -inf, NaN is ignored).
-        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
-            m0 = fmaxf(m0, x[j].x); m1 = fmaxf(m1, x[j].y); m2 = fmaxf(m2, x[j].z); m3 = fmaxf(m3, x[j].w);
+    while (true) {
+        // next needed work item (the index after it is fetched now and used next time)
+        int it = 0;
+        if (lane == 0) {
+            it = pref;
+            while (it < p.n_items && !row_needed(p, row_info(p, it / p.chunks))) it = atomicAdd(p.work, 1);
+            if (it < p.n_items) pref = atomicAdd(p.work, 1);
         }
-        const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-        if (d.flags & 1) {
-            // New item: reset the list; lower bound = k-th largest lane maximum of this stage
-            // (k distinct elements reach it, so the chunk's -- and the row's -- k-th best does).
-            lv = -INFINITY; lid = SENT_ID;
-            float m = mx;
-            int dummy = lane;
-            warp_sort_desc(m, dummy, lane);
-            lb = __shfl_sync(FULL, m, k - 1);
-            if (lane == 0 && lb > -INFINITY) atomicMax(rb_ptr, float_key(lb));
-            published = lb;
-        }
-        // Row-wide bound published by the other chunks of the row (any chunk's k-th best is
-        // a lower bound of the row's k-th best, so filtering by it is exact).
-        lb = fmaxf(lb, key_float(rb_key));
-        float thr_v = __shfl_sync(FULL, lv, k - 1);
-        int thr_id = __shfl_sync(FULL, lid, k - 1);
-        float cut = fmaxf(lb, thr_v);
-        if (__any_sync(FULL, mx >= cut)) {
-            // Candidates: values reaching the cut (a value test only; an entry equal to the
-            // k-th value with a larger id is a harmless extra for the exact merge).  Lanes
-            // append with a shared-memory atomic; an overflow falls back to exact rounds.
-            const int pre = ccount;
-            if (mx >= cut) {
+        it = __shfl_sync(FULL, it, 0);
+        if (it >= p.n_items) break;
+        const int row = it / p.chunks, c = it % p.chunks;
+        const RowInfo ri = row_info(p, row);
+        int head, body;
+        row_split(ri.ptr, p.V, head, body);
+        const int s0 = head + min(c * p.chunk_elems, body);
+        const int s1 = head + min(body, (c + 1) * p.chunk_elems);
+        const float4* src = reinterpret_cast<const float4*>(ri.ptr + s0);
+        const int n4 = s1 > s0 ? (s1 - s0) >> 2 : 0;
+        unsigned* rb_ptr = p.row_bound + row;
+
+        float lv = -INFINITY, lb = -INFINITY, published = -INFINITY;
+        int lid = SENT_ID;
+        int ccount = 0;
+        for (int i0 = 0; i0 < n4; i0 += 32 * VS_UNROLL) {
+            const unsigned rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
+            float4 x[VS_UNROLL];
 #pragma unroll
-                for (int j = 0; j < VT_STAGE_ELEMS / 128; ++j) {
+            for (int u = 0; u < VS_UNROLL; ++u) {
+                const int idx = i0 + lane + 32 * u;
+                x[u] = idx < n4 ? __ldcs(src + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float xc = pick4(x[j], c);
-                        if (xc >= cut) {
-                            const int pos = atomicAdd(&ccnt_s[warp], 1);
-                            if (pos < VT_CAND_CAP) {
-                                cbuf_v[pos] = xc;
-                                cbuf_id[pos] = d.start + 4 * (lane + 32 * j) + c;
+            for (int u = 0; u < VS_UNROLL; ++u) {
+                m0 = fmaxf(m0, x[u].x); m1 = fmaxf(m1, x[u].y); m2 = fmaxf(m2, x[u].z); m3 = fmaxf(m3, x[u].w);
+            }
+            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            if (i0 == 0) {
+                // k distinct elements reach the k-th largest lane maximum: a lower bound of
+                // the chunk's (and the row's) k-th best.
+                float m = mx;
+                int dummy = lane;
+                warp_sort_desc(m, dummy, lane);
+                lb = __shfl_sync(FULL, m, k - 1);
+                if (lane == 0 && lb > -INFINITY) atomicMax(rb_ptr, float_key(lb));
+                published = lb;
+            }
+            lb = fmaxf(lb, key_float(rb_key));
+            const float thr_v = __shfl_sync(FULL, lv, k - 1);
+            const float cut = fmaxf(lb, thr_v);
+            if (__any_sync(FULL, mx >= cut)) {
+                // value test only: an entry equal to the k-th value with a larger id is a
+                // harmless extra for the exact merge
+                const int pre = ccount;
+                if (mx >= cut) {
+#pragma unroll
+                    for (int u = 0; u < VS_UNROLL; ++u) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float xc = pick4(x[u], q);
+                            if (xc >= cut) {
+                                const int pos = atomicAdd(&ccnt_s[warp], 1);
+                                if (pos < VT_CAND_CAP) {
+                                    cbuf_v[pos] = xc;
+                                    cbuf_id[pos] = s0 + 4 * (i0 + lane + 32 * u) + q;
+                                }
                             }
                         }
                     }
                 }
+                __syncwarp();
+                ccount = *reinterpret_cast<volatile int*>(&ccnt_s[warp]);
+                if (ccount > VT_CAND_CAP) {
+                    ccount = pre;
+                    exact_rounds(x, s0 + 4 * i0, lb, lv, lid, cbuf_v, cbuf_id, ccount, k, lane);
+                }
+                __syncwarp();
+                if (lane == 0) ccnt_s[warp] = ccount;
+                __syncwarp();
             }
-            __syncwarp();
-            ccount = *reinterpret_cast<volatile int*>(&ccnt_s[warp]);
-            if (ccount > VT_CAND_CAP) {
-                ccount = pre;
-                exact_rounds(x, d.start, lb, lv, lid, cbuf_v, cbuf_id, ccount, k, lane);
+            if (ccount >= 32 || (ccount > 0 && __shfl_sync(FULL, lid, k - 1) == SENT_ID)) {
+                flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
+                ccount = 0;
+                if (lane == 0) ccnt_s[warp] = 0;
+                __syncwarp();
             }
-            __syncwarp();
-            if (lane == 0) ccnt_s[warp] = ccount;
-            __syncwarp();
-        }
-        if (ccount >= 32 || (ccount > 0 && __shfl_sync(FULL, lid, k - 1) == SENT_ID)) {
-            flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
-            ccount = 0;
-            if (lane == 0) ccnt_s[warp] = 0;
-            __syncwarp();
-        }
-        {
             const float kth = __shfl_sync(FULL, lv, k - 1);
             if (kth > published) {
                 if (lane == 0) atomicMax(rb_ptr, float_key(kth));
@@ -615,45 +483,34 @@ __global__ void __launch_bounds__(VT_THREADS, 1) verify_kernel(const VerifyParam
                 lb = fmaxf(lb, kth);
             }
         }
-
-        if (d.flags & 2) {
-            // End of the item: scalar head / tail of the row, publish the chunk list.
-            const int row = d.item / p.chunks, c = d.item % p.chunks;
-            const RowInfo ri = row_info(p, row);
-            int head, body;
-            row_split(ri.ptr, p.V, head, body);
-            const int tail0 = head + body, tail = p.V - tail0;
-            if (ccount > 0) {
-                flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
-                ccount = 0;
-                if (lane == 0) ccnt_s[warp] = 0;
-                __syncwarp();
-            }
-            if (c == 0 && head > 0) {
-                const bool has = lane < head;
-                offer_round(lv, lid, has, has ? ri.ptr[lane] : 0.0f, lane, lane);
-            }
-            if (c == p.chunks - 1 && tail > 0) {
-                const bool has = lane < tail;
-                offer_round(lv, lid, has, has ? ri.ptr[tail0 + lane] : 0.0f, tail0 + lane, lane);
-            }
-            const size_t o = ((size_t)row * p.chunks + c) * LISTN + lane;
-            p.cl_v[o] = lv;
-            p.cl_id[o] = lid;
-            __threadfence();
+        if (ccount > 0) {
+            flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
+            if (lane == 0) ccnt_s[warp] = 0;
             __syncwarp();
-            int prev = 0;
-            if (lane == 0) prev = atomicAdd(p.row_cnt + row, 1);
-            prev = __shfl_sync(FULL, prev, 0);
-            if (prev == p.chunks - 1) {
-                __threadfence();
-                finish_row(p, row, lane);
-            }
         }
-
-        inflight += more - 1;
-        slot = (slot + 1 == VT_STAGES) ? 0 : slot + 1;
+        // scalar head / tail of the row
+        const int tail0 = head + body, tail = p.V - tail0;
+        if (c == 0 && head > 0) {
+            const bool has = lane < head;
+            offer_round(lv, lid, has, has ? ri.ptr[lane] : 0.0f, lane, lane);
+        }
+        if (c == p.chunks - 1 && tail > 0) {
+            const bool has = lane < tail;
+            offer_round(lv, lid, has, has ? ri.ptr[tail0 + lane] : 0.0f, tail0 + lane, lane);
+        }
+        // publish the chunk list; the last chunk of the row finishes it
+        const size_t o = ((size_t)row * p.chunks + c) * LISTN + lane;
+        p.cl_v[o] = lv;
+        p.cl_id[o] = lid;
+        __threadfence();
         __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(p.row_cnt + row, 1);
+        prev = __shfl_sync(FULL, prev, 0);
+        if (prev == p.chunks - 1) {
+            __threadfence();
+            finish_row(p, row, lane);
+        }
     }
 }
 
@@ -671,12 +528,12 @@ static Plan make_plan(int n_rows_max, int n_seq, int V) {
     pl.n_rows = n_rows_max;
     const int per_row = std::max(1, (VT_TARGET_ITEMS + n_rows_max - 1) / n_rows_max);
     long long ch = ((long long)V + per_row - 1) / per_row;
-    ch = ((ch + VT_STAGE_ELEMS - 1) / VT_STAGE_ELEMS) * VT_STAGE_ELEMS;
-    if (ch < VT_STAGE_ELEMS) ch = VT_STAGE_ELEMS;
+    ch = ((ch + VT_CHUNK_QUANTUM - 1) / VT_CHUNK_QUANTUM) * VT_CHUNK_QUANTUM;
+    if (ch < VT_CHUNK_QUANTUM) ch = VT_CHUNK_QUANTUM;
     long long chunks = ((long long)V + ch - 1) / ch;
     if (chunks > VT_MAX_CHUNKS) {
         chunks = VT_MAX_CHUNKS;
-        ch = (((long long)V + chunks - 1) / chunks + VT_STAGE_ELEMS - 1) / VT_STAGE_ELEMS * VT_STAGE_ELEMS;
+        ch = (((long long)V + chunks - 1) / chunks + VT_CHUNK_QUANTUM - 1) / VT_CHUNK_QUANTUM * VT_CHUNK_QUANTUM;
         chunks = ((long long)V + ch - 1) / ch;
     }
     pl.chunks = (int)chunks;
@@ -720,18 +577,12 @@ static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream
     prm.chunk_elems = pl.chunk_elems;
     prm.n_items = prm.n_rows * pl.chunks;
 
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, VT_SMEM) != cudaSuccess)
-            return set_error(SPEC_E_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
-        attr_done = true;
-    }
     cudaError_t e = cudaMemsetAsync(ws, 0, pl.counters_bytes, st);
     if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
     const int nsm = sm_count();
     if (nsm <= 0) return set_error(SPEC_E_CUDA, "no CUDA device");
-    const int grid = std::max(1, std::min(nsm, (prm.n_items + VT_WARPS - 1) / VT_WARPS));
-    verify_kernel<<<grid, VT_THREADS, VT_SMEM, st>>>(prm);
+    const int grid = std::max(1, std::min(nsm * VT_BLOCKS_PER_SM, (prm.n_items + VT_WARPS - 1) / VT_WARPS));
+    verify_kernel<<<grid, VT_THREADS, 0, st>>>(prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "verify_kernel launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
