@@ -151,9 +151,13 @@ class DenseVerifyWorkload:
     name = "dense-8b-verify-k4"
     dtype = "bf16"
 
-    def __init__(self, K=4, prompt_len=1024, alpha=0.7, n_gen=512):
+    def __init__(self, K=4, prompt_len=1024, alpha=0.7, n_gen=512, layers=None):
+        import dataclasses
         import synth
         self.shape = synth.QWEN_8B
+        if layers is not None and layers != self.shape.n_layers:
+            # a slice of the 8B shape with fewer layers (small cases for profiler captures)
+            self.shape = dataclasses.replace(self.shape, n_layers=layers, name=f"dense-8b-{layers}l")
         self.K, self.prompt_len, self.alpha, self.n_gen = K, prompt_len, alpha, n_gen
 
     def config(self):
@@ -541,6 +545,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=10)
+    ap.add_argument("--gen", type=int, default=512, help="tokens of the recorded greedy trajectory (8B workload)")
+    ap.add_argument("--layers", type=int, default=None, help="layers of the 8B shape (profiler captures only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -552,7 +558,8 @@ def main():
     rank, world, local = dist_setup()
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
-    wl = WORKLOADS[args.workload]()
+    wl = WORKLOADS[args.workload](n_gen=args.gen, layers=args.layers) if args.workload == DenseVerifyWorkload.name \
+        else WORKLOADS[args.workload]()
     n_total = args.warmup + args.steps
     wl.setup(dev, max(n_total, args.profile_steps))
     stream = torch.cuda.current_stream()
