@@ -29,10 +29,16 @@
 
 namespace sv {
 
+#ifndef TC_MAX_ATOMS
+#define TC_MAX_ATOMS 4          // most 64-element K atoms (128-byte swizzle spans) per stage
+#endif
+#ifndef TC_MIN_STAGES
+#define TC_MIN_STAGES 3         // fewest pipeline stages a launch may use
+#endif
 constexpr int TC_THREADS = 192;
 constexpr int TC_BM = 128;
-constexpr int TC_BK = 64;
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;       // 16 KB
+constexpr int TC_ATOM = 64;                          // K elements per atom = accumulation unit
+constexpr int TC_ATOM_A = TC_BM * TC_ATOM * 2;       // 16 KB: one 128-row x 64 A atom
 constexpr int TC_MAX_NTOK = 256;
 constexpr int TC_MAX_STAGES = 8;
 constexpr int TC_CW = 16;                           // epilogue column chunk
@@ -44,9 +50,10 @@ struct TcParams {
     CUtensorMap wmap[3];
     CUtensorMap xmap;
     int gid;
-    int n_tiles, KB;
+    int n_tiles, KB;          // tiles; K atoms per tile (the stream-K unit)
     int ntok, M, x_row0;
-    int stages, stage_bytes;
+    int stages, stage_bytes;  // ring slots; bytes per slot
+    int atoms;                // most atoms per stage (stages never cross a segment end)
     int hq, hkv;
     float* partial;          // [grid][2][128][ntok]
     int* tile_cnt;           // [n_tiles], zero between launches
@@ -140,7 +147,9 @@ __device__ __forceinline__ void tile_rows(const TcParams& p, int tile, const CUt
     }
 }
 
-__device__ __forceinline__ long long range_start(long long T, int G, int c) { return (long long)c * T / G; }
+__device__ __forceinline__ long long range_start(long long T, int G, int c) {
+    return (long long)(((unsigned long long)c * (unsigned long long)T) / (unsigned)G);
+}
 
 // CTA whose k-block range contains k-block x.
 __device__ __forceinline__ int owner_cta(long long T, int G, long long x) {
@@ -149,6 +158,42 @@ __device__ __forceinline__ int owner_cta(long long T, int G, long long x) {
     while (c + 1 < G && range_start(T, G, c + 1) <= x) ++c;
     return c;
 }
+
+// One K atom of a stage: the tile's 128 weight rows as two 64-row boxes (A) and the token
+// rows in boxes of 16 (B), at K coordinate kc.
+__device__ __forceinline__ void load_atom_a(const TcParams& p, int tile, int kc, uint32_t a_dst, uint32_t fb,
+                                            uint64_t pol) {
+    const CUtensorMap *m0, *m1;
+    int r0, r1;
+    tile_rows(p, tile, m0, r0, m1, r1);
+    tma_load_2d(a_dst, m0, kc, r0, fb, pol);
+    tma_load_2d(a_dst + TC_ATOM_A / 2, m1, kc, r1, fb, pol);
+}
+
+__device__ __forceinline__ void load_atom_b(const TcParams& p, int kc, uint32_t b_dst, uint32_t fb, uint64_t pol) {
+    for (int t = 0; t < p.ntok / 16; ++t) tma_load_2d(b_dst + t * 2048, &p.xmap, kc, p.x_row0 + t * 16, fb, pol);
+}
+
+// Walk of a CTA's atom range in pipeline stages: a stage holds up to p.atoms consecutive
+// atoms of one tile segment.  Producer and MMA issuer walk it identically.
+struct StageWalk {
+    long long g, s1;
+    int KB, A;
+    __device__ __forceinline__ StageWalk(long long s0_, long long s1_, int KB_, int A_)
+        : g(s0_), s1(s1_), KB(KB_), A(A_) {}
+    __device__ __forceinline__ bool done() const { return g >= s1; }
+    // atoms of the current stage, its tile, its first atom within the tile, and whether it
+    // starts / ends a segment
+    __device__ __forceinline__ void cur(int& n, int& tile, int& k_in_tile, bool& seg_first, bool& seg_last,
+                                        long long seg_start_of_g) const {
+        tile = (int)(g / KB);
+        k_in_tile = (int)(g - (long long)tile * KB);
+        const long long seg_end = min(s1, (long long)(tile + 1) * KB);
+        n = (int)min((long long)A, seg_end - g);
+        seg_first = (g == seg_start_of_g);
+        seg_last = (g + n == seg_end);
+    }
+};
 
 // Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
 __device__ __forceinline__ void epi_chunk(const TcParams& p, const float* xs, int tile, int c0, int etid) {
@@ -210,88 +255,105 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         if (lane == 0) {
             const uint64_t pw = policy_evict_first();
             const uint64_t px = policy_evict_last();
-            const uint32_t tx = (uint32_t)(TC_A_BYTES + p.ntok * TC_BK * 2);
             // The first ring's worth of weight tiles does not depend on the previous kernel:
             // issue it before waiting for that kernel, then the activations.
-            const long long pre = min((long long)S, s1 - s0);
-            for (long long i = 0; i < pre; ++i) {
-                const long long g = s0 + i;
-                const int tile = (int)(g / p.KB), kb = (int)(g % p.KB);
+            const uint32_t per_atom_tx = (uint32_t)(TC_ATOM_A + p.ntok * TC_ATOM * 2);
+            const uint32_t b_off = (uint32_t)(p.atoms * TC_ATOM_A);
+            StageWalk w(s0, s1, p.KB, p.atoms);
+            long long i = 0;
+            long long seg0 = s0;
+            for (; i < S && !w.done(); ++i) {
+                int n, tile, kt;
+                bool sf, sl;
+                w.cur(n, tile, kt, sf, sl, seg0);
                 const uint32_t fb = smem_u32(&full_bar[i]);
-                mbar_arrive_expect_tx(fb, tx);
+                mbar_arrive_expect_tx(fb, per_atom_tx * n);
                 const uint32_t a_dst = base + (uint32_t)i * p.stage_bytes;
-                const CUtensorMap *m0, *m1;
-                int r0, r1;
-                tile_rows(p, tile, m0, r0, m1, r1);
-                tma_load_2d(a_dst, m0, kb * TC_BK, r0, fb, pw);
-                tma_load_2d(a_dst + TC_A_BYTES / 2, m1, kb * TC_BK, r1, fb, pw);
+                for (int at = 0; at < n; ++at) load_atom_a(p, tile, (kt + at) * TC_ATOM, a_dst + at * TC_ATOM_A, fb, pw);
+                w.g += n;
+                if (sl) seg0 = w.g;
             }
             pdl_wait();
-            for (long long i = 0; i < pre; ++i) {
-                const int kb = (int)((s0 + i) % p.KB);
-                const uint32_t b_dst = base + (uint32_t)i * p.stage_bytes + TC_A_BYTES;
-                for (int t = 0; t < p.ntok / 16; ++t)
-                    tma_load_2d(b_dst + t * 2048, &p.xmap, kb * TC_BK, p.x_row0 + t * 16, smem_u32(&full_bar[i]), px);
+            {
+                StageWalk w2(s0, s1, p.KB, p.atoms);
+                long long sg = s0;
+                for (long long j = 0; j < i; ++j) {
+                    int n, tile, kt;
+                    bool sf, sl;
+                    w2.cur(n, tile, kt, sf, sl, sg);
+                    const uint32_t b_dst = base + (uint32_t)j * p.stage_bytes + b_off;
+                    for (int at = 0; at < n; ++at)
+                        load_atom_b(p, (kt + at) * TC_ATOM, b_dst + at * p.ntok * TC_ATOM * 2, smem_u32(&full_bar[j]), px);
+                    w2.g += n;
+                    if (sl) sg = w2.g;
+                }
             }
-            long long i = pre;
-            for (long long g = s0 + pre; g < s1; ++g, ++i) {
-                const int tile = (int)(g / p.KB), kb = (int)(g % p.KB);
+            for (; !w.done(); ++i) {
+                int n, tile, kt;
+                bool sf, sl;
+                w.cur(n, tile, kt, sf, sl, seg0);
                 const int s = (int)(i % S);
                 if (!mbar_wait(smem_u32(&empty_bar[s]), (uint32_t)(((i / S) & 1) ^ 1))) {
                     atomicExch(p.err, SPEC_E_TIMEOUT);
                     break;
                 }
                 const uint32_t fb = smem_u32(&full_bar[s]);
-                mbar_arrive_expect_tx(fb, tx);
+                mbar_arrive_expect_tx(fb, per_atom_tx * n);
                 const uint32_t a_dst = base + (uint32_t)s * p.stage_bytes;
-                const CUtensorMap *m0, *m1;
-                int r0, r1;
-                tile_rows(p, tile, m0, r0, m1, r1);
-                tma_load_2d(a_dst, m0, kb * TC_BK, r0, fb, pw);
-                tma_load_2d(a_dst + TC_A_BYTES / 2, m1, kb * TC_BK, r1, fb, pw);
-                const uint32_t b_dst = a_dst + TC_A_BYTES;
-                for (int t = 0; t < p.ntok / 16; ++t)
-                    tma_load_2d(b_dst + t * 2048, &p.xmap, kb * TC_BK, p.x_row0 + t * 16, fb, px);
+                for (int at = 0; at < n; ++at) {
+                    load_atom_a(p, tile, (kt + at) * TC_ATOM, a_dst + at * TC_ATOM_A, fb, pw);
+                    load_atom_b(p, (kt + at) * TC_ATOM, a_dst + b_off + at * p.ntok * TC_ATOM * 2, fb, px);
+                }
+                w.g += n;
+                if (sl) seg0 = w.g;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(p.ntok);
-            long long i = 0;
+            const uint32_t b_off = (uint32_t)(p.atoms * TC_ATOM_A);
+            StageWalk w(s0, s1, p.KB, p.atoms);
+            long long i = 0, seg0 = s0;
             int si = 0;
             bool ok = true;
-            long long g = s0;
-            while (ok && g < s1) {
-                const int tile = (int)(g / p.KB);
-                const long long seg_end = min(s1, (long long)(tile + 1) * p.KB);
+            uint32_t d_tmem = tmem;
+            while (ok && !w.done()) {
+                int n, tile, kt;
+                bool sf, sl;
+                w.cur(n, tile, kt, sf, sl, seg0);
                 const int buf = si & 1;
-                if (!mbar_wait(smem_u32(&acce[buf]), (uint32_t)(((si >> 1) & 1) ^ 1))) {
-                    atomicExch(p.err, SPEC_E_TIMEOUT);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(buf * p.ntok);
-                const long long seg_start = g;
-                for (; g < seg_end; ++g, ++i) {
-                    const int s = (int)(i % S);
-                    if (!mbar_wait(smem_u32(&full_bar[s]), (uint32_t)((i / S) & 1))) {
+                if (sf) {
+                    if (!mbar_wait(smem_u32(&acce[buf]), (uint32_t)(((si >> 1) & 1) ^ 1))) {
                         atomicExch(p.err, SPEC_E_TIMEOUT);
-                        ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = base + (uint32_t)s * p.stage_bytes;
-                    const uint32_t b_addr = a_addr + TC_A_BYTES;
-                    const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128(b_addr);
-#pragma unroll
-                    for (int kk = 0; kk < TC_BK / 16; ++kk)
-                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                                 (g != seg_start || kk > 0) ? 1u : 0u);
-                    mma_commit(smem_u32(&empty_bar[s]));
+                    d_tmem = tmem + (uint32_t)(buf * p.ntok);
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&accf[buf]));
-                ++si;
+                const int s = (int)(i % S);
+                if (!mbar_wait(smem_u32(&full_bar[s]), (uint32_t)((i / S) & 1))) {
+                    atomicExch(p.err, SPEC_E_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = base + (uint32_t)s * p.stage_bytes;
+                for (int at = 0; at < n; ++at) {
+                    const uint64_t ad = smem_desc_sw128(a_addr + at * TC_ATOM_A);
+                    const uint64_t bd = smem_desc_sw128(a_addr + b_off + at * p.ntok * TC_ATOM * 2);
+#pragma unroll
+                    for (int kk = 0; kk < TC_ATOM / 16; ++kk)
+                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                 (!sf || at > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&empty_bar[s]));
+                ++i;
+                w.g += n;
+                if (sl) {
+                    mma_commit(smem_u32(&accf[buf]));
+                    ++si;
+                    seg0 = w.g;
+                }
             }
             // make sure no MMA is still writing tensor memory before it is freed
             mma_commit(smem_u32(&done_bar));
@@ -354,17 +416,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 epi_bar();
                 if (last_flag) {
                     __threadfence();
+                    // contributors in CTA order; the first one's slot is 1 unless its range
+                    // starts exactly at the tile, every later one starts inside the tile
+                    const int wc_lo = (range_start(T, G, c_lo) >= tile_k0) ? 0 : 1;
                     for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
                         float acc[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-                        for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            const int wc = (range_start(T, G, cc) >= tile_k0) ? 0 : 1;
-                            const float* src = p.partial + (((size_t)cc * 2 + wc) * TC_BM + row) * p.ntok + c0;
+                        for (int cb = c_lo; cb <= c_hi; cb += 8) {
+                            float4 part[8][4];
 #pragma unroll
-                            for (int j = 0; j < 16; j += 4) {
-                                const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src + j));
-                                acc[j] += t4.x; acc[j + 1] += t4.y; acc[j + 2] += t4.z; acc[j + 3] += t4.w;
+                            for (int u = 0; u < 8; ++u) {
+                                const int cc = cb + u;
+                                if (cc <= c_hi) {
+                                    const int wc = cc == c_lo ? wc_lo : 0;
+                                    const float* src = p.partial + (((size_t)cc * 2 + wc) * TC_BM + row) * p.ntok + c0;
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j)
+                                        part[u][j] = __ldcg(reinterpret_cast<const float4*>(src + 4 * j));
+                                }
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                if (cb + u <= c_hi) {
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        acc[4 * j] += part[u][j].x; acc[4 * j + 1] += part[u][j].y;
+                                        acc[4 * j + 2] += part[u][j].z; acc[4 * j + 3] += part[u][j].w;
+                                    }
+                                }
                             }
                         }
 #pragma unroll
@@ -544,11 +624,19 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, 
     p.x_row0 = (int)(off / ((size_t)Kdim * 2));
     p.xmap = *xm;
     p.gid = gid;
-    p.KB = Kdim / TC_BK;
+    p.KB = Kdim / TC_ATOM;
     p.ntok = (M + 15) & ~15;
     p.M = M;
-    p.stage_bytes = TC_A_BYTES + p.ntok * TC_BK * 2;
-    p.stages = std::min(TC_MAX_STAGES, (TC_SMEM_MAX - 1024 - TC_XBYTES - 256) / p.stage_bytes);
+    // the widest stage (most K atoms) that still leaves TC_MIN_STAGES ring slots; the
+    // stream-K split is in atoms, so this choice changes no result bit
+    const int budget = TC_SMEM_MAX - 1024 - TC_XBYTES - 256;
+    const int per_atom = TC_ATOM_A + p.ntok * TC_ATOM * 2;
+    p.atoms = 1;
+    for (int a = TC_MAX_ATOMS; a > 1; a >>= 1)
+        if (budget / (a * per_atom) >= TC_MIN_STAGES) { p.atoms = a; break; }
+    p.stage_bytes = p.atoms * per_atom;
+    p.stages = std::min(TC_MAX_STAGES, budget / p.stage_bytes);
+    if (p.stages < 2) return set_error(SPEC_E_RANGE, "GEMM stage does not fit in shared memory");
     p.hq = m.n_q_heads;
     p.hkv = m.n_kv_heads;
     p.partial = t->partial;
