@@ -65,7 +65,6 @@ template <typename T>
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_split_kernel(const AttnArgs a) {
     extern __shared__ __align__(128) uint8_t sm_raw[];
     __shared__ __align__(8) uint64_t bar;
-    __shared__ int last_flag;
     const int hd = a.hd, split = a.split_keys;
     T* Ks = reinterpret_cast<T*>(sm_raw);                               // [split][hd]
     T* Vs = Ks + (size_t)split * hd;                                    // [split][hd]
@@ -171,53 +170,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_split_kernel(const AttnAr
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 if (e < dpl) dst[e] = o[e];
-            if (lane == 0) a.part_ml[pbase + rt + ri] = make_float2(mx, l);
+            if (lane == 0) a.part_ml[pbase + rt + ri] = make_float2(mx * 1.4426950408889634f, l);
         }
     }
-    if (!ok) {
-        // The copy never completed: give it one more bounded wait, leave the outputs of this
-        // head unwritten and return.
-        mbar_wait(bar_u, 0);
-        return;
-    }
-    // ---- arrival; the last split of this (sequence, kv head) combines ----
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int nsplit = (Ltot + split - 1) / split;
-        const int prev = atomicAdd(a.att_cnt + b * a.hkv + g, 1);
-        last_flag = prev == nsplit - 1;
-        if (last_flag) a.att_cnt[b * a.hkv + g] = 0;
-    }
-    __syncthreads();
-    if (!last_flag) return;
-    __threadfence();
-    const size_t cbase = ((size_t)b * a.hkv + g) * a.n_chunks;
-    T* O = static_cast<T*>(a.o);
-    for (int r = warp; r < R; r += ATT_THREADS / 32) {
-        const int t = r / G, hh = r - t * G;
-        const int pos = L0 + t;
-        const int ns = pos / split + 1;
-        float mt = -INFINITY;
-        for (int c = 0; c < ns; ++c) mt = fmaxf(mt, __ldcg(&a.part_ml[(cbase + c) * R + r].x));
-        float o[8], l = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = 0.0f;
-        for (int c = 0; c < ns; ++c) {
-            const float2 ml = __ldcg(&a.part_ml[(cbase + c) * R + r]);
-            const float w = expf(ml.x - mt);
-            const float* src = a.part_o + ((cbase + c) * R + r) * hd + lane * dpl;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (e < dpl) o[e] = fmaf(w, __ldcg(src + e), o[e]);
-            l = fmaf(w, ml.y, l);
-        }
-        const size_t m = (size_t)b * a.T + t;
-        T* dst = O + (m * a.hq + (size_t)g * G + hh) * hd + lane * dpl;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (e < dpl) dst[e] = from_f32<T>(o[e] / l);
-    }
+    if (!ok) mbar_wait(bar_u, 0);   // the copy never completed: one more bounded wait, then return
 }
 
 
@@ -255,7 +211,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnArgs a) {
     extern __shared__ __align__(128) uint8_t sm_raw[];
     __shared__ float wmax[4][MMA_RT], wsum[4][MMA_RT];
-    __shared__ int last_flag;
     __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm_raw);
     __nv_bfloat16* Vs = Ks + MMA_SPLIT * MMA_PITCH;
     __nv_bfloat16* Qs = Vs + MMA_SPLIT * MMA_PITCH;
@@ -440,42 +395,64 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnArgs a) {
             }
         }
     }
-    // ---- arrival; the last split of this (sequence, kv head) combines ----
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int nsplit = (Ltot + MMA_SPLIT - 1) / MMA_SPLIT;
-        const int prev = atomicAdd(a.att_cnt + b * a.hkv + g, 1);
-        last_flag = prev == nsplit - 1;
-        if (last_flag) a.att_cnt[b * a.hkv + g] = 0;
-    }
-    __syncthreads();
-    if (!last_flag) return;
-    __threadfence();
+}
+
+// Combine of the splits of every query row: one warp per row; the row's splits
+// 0..pos/SPLIT are reduced in a fixed order (lanes over splits for the max and the sum,
+// then the output in split order), so the result depends only on the row's position.
+template <typename T>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int G = a.hq / a.hkv;
+    const int R = a.T * G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 4 + warp;
+    const int g = blockIdx.y, b = blockIdx.z;
+    if (r >= R) return;
+    const int slot = a.seq_ids[b];
+    const int t = r / G, hh = r - t * G;
+    const int ns = (a.seq_len[slot] + t) / a.split_keys + 1;
     const size_t cbase = ((size_t)b * a.hkv + g) * a.n_chunks;
-    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o);
-    for (int r = warp; r < R; r += 4) {
-        const int t = r / G, hh = r - t * G;
-        const int ns = (L0 + t) / MMA_SPLIT + 1;
-        float mt = -INFINITY;
-        for (int c = 0; c < ns; ++c) mt = fmaxf(mt, __ldcg(&a.part_ml[(cbase + c) * R + r].x));
-        float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        float l = 0.0f;
-        for (int c = 0; c < ns; ++c) {
-            const float2 ml = __ldcg(&a.part_ml[(cbase + c) * R + r]);
-            const float w = exp2f(ml.x - mt);
-            const float4 src = __ldcg(reinterpret_cast<const float4*>(a.part_o + ((cbase + c) * R + r) * 128 + lane * 4));
-            o[0] = fmaf(w, src.x, o[0]);
-            o[1] = fmaf(w, src.y, o[1]);
-            o[2] = fmaf(w, src.z, o[2]);
-            o[3] = fmaf(w, src.w, o[3]);
-            l = fmaf(w, ml.y, l);
-        }
-        const size_t m = (size_t)b * a.T + t;
-        __nv_bfloat16* dst = O + (m * a.hq + (size_t)g * G + hh) * 128 + lane * 4;
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[0] / l, o[1] / l);
-        *reinterpret_cast<uint32_t*>(dst + 2) = pack_bf16(o[2] / l, o[3] / l);
+    float mloc = -INFINITY;
+    for (int c = lane; c < ns; c += 32) mloc = fmaxf(mloc, a.part_ml[(cbase + c) * R + r].x);
+    const float mt = warp_max(mloc);
+    float lloc = 0.0f;
+    for (int c = lane; c < ns; c += 32) {
+        const float2 ml = a.part_ml[(cbase + c) * R + r];
+        lloc = fmaf(exp2f(ml.x - mt), ml.y, lloc);
     }
+    const float l = warp_sum(lloc);
+    const int dpl = a.hd / 32;
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = 0.0f;
+    for (int c0 = 0; c0 < ns; c0 += 8) {
+        float w[8];
+        float v[8][8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u;
+            w[u] = 0.0f;
+            if (c < ns) {
+                w[u] = exp2f(a.part_ml[(cbase + c) * R + r].x - mt);
+                const float* src = a.part_o + ((cbase + c) * R + r) * a.hd + lane * dpl;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[u][e] = e < dpl ? src[e] : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (c0 + u < ns) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(w[u], v[u][e], o[e]);
+            }
+    }
+    const size_t m = (size_t)b * a.T + t;
+    T* dst = static_cast<T*>(a.o) + (m * a.hq + (size_t)g * G + hh) * a.hd + lane * dpl;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        if (e < dpl) dst[e] = from_f32<T>(o[e] / l);
 }
 
 constexpr size_t MMA_SMEM = sizeof(__nv_bfloat16) * ((size_t)3 * 64 * MMA_PITCH + (size_t)MMA_RT * MMA_PPITCH);
@@ -487,15 +464,23 @@ size_t attn_smem(int hd, int esize) {
 
 int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, cudaStream_t st) {
     const int nsplit = (max_len_after + a.split_keys - 1) / a.split_keys;
+    const int G = a.hq / a.hkv;
+    const dim3 cgrid((a.T * G + 3) / 4, a.hkv, B);
     if (use_mma_path(a.hd, c.esize)) {
         attn_mma_kernel<<<dim3(nsplit, a.hkv, B), 128, MMA_SMEM, st>>>(a);
-        return 1;
+        attn_combine_kernel<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a);
+        return 2;
     }
     const size_t smem = attn_smem(a.hd, c.esize);
     const dim3 grid(nsplit, a.hkv, B);
-    if (c.cfg.dtype == SPEC_BF16) attn_split_kernel<__nv_bfloat16><<<grid, ATT_THREADS, smem, st>>>(a);
-    else attn_split_kernel<float><<<grid, ATT_THREADS, smem, st>>>(a);
-    return 1;
+    if (c.cfg.dtype == SPEC_BF16) {
+        attn_split_kernel<__nv_bfloat16><<<grid, ATT_THREADS, smem, st>>>(a);
+        attn_combine_kernel<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a);
+    } else {
+        attn_split_kernel<float><<<grid, ATT_THREADS, smem, st>>>(a);
+        attn_combine_kernel<float><<<cgrid, 128, 0, st>>>(a);
+    }
+    return 2;
 }
 
 int attention_set_smem_limits(int hd) {

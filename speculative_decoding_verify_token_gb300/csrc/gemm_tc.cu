@@ -35,6 +35,9 @@ namespace sv {
 #ifndef TC_MIN_STAGES
 #define TC_MIN_STAGES 3         // fewest pipeline stages a launch may use
 #endif
+#ifndef TC_CTAS_PER_SM
+#define TC_CTAS_PER_SM 1        // resident GEMM CTAs per SM (shared memory split between them)
+#endif
 constexpr int TC_THREADS = 192;
 constexpr int TC_BM = 128;
 constexpr int TC_ATOM = 64;                          // K elements per atom = accumulation unit
@@ -44,7 +47,7 @@ constexpr int TC_MAX_STAGES = 8;
 constexpr int TC_CW = 16;                           // epilogue column chunk
 constexpr int TC_XPITCH = TC_CW + 1;
 constexpr int TC_XBYTES = TC_BM * TC_XPITCH * 4;
-constexpr int TC_SMEM_MAX = 226 * 1024;   // dynamic bytes (static barriers stay below the 227 KB cap)
+constexpr int TC_SMEM_MAX = (TC_CTAS_PER_SM == 1 ? 226 : 112) * 1024;   // dynamic bytes per CTA
 
 struct TcParams {
     CUtensorMap wmap[3];
@@ -60,6 +63,16 @@ struct TcParams {
     int* err;
     EpiArgs e;
 };
+
+#ifdef TC_TRACE
+// Per-CTA timeline of the last launch of each GEMM kind (profiling builds only):
+// [gid][cta][0 entry, 1 set-up done, 2 first stage ready, 3 last MMA issued,
+//            4 last accumulator ready, 5 exit]
+__device__ unsigned long long g_tc_trace[5][1024][6];
+#define TC_STAMP(i) g_tc_trace[p.gid][blockIdx.x][i] = globaltimer_ns()
+#else
+#define TC_STAMP(i) ((void)0)
+#endif
 
 // ---- PTX wrappers --------------------------------------------------------------------------
 
@@ -210,7 +223,7 @@ __device__ __forceinline__ void epi_chunk(const TcParams& p, const float* xs, in
     }
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[TC_MAX_STAGES], empty_bar[TC_MAX_STAGES];
     __shared__ __align__(8) uint64_t accf[2], acce[2], done_bar;
@@ -218,6 +231,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     __shared__ int last_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) TC_STAMP(0);
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     float* xs = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)) + p.stages * p.stage_bytes);
     const int G = gridDim.x, cta = blockIdx.x;
@@ -249,6 +263,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_sh;
+    if (threadIdx.x == 0) TC_STAMP(1);
     pdl_launch_dependents();
 
     if (warp == 0) {
@@ -336,6 +351,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     ok = false;
                     break;
                 }
+                if (i == 0) TC_STAMP(2);
                 tc_fence_after();
                 const uint32_t a_addr = base + (uint32_t)s * p.stage_bytes;
                 for (int at = 0; at < n; ++at) {
@@ -355,6 +371,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     seg0 = w.g;
                 }
             }
+            TC_STAMP(3);
             // make sure no MMA is still writing tensor memory before it is freed
             mma_commit(smem_u32(&done_bar));
             mbar_wait(smem_u32(&done_bar), 0);
@@ -378,6 +395,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 break;
             }
             tc_fence_after();
+            if (etid == 0 && seg_end == s1) TC_STAMP(4);
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.ntok);
             if (full_tile) {
                 for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
@@ -423,10 +441,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         float acc[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-                        for (int cb = c_lo; cb <= c_hi; cb += 8) {
-                            float4 part[8][4];
+                        for (int cb = c_lo; cb <= c_hi; cb += 4) {
+                            float4 part[4][4];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
+                            for (int u = 0; u < 4; ++u) {
                                 const int cc = cb + u;
                                 if (cc <= c_hi) {
                                     const int wc = cc == c_lo ? wc_lo : 0;
@@ -437,7 +455,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                 }
                             }
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
+                            for (int u = 0; u < 4; ++u) {
                                 if (cb + u <= c_hi) {
 #pragma unroll
                                     for (int j = 0; j < 4; ++j) {
@@ -463,6 +481,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x == 0) TC_STAMP(5);
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(ncols) : "memory");
 }
@@ -545,7 +564,7 @@ int tc_create(Ctx& c) {
     if (rc == SPEC_OK) rc = make_map(&t->xn, c.Xn, c.Mmax, d, 16);
     if (rc == SPEC_OK) rc = make_map(&t->xo, c.O, c.Mmax, qd, 16);
     if (rc == SPEC_OK) rc = make_map(&t->xh, c.H, c.Mmax, F, 16);
-    t->grid = c.num_sms;
+    t->grid = c.num_sms * TC_CTAS_PER_SM;
     const int max_tiles = (int)std::max<uint64_t>({V / 128, F / 64, d / 128, qd / 128 + 2 * kvd / 128});
     if (rc == SPEC_OK) {
         void *a = nullptr, *b = nullptr, *e = nullptr;
@@ -585,6 +604,12 @@ void tc_destroy(Ctx& c) {
     c.tc = nullptr;
     c.use_tc = false;
 }
+
+#ifdef TC_TRACE
+extern "C" int spec_debug_tc_trace(unsigned long long* out) {
+    return cudaMemcpyFromSymbol(out, g_tc_trace, sizeof(g_tc_trace)) == cudaSuccess ? 0 : -6;
+}
+#endif
 
 int tc_error_word(Ctx& c, int* out) {
     if (!c.tc) { *out = 0; return SPEC_OK; }
