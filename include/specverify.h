@@ -158,7 +158,7 @@ typedef struct spec_ctx spec_ctx;
 
 /* Create a context bound to `stream` (cudaStream_t as void*): allocates the KV pool,
  * activations and workspaces on the current device.  SPEC_E_INVAL on a bad shape
- * (head_dim a multiple of 32 and <= 256, d_model / ffn_dim / heads*head_dim multiples of 8,
+ * (head_dim a multiple of 32 and <= 256, d_model <= 8192, d_model / ffn_dim / heads*head_dim multiples of 8,
  * n_q_heads a multiple of n_kv_heads), SPEC_E_NOMEM when an allocation fails. */
 int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* limits, void* stream, spec_ctx** out);
 

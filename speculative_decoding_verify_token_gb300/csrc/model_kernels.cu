@@ -8,6 +8,28 @@
 
 namespace sv {
 
+// 4 consecutive elements of T as floats / stored from floats.
+template <typename T> struct Quad;
+template <> struct Quad<float> {
+    __device__ __forceinline__ static float4 load(const float* p) { return *reinterpret_cast<const float4*>(p); }
+    __device__ __forceinline__ static void store(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+};
+template <> struct Quad<__nv_bfloat16> {
+    __device__ __forceinline__ static float4 load(const __nv_bfloat16* p) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                           __uint_as_float(u.y & 0xffff0000u));
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16* p, float4 v) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&a);
+        u.y = *reinterpret_cast<uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(p) = u;
+    }
+};
+
+
 // X[m][:] = E[tok[m]][:] in fp32; token m = b*T + t belongs to slot seq_ids[b] at
 // position seq_len[slot] + t.  Ids outside [0, V) are embedded as token 0.
 template <typename T>
@@ -27,31 +49,54 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
         tok_pos[m] = seq_len[slot] + t;
     }
     const T* row = E + (size_t)tok * d;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) X[(size_t)m * d + i] = to_f32<T>(row[i]);
+    float4* xr = reinterpret_cast<float4*>(X + (size_t)m * d);
+    for (int i = threadIdx.x; i < (d >> 2); i += blockDim.x) xr[i] = Quad<T>::load(row + 4 * i);
 }
 
-// Xn[m] = X[m] / sqrt(mean(X[m]^2) + eps) * g, stored in the model dtype.
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_VEC = 8;      // float4 per thread held in registers: d <= 8192
+
+// Xn[m] = X[m] / sqrt(mean(X[m]^2) + eps) * g, stored in the model dtype.  All loads of a
+// row are issued at once; the sum of squares is reduced in a fixed order (per thread, then
+// warp butterfly, then warps in order), so a row's result does not depend on M.
 template <typename T>
-__global__ void rmsnorm_kernel(const float* __restrict__ X, const T* __restrict__ g, T* __restrict__ Xn, int d,
-                               float eps) {
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __restrict__ X, const T* __restrict__ g,
+                                                               T* __restrict__ Xn, int d, float eps) {
     pdl_launch_dependents();
     const int m = blockIdx.x;
-    const float* x = X + (size_t)m * d;
+    const int n4 = d >> 2;
+    const float4* x4 = reinterpret_cast<const float4*>(X + (size_t)m * d);
+    float4 v[NORM_VEC];
     float ss = 0.0f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) ss += x[i] * x[i];
-    __shared__ float red[32];
+#pragma unroll
+    for (int j = 0; j < NORM_VEC; ++j) {
+        const int i = threadIdx.x + NORM_THREADS * j;
+        v[j] = i < n4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < NORM_VEC; ++j) {
+        ss = fmaf(v[j].x, v[j].x, ss);
+        ss = fmaf(v[j].y, v[j].y, ss);
+        ss = fmaf(v[j].z, v[j].z, ss);
+        ss = fmaf(v[j].w, v[j].w, ss);
+    }
+    __shared__ float red[NORM_THREADS / 32];
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
-        if (threadIdx.x == 0) red[0] = v;
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NORM_THREADS / 32; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+#pragma unroll
+    for (int j = 0; j < NORM_VEC; ++j) {
+        const int i = threadIdx.x + NORM_THREADS * j;
+        if (i < n4) {
+            const float4 gg = Quad<T>::load(g + 4 * i);
+            Quad<T>::store(Xn + (size_t)m * d + 4 * i,
+                           make_float4(v[j].x * inv * gg.x, v[j].y * inv * gg.y, v[j].z * inv * gg.z, v[j].w * inv * gg.w));
+        }
     }
-    __syncthreads();
-    const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        Xn[(size_t)m * d + i] = from_f32<T>(x[i] * inv * to_f32<T>(g[i]));
 }
 
 // table[pos][j] = (cos, sin)(pos * theta^(-2j/hd)), evaluated in double precision.
@@ -101,7 +146,7 @@ void launch_embed(const Ctx& c, int M, int T, cudaStream_t st) {
 }
 
 void launch_rmsnorm(const Ctx& c, const float* X, const void* g, void* Xn, int M, cudaStream_t st) {
-    const int threads = c.cfg.d_model >= 1024 ? 512 : 256;
+    const int threads = NORM_THREADS;
     if (c.cfg.dtype == SPEC_BF16)
         rmsnorm_kernel<__nv_bfloat16><<<M, threads, 0, st>>>(X, static_cast<const __nv_bfloat16*>(g),
                                                              static_cast<__nv_bfloat16*>(Xn), c.cfg.d_model,

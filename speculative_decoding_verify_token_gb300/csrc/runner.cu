@@ -347,6 +347,7 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
     if (m.n_layers < 1 || m.d_model < 8 || m.d_model % 8 || m.n_q_heads < 1 || m.n_kv_heads < 1 ||
         m.n_q_heads % m.n_kv_heads || m.head_dim < 32 || m.head_dim % 32 || m.head_dim > 256 ||
         (m.n_q_heads * m.head_dim) % 8 || m.ffn_dim < 8 || m.ffn_dim % 8 || m.vocab < 2 || m.vocab % 2 ||
+        m.d_model > 8192 ||
         !(m.rope_theta > 0.0f) || !(m.rms_eps >= 0.0f) || (m.dtype != SPEC_F32 && m.dtype != SPEC_BF16))
         return set_error(SPEC_E_INVAL, "bad model shape");
     spec_ctx_limits lim = *limits;

@@ -35,14 +35,16 @@ namespace sv {
 
 constexpr int VT_WARPS = 8;
 constexpr int VT_THREADS = VT_WARPS * 32;
-constexpr int VT_BLOCKS_PER_SM = 3;
-constexpr int VS_UNROLL = 8;                         // 16-byte loads in flight per lane
+constexpr int VT_BLOCKS_PER_SM = 2;
+constexpr int VS_UNROLL = 8;                         // 16-byte loads per lane per iteration (x2 in flight)
 constexpr int VT_CHUNK_QUANTUM = 1024;               // chunk sizes are multiples of this
 constexpr int LISTN = 32;
 constexpr int VT_TARGET_ITEMS = 4096;
 constexpr int VT_MAX_CHUNKS = 128;
 constexpr int VT_MAX_K = 64;
-constexpr int VT_CAND_CAP = 256;          // per-warp candidate buffer (entries)
+// per-warp candidate buffer: a flush leaves < 32 entries and one iteration adds at most
+// 32 * 4 * VS_UNROLL, so it never overflows
+constexpr int VT_CAND_CAP = 32 + 32 * 4 * 8;
 
 enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
 
@@ -157,38 +159,6 @@ __device__ __forceinline__ void flush_candidates(float& lv, int& lid, const floa
         warp_merge_desc(lv, lid, v, id, lane);
     }
     __syncwarp();
-}
-
-// Exact path for a stage whose candidates overflowed the buffer (e.g. many equal values):
-// lanes offer one element per round, tested exactly against the running k-th entry.
-__device__ __noinline__ void exact_rounds(const float4 (&x)[VS_UNROLL], int start, float lb, float& lv,
-                                          int& lid, float* cv, int* ci, int& ccount, int k, int lane) {
-    for (int j = 0; j < VS_UNROLL; ++j) {
-        for (int c = 0; c < 4; ++c) {
-            const float thr_v = __shfl_sync(FULL, lv, k - 1);
-            const int thr_id = __shfl_sync(FULL, lid, k - 1);
-            float4 xj = x[0];
-#pragma unroll
-            for (int q = 1; q < VS_UNROLL; ++q)
-                if (q == j) xj = x[q];
-            const float xc = pick4(xj, c);
-            const int id = start + 4 * (lane + 32 * j) + c;
-            const bool has = xc >= lb && better(xc, id, thr_v, thr_id);
-            const unsigned bal = __ballot_sync(FULL, has);
-            if (bal == 0) continue;
-            if (ccount + 32 > VT_CAND_CAP) {
-                flush_candidates(lv, lid, cv, ci, ccount, lane);
-                ccount = 0;
-            }
-            if (has) {
-                const int pos = ccount + __popc(bal & ((1u << lane) - 1u));
-                cv[pos] = xc;
-                ci[pos] = id;
-            }
-            ccount += __popc(bal);
-            __syncwarp();
-        }
-    }
 }
 
 // Truncated distribution of a merged row list (lane j = j-th best), written to rd_*.
@@ -372,9 +342,81 @@ __device__ void finish_row(const VerifyParams& p, int row, int lane) {
 
 
 // One warp streams one (row, chunk) work item at a time: coalesced 16-byte streaming loads,
-// VS_UNROLL of them in flight per lane, several CTAs per SM so that enough warps hide the
-// HBM latency.  Per iteration of 1024 elements the common path is the lane maximum and one
-// vote against the running cut; only lanes whose maximum reaches it look at elements.
+// two register tiles of VS_UNROLL float4 per lane so that the next 4 KB of the row is in
+// flight while the current 4 KB is examined, 2 CTAs of 8 warps per SM.  Per 1024 elements
+// the common path is a lane maximum (per float4 first) and one vote against the running
+// cut; only the float4s whose maximum reaches the cut are looked at element by element.
+struct TopkState {
+    float lv, lb, published;
+    int lid, ccount;
+};
+
+__device__ __forceinline__ void examine_tile(const VerifyParams& p, const float4 (&x)[VS_UNROLL], int i0, int s0,
+                                             bool first, unsigned rb_key, unsigned* rb_ptr, TopkState& st,
+                                             float* cbuf_v, int* cbuf_id, int* ccnt, int lane) {
+    const int k = p.top_k;
+    float mu[VS_UNROLL];
+#pragma unroll
+    for (int u = 0; u < VS_UNROLL; ++u) mu[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+    float mx = mu[0];
+#pragma unroll
+    for (int u = 1; u < VS_UNROLL; ++u) mx = fmaxf(mx, mu[u]);
+    if (first) {
+        // k distinct elements reach the k-th largest lane maximum: a lower bound of the
+        // chunk's (and the row's) k-th best.
+        float m = mx;
+        int dummy = lane;
+        warp_sort_desc(m, dummy, lane);
+        st.lb = __shfl_sync(FULL, m, k - 1);
+        if (lane == 0 && st.lb > -INFINITY) atomicMax(rb_ptr, float_key(st.lb));
+        st.published = st.lb;
+    }
+    st.lb = fmaxf(st.lb, key_float(rb_key));
+    const float cut = fmaxf(st.lb, __shfl_sync(FULL, st.lv, k - 1));
+    if (__any_sync(FULL, mx >= cut)) {
+        // value test only: an entry equal to the k-th value with a larger id is a harmless
+        // extra for the exact merge
+        if (mx >= cut) {
+#pragma unroll
+            for (int u = 0; u < VS_UNROLL; ++u) {
+                if (mu[u] >= cut) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float xc = pick4(x[u], q);
+                        if (xc >= cut) {
+                            const int pos = atomicAdd(ccnt, 1);
+                            cbuf_v[pos] = xc;
+                            cbuf_id[pos] = s0 + 4 * (i0 + lane + 32 * u) + q;
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        st.ccount = *reinterpret_cast<volatile int*>(ccnt);
+    }
+    if (st.ccount >= 32 || (st.ccount > 0 && __shfl_sync(FULL, st.lid, k - 1) == SENT_ID)) {
+        flush_candidates(st.lv, st.lid, cbuf_v, cbuf_id, st.ccount, lane);
+        st.ccount = 0;
+        if (lane == 0) *ccnt = 0;
+        __syncwarp();
+    }
+    const float kth = __shfl_sync(FULL, st.lv, k - 1);
+    if (kth > st.published) {
+        if (lane == 0) atomicMax(rb_ptr, float_key(kth));
+        st.published = kth;
+        st.lb = fmaxf(st.lb, kth);
+    }
+}
+
+__device__ __forceinline__ void load_tile(float4 (&x)[VS_UNROLL], const float4* src, int i0, int n4, int lane) {
+#pragma unroll
+    for (int u = 0; u < VS_UNROLL; ++u) {
+        const int idx = i0 + lane + 32 * u;
+        x[u] = idx < n4 ? __ldcs(src + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+}
+
 __global__ void __launch_bounds__(VT_THREADS, VT_BLOCKS_PER_SM) verify_kernel(const VerifyParams p) {
     __shared__ float cand_v[VT_WARPS][VT_CAND_CAP];
     __shared__ int cand_id[VT_WARPS][VT_CAND_CAP];
@@ -384,11 +426,12 @@ __global__ void __launch_bounds__(VT_THREADS, VT_BLOCKS_PER_SM) verify_kernel(co
     const int warp = threadIdx.x >> 5;
     float* cbuf_v = cand_v[warp];
     int* cbuf_id = cand_id[warp];
-    if (lane == 0) ccnt_s[warp] = 0;
+    int* ccnt = &ccnt_s[warp];
+    if (lane == 0) *ccnt = 0;
     __syncwarp();
-    const int k = p.top_k;
     int pref = 0;
     if (lane == 0) pref = atomicAdd(p.work, 1);
+    constexpr int STEP = 32 * VS_UNROLL;
 
     while (true) {
         // next needed work item (the index after it is fetched now and used next time)
@@ -410,82 +453,24 @@ __global__ void __launch_bounds__(VT_THREADS, VT_BLOCKS_PER_SM) verify_kernel(co
         const int n4 = s1 > s0 ? (s1 - s0) >> 2 : 0;
         unsigned* rb_ptr = p.row_bound + row;
 
-        float lv = -INFINITY, lb = -INFINITY, published = -INFINITY;
-        int lid = SENT_ID;
-        int ccount = 0;
-        for (int i0 = 0; i0 < n4; i0 += 32 * VS_UNROLL) {
-            const unsigned rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
-            float4 x[VS_UNROLL];
-#pragma unroll
-            for (int u = 0; u < VS_UNROLL; ++u) {
-                const int idx = i0 + lane + 32 * u;
-                x[u] = idx < n4 ? __ldcs(src + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
-            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < VS_UNROLL; ++u) {
-                m0 = fmaxf(m0, x[u].x); m1 = fmaxf(m1, x[u].y); m2 = fmaxf(m2, x[u].z); m3 = fmaxf(m3, x[u].w);
-            }
-            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-            if (i0 == 0) {
-                // k distinct elements reach the k-th largest lane maximum: a lower bound of
-                // the chunk's (and the row's) k-th best.
-                float m = mx;
-                int dummy = lane;
-                warp_sort_desc(m, dummy, lane);
-                lb = __shfl_sync(FULL, m, k - 1);
-                if (lane == 0 && lb > -INFINITY) atomicMax(rb_ptr, float_key(lb));
-                published = lb;
-            }
-            lb = fmaxf(lb, key_float(rb_key));
-            const float thr_v = __shfl_sync(FULL, lv, k - 1);
-            const float cut = fmaxf(lb, thr_v);
-            if (__any_sync(FULL, mx >= cut)) {
-                // value test only: an entry equal to the k-th value with a larger id is a
-                // harmless extra for the exact merge
-                const int pre = ccount;
-                if (mx >= cut) {
-#pragma unroll
-                    for (int u = 0; u < VS_UNROLL; ++u) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float xc = pick4(x[u], q);
-                            if (xc >= cut) {
-                                const int pos = atomicAdd(&ccnt_s[warp], 1);
-                                if (pos < VT_CAND_CAP) {
-                                    cbuf_v[pos] = xc;
-                                    cbuf_id[pos] = s0 + 4 * (i0 + lane + 32 * u) + q;
-                                }
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                ccount = *reinterpret_cast<volatile int*>(&ccnt_s[warp]);
-                if (ccount > VT_CAND_CAP) {
-                    ccount = pre;
-                    exact_rounds(x, s0 + 4 * i0, lb, lv, lid, cbuf_v, cbuf_id, ccount, k, lane);
-                }
-                __syncwarp();
-                if (lane == 0) ccnt_s[warp] = ccount;
-                __syncwarp();
-            }
-            if (ccount >= 32 || (ccount > 0 && __shfl_sync(FULL, lid, k - 1) == SENT_ID)) {
-                flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
-                ccount = 0;
-                if (lane == 0) ccnt_s[warp] = 0;
-                __syncwarp();
-            }
-            const float kth = __shfl_sync(FULL, lv, k - 1);
-            if (kth > published) {
-                if (lane == 0) atomicMax(rb_ptr, float_key(kth));
-                published = kth;
-                lb = fmaxf(lb, kth);
-            }
+        TopkState st;
+        st.lv = -INFINITY; st.lb = -INFINITY; st.published = -INFINITY; st.lid = SENT_ID; st.ccount = 0;
+        float4 xa[VS_UNROLL], xb[VS_UNROLL];
+        if (n4 > 0) load_tile(xa, src, 0, n4, lane);
+        for (int i0 = 0; i0 < n4; i0 += 2 * STEP) {
+            unsigned rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
+            if (i0 + STEP < n4) load_tile(xb, src, i0 + STEP, n4, lane);
+            examine_tile(p, xa, i0, s0, i0 == 0, rb_key, rb_ptr, st, cbuf_v, cbuf_id, ccnt, lane);
+            if (i0 + STEP >= n4) break;
+            rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
+            if (i0 + 2 * STEP < n4) load_tile(xa, src, i0 + 2 * STEP, n4, lane);
+            examine_tile(p, xb, i0 + STEP, s0, false, rb_key, rb_ptr, st, cbuf_v, cbuf_id, ccnt, lane);
         }
-        if (ccount > 0) {
-            flush_candidates(lv, lid, cbuf_v, cbuf_id, ccount, lane);
-            if (lane == 0) ccnt_s[warp] = 0;
+        float lv = st.lv;
+        int lid = st.lid;
+        if (st.ccount > 0) {
+            flush_candidates(lv, lid, cbuf_v, cbuf_id, st.ccount, lane);
+            if (lane == 0) *ccnt = 0;
             __syncwarp();
         }
         // scalar head / tail of the row
@@ -700,3 +685,4 @@ extern "C" int spec_sample_logits(int R, int V, const float* logits, const float
     prm.out_tokens = out_tokens;
     return launch_verify(prm, pl, workspace, static_cast<cudaStream_t>(stream));
 }
+
