@@ -109,6 +109,33 @@ int spec_verify_logits(int B, int K, int V,
  * distribution q ([MTP-fixes] "Truncation has to match on both sides").
  * out_tokens [R] (device).  Workspace rules as for spec_verify_logits.
  * ---------------------------------------------------------------------------------- */
+/* ------------------------------------------------------------------------------------
+ * spec_verify_logits without a caller workspace, for callers that cannot allocate
+ * device memory: for example code that runs while a CUDA graph is being captured (where
+ * cudaMalloc is not allowed), a serving loop that must not stall on the allocator,
+ * or a host that owns a fixed device-memory budget and forbids new allocations.  No
+ * counterpart on the pages: this is an interface convenience of this library.
+ *
+ * Same arguments and outputs as spec_verify_logits, minus the workspace.  The scratch is
+ * one fixed array of spec_verify_logits_noalloc_max_bytes() (8 MiB) compiled into the
+ * library, present on every GPU that loads it until the process exits; sizes whose
+ * workspace (spec_verify_logits_workspace_bytes) exceeds it are rejected with
+ * SPEC_E_RANGE.  The call allocates nothing: no cudaMalloc/cudaFree or allocating library
+ * routine.  The first call on a device looks up the array's device address once
+ * (cudaGetSymbolAddress, with that device current) and caches it: make that first call
+ * before any stream capture.  Every call shares the one array (what must start at zero is
+ * cleared on the stream at each call), so calls that overlap on the GPU -- on different
+ * streams, or from several host threads -- race and must be serialised by the caller.
+ * ---------------------------------------------------------------------------------- */
+size_t spec_verify_logits_noalloc_max_bytes(void);
+
+int spec_verify_logits_noalloc(int B, int K, int V,
+                               const float* target_logits, const float* draft_logits,
+                               const int32_t* draft_tokens, const int32_t* draft_len,
+                               const float* uniforms, const spec_sampling* sampling /* host */,
+                               int32_t* accepted_len, int32_t* next_token,
+                               int32_t* out_ids, float* out_probs, int32_t* seq_status, void* stream);
+
 size_t spec_sample_logits_workspace_bytes(int R, int V);
 
 int spec_sample_logits(int R, int V, const float* logits, const float* uniforms,

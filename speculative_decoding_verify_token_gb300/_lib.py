@@ -66,6 +66,9 @@ SIGNATURES = {
     "spec_verify_logits": (c_int, [c_int, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp,
                                    ctypes.POINTER(SpecSampling), c_vp, c_vp, c_vp, c_vp, c_vp,
                                    c_vp, c_size, c_vp]),
+    "spec_verify_logits_noalloc_max_bytes": (c_size, []),
+    "spec_verify_logits_noalloc": (c_int, [c_int, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                           ctypes.POINTER(SpecSampling), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "spec_sample_logits_workspace_bytes": (c_size, [c_int, c_int]),
     "spec_sample_logits": (c_int, [c_int, c_int, c_vp, c_vp, ctypes.POINTER(SpecSampling), c_vp,
                                    c_vp, c_size, c_vp]),

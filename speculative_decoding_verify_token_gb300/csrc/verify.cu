@@ -27,6 +27,7 @@
 #include <cstring>
 #include <cmath>
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "host_util.h"
@@ -686,3 +687,53 @@ extern "C" int spec_sample_logits(int R, int V, const float* logits, const float
     return launch_verify(prm, pl, workspace, static_cast<cudaStream_t>(stream));
 }
 
+// ---- allocation-free variant -------------------------------------------------------------
+//
+// Scratch for spec_verify_logits_noalloc: a fixed-size array that every GPU loading the
+// library holds for the life of the process.  Host code may not pass `g_noalloc_scratch`
+// to a kernel (on the host the name is only a stand-in); the device address is looked up
+// once per device with cudaGetSymbolAddress and cached.
+namespace sv {
+constexpr size_t NOALLOC_SCRATCH_BYTES = 8u << 20;      // 8 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+constexpr int NOALLOC_MAX_DEVICES = 64;
+static void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+static std::mutex g_noalloc_mu;
+
+static int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return set_error(SPEC_E_RANGE, "device ordinal %d too large", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return set_error(SPEC_E_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SPEC_OK;
+}
+}  // namespace sv
+
+extern "C" size_t spec_verify_logits_noalloc_max_bytes(void) { return sv::NOALLOC_SCRATCH_BYTES; }
+
+extern "C" int spec_verify_logits_noalloc(int B, int K, int V, const float* target_logits, const float* draft_logits,
+                                          const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
+                                          const spec_sampling* sampling, int32_t* accepted_len, int32_t* next_token,
+                                          int32_t* out_ids, float* out_probs, int32_t* seq_status, void* stream) {
+    clear_error();
+    const size_t need = spec_verify_logits_workspace_bytes(B, K, V);
+    if (need == 0) return set_error(SPEC_E_INVAL, "bad sizes B=%d K=%d V=%d", B, K, V);
+    if (need > sv::NOALLOC_SCRATCH_BYTES)
+        return set_error(SPEC_E_RANGE, "B=%d K=%d V=%d needs %zu bytes of scratch, above the built-in %zu", B, K, V,
+                         need, sv::NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    const int rc = sv::noalloc_scratch(&scratch);
+    if (rc != SPEC_OK) return rc;
+    return sv::verify_into(B, K, V, target_logits, draft_logits, draft_tokens, draft_len, uniforms, sampling,
+                           accepted_len, next_token, out_ids, out_probs, seq_status, scratch,
+                           sv::NOALLOC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
+}
