@@ -243,6 +243,10 @@ int spec_seq_reset(spec_ctx* ctx, int seq_id);
  * changes any result bit. */
 #define SPEC_OPT_GRAPHS 1
 #define SPEC_OPT_PDL    2
+/* SPEC_OPT_L2_PREFETCH (value 0..64, default 12): once a GEMM has issued all its loads, each
+ * of its CTAs warms L2 with this many 64-column atoms (16 KB each) of the weights it will
+ * stream first in the next GEMM of the pass; 0 disables.  Changes no result bit. */
+#define SPEC_OPT_L2_PREFETCH 3
 int spec_set_option(spec_ctx* ctx, int option, int value);
 
 /* Per-kernel-class timing of the context's passes with CUDA events recorded on its

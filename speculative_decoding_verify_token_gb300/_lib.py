@@ -52,6 +52,7 @@ class SpecCtxLimits(ctypes.Structure):
 
 SPEC_OPT_GRAPHS = 1
 SPEC_OPT_PDL = 2
+SPEC_OPT_L2_PREFETCH = 3
 SPEC_PROF_CLASSES = 8
 PROF_CLASS_NAMES = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head", "attention",
                     "verify", "other"]

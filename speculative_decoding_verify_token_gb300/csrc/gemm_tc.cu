@@ -58,6 +58,10 @@ struct TcParams {
     int stages, stage_bytes;  // ring slots; bytes per slot
     int atoms;                // most atoms per stage (stages never cross a segment end)
     int hq, hkv;
+    // L2 prefetch of the next GEMM's first weight atoms of this CTA's range (issued by the
+    // producer once its own loads are all issued)
+    CUtensorMap nwmap[3];
+    int ngid, n_ntiles, n_KB, n_atoms;       // n_atoms = 0: no prefetch
     float* partial;          // [grid][2][128][ntok]
     int* tile_cnt;           // [n_tiles], zero between launches
     int* err;
@@ -141,23 +145,33 @@ __device__ __forceinline__ int epi_any(int pred) {
 
 // ---- tile geometry --------------------------------------------------------------------------
 
-__device__ __forceinline__ void tile_rows(const TcParams& p, int tile, const CUtensorMap*& m0, int& r0,
-                                          const CUtensorMap*& m1, int& r1) {
-    if (p.gid == GEMM_QKV) {
+__device__ __forceinline__ void tile_rows_of(int gid, const CUtensorMap* maps, int hq, int hkv, int tile,
+                                             const CUtensorMap*& m0, int& r0, const CUtensorMap*& m1, int& r1) {
+    if (gid == GEMM_QKV) {
         int t = tile, w = 0;
-        if (t >= p.hq) { t -= p.hq; w = 1; if (t >= p.hkv) { t -= p.hkv; w = 2; } }
-        m0 = m1 = &p.wmap[w];
+        if (t >= hq) { t -= hq; w = 1; if (t >= hkv) { t -= hkv; w = 2; } }
+        m0 = m1 = &maps[w];
         r0 = t * TC_BM;
         r1 = r0 + 64;
-    } else if (p.gid == GEMM_GU) {
-        m0 = &p.wmap[0];
-        m1 = &p.wmap[1];
+    } else if (gid == GEMM_GU) {
+        m0 = &maps[0];
+        m1 = &maps[1];
         r0 = r1 = tile * 64;
     } else {
-        m0 = m1 = &p.wmap[0];
+        m0 = m1 = &maps[0];
         r0 = tile * TC_BM;
         r1 = r0 + 64;
     }
+}
+
+__device__ __forceinline__ void tile_rows(const TcParams& p, int tile, const CUtensorMap*& m0, int& r0,
+                                          const CUtensorMap*& m1, int& r1) {
+    tile_rows_of(p.gid, p.wmap, p.hq, p.hkv, tile, m0, r0, m1, r1);
+}
+
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
 }
 
 __device__ __forceinline__ long long range_start(long long T, int G, int c) {
@@ -321,6 +335,21 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 }
                 w.g += n;
                 if (sl) seg0 = w.g;
+            }
+            if (p.n_atoms > 0) {
+                // warm L2 with the first atoms this CTA index will stream in the next GEMM,
+                // so HBM keeps working while the kernels in between run
+                const long long T2 = (long long)p.n_ntiles * p.n_KB;
+                const long long a0 = range_start(T2, G, cta);
+                const long long a1 = min(range_start(T2, G, cta + 1), a0 + p.n_atoms);
+                for (long long g = a0; g < a1; ++g) {
+                    const int tile = (int)(g / p.n_KB), kt = (int)(g % p.n_KB);
+                    const CUtensorMap *m0, *m1;
+                    int r0, r1;
+                    tile_rows_of(p.ngid, p.nwmap, p.hq, p.hkv, tile, m0, r0, m1, r1);
+                    tma_prefetch_l2(m0, kt * TC_ATOM, r0);
+                    tma_prefetch_l2(m1, kt * TC_ATOM, r1);
+                }
             }
         }
     } else if (warp == 1) {
@@ -616,6 +645,25 @@ int tc_error_word(Ctx& c, int* out) {
     return cudaMemcpy(out, c.tc->err, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess ? SPEC_OK : SPEC_E_CUDA;
 }
 
+// Weight maps, tile count and K atoms per tile of GEMM `gid` of `layer`.
+static void gemm_geometry(const Ctx& c, int gid, int layer, CUtensorMap* maps, int& n_tiles, int& KB) {
+    const TcGemm* t = c.tc;
+    const spec_model_cfg& m = c.cfg;
+    const int d = m.d_model, qd = m.n_q_heads * m.head_dim, F = m.ffn_dim;
+    switch (gid) {
+    case GEMM_QKV:
+        maps[0] = t->layers[layer].q; maps[1] = t->layers[layer].k; maps[2] = t->layers[layer].v;
+        n_tiles = m.n_q_heads + 2 * m.n_kv_heads; KB = d / TC_ATOM;
+        break;
+    case GEMM_O: maps[0] = t->layers[layer].o; n_tiles = d / TC_BM; KB = qd / TC_ATOM; break;
+    case GEMM_GU:
+        maps[0] = t->layers[layer].g; maps[1] = t->layers[layer].u; n_tiles = F / 64; KB = d / TC_ATOM;
+        break;
+    case GEMM_DOWN: maps[0] = t->layers[layer].d; n_tiles = d / TC_BM; KB = F / TC_ATOM; break;
+    default: maps[0] = t->lm; n_tiles = m.vocab / TC_BM; KB = d / TC_ATOM; break;
+    }
+}
+
 int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, cudaStream_t st) {
     TcGemm* t = c.tc;
     const spec_model_cfg& m = c.cfg;
@@ -668,6 +716,18 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, 
     p.tile_cnt = t->tile_cnt;
     p.err = t->err;
     p.e = e;
+    // the next GEMM of the pass (QKV -> O -> gate/up -> down -> next layer's QKV or lm_head)
+    p.n_atoms = 0;
+    if (c.l2_prefetch_atoms > 0 && gid != GEMM_LM) {
+        int ngid = gid + 1, nlayer = layer;
+        if (gid == GEMM_DOWN) {
+            ngid = layer + 1 < m.n_layers ? GEMM_QKV : GEMM_LM;
+            nlayer = layer + 1 < m.n_layers ? layer + 1 : -1;
+        }
+        gemm_geometry(c, ngid, nlayer, p.nwmap, p.n_ntiles, p.n_KB);
+        p.ngid = ngid;
+        p.n_atoms = c.l2_prefetch_atoms;
+    }
     const long long T = (long long)p.n_tiles * p.KB;
     const int grid = (int)std::min<long long>(t->grid, T);
     const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + TC_XBYTES;

@@ -103,6 +103,7 @@ struct Ctx {
     // CUDA graphs of the decoder pass per (B, T); programmatic dependent launch
     bool use_graphs = true;
     bool use_pdl = true;
+    int l2_prefetch_atoms = 12;            // next-GEMM weight atoms per CTA warmed into L2
     cudaStream_t cap_stream = nullptr;     // private stream the graphs are captured on
     struct GraphEntry { int B, T; cudaGraphExec_t exec; long long kernels; };
     std::vector<GraphEntry> graphs;

@@ -615,6 +615,10 @@ extern "C" int spec_set_option(spec_ctx* c, int option, int value) {
     } else if (option == SPEC_OPT_PDL) {
         c->use_pdl = value != 0;
         drop_graphs(*c);
+    } else if (option == SPEC_OPT_L2_PREFETCH) {
+        if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "L2 prefetch atoms must be in [0, 64]");
+        c->l2_prefetch_atoms = value;
+        drop_graphs(*c);
     } else {
         return set_error(SPEC_E_INVAL, "unknown option %d", option);
     }
