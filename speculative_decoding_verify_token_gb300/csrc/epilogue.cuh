@@ -8,6 +8,11 @@
 //  * EPI_SWIGLU : the pair is (gate f, up f) -> H[m][f] = silu(gate) * up;
 //  * EPI_RESID  : the pair is (2p, 2p + 1) -> X[m][n] += acc (fp32 residual stream);
 //  * EPI_STORE  : the pair is (2p, 2p + 1) -> out[m][n] = acc (fp32 logits).
+//
+// Fused RMSNorm (tensor-core GEMM only): RMSNorm(x) W^T = (x * g) W^T / rms(x), so a
+// residual epilogue that also writes xg = bf16(x_new * g_next) and, per 128-column tile
+// of x, the sum of x_new^2 lets the GEMM that consumes the normed row apply 1/rms(x) to
+// its accumulators; no separate normalisation kernel runs.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -36,6 +41,16 @@ struct EpiArgs {
     // RESID / STORE
     float* x;                   // [M][ldx]
     int ldx;
+    // fused RMSNorm, producer side (RESID): xg_out = bf16(x_new * g_next), ssq_out[t][m] =
+    // sum of x_new[m][n]^2 over the 128 columns n of tile t (fixed order)
+    void* xg_out;               // [M][ldx] bf16 or nullptr
+    const void* g_next;         // [ldx] bf16
+    float* ssq_out;             // [ldx / 128][ssq_ld]
+    // consumer side: accumulators of token m are scaled by 1/sqrt(sum_t ssq_in[t][row0 + m]
+    // / norm_d + eps), the tiles summed in order
+    const float* ssq_in;        // [n_ssq][ssq_ld] or nullptr
+    int n_ssq, ssq_ld, ssq_row0;
+    float norm_d, eps;
 };
 
 template <typename T> __device__ __forceinline__ T from_f32(float v);

@@ -17,7 +17,9 @@
 //    only on the weight shape and the SM count, so a token's outputs are bit-identical for
 //    every M (a decode step and a verify pass agree exactly);
 //  * fused epilogues (RoPE + paged KV append, SwiGLU, residual add, fp32 logits) shared
-//    with the CUDA-core GEMM.
+//    with the CUDA-core GEMM, and a fused RMSNorm: the residual GEMMs also write
+//    bf16(x * g) of the next norm and per-tile sums of squares, and the GEMM reading that
+//    normed row scales its accumulators by 1/rms of the token.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <algorithm>
@@ -47,7 +49,9 @@ constexpr int TC_MAX_STAGES = 8;
 constexpr int TC_CW = 16;                           // epilogue column chunk
 constexpr int TC_XPITCH = TC_CW + 1;
 constexpr int TC_XBYTES = TC_BM * TC_XPITCH * 4;
-constexpr int TC_SMEM_MAX = (TC_CTAS_PER_SM == 1 ? 226 : 112) * 1024;   // dynamic bytes per CTA
+// dynamic bytes per CTA: with one CTA per SM, three stages of four atoms at 16 tokens plus
+// the staging tile and the alignment slack, leaving 1.5 KB of the 227 KB for static data
+constexpr int TC_SMEM_MAX = TC_CTAS_PER_SM == 1 ? 230912 : 110 * 1024;
 
 struct TcParams {
     CUtensorMap wmap[3];
@@ -223,17 +227,55 @@ struct StageWalk {
 };
 
 // Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
-__device__ __forceinline__ void epi_chunk(const TcParams& p, const float* xs, int tile, int c0, int etid) {
+// inv_s[m] = 1/rms of token m when the GEMM consumes a normed row; red = [4 warps][16]
+// scratch of the sums of squares when it produces one.
+__device__ __forceinline__ void epi_chunk(const TcParams& p, const float* xs, const float* inv_s,
+                                          float (*red)[TC_CW], int tile, int c0, int etid) {
     const int i = etid & 63;
     const int half = etid >> 6;
     const bool adjacent = (p.gid == GEMM_O || p.gid == GEMM_DOWN || p.gid == GEMM_LM);
     const int r0 = adjacent ? 2 * i : i;
     const int r1 = adjacent ? 2 * i + 1 : i + 64;
     const int pidx = tile * 64 + i;
+    if (p.e.kind == EPI_RESID && p.e.xg_out != nullptr) {
+        // x += acc; xg = bf16(x * g_next); per token, the tile's sum of x^2 (each warp's
+        // 32 pairs by a butterfly, then the two warps of a half in order)
+        const int n0 = 2 * pidx;
+        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(
+            static_cast<const __nv_bfloat16*>(p.e.g_next) + n0);
+        const float2 g = __bfloat1622float2(g2);
+        const int wq = (etid >> 5) & 1;
+        for (int cc = half; cc < TC_CW; cc += 2) {
+            const int m = c0 + cc;
+            if (m >= p.M) break;        // uniform over a warp: a warp holds one half
+            float2* x = reinterpret_cast<float2*>(p.e.x + (size_t)m * p.e.ldx + n0);
+            float2 xv = *x;
+            xv.x += xs[r0 * TC_XPITCH + cc];
+            xv.y += xs[r1 * TC_XPITCH + cc];
+            *x = xv;
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.e.xg_out) + (size_t)m * p.e.ldx + n0) =
+                __floats2bfloat162_rn(xv.x * g.x, xv.y * g.y);
+            const float sq = warp_sum(fmaf(xv.x, xv.x, xv.y * xv.y));
+            if ((etid & 31) == 0) red[half * 2 + wq][cc] = sq;
+        }
+        epi_bar();
+        if (etid < TC_CW && c0 + etid < p.M) {
+            const int h = etid & 1;
+            p.e.ssq_out[(size_t)tile * p.e.ssq_ld + c0 + etid] = red[2 * h][etid] + red[2 * h + 1][etid];
+        }
+        return;
+    }
+    const bool scaled = p.e.ssq_in != nullptr;
     for (int cc = half; cc < TC_CW; cc += 2) {
         const int m = c0 + cc;
         if (m >= p.M) break;
-        epi_pair<__nv_bfloat16>(p.e, m, pidx, xs[r0 * TC_XPITCH + cc], xs[r1 * TC_XPITCH + cc]);
+        float a0 = xs[r0 * TC_XPITCH + cc], a1 = xs[r1 * TC_XPITCH + cc];
+        if (scaled) {
+            const float s = inv_s[m];
+            a0 *= s;
+            a1 *= s;
+        }
+        epi_pair<__nv_bfloat16>(p.e, m, pidx, a0, a1);
     }
 }
 
@@ -243,6 +285,8 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
     __shared__ __align__(8) uint64_t accf[2], acce[2], done_bar;
     __shared__ uint32_t tmem_sh;
     __shared__ int last_flag;
+    __shared__ float inv_s[TC_MAX_NTOK];
+    __shared__ float red_s[4][TC_CW];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) TC_STAMP(0);
@@ -410,6 +454,16 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const int etid = threadIdx.x - 64;
+        if (p.e.ssq_in != nullptr) {
+            // 1/rms of every token of the launch, its tiles' sums of squares added in order
+            for (int m = etid; m < p.M; m += 128) {
+                const float* src = p.e.ssq_in + p.e.ssq_row0 + m;
+                float ss = 0.0f;
+                for (int t = 0; t < p.e.n_ssq; ++t) ss += src[(size_t)t * p.e.ssq_ld];
+                inv_s[m] = 1.0f / sqrtf(ss / p.e.norm_d + p.e.eps);
+            }
+            epi_bar();
+        }
         int si = 0;
         long long g = s0;
         while (g < s1) {
@@ -437,7 +491,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 #pragma unroll
                     for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = v[j];
                     epi_bar();
-                    epi_chunk(p, xs, tile, c0, etid);
+                    epi_chunk(p, xs, inv_s, red_s, tile, c0, etid);
                     epi_bar();
                 }
             } else {
@@ -497,7 +551,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 #pragma unroll
                         for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = acc[j];
                         epi_bar();
-                        epi_chunk(p, xs, tile, c0, etid);
+                        epi_chunk(p, xs, inv_s, red_s, tile, c0, etid);
                         epi_bar();
                     }
                     if (etid == 0) p.tile_cnt[tile] = 0;
@@ -702,7 +756,7 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, 
     p.M = M;
     // the widest stage (most K atoms) that still leaves TC_MIN_STAGES ring slots; the
     // stream-K split is in atoms, so this choice changes no result bit
-    const int budget = TC_SMEM_MAX - 1024 - TC_XBYTES - 256;
+    const int budget = TC_SMEM_MAX - 1024 - TC_XBYTES;
     const int per_atom = TC_ATOM_A + p.ntok * TC_ATOM * 2;
     p.atoms = 1;
     for (int a = TC_MAX_ATOMS; a > 1; a >>= 1)

@@ -77,6 +77,10 @@ struct Ctx {
     void* Q = nullptr;              // [Mmax][hq*hd]
     void* O = nullptr;              // [Mmax][hq*hd]
     void* H = nullptr;              // [Mmax][F]
+    // fused RMSNorm (tensor-core path): per-128-column-tile sums of squares of the residual
+    // stream feeding the attention norm (a) and the FFN norm (f), [d/128][Mmax] each
+    float* ssq_a = nullptr;
+    float* ssq_f = nullptr;
     float* logits = nullptr;        // [Mmax][V]
     int* d_tokens = nullptr;        // [Mmax]
     int* d_tok_seq = nullptr;
@@ -114,7 +118,7 @@ struct Ctx {
 };
 
 // kernels
-void launch_embed(const Ctx& c, int M, int T, cudaStream_t st);
+void launch_embed(const Ctx& c, int M, int T, cudaStream_t st, bool fused_norm);
 void launch_rmsnorm(const Ctx& c, const float* X, const void* g, void* Xn, int M, cudaStream_t st);
 void launch_rope_table(float2* table, int max_pos, int hd, double theta, cudaStream_t st);
 void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens, int B, cudaStream_t st);

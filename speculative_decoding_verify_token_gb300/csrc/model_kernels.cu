@@ -31,12 +31,15 @@ template <> struct Quad<__nv_bfloat16> {
 
 
 // X[m][:] = E[tok[m]][:] in fp32; token m = b*T + t belongs to slot seq_ids[b] at
-// position seq_len[slot] + t.  Ids outside [0, V) are embedded as token 0.
+// position seq_len[slot] + t.  Ids outside [0, V) are embedded as token 0.  With Xg set
+// (fused RMSNorm of the tensor-core path) it also writes Xg[m] = bf16(X[m] * g) and, per
+// 128-column tile t, ssq[t][m] = sum of X[m][n]^2 over the tile (one warp per tile).
 template <typename T>
 __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restrict__ seq_ids,
                              const int* __restrict__ seq_len, int T_per_seq, const T* __restrict__ E,
                              float* __restrict__ X, int* __restrict__ tok_seq, int* __restrict__ tok_pos, int d,
-                             int V) {
+                             int V, T* __restrict__ Xg, const T* __restrict__ g, float* __restrict__ ssq,
+                             int ssq_ld) {
     pdl_launch_dependents();
     const int m = blockIdx.x;
     const int b = m / T_per_seq;
@@ -49,8 +52,26 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
         tok_pos[m] = seq_len[slot] + t;
     }
     const T* row = E + (size_t)tok * d;
-    float4* xr = reinterpret_cast<float4*>(X + (size_t)m * d);
-    for (int i = threadIdx.x; i < (d >> 2); i += blockDim.x) xr[i] = Quad<T>::load(row + 4 * i);
+    float* xr = X + (size_t)m * d;
+    if (Xg == nullptr) {
+        for (int i = threadIdx.x; i < (d >> 2); i += blockDim.x)
+            reinterpret_cast<float4*>(xr)[i] = Quad<T>::load(row + 4 * i);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int tile = warp; tile < (d >> 7); tile += blockDim.x >> 5) {
+        const int c = tile * 128 + lane * 4;
+        const float4 v = Quad<T>::load(row + c);
+        *reinterpret_cast<float4*>(xr + c) = v;
+        const float4 gg = Quad<T>::load(g + c);
+        Quad<T>::store(Xg + (size_t)m * d + c, make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w));
+        float sq = v.x * v.x;
+        sq = fmaf(v.y, v.y, sq);
+        sq = fmaf(v.z, v.z, sq);
+        sq = fmaf(v.w, v.w, sq);
+        sq = warp_sum(sq);
+        if (lane == 0) ssq[(size_t)tile * ssq_ld + m] = sq;
+    }
 }
 
 constexpr int NORM_THREADS = 256;
@@ -134,15 +155,18 @@ __global__ void advance_len_kernel(const int* __restrict__ seq_ids, int* __restr
     else seq_len[slot] -= K - a;
 }
 
-void launch_embed(const Ctx& c, int M, int T, cudaStream_t st) {
-    if (c.cfg.dtype == SPEC_BF16)
-        embed_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T,
-                                                       static_cast<const __nv_bfloat16*>(c.w.embed), c.X, c.d_tok_seq,
-                                                       c.d_tok_pos, c.cfg.d_model, c.cfg.vocab);
-    else
+void launch_embed(const Ctx& c, int M, int T, cudaStream_t st, bool fused_norm) {
+    if (c.cfg.dtype == SPEC_BF16) {
+        using bf = __nv_bfloat16;
+        embed_kernel<bf><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T, static_cast<const bf*>(c.w.embed),
+                                            c.X, c.d_tok_seq, c.d_tok_pos, c.cfg.d_model, c.cfg.vocab,
+                                            fused_norm ? static_cast<bf*>(c.Xn) : nullptr,
+                                            static_cast<const bf*>(c.w.layers[0].attn_norm), c.ssq_a, c.Mmax);
+    } else {
         embed_kernel<float><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T,
                                                static_cast<const float*>(c.w.embed), c.X, c.d_tok_seq, c.d_tok_pos,
-                                               c.cfg.d_model, c.cfg.vocab);
+                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0);
+    }
 }
 
 void launch_rmsnorm(const Ctx& c, const float* X, const void* g, void* Xn, int M, cudaStream_t st) {

@@ -236,7 +236,9 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     const int M = B * T;
     const int d = m.d_model, hd = m.head_dim, hq = m.n_q_heads, hkv = m.n_kv_heads, F = m.ffn_dim;
     cudaStream_t st = c.stream;
-    launch_embed(c, M, T, st);
+    // the tensor-core path folds every RMSNorm into the GEMMs around it (see epilogue.cuh)
+    const bool fused = c.use_tc;
+    launch_embed(c, M, T, st, fused);
     c.launches += 1;
     int max_after = 0;
     double kv_bytes = 0.0;    // keys + values read per layer (upper bound of the lengths) + written
@@ -246,13 +248,25 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     }
     if (graph_mode) max_after = c.lim.max_ctx;   // the graph is replayed at any length
 
+    // consumer / producer halves of the fused norm
+    auto norm_in = [&](EpiArgs& e, const float* ssq, int row0) {
+        if (!fused) return;
+        e.ssq_in = ssq; e.n_ssq = d / 128; e.ssq_ld = c.Mmax; e.ssq_row0 = row0;
+        e.norm_d = (float)d; e.eps = m.rms_eps;
+    };
+    auto norm_out = [&](EpiArgs& e, float* ssq, const void* g) {
+        if (!fused) return;
+        e.xg_out = c.Xn; e.g_next = g; e.ssq_out = ssq; e.ssq_ld = c.Mmax;
+    };
     EpiArgs eq{};
     eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
     eq.tok_seq = c.d_tok_seq; eq.tok_pos = c.d_tok_pos; eq.rope = c.d_rope; eq.hq = hq; eq.hkv = hkv; eq.hd = hd;
+    norm_in(eq, c.ssq_a, 0);
     EpiArgs er{};
     er.kind = EPI_RESID; er.M = M; er.x = c.X; er.ldx = d;
     EpiArgs es{};
     es.kind = EPI_SWIGLU; es.M = M; es.h_out = c.H; es.F = F;
+    norm_in(es, c.ssq_f, 0);
     AttnArgs aa{};
     aa.q = c.Q; aa.o = c.O; aa.block_table = c.d_block_table; aa.max_pages = c.max_pages; aa.seq_ids = c.d_seq_ids;
     aa.seq_len = c.d_seq_len; aa.T = T; aa.hq = hq; aa.hkv = hkv; aa.hd = hd; aa.scale = 1.0f / sqrtf((float)hd);
@@ -262,8 +276,10 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     int rc;
     for (int l = 0; l < m.n_layers; ++l) {
         const LayerWeights& L = c.w.layers[l];
-        launch_rmsnorm(c, c.X, L.attn_norm, c.Xn, M, st);
-        c.launches += 1;
+        if (!fused) {
+            launch_rmsnorm(c, c.X, L.attn_norm, c.Xn, M, st);
+            c.launches += 1;
+        }
         eq.k_layer = layer_pool(c, c.k_pool, l);
         eq.v_layer = layer_pool(c, c.v_pool, l);
         if ((rc = gemm(c, GEMM_QKV, l, L.wq, L.wk, L.wv, d, (hq + 2 * hkv) * hd / 2, c.Xn, eq)) != SPEC_OK) return rc;
@@ -273,19 +289,26 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
             ProfScope ps(c, 5, kv_bytes);
             c.launches += launch_attention(c, aa, B, max_after, st);
         }
+        norm_out(er, c.ssq_f, L.ffn_norm);
         if ((rc = gemm(c, GEMM_O, l, L.wo, nullptr, nullptr, hq * hd, d / 2, c.O, er)) != SPEC_OK) return rc;
-        launch_rmsnorm(c, c.X, L.ffn_norm, c.Xn, M, st);
-        c.launches += 1;
+        if (!fused) {
+            launch_rmsnorm(c, c.X, L.ffn_norm, c.Xn, M, st);
+            c.launches += 1;
+        }
         if ((rc = gemm(c, GEMM_GU, l, L.wg, L.wu, nullptr, d, F, c.Xn, es)) != SPEC_OK) return rc;
+        norm_out(er, c.ssq_a, l + 1 < m.n_layers ? c.w.layers[l + 1].attn_norm : c.w.final_norm);
         if ((rc = gemm(c, GEMM_DOWN, l, L.wd, nullptr, nullptr, F, d / 2, c.H, er)) != SPEC_OK) return rc;
     }
     if (logits_out != nullptr) {
         const int rows = last_only ? 1 : M;
         const size_t off = last_only ? (size_t)(M - 1) : 0;
-        launch_rmsnorm(c, c.X + off * d, c.w.final_norm, static_cast<uint8_t*>(c.Xn) + off * d * c.esize, rows, st);
-        c.launches += 1;
+        if (!fused) {
+            launch_rmsnorm(c, c.X + off * d, c.w.final_norm, static_cast<uint8_t*>(c.Xn) + off * d * c.esize, rows, st);
+            c.launches += 1;
+        }
         EpiArgs el{};
         el.kind = EPI_STORE; el.M = rows; el.x = logits_out; el.ldx = m.vocab;
+        norm_in(el, c.ssq_a, (int)off);
         if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2,
                        static_cast<uint8_t*>(c.Xn) + off * d * c.esize, el)) != SPEC_OK)
             return rc;
@@ -385,6 +408,8 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
           ok(dalloc(*c, &c->Q, (size_t)c->esize * c->Mmax * qd, true)) &&
           ok(dalloc(*c, &c->O, (size_t)c->esize * c->Mmax * qd, true)) &&
           ok(dalloc(*c, &c->H, (size_t)c->esize * c->Mmax * m.ffn_dim, true)) &&
+          ok(dalloc(*c, &c->ssq_a, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&
+          ok(dalloc(*c, &c->ssq_f, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&
           ok(dalloc(*c, &c->logits, sizeof(float) * (size_t)c->Mmax * m.vocab)) &&
           ok(dalloc(*c, &c->d_tokens, sizeof(int) * c->Mmax, true)) &&
           ok(dalloc(*c, &c->d_tok_seq, sizeof(int) * c->Mmax, true)) &&
