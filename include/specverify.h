@@ -247,13 +247,25 @@ int spec_seq_reset(spec_ctx* ctx, int seq_id);
  * of its CTAs warms L2 with this many 64-column atoms (16 KB each) of the weights it will
  * stream first in the next GEMM of the pass; 0 disables.  Changes no result bit. */
 #define SPEC_OPT_L2_PREFETCH 3
+/* SPEC_OPT_PERSISTENT (default 0): 1 runs a verify or decode pass of at most 32 tokens
+ * (B*(K+1)) of a bf16 model on the tensor-core path as one persistent cooperative kernel
+ * (one CTA per SM) in which the phases of the pass hand off through counters in global
+ * memory instead of kernel boundaries; 0 launches one kernel per step.  Same result bits
+ * either way.  SPEC_OPT_PF_ATOMS (1, 2 or 4; default 4): 64-column K atoms per shared-memory
+ * stage of that kernel's weight ring.  SPEC_OPT_PF_L2_AHEAD (0..256, default 0): weight
+ * atoms (16 KB each) per CTA prefetched into L2 ahead of that ring, so that HBM keeps
+ * streaming while a phase waits for its inputs. */
+#define SPEC_OPT_PERSISTENT 4
+#define SPEC_OPT_PF_ATOMS 5
+#define SPEC_OPT_PF_L2_AHEAD 6
 int spec_set_option(spec_ctx* ctx, int option, int value);
 
 /* Per-kernel-class timing of the context's passes with CUDA events recorded on its
  * stream around each launch (off by default; meant for a measurement pass).  Classes:
  * 0 QKV GEMM, 1 O GEMM, 2 gate/up GEMM, 3 down GEMM, 4 lm_head GEMM, 5 attention,
- * 6 fused verify, 7 other small kernels. */
-#define SPEC_PROF_CLASSES 8
+ * 6 fused verify, 7 other small kernels, 8 persistent decoder pass (SPEC_OPT_PERSISTENT;
+ * bytes = weights + KV pages + logits of the pass). */
+#define SPEC_PROF_CLASSES 9
 int spec_profile(spec_ctx* ctx, int enable);
 
 /* Synchronise the context stream and return, per class, the summed event time (ms), the

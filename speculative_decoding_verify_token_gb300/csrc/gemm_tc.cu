@@ -24,10 +24,8 @@
 #include <cuda_bf16.h>
 #include <algorithm>
 
-#include "common.cuh"
-#include "epilogue.cuh"
 #include "host_util.h"
-#include "model.h"
+#include "tc_common.cuh"
 
 namespace sv {
 
@@ -40,15 +38,6 @@ namespace sv {
 #ifndef TC_CTAS_PER_SM
 #define TC_CTAS_PER_SM 1        // resident GEMM CTAs per SM (shared memory split between them)
 #endif
-constexpr int TC_THREADS = 192;
-constexpr int TC_BM = 128;
-constexpr int TC_ATOM = 64;                          // K elements per atom = accumulation unit
-constexpr int TC_ATOM_A = TC_BM * TC_ATOM * 2;       // 16 KB: one 128-row x 64 A atom
-constexpr int TC_MAX_NTOK = 256;
-constexpr int TC_MAX_STAGES = 8;
-constexpr int TC_CW = 16;                           // epilogue column chunk
-constexpr int TC_XPITCH = TC_CW + 1;
-constexpr int TC_XBYTES = TC_BM * TC_XPITCH * 4;
 // dynamic bytes per CTA: with one CTA per SM, three stages of four atoms at 16 tokens plus
 // the staging tile and the alignment slack, leaving 1.5 KB of the 227 KB for static data
 constexpr int TC_SMEM_MAX = TC_CTAS_PER_SM == 1 ? 230912 : 110 * 1024;
@@ -82,112 +71,9 @@ __device__ unsigned long long g_tc_trace[5][1024][6];
 #define TC_STAMP(i) ((void)0)
 #endif
 
-// ---- PTX wrappers --------------------------------------------------------------------------
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                            uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol) : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// K-major operand, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// 1 if any of the 128 epilogue threads passes pred != 0 (and a barrier among them).
-__device__ __forceinline__ int epi_any(int pred) {
-    int r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
-        : "=r"(r) : "r"(pred) : "memory");
-    return r;
-}
-
-// ---- tile geometry --------------------------------------------------------------------------
-
-__device__ __forceinline__ void tile_rows_of(int gid, const CUtensorMap* maps, int hq, int hkv, int tile,
-                                             const CUtensorMap*& m0, int& r0, const CUtensorMap*& m1, int& r1) {
-    if (gid == GEMM_QKV) {
-        int t = tile, w = 0;
-        if (t >= hq) { t -= hq; w = 1; if (t >= hkv) { t -= hkv; w = 2; } }
-        m0 = m1 = &maps[w];
-        r0 = t * TC_BM;
-        r1 = r0 + 64;
-    } else if (gid == GEMM_GU) {
-        m0 = &maps[0];
-        m1 = &maps[1];
-        r0 = r1 = tile * 64;
-    } else {
-        m0 = m1 = &maps[0];
-        r0 = tile * TC_BM;
-        r1 = r0 + 64;
-    }
-}
-
 __device__ __forceinline__ void tile_rows(const TcParams& p, int tile, const CUtensorMap*& m0, int& r0,
                                           const CUtensorMap*& m1, int& r1) {
     tile_rows_of(p.gid, p.wmap, p.hq, p.hkv, tile, m0, r0, m1, r1);
-}
-
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
-}
-
-__device__ __forceinline__ long long range_start(long long T, int G, int c) {
-    return (long long)(((unsigned long long)c * (unsigned long long)T) / (unsigned)G);
-}
-
-// CTA whose k-block range contains k-block x.
-__device__ __forceinline__ int owner_cta(long long T, int G, long long x) {
-    int c = (int)(((x + 1) * G + T - 1) / T) - 1;
-    while (c > 0 && range_start(T, G, c) > x) --c;
-    while (c + 1 < G && range_start(T, G, c + 1) <= x) ++c;
-    return c;
 }
 
 // One K atom of a stage: the tile's 128 weight rows as two 64-row boxes (A) and the token
@@ -203,80 +89,6 @@ __device__ __forceinline__ void load_atom_a(const TcParams& p, int tile, int kc,
 
 __device__ __forceinline__ void load_atom_b(const TcParams& p, int kc, uint32_t b_dst, uint32_t fb, uint64_t pol) {
     for (int t = 0; t < p.ntok / 16; ++t) tma_load_2d(b_dst + t * 2048, &p.xmap, kc, p.x_row0 + t * 16, fb, pol);
-}
-
-// Walk of a CTA's atom range in pipeline stages: a stage holds up to p.atoms consecutive
-// atoms of one tile segment.  Producer and MMA issuer walk it identically.
-struct StageWalk {
-    long long g, s1;
-    int KB, A;
-    __device__ __forceinline__ StageWalk(long long s0_, long long s1_, int KB_, int A_)
-        : g(s0_), s1(s1_), KB(KB_), A(A_) {}
-    __device__ __forceinline__ bool done() const { return g >= s1; }
-    // atoms of the current stage, its tile, its first atom within the tile, and whether it
-    // starts / ends a segment
-    __device__ __forceinline__ void cur(int& n, int& tile, int& k_in_tile, bool& seg_first, bool& seg_last,
-                                        long long seg_start_of_g) const {
-        tile = (int)(g / KB);
-        k_in_tile = (int)(g - (long long)tile * KB);
-        const long long seg_end = min(s1, (long long)(tile + 1) * KB);
-        n = (int)min((long long)A, seg_end - g);
-        seg_first = (g == seg_start_of_g);
-        seg_last = (g + n == seg_end);
-    }
-};
-
-// Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
-// inv_s[m] = 1/rms of token m when the GEMM consumes a normed row; red = [4 warps][16]
-// scratch of the sums of squares when it produces one.
-__device__ __forceinline__ void epi_chunk(const TcParams& p, const float* xs, const float* inv_s,
-                                          float (*red)[TC_CW], int tile, int c0, int etid) {
-    const int i = etid & 63;
-    const int half = etid >> 6;
-    const bool adjacent = (p.gid == GEMM_O || p.gid == GEMM_DOWN || p.gid == GEMM_LM);
-    const int r0 = adjacent ? 2 * i : i;
-    const int r1 = adjacent ? 2 * i + 1 : i + 64;
-    const int pidx = tile * 64 + i;
-    if (p.e.kind == EPI_RESID && p.e.xg_out != nullptr) {
-        // x += acc; xg = bf16(x * g_next); per token, the tile's sum of x^2 (each warp's
-        // 32 pairs by a butterfly, then the two warps of a half in order)
-        const int n0 = 2 * pidx;
-        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(
-            static_cast<const __nv_bfloat16*>(p.e.g_next) + n0);
-        const float2 g = __bfloat1622float2(g2);
-        const int wq = (etid >> 5) & 1;
-        for (int cc = half; cc < TC_CW; cc += 2) {
-            const int m = c0 + cc;
-            if (m >= p.M) break;        // uniform over a warp: a warp holds one half
-            float2* x = reinterpret_cast<float2*>(p.e.x + (size_t)m * p.e.ldx + n0);
-            float2 xv = *x;
-            xv.x += xs[r0 * TC_XPITCH + cc];
-            xv.y += xs[r1 * TC_XPITCH + cc];
-            *x = xv;
-            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.e.xg_out) + (size_t)m * p.e.ldx + n0) =
-                __floats2bfloat162_rn(xv.x * g.x, xv.y * g.y);
-            const float sq = warp_sum(fmaf(xv.x, xv.x, xv.y * xv.y));
-            if ((etid & 31) == 0) red[half * 2 + wq][cc] = sq;
-        }
-        epi_bar();
-        if (etid < TC_CW && c0 + etid < p.M) {
-            const int h = etid & 1;
-            p.e.ssq_out[(size_t)tile * p.e.ssq_ld + c0 + etid] = red[2 * h][etid] + red[2 * h + 1][etid];
-        }
-        return;
-    }
-    const bool scaled = p.e.ssq_in != nullptr;
-    for (int cc = half; cc < TC_CW; cc += 2) {
-        const int m = c0 + cc;
-        if (m >= p.M) break;
-        float a0 = xs[r0 * TC_XPITCH + cc], a1 = xs[r1 * TC_XPITCH + cc];
-        if (scaled) {
-            const float s = inv_s[m];
-            a0 *= s;
-            a1 *= s;
-        }
-        epi_pair<__nv_bfloat16>(p.e, m, pidx, a0, a1);
-    }
 }
 
 __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(const __grid_constant__ TcParams p) {
@@ -459,7 +271,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
             for (int m = etid; m < p.M; m += 128) {
                 const float* src = p.e.ssq_in + p.e.ssq_row0 + m;
                 float ss = 0.0f;
-                for (int t = 0; t < p.e.n_ssq; ++t) ss += src[(size_t)t * p.e.ssq_ld];
+                for (int t = 0; t < p.e.n_ssq; ++t) ss += __ldcg(src + (size_t)t * p.e.ssq_ld);
                 inv_s[m] = 1.0f / sqrtf(ss / p.e.norm_d + p.e.eps);
             }
             epi_bar();
@@ -491,7 +303,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 #pragma unroll
                     for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = v[j];
                     epi_bar();
-                    epi_chunk(p, xs, inv_s, red_s, tile, c0, etid);
+                    epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid);
                     epi_bar();
                 }
             } else {
@@ -551,7 +363,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 #pragma unroll
                         for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = acc[j];
                         epi_bar();
-                        epi_chunk(p, xs, inv_s, red_s, tile, c0, etid);
+                        epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid);
                         epi_bar();
                     }
                     if (etid == 0) p.tile_cnt[tile] = 0;
@@ -586,6 +398,7 @@ struct TcGemm {
     float* partial = nullptr;
     int* tile_cnt = nullptr;
     int* err = nullptr;
+    int n_tile_cnt = 0;
     int grid = 0;
 };
 
@@ -661,6 +474,7 @@ int tc_create(Ctx& c) {
         }
         t->partial = static_cast<float*>(a);
         t->tile_cnt = static_cast<int*>(b);
+        t->n_tile_cnt = max_tiles;
         t->err = static_cast<int*>(e);
     }
     if (rc == SPEC_OK &&
@@ -693,6 +507,33 @@ extern "C" int spec_debug_tc_trace(unsigned long long* out) {
     return cudaMemcpyFromSymbol(out, g_tc_trace, sizeof(g_tc_trace)) == cudaSuccess ? 0 : -6;
 }
 #endif
+
+// Tensor maps and workspace of the context's GEMMs for the persistent pass: wmaps [7L + 1]
+// (q k v o g u d per layer, then lm_head) and xmaps [3] (Xn, O, H); either may be null.
+int tc_export(const Ctx& c, CUtensorMap* wmaps, CUtensorMap* xmaps, float** partial, int** tile_cnt, int* n_tile_cnt,
+              int** err) {
+    const TcGemm* t = c.tc;
+    if (!t) return set_error(SPEC_E_STATE, "tensor-core GEMM not planned");
+    const spec_model_cfg& m = c.cfg;
+    if (wmaps) {
+        for (int l = 0; l < m.n_layers; ++l) {
+            const TcLayerMaps& L = t->layers[l];
+            CUtensorMap* w = wmaps + (size_t)7 * l;
+            w[0] = L.q; w[1] = L.k; w[2] = L.v; w[3] = L.o; w[4] = L.g; w[5] = L.u; w[6] = L.d;
+        }
+        wmaps[(size_t)7 * m.n_layers] = t->lm;
+    }
+    if (xmaps) {
+        xmaps[0] = t->xn;
+        xmaps[1] = t->xo;
+        xmaps[2] = t->xh;
+    }
+    *partial = t->partial;
+    *tile_cnt = t->tile_cnt;
+    *n_tile_cnt = t->n_tile_cnt;
+    *err = t->err;
+    return SPEC_OK;
+}
 
 int tc_error_word(Ctx& c, int* out) {
     if (!c.tc) { *out = 0; return SPEC_OK; }

@@ -1,0 +1,202 @@
+// Device pieces of the tcgen05 skinny GEMM shared by the per-GEMM kernel and the
+// persistent decoder kernel: PTX wrappers (TMA tensor loads, tcgen05 MMA / commit / TMEM
+// loads), the shared-memory and instruction descriptors, the stream-K partition of the
+// (tile, K atom) space and the epilogue of one staged accumulator chunk.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "model.h"
+
+namespace sv {
+
+constexpr int TC_THREADS = 192;
+constexpr int TC_BM = 128;
+constexpr int TC_ATOM = 64;                          // K elements per atom = accumulation unit
+constexpr int TC_ATOM_A = TC_BM * TC_ATOM * 2;       // 16 KB: one 128-row x 64 A atom
+constexpr int TC_MAX_NTOK = 256;
+constexpr int TC_MAX_STAGES = 8;
+constexpr int TC_CW = 16;                           // epilogue column chunk
+constexpr int TC_XPITCH = TC_CW + 1;
+constexpr int TC_XBYTES = TC_BM * TC_XPITCH * 4;
+// ---- PTX wrappers --------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 1 if any of the 128 epilogue threads passes pred != 0 (and a barrier among them).
+__device__ __forceinline__ int epi_any(int pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(pred) : "memory");
+    return r;
+}
+
+// ---- tile geometry --------------------------------------------------------------------------
+
+__device__ __forceinline__ void tile_rows_of(int gid, const CUtensorMap* maps, int hq, int hkv, int tile,
+                                             const CUtensorMap*& m0, int& r0, const CUtensorMap*& m1, int& r1) {
+    if (gid == GEMM_QKV) {
+        int t = tile, w = 0;
+        if (t >= hq) { t -= hq; w = 1; if (t >= hkv) { t -= hkv; w = 2; } }
+        m0 = m1 = &maps[w];
+        r0 = t * TC_BM;
+        r1 = r0 + 64;
+    } else if (gid == GEMM_GU) {
+        m0 = &maps[0];
+        m1 = &maps[1];
+        r0 = r1 = tile * 64;
+    } else {
+        m0 = m1 = &maps[0];
+        r0 = tile * TC_BM;
+        r1 = r0 + 64;
+    }
+}
+
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
+}
+
+__device__ __forceinline__ long long range_start(long long T, int G, int c) {
+    return (long long)(((unsigned long long)c * (unsigned long long)T) / (unsigned)G);
+}
+
+// CTA whose k-block range contains k-block x.
+__device__ __forceinline__ int owner_cta(long long T, int G, long long x) {
+    int c = (int)(((x + 1) * G + T - 1) / T) - 1;
+    while (c > 0 && range_start(T, G, c) > x) --c;
+    while (c + 1 < G && range_start(T, G, c + 1) <= x) ++c;
+    return c;
+}
+
+// Walk of a CTA's atom range in pipeline stages: a stage holds up to p.atoms consecutive
+// atoms of one tile segment.  Producer and MMA issuer walk it identically.
+struct StageWalk {
+    long long g, s1;
+    int KB, A;
+    __device__ __forceinline__ StageWalk(long long s0_, long long s1_, int KB_, int A_)
+        : g(s0_), s1(s1_), KB(KB_), A(A_) {}
+    __device__ __forceinline__ bool done() const { return g >= s1; }
+    // atoms of the current stage, its tile, its first atom within the tile, and whether it
+    // starts / ends a segment
+    __device__ __forceinline__ void cur(int& n, int& tile, int& k_in_tile, bool& seg_first, bool& seg_last,
+                                        long long seg_start_of_g) const {
+        tile = (int)(g / KB);
+        k_in_tile = (int)(g - (long long)tile * KB);
+        const long long seg_end = min(s1, (long long)(tile + 1) * KB);
+        n = (int)min((long long)A, seg_end - g);
+        seg_first = (g == seg_start_of_g);
+        seg_last = (g + n == seg_end);
+    }
+};
+
+// Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
+// inv_s[m] = 1/rms of token m when the GEMM consumes a normed row; red = [4 warps][16]
+// scratch of the sums of squares when it produces one.
+__device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, const float* xs, const float* inv_s,
+                                          float (*red)[TC_CW], int tile, int c0, int etid) {
+    const int i = etid & 63;
+    const int half = etid >> 6;
+    const bool adjacent = (gid == GEMM_O || gid == GEMM_DOWN || gid == GEMM_LM);
+    const int r0 = adjacent ? 2 * i : i;
+    const int r1 = adjacent ? 2 * i + 1 : i + 64;
+    const int pidx = tile * 64 + i;
+    if (e.kind == EPI_RESID && e.xg_out != nullptr) {
+        // x += acc; xg = bf16(x * g_next); per token, the tile's sum of x^2 (each warp's
+        // 32 pairs by a butterfly, then the two warps of a half in order)
+        const int n0 = 2 * pidx;
+        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(
+            static_cast<const __nv_bfloat16*>(e.g_next) + n0);
+        const float2 g = __bfloat1622float2(g2);
+        const int wq = (etid >> 5) & 1;
+        for (int cc = half; cc < TC_CW; cc += 2) {
+            const int m = c0 + cc;
+            if (m >= M) break;        // uniform over a warp: a warp holds one half
+            float2* x = reinterpret_cast<float2*>(e.x + (size_t)m * e.ldx + n0);
+            float2 xv = __ldcg(x);        // written by other CTAs of a persistent pass: not from L1
+            xv.x += xs[r0 * TC_XPITCH + cc];
+            xv.y += xs[r1 * TC_XPITCH + cc];
+            *x = xv;
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(e.xg_out) + (size_t)m * e.ldx + n0) =
+                __floats2bfloat162_rn(xv.x * g.x, xv.y * g.y);
+            const float sq = warp_sum(fmaf(xv.x, xv.x, xv.y * xv.y));
+            if ((etid & 31) == 0) red[half * 2 + wq][cc] = sq;
+        }
+        epi_bar();
+        if (etid < TC_CW && c0 + etid < M) {
+            const int h = etid & 1;
+            e.ssq_out[(size_t)tile * e.ssq_ld + c0 + etid] = red[2 * h][etid] + red[2 * h + 1][etid];
+        }
+        return;
+    }
+    const bool scaled = e.ssq_in != nullptr;
+    for (int cc = half; cc < TC_CW; cc += 2) {
+        const int m = c0 + cc;
+        if (m >= M) break;
+        float a0 = xs[r0 * TC_XPITCH + cc], a1 = xs[r1 * TC_XPITCH + cc];
+        if (scaled) {
+            const float s = inv_s[m];
+            a0 *= s;
+            a1 *= s;
+        }
+        epi_pair<__nv_bfloat16>(e, m, pidx, a0, a1);
+    }
+}
+
+}  // namespace sv
