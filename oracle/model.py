@@ -6,6 +6,12 @@ pending token and the K drafts ([SD-Apple] "How speculative decoding works"; [Dr
 plain attention layer is rolled back by slicing off the rejected entries ([SD-Apple]
 "Why this needed a patch to mlx_lm at all").
 
+For the bf16 model configurations the KV cache holds keys and values in the model's
+dtype, as the pages' bf16 runtimes do (mlx-optiq "Speculative decoding on Apple Silicon",
+section "Assistant drafter: Gemma-4", traces its verify/decode differences to bf16
+attention precision): each key and value is rounded to bfloat16 (nearest, ties to even)
+when it enters the cache.  Everything else stays float64.
+
 The decoder itself is not printed on the pages; it is the plain Llama/Qwen-style
 reading: x = E[tok]; per layer h = RMSNorm(x), q,k,v = h W_q^T, h W_k^T, h W_v^T,
 rotate-half RoPE on q and k at absolute positions, causal GQA softmax attention with
@@ -17,7 +23,8 @@ inverse frequency theta^(-2j/hd).
 Parity status: pinned -- attention against torch's scaled_dot_product_attention
 (float64, CPU), RMSNorm and RoPE against closed forms and invariants (norm
 preservation, relative-position dependence), incremental decoding against a full
-forward, and the trim invariant -- see tests/test_oracle_model.py.
+forward, the trim invariant, and the bfloat16 rounding against hand-worked ties and
+torch's conversion -- see tests/test_oracle_model.py.
 """
 import numpy as np
 
@@ -72,6 +79,16 @@ def silu(x):
     return x / (1.0 + np.exp(-x))
 
 
+def round_bf16(x):
+    """Nearest bfloat16 value (8 significant bits, ties to even), as float64.
+
+    x = m 2^e with 1/2 <= |m| < 1 (frexp); m 2^8 rounded to an integer (half to even)
+    keeps 8 significant bits.  Values here are far from bfloat16's range limits.
+    """
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.round(np.ldexp(m, 8)), e - 8)
+
+
 class KVList:
     """Per-layer lists of keys and values [T, Hkv, hd]; trimmed by slicing."""
 
@@ -102,6 +119,7 @@ class Decoder:
 
     def __init__(self, shape, weights):
         self.s = shape
+        self.kv_bf16 = shape.dtype == "bf16"     # the cache stores the model dtype
         if isinstance(weights, dict):
             cache = {}
 
@@ -135,6 +153,8 @@ class Decoder:
             v = (h @ w(p + "wv").T).reshape(T, s.n_kv_heads, s.head_dim)
             q = rope(q, pos, s.rope_theta)
             k = rope(k, pos, s.rope_theta)
+            if self.kv_bf16:
+                k, v = round_bf16(k), round_bf16(v)
             cache.append(l, k, v)
             o = causal_gqa_attention(q, cache.k[l], cache.v[l], pos)
             x = x + o.reshape(T, s.q_dim) @ w(p + "wo").T

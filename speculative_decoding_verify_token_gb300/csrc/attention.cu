@@ -182,7 +182,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnArgs a) {
     sm.Ks = reinterpret_cast<__nv_bfloat16*>(sm_raw);
     sm.Vs = sm.Ks + MMA_SPLIT * MMA_PITCH;
     sm.Qs = sm.Vs + MMA_SPLIT * MMA_PITCH;
-    sm.Ps = sm.Qs + MMA_RT * MMA_PITCH;
+    sm.Qlo = sm.Qs + MMA_RT * MMA_PITCH;
+    sm.Ps = sm.Qlo + MMA_RT * MMA_PITCH;
     sm.wmax = wmax;
     sm.wsum = wsum;
     attn_mma_item(a, blockIdx.x, blockIdx.y, blockIdx.z, sm, threadIdx.x, [] { __syncthreads(); },

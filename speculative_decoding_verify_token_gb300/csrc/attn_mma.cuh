@@ -17,14 +17,14 @@ constexpr int MMA_RT = 64;                     // query rows per tile (4 m16 til
 constexpr int MMA_PITCH = 136;                 // bf16 row pitch of K, V, Q in smem (272 B)
 constexpr int MMA_PPITCH = 72;                 // bf16 row pitch of P (144 B)
 
-// Shared memory of one attention item: K, V, Q [64][MMA_PITCH] and P [64][MMA_PPITCH] bf16
-// (dynamic) and the per-warp row statistics.
+// Shared memory of one attention item: K, V, Q, Q lo [64][MMA_PITCH] and P [64][MMA_PPITCH]
+// bf16 (dynamic) and the per-warp row statistics.
 struct AttnSmem {
-    __nv_bfloat16 *Ks, *Vs, *Qs, *Ps;
+    __nv_bfloat16 *Ks, *Vs, *Qs, *Qlo, *Ps;     // Qlo: lo halves of split queries
     float (*wmax)[MMA_RT];
     float (*wsum)[MMA_RT];
 };
-constexpr size_t MMA_SMEM = sizeof(__nv_bfloat16) * ((size_t)3 * 64 * MMA_PITCH + (size_t)MMA_RT * MMA_PPITCH);
+constexpr size_t MMA_SMEM = sizeof(__nv_bfloat16) * ((size_t)4 * 64 * MMA_PITCH + (size_t)MMA_RT * MMA_PPITCH);
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
@@ -65,6 +65,8 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
     __nv_bfloat16* Ks = sm.Ks;
     __nv_bfloat16* Vs = sm.Vs;
     __nv_bfloat16* Qs = sm.Qs;
+    __nv_bfloat16* Qlo = sm.Qlo;
+    const bool qsplit = a.q_lo_off != 0;
     __nv_bfloat16* Ps = sm.Ps;
     float (*wmax)[MMA_RT] = sm.wmax;
     float (*wsum)[MMA_RT] = sm.wsum;
@@ -125,9 +127,12 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
             if (ri < nr) {
                 const int r = rt + ri, t = r / G, hh = r - t * G;
                 const size_t m = (size_t)b * a.T + t;
-                cp_async16(smem_u32(Qs + ri * MMA_PITCH + ch * 8), Q + (m * a.hq + (size_t)g * G + hh) * 128 + ch * 8);
+                const __nv_bfloat16* src = Q + (m * a.hq + (size_t)g * G + hh) * 128 + ch * 8;
+                cp_async16(smem_u32(Qs + ri * MMA_PITCH + ch * 8), src);
+                if (qsplit) cp_async16(smem_u32(Qlo + ri * MMA_PITCH + ch * 8), src + a.q_lo_off);
             } else {
                 *reinterpret_cast<uint4*>(Qs + ri * MMA_PITCH + ch * 8) = make_uint4(0, 0, 0, 0);
+                if (qsplit) *reinterpret_cast<uint4*>(Qlo + ri * MMA_PITCH + ch * 8) = make_uint4(0, 0, 0, 0);
             }
         }
         cp_async_wait_all();
@@ -158,6 +163,11 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
                     ldsm_x4(smem_u32(Qs + row * MMA_PITCH + col), a0, a1, a2, a3);
                     mma16816(sacc[mt][0], a0, a1, a2, a3, b0, b1);
                     mma16816(sacc[mt][1], a0, a1, a2, a3, b2, b3);
+                    if (qsplit) {      // q_lo K^T into the same scores
+                        ldsm_x4(smem_u32(Qlo + row * MMA_PITCH + col), a0, a1, a2, a3);
+                        mma16816(sacc[mt][0], a0, a1, a2, a3, b0, b1);
+                        mma16816(sacc[mt][1], a0, a1, a2, a3, b2, b3);
+                    }
                 }
             }
         }
@@ -314,7 +324,7 @@ __device__ __forceinline__ void attn_combine_row_dpl(const AttnArgs& a, int r, i
     const size_t m = (size_t)b * a.T + t;
     T* dst = static_cast<T*>(a.o) + (m * a.hq + (size_t)g * G + hh) * a.hd + lane * DPL;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) dst[e] = from_f32<T>(o[e] / l);
+    for (int e = 0; e < DPL; ++e) store_split<T>(dst + e, a.o_lo_off, o[e] / l);
 }
 
 // Combine of the splits of one query row r of kv head g of sequence b, by one warp (lane =

@@ -9,6 +9,11 @@
 //  * EPI_RESID  : the pair is (2p, 2p + 1) -> X[m][n] += acc (fp32 residual stream);
 //  * EPI_STORE  : the pair is (2p, 2p + 1) -> out[m][n] = acc (fp32 logits).
 //
+// Split activations (tensor-core path): a bf16 GEMM input x is stored as two bf16 halves,
+// hi = bf16(x) and lo = bf16(x - hi), lo_off elements apart, and the GEMM accumulates
+// W hi + W lo (about 16 significant bits of x instead of 8); the queries are split the same
+// way for the attention.  lo_off = 0 stores hi only.
+//
 // Fused RMSNorm (tensor-core GEMM only): RMSNorm(x) W^T = (x * g) W^T / rms(x), so a
 // residual epilogue that also writes xg = bf16(x_new * g_next) and, per 128-column tile
 // of x, the sum of x_new^2 lets the GEMM that consumes the normed row apply 1/rms(x) to
@@ -41,6 +46,8 @@ struct EpiArgs {
     // RESID / STORE
     float* x;                   // [M][ldx]
     int ldx;
+    size_t lo_off;              // split activations: elements from a hi value to its lo half
+    int m0;                     // token offset of this launch (rows m0 .. m0 + M - 1)
     // fused RMSNorm, producer side (RESID): xg_out = bf16(x_new * g_next), ssq_out[t][m] =
     // sum of x_new[m][n]^2 over the 128 columns n of tile t (fixed order)
     void* xg_out;               // [M][ldx] bf16 or nullptr
@@ -63,6 +70,16 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Store v at p, and its bf16 remainder at p + lo_off when lo_off != 0 (bf16 only).
+template <typename T> __device__ __forceinline__ void store_split(T* p, size_t lo_off, float v);
+template <> __device__ __forceinline__ void store_split<float>(float* p, size_t, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void store_split<__nv_bfloat16>(__nv_bfloat16* p, size_t lo_off, float v) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    *p = h;
+    if (lo_off) p[lo_off] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
 // Row pair of pair index p for the QKV layout: head slot hs in [0, hq + 2 hkv), j < hd/2.
 __device__ __forceinline__ void qkv_pair_rows(int p, int hd, int& hs, int& j) {
     const int half = hd >> 1;
@@ -71,7 +88,8 @@ __device__ __forceinline__ void qkv_pair_rows(int p, int hd, int& hs, int& j) {
 }
 
 template <typename T>
-__device__ __forceinline__ void epi_pair(const EpiArgs& e, int m, int p, float a0, float a1) {
+__device__ __forceinline__ void epi_pair(const EpiArgs& e, int m_local, int p, float a0, float a1) {
+    const int m = m_local + e.m0;
     switch (e.kind) {
     case EPI_QKV: {
         int hs, j;
@@ -86,8 +104,8 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& e, int m, int p, float a
         }
         if (hs < e.hq) {
             T* q = static_cast<T*>(e.q_out) + (size_t)m * e.hq * e.hd + (size_t)hs * e.hd;
-            q[j] = from_f32<T>(a0);
-            q[j + half] = from_f32<T>(a1);
+            store_split<T>(q + j, e.lo_off, a0);
+            store_split<T>(q + j + half, e.lo_off, a1);
         } else {
             const bool is_k = hs < e.hq + e.hkv;
             const int kvh = is_k ? hs - e.hq : hs - e.hq - e.hkv;
@@ -100,7 +118,7 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& e, int m, int p, float a
         break;
     }
     case EPI_SWIGLU:
-        static_cast<T*>(e.h_out)[(size_t)m * e.F + p] = from_f32<T>(silu_f(a0) * a1);
+        store_split<T>(static_cast<T*>(e.h_out) + (size_t)m * e.F + p, e.lo_off, silu_f(a0) * a1);
         break;
     case EPI_RESID: {
         float* x = e.x + (size_t)m * e.ldx + 2 * p;

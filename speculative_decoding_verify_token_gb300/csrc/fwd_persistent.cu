@@ -64,6 +64,8 @@ struct PfParams {
     const void* const* gains;   // [2L + 1]: attn_norm and ffn_norm of each layer, final_norm
     int L, d, hq, hkv, hd, F, V;
     int M, T, B, ntok;
+    BRows br;                   // rows of the activation operand (split activations)
+    int x_lo_row;               // first lo row of the split activations (= M)
     int stages, atoms, stage_bytes;
     int l2_ahead;               // weight atoms prefetched into L2 ahead of the ring
     EpiArgs eq, eo, es, ed, el;  // epilogues of QKV, O, gate/up, down, lm_head (layer fields set per phase)
@@ -349,7 +351,7 @@ __device__ __noinline__ long long pf_activations(const PfParams& P, const PfShar
     const int S = P.stages;
     const int cta = blockIdx.x;
     const uint32_t b_off = (uint32_t)(P.atoms * TC_ATOM_A);
-    const uint32_t per_atom_b = (uint32_t)(P.ntok * TC_ATOM * 2);
+    const uint32_t per_atom_b = (uint32_t)(P.br.nb * TC_ATOM * 2);
     long long i = 0;
     for (int ph = 0; ph <= 4 * P.L; ++ph) {
         const PhGeom g = ph_geom(P, ph);
@@ -373,9 +375,15 @@ __device__ __noinline__ long long pf_activations(const PfParams& P, const PfShar
             const uint32_t fb = smem_u32(&sh.full_b[s]);
             mbar_arrive_expect_tx(fb, (uint32_t)n * per_atom_b);
             const uint32_t b_dst = sh.base + (uint32_t)s * P.stage_bytes + b_off;
-            for (int at = 0; at < n; ++at)
-                for (int t = 0; t < P.ntok / 16; ++t)
-                    tma_load_2d(b_dst + at * per_atom_b + t * 2048, g.x, (kt + at) * TC_ATOM, t * 16, fb, px);
+            for (int at = 0; at < n; ++at) {
+                const int kc = (kt + at) * TC_ATOM;
+                const uint32_t b_at = b_dst + at * per_atom_b;
+                for (int t = 0; t < P.br.nr0 / 16; ++t)
+                    tma_load_2d(b_at + t * 2048, g.x, kc, P.br.b_row0 + t * 16, fb, px);
+                if (P.br.b_row1 >= 0)
+                    for (int t = 0; t < (P.br.nb - P.br.nr0) / 16; ++t)
+                        tma_load_2d(b_at + (P.br.nr0 + t * 16) * 128, g.x, kc, P.br.b_row1 + t * 16, fb, px);
+            }
             ++i;
             w.g += n;
             if (sl) seg0 = w.g;
@@ -388,7 +396,8 @@ __device__ __noinline__ long long pf_activations(const PfParams& P, const PfShar
 __device__ __noinline__ long long pf_mma(const PfParams& P, const PfShared& sh, uint32_t tmem) {
     const int S = P.stages;
     const int cta = blockIdx.x;
-    const uint32_t idesc = idesc_bf16(P.ntok);
+    const int acc_cols = P.br.acc_stride;
+    const uint32_t idesc = idesc_bf16(P.br.nb);     // at most 64 rows: one MMA
     const uint32_t b_off = (uint32_t)(P.atoms * TC_ATOM_A);
     long long i = 0;
     int si = 0;
@@ -408,7 +417,7 @@ __device__ __noinline__ long long pf_mma(const PfParams& P, const PfShared& sh, 
                 if (!pf_bar_wait(smem_u32(&sh.acce[buf]), (uint32_t)(((si >> 1) & 1) ^ 1), sh.abort_flag, P.err))
                     return i;
                 tc_fence_after();
-                d_tmem = tmem + (uint32_t)(buf * P.ntok);
+                d_tmem = tmem + (uint32_t)(buf * acc_cols);
             }
             const int s = (int)(i % S);
             const uint32_t par = (uint32_t)((i / S) & 1);
@@ -418,14 +427,11 @@ __device__ __noinline__ long long pf_mma(const PfParams& P, const PfShared& sh, 
             tc_fence_after();
             if (w.g == s0) PF_STAMP(ph, 3);
             const uint32_t a_addr = sh.base + (uint32_t)s * P.stage_bytes;
-            for (int at = 0; at < n; ++at) {
-                const uint64_t ad = smem_desc_sw128(a_addr + at * TC_ATOM_A);
-                const uint64_t bd = smem_desc_sw128(a_addr + b_off + at * P.ntok * TC_ATOM * 2);
-#pragma unroll
-                for (int kk = 0; kk < TC_ATOM / 16; ++kk)
-                    mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                             (!sf || at > 0 || kk > 0) ? 1u : 0u);
-            }
+            const uint64_t ad0 = smem_desc_sw128(a_addr), bd0 = smem_desc_sw128(a_addr + b_off);
+            const uint64_t a_step = TC_ATOM_A >> 4, b_step = (uint64_t)(P.br.nb * TC_ATOM * 2) >> 4;
+            for (int at = 0; at < n; ++at)
+                mma_bf16_atom(d_tmem, ad0 + (uint64_t)at * a_step, bd0 + (uint64_t)at * b_step, idesc,
+                              (!sf || at > 0) ? 1u : 0u);
             mma_commit(smem_u32(&sh.empty_bar[s]));
             ++i;
             w.g += n;
@@ -490,12 +496,12 @@ __device__ __noinline__ bool pf_gemm_epilogue(const PfParams& P, const PfShared&
 #ifdef PF_TRACE
         t_acc = globaltimer_ns();
 #endif
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * P.ntok);
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * P.br.acc_stride);
         bool finished = false;
         if (full_tile) {
             for (int c0 = 0; c0 < P.ntok; c0 += TC_CW) {
                 float v[16];
-                tmem_ld16(taddr + c0, v);
+                acc_ld16(taddr, c0, P.br.lo_col, v);
                 if (c0 + TC_CW >= P.ntok) {
                     tc_fence_before();
                     mbar_arrive(smem_u32(&sh.acce[buf]));
@@ -512,7 +518,7 @@ __device__ __noinline__ bool pf_gemm_epilogue(const PfParams& P, const PfShared&
             float* dst = P.partial + (((size_t)cta * 2 + which) * TC_BM + row) * P.ntok;
             for (int c0 = 0; c0 < P.ntok; c0 += TC_CW) {
                 float v[16];
-                tmem_ld16(taddr + c0, v);
+                acc_ld16(taddr, c0, P.br.lo_col, v);
 #pragma unroll
                 for (int j = 0; j < 16; j += 4)
                     *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -611,12 +617,21 @@ __device__ __noinline__ void pf_embed(const PfParams& P) {
             const uint2 gu = *reinterpret_cast<const uint2*>(gain + c);
             const float4 gg = make_float4(__uint_as_float(gu.x << 16), __uint_as_float(gu.x & 0xffff0000u),
                                           __uint_as_float(gu.y << 16), __uint_as_float(gu.y & 0xffff0000u));
-            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * gg.x, v.y * gg.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * gg.z, v.w * gg.w);
+            const float4 y = make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w);
+            __nv_bfloat162 h01 = __floats2bfloat162_rn(y.x, y.y);
+            __nv_bfloat162 h23 = __floats2bfloat162_rn(y.z, y.w);
             uint2 o;
-            o.x = *reinterpret_cast<uint32_t*>(&lo);
-            o.y = *reinterpret_cast<uint32_t*>(&hi);
+            o.x = *reinterpret_cast<uint32_t*>(&h01);
+            o.y = *reinterpret_cast<uint32_t*>(&h23);
             *reinterpret_cast<uint2*>(P.Xn + (size_t)m * P.d + c) = o;
+            if (P.br.lo_col) {   // bf16 remainders (split activations)
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                __nv_bfloat162 l01 = __floats2bfloat162_rn(y.x - f01.x, y.y - f01.y);
+                __nv_bfloat162 l23 = __floats2bfloat162_rn(y.z - f23.x, y.w - f23.y);
+                o.x = *reinterpret_cast<uint32_t*>(&l01);
+                o.y = *reinterpret_cast<uint32_t*>(&l23);
+                *reinterpret_cast<uint2*>(P.Xn + (size_t)P.x_lo_row * P.d + (size_t)m * P.d + c) = o;
+            }
             float sq = v.x * v.x;
             sq = fmaf(v.y, v.y, sq);
             sq = fmaf(v.z, v.z, sq);
@@ -727,10 +742,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_kernel(const __grid_constant
     sh.att.Ks = reinterpret_cast<__nv_bfloat16*>(gbase + (size_t)P.stages * P.stage_bytes + TC_XBYTES);
     sh.att.Vs = sh.att.Ks + MMA_SPLIT * MMA_PITCH;
     sh.att.Qs = sh.att.Vs + MMA_SPLIT * MMA_PITCH;
-    sh.att.Ps = sh.att.Qs + MMA_RT * MMA_PITCH;
+    sh.att.Qlo = sh.att.Qs + MMA_RT * MMA_PITCH;
+    sh.att.Ps = sh.att.Qlo + MMA_RT * MMA_PITCH;
     sh.att.wmax = wmax;
     sh.att.wsum = wsum;
-    const uint32_t ncols = (uint32_t)max(32, 1 << (32 - __clz(2 * P.ntok - 1)));
+    const int acc_cols = P.br.acc_stride;
+    const uint32_t ncols = (uint32_t)max(32, 1 << (32 - __clz(2 * acc_cols - 1)));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.stages; ++s) {
@@ -902,7 +919,9 @@ int pf_launch(Ctx& c, int B, int T, const EpiArgs& eq, const EpiArgs& eo, const 
     P.F = m.ffn_dim; P.V = m.vocab;
     P.M = B * T; P.T = T; P.B = B;
     P.ntok = (P.M + 15) & ~15;
-    const int per_atom = TC_ATOM_A + P.ntok * TC_ATOM * 2;
+    P.br = b_rows(c.split, P.M, 0, P.M);
+    P.x_lo_row = P.M;
+    const int per_atom = TC_ATOM_A + P.br.nb * TC_ATOM * 2;
     const int budget = PF_SMEM_LIMIT - pl->static_smem - 1024 - TC_XBYTES - (int)MMA_SMEM;
     P.atoms = std::max(1, std::min(PF_MAX_ATOMS, c.pf_atoms));
     while (P.atoms > 1 && budget / (P.atoms * per_atom) < 2) P.atoms >>= 1;

@@ -47,7 +47,8 @@ struct TcParams {
     CUtensorMap xmap;
     int gid;
     int n_tiles, KB;          // tiles; K atoms per tile (the stream-K unit)
-    int ntok, M, x_row0;
+    int ntok, M, x_row0;      // ntok = M rounded up to 16 (stride of the partial sums)
+    BRows br;                 // rows of the activation operand (split activations)
     int stages, stage_bytes;  // ring slots; bytes per slot
     int atoms;                // most atoms per stage (stages never cross a segment end)
     int hq, hkv;
@@ -88,7 +89,10 @@ __device__ __forceinline__ void load_atom_a(const TcParams& p, int tile, int kc,
 }
 
 __device__ __forceinline__ void load_atom_b(const TcParams& p, int kc, uint32_t b_dst, uint32_t fb, uint64_t pol) {
-    for (int t = 0; t < p.ntok / 16; ++t) tma_load_2d(b_dst + t * 2048, &p.xmap, kc, p.x_row0 + t * 16, fb, pol);
+    for (int t = 0; t < p.br.nr0 / 16; ++t) tma_load_2d(b_dst + t * 2048, &p.xmap, kc, p.br.b_row0 + t * 16, fb, pol);
+    if (p.br.b_row1 >= 0)
+        for (int t = 0; t < (p.br.nb - p.br.nr0) / 16; ++t)
+            tma_load_2d(b_dst + (p.br.nr0 + t * 16) * 128, &p.xmap, kc, p.br.b_row1 + t * 16, fb, pol);
 }
 
 __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(const __grid_constant__ TcParams p) {
@@ -108,7 +112,10 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
     const long long T = (long long)p.n_tiles * p.KB;
     const long long s0 = range_start(T, G, cta), s1 = range_start(T, G, cta + 1);
     const int S = p.stages;
-    const uint32_t ncols = (uint32_t)max(32, 1 << (32 - __clz(2 * p.ntok - 1)));
+    // accumulator buffers of br.acc_stride columns: two while they fit the 512 TMEM columns
+    const int acc_cols = p.br.acc_stride;
+    const int nbuf = 2 * acc_cols <= 512 ? 2 : 1;
+    const uint32_t ncols = (uint32_t)min(512, max(32, 1 << (32 - __clz(nbuf * acc_cols - 1))));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
             const uint64_t px = policy_evict_last();
             // The first ring's worth of weight tiles does not depend on the previous kernel:
             // issue it before waiting for that kernel, then the activations.
-            const uint32_t per_atom_tx = (uint32_t)(TC_ATOM_A + p.ntok * TC_ATOM * 2);
+            const uint32_t per_atom_tx = (uint32_t)(TC_ATOM_A + p.br.nb * TC_ATOM * 2);
             const uint32_t b_off = (uint32_t)(p.atoms * TC_ATOM_A);
             StageWalk w(s0, s1, p.KB, p.atoms);
             long long i = 0;
@@ -168,7 +175,8 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                     w2.cur(n, tile, kt, sf, sl, sg);
                     const uint32_t b_dst = base + (uint32_t)j * p.stage_bytes + b_off;
                     for (int at = 0; at < n; ++at)
-                        load_atom_b(p, (kt + at) * TC_ATOM, b_dst + at * p.ntok * TC_ATOM * 2, smem_u32(&full_bar[j]), px);
+                        load_atom_b(p, (kt + at) * TC_ATOM, b_dst + at * p.br.nb * TC_ATOM * 2, smem_u32(&full_bar[j]),
+                                    px);
                     w2.g += n;
                     if (sl) sg = w2.g;
                 }
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 const uint32_t a_dst = base + (uint32_t)s * p.stage_bytes;
                 for (int at = 0; at < n; ++at) {
                     load_atom_a(p, tile, (kt + at) * TC_ATOM, a_dst + at * TC_ATOM_A, fb, pw);
-                    load_atom_b(p, (kt + at) * TC_ATOM, a_dst + b_off + at * p.ntok * TC_ATOM * 2, fb, px);
+                    load_atom_b(p, (kt + at) * TC_ATOM, a_dst + b_off + at * p.br.nb * TC_ATOM * 2, fb, px);
                 }
                 w.g += n;
                 if (sl) seg0 = w.g;
@@ -210,7 +218,13 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(p.ntok);
+            // one MMA of N = br.nb while that fits an instruction, else two (rows [0, 256)
+            // and [256, nb) of B into the matching accumulator columns)
+            const int nb = p.br.nb;
+            const bool one = nb <= TC_MMA_NMAX;
+            const uint32_t idesc = idesc_bf16(one ? nb : TC_MMA_NMAX);
+            const uint32_t idesc1 = one ? 0u : idesc_bf16(nb - TC_MMA_NMAX);
+            const uint64_t a_step = TC_ATOM_A >> 4, b_step = (uint64_t)(nb * TC_ATOM * 2) >> 4;
             const uint32_t b_off = (uint32_t)(p.atoms * TC_ATOM_A);
             StageWalk w(s0, s1, p.KB, p.atoms);
             long long i = 0, seg0 = s0;
@@ -221,14 +235,14 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 int n, tile, kt;
                 bool sf, sl;
                 w.cur(n, tile, kt, sf, sl, seg0);
-                const int buf = si & 1;
+                const int buf = si % nbuf;
                 if (sf) {
-                    if (!mbar_wait(smem_u32(&acce[buf]), (uint32_t)(((si >> 1) & 1) ^ 1))) {
+                    if (!mbar_wait(smem_u32(&acce[buf]), (uint32_t)(((si / nbuf) & 1) ^ 1))) {
                         atomicExch(p.err, SPEC_E_TIMEOUT);
                         break;
                     }
                     tc_fence_after();
-                    d_tmem = tmem + (uint32_t)(buf * p.ntok);
+                    d_tmem = tmem + (uint32_t)(buf * acc_cols);
                 }
                 const int s = (int)(i % S);
                 if (!mbar_wait(smem_u32(&full_bar[s]), (uint32_t)((i / S) & 1))) {
@@ -239,13 +253,22 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 if (i == 0) TC_STAMP(2);
                 tc_fence_after();
                 const uint32_t a_addr = base + (uint32_t)s * p.stage_bytes;
-                for (int at = 0; at < n; ++at) {
-                    const uint64_t ad = smem_desc_sw128(a_addr + at * TC_ATOM_A);
-                    const uint64_t bd = smem_desc_sw128(a_addr + b_off + at * p.ntok * TC_ATOM * 2);
-#pragma unroll
-                    for (int kk = 0; kk < TC_ATOM / 16; ++kk)
-                        mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                                 (!sf || at > 0 || kk > 0) ? 1u : 0u);
+                // descriptors of atom 0; each further atom is TC_ATOM_A (A) and nb rows of 128 B
+                // (B) further on (the address field counts 16-byte units)
+                const uint64_t ad0 = smem_desc_sw128(a_addr);
+                const uint64_t bd0 = smem_desc_sw128(a_addr + b_off);
+                if (one) {
+                    for (int at = 0; at < n; ++at)
+                        mma_bf16_atom(d_tmem, ad0 + (uint64_t)at * a_step, bd0 + (uint64_t)at * b_step, idesc,
+                                      (!sf || at > 0) ? 1u : 0u);
+                } else {
+                    // B rows [0, 256) into columns [0, 256), rows [256, nb) into [256, nb)
+                    for (int at = 0; at < n; ++at) {
+                        const uint64_t ad = ad0 + (uint64_t)at * a_step, bd = bd0 + (uint64_t)at * b_step;
+                        mma_bf16_atom(d_tmem, ad, bd, idesc, (!sf || at > 0) ? 1u : 0u);
+                        mma_bf16_atom(d_tmem + TC_MMA_NMAX, ad, bd + (uint64_t)((TC_MMA_NMAX * TC_ATOM * 2) >> 4),
+                                      idesc1, (!sf || at > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(smem_u32(&empty_bar[s]));
                 ++i;
@@ -283,19 +306,19 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
             const long long tile_k0 = (long long)tile * p.KB;
             const long long seg_end = min(s1, tile_k0 + p.KB);
             const bool full_tile = (g == tile_k0) && (seg_end == tile_k0 + p.KB);
-            const int buf = si & 1;
-            const bool okw = mbar_wait(smem_u32(&accf[buf]), (uint32_t)((si >> 1) & 1));
+            const int buf = si % nbuf;
+            const bool okw = mbar_wait(smem_u32(&accf[buf]), (uint32_t)((si / nbuf) & 1));
             if (epi_any(okw ? 0 : 1)) {
                 if (etid == 0) atomicExch(p.err, SPEC_E_TIMEOUT);
                 break;
             }
             tc_fence_after();
             if (etid == 0 && seg_end == s1) TC_STAMP(4);
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.ntok);
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * acc_cols);
             if (full_tile) {
                 for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
                     float v[16];
-                    tmem_ld16(taddr + c0, v);
+                    acc_ld16(taddr, c0, p.br.lo_col, v);
                     if (c0 + TC_CW >= p.ntok) {
                         tc_fence_before();
                         mbar_arrive(smem_u32(&acce[buf]));
@@ -311,7 +334,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 float* dst = p.partial + (((size_t)cta * 2 + which) * TC_BM + row) * p.ntok;
                 for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
                     float v[16];
-                    tmem_ld16(taddr + c0, v);
+                    acc_ld16(taddr, c0, p.br.lo_col, v);
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
                         *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -435,7 +458,7 @@ static int make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
 bool tc_supported(const Ctx& c) {
     const spec_model_cfg& m = c.cfg;
     return m.dtype == SPEC_BF16 && m.head_dim == 128 && m.d_model % 128 == 0 && m.vocab % 128 == 0 &&
-           m.ffn_dim % 64 == 0 && (m.n_q_heads * m.head_dim) % 64 == 0 && c.Mmax <= TC_MAX_NTOK && encode_fn();
+           m.ffn_dim % 64 == 0 && (m.n_q_heads * m.head_dim) % 64 == 0 && encode_fn();
 }
 
 int tc_create(Ctx& c) {
@@ -457,14 +480,15 @@ int tc_create(Ctx& c) {
             break;
     }
     if (rc == SPEC_OK) rc = make_map(&t->lm, c.w.lm_head, V, d, 64);
-    if (rc == SPEC_OK) rc = make_map(&t->xn, c.Xn, c.Mmax, d, 16);
-    if (rc == SPEC_OK) rc = make_map(&t->xo, c.O, c.Mmax, qd, 16);
-    if (rc == SPEC_OK) rc = make_map(&t->xh, c.H, c.Mmax, F, 16);
+    // GEMM inputs as [2][Mmax][cols]: bf16 hi rows, then the lo remainders
+    if (rc == SPEC_OK) rc = make_map(&t->xn, c.Xn, 2 * (uint64_t)c.Mmax, d, 16);
+    if (rc == SPEC_OK) rc = make_map(&t->xo, c.O, 2 * (uint64_t)c.Mmax, qd, 16);
+    if (rc == SPEC_OK) rc = make_map(&t->xh, c.H, 2 * (uint64_t)c.Mmax, F, 16);
     t->grid = c.num_sms * TC_CTAS_PER_SM;
     const int max_tiles = (int)std::max<uint64_t>({V / 128, F / 64, d / 128, qd / 128 + 2 * kvd / 128});
     if (rc == SPEC_OK) {
         void *a = nullptr, *b = nullptr, *e = nullptr;
-        if (cudaMalloc(&a, sizeof(float) * (size_t)t->grid * 2 * TC_BM * TC_MAX_NTOK) != cudaSuccess ||
+        if (cudaMalloc(&a, sizeof(float) * (size_t)t->grid * 2 * TC_BM * ((c.Mmax + 15) & ~15)) != cudaSuccess ||
             cudaMalloc(&b, sizeof(int) * (size_t)max_tiles) != cudaSuccess ||
             cudaMalloc(&e, sizeof(int)) != cudaSuccess) {
             rc = set_error(SPEC_E_NOMEM, "tensor-core GEMM workspace allocation failed");
@@ -489,6 +513,7 @@ int tc_create(Ctx& c) {
     }
     c.tc = t;
     c.use_tc = true;
+    c.split = true;
     return SPEC_OK;
 }
 
@@ -500,6 +525,7 @@ void tc_destroy(Ctx& c) {
     delete c.tc;
     c.tc = nullptr;
     c.use_tc = false;
+    c.split = false;
 }
 
 #ifdef TC_TRACE
@@ -559,7 +585,8 @@ static void gemm_geometry(const Ctx& c, int gid, int layer, CUtensorMap* maps, i
     }
 }
 
-int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, cudaStream_t st) {
+static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int pass_M, const EpiArgs& e,
+                          cudaStream_t st) {
     TcGemm* t = c.tc;
     const spec_model_cfg& m = c.cfg;
     if (M < 1 || M > TC_MAX_NTOK) return set_error(SPEC_E_RANGE, "GEMM with M=%d tokens (max %d)", M, TC_MAX_NTOK);
@@ -598,9 +625,10 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, 
     // the widest stage (most K atoms) that still leaves TC_MIN_STAGES ring slots; the
     // stream-K split is in atoms, so this choice changes no result bit
     const int budget = TC_SMEM_MAX - 1024 - TC_XBYTES;
-    const int per_atom = TC_ATOM_A + p.ntok * TC_ATOM * 2;
+    p.br = b_rows(c.split, M, p.x_row0, pass_M);
+    const int per_atom = TC_ATOM_A + p.br.nb * TC_ATOM * 2;
     p.atoms = 1;
-    for (int a = TC_MAX_ATOMS; a > 1; a >>= 1)
+    for (int a = TC_MAX_ATOMS; a > 1; --a)
         if (budget / (a * per_atom) >= TC_MIN_STAGES) { p.atoms = a; break; }
     p.stage_bytes = p.atoms * per_atom;
     p.stages = std::min(TC_MAX_STAGES, budget / p.stage_bytes);
@@ -639,6 +667,31 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, const EpiArgs& e, 
     const cudaError_t err = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, p);
     if (err != cudaSuccess) return set_error(SPEC_E_CUDA, "tc_gemm_kernel launch: %s", cudaGetErrorString(err));
     return 1;
+}
+
+// More tokens than one launch holds run as launches over equal chunks of whole 16-token
+// groups (each streams the weights again); every token sees the same arithmetic as in a
+// single launch, so the results do not depend on the split.
+int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, int pass_M, const EpiArgs& e, cudaStream_t st) {
+    if (M <= TC_MAX_NTOK) return tc_gemm_launch(c, gid, layer, X, M, pass_M, e, st);
+    const spec_model_cfg& m = c.cfg;
+    const int Kdim = gid == GEMM_O ? m.n_q_heads * m.head_dim : (gid == GEMM_DOWN ? m.ffn_dim : m.d_model);
+    const int n = (M + TC_MAX_NTOK - 1) / TC_MAX_NTOK;
+    int launched = 0, m0 = 0;
+    for (int i = 0; i < n; ++i) {
+        const int rest = M - m0, parts = n - i;
+        const int chunk = std::min(rest, (((rest + parts - 1) / parts) + 15) & ~15);
+        EpiArgs ec = e;
+        ec.M = chunk;
+        ec.m0 = e.m0 + m0;
+        if (ec.ssq_in) ec.ssq_row0 = e.ssq_row0 + m0;
+        const int r = tc_gemm_launch(c, gid, layer, static_cast<const uint8_t*>(X) + (size_t)m0 * Kdim * 2, chunk, pass_M,
+                                     ec, st);
+        if (r < 0) return r;
+        launched += r;
+        m0 += chunk;
+    }
+    return launched;
 }
 
 }  // namespace sv

@@ -38,6 +38,8 @@ struct AttnArgs {
     float* part_o;            // [B][hkv][n_chunks][T*G][hd]
     float2* part_ml;          // [B][hkv][n_chunks][T*G]
     int* att_cnt;             // [slots * hkv] arrival counters, zero between passes
+    size_t q_lo_off;          // split activations: elements from a query (output) value to
+    size_t o_lo_off;          // its bf16 lo half; 0 = not split
 };
 
 struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
@@ -74,10 +76,13 @@ struct Ctx {
     // activations
     int Mmax = 0;
     float* X = nullptr;             // [Mmax][d]
+    // GEMM inputs and queries; bf16 models hold two halves, [2][Mmax][...] (hi, then the
+    // lo remainders, used by the tensor-core path)
     void* Xn = nullptr;             // [Mmax][d]
     void* Q = nullptr;              // [Mmax][hq*hd]
     void* O = nullptr;              // [Mmax][hq*hd]
     void* H = nullptr;              // [Mmax][F]
+    bool split = false;             // activations split into bf16 hi + lo (tensor-core path)
     // fused RMSNorm (tensor-core path): per-128-column-tile sums of squares of the residual
     // stream feeding the attention norm (a) and the FFN norm (f), [d/128][Mmax] each
     float* ssq_a = nullptr;
@@ -141,7 +146,8 @@ int attention_split_keys(int hd, int esize);
 int tc_create(Ctx& c);                       // plans + tensor maps, after weights are loaded
 void tc_destroy(Ctx& c);
 // returns kernels launched, or a negative SPEC_E_* code
-int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, const EpiArgs& e, cudaStream_t st);
+// X = first row of the launch's tokens within the GEMM input of a pass of pass_M tokens
+int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, int pass_M, const EpiArgs& e, cudaStream_t st);
 bool tc_supported(const Ctx& c);
 int tc_error_word(Ctx& c, int* out);          // device error word of the tensor-core GEMM (synchronous)
 

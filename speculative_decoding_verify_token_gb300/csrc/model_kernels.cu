@@ -39,7 +39,7 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
                              const int* __restrict__ seq_len, int T_per_seq, const T* __restrict__ E,
                              float* __restrict__ X, int* __restrict__ tok_seq, int* __restrict__ tok_pos, int d,
                              int V, T* __restrict__ Xg, const T* __restrict__ g, float* __restrict__ ssq,
-                             int ssq_ld) {
+                             int ssq_ld, size_t lo_off) {
     pdl_launch_dependents();
     const int m = blockIdx.x;
     const int b = m / T_per_seq;
@@ -64,7 +64,13 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
         const float4 v = Quad<T>::load(row + c);
         *reinterpret_cast<float4*>(xr + c) = v;
         const float4 gg = Quad<T>::load(g + c);
-        Quad<T>::store(Xg + (size_t)m * d + c, make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w));
+        const float4 y = make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w);
+        Quad<T>::store(Xg + (size_t)m * d + c, y);
+        if (lo_off) {      // bf16 remainder (split activations)
+            const float4 h = make_float4(to_f32<T>(from_f32<T>(y.x)), to_f32<T>(from_f32<T>(y.y)),
+                                         to_f32<T>(from_f32<T>(y.z)), to_f32<T>(from_f32<T>(y.w)));
+            Quad<T>::store(Xg + lo_off + (size_t)m * d + c, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
+        }
         float sq = v.x * v.x;
         sq = fmaf(v.y, v.y, sq);
         sq = fmaf(v.z, v.z, sq);
@@ -161,11 +167,12 @@ void launch_embed(const Ctx& c, int M, int T, cudaStream_t st, bool fused_norm) 
         embed_kernel<bf><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T, static_cast<const bf*>(c.w.embed),
                                             c.X, c.d_tok_seq, c.d_tok_pos, c.cfg.d_model, c.cfg.vocab,
                                             fused_norm ? static_cast<bf*>(c.Xn) : nullptr,
-                                            static_cast<const bf*>(c.w.layers[0].attn_norm), c.ssq_a, c.Mmax);
+                                            static_cast<const bf*>(c.w.layers[0].attn_norm), c.ssq_a, c.Mmax,
+                                            c.split ? (size_t)M * c.cfg.d_model : 0);
     } else {
         embed_kernel<float><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T,
                                                static_cast<const float*>(c.w.embed), c.X, c.d_tok_seq, c.d_tok_pos,
-                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0);
+                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0, 0);
     }
 }
 

@@ -216,10 +216,10 @@ static inline void* layer_pool(const Ctx& c, void* pool, int l) {
 }
 
 static int gemm(Ctx& c, int gid, int layer, const void* wa, const void* wb, const void* wc, int K, int n_pairs,
-                const void* X, const EpiArgs& e) {
+                const void* X, const EpiArgs& e, int pass_M) {
     ProfScope ps(c, gid, gemm_weight_bytes(c, gid));
     if (c.use_tc) {
-        const int n = tc_gemm(c, gid, layer, X, e.M, e, c.stream);
+        const int n = tc_gemm(c, gid, layer, X, e.M, pass_M, e, c.stream);
         if (n < 0) return n;
         c.launches += n;
         return SPEC_OK;
@@ -257,20 +257,26 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         if (!fused) return;
         e.xg_out = c.Xn; e.g_next = g; e.ssq_out = ssq; e.ssq_ld = c.Mmax;
     };
+    // split activations: the lo halves of a pass of M tokens follow its M hi rows
+    const size_t qlo = c.split ? (size_t)M * hq * hd : 0;
     EpiArgs eq{};
     eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
     eq.tok_seq = c.d_tok_seq; eq.tok_pos = c.d_tok_pos; eq.rope = c.d_rope; eq.hq = hq; eq.hkv = hkv; eq.hd = hd;
     norm_in(eq, c.ssq_a, 0);
+    eq.lo_off = qlo;
     EpiArgs er{};
     er.kind = EPI_RESID; er.M = M; er.x = c.X; er.ldx = d;
+    er.lo_off = c.split ? (size_t)M * d : 0;
     EpiArgs es{};
     es.kind = EPI_SWIGLU; es.M = M; es.h_out = c.H; es.F = F;
+    es.lo_off = c.split ? (size_t)M * F : 0;
     norm_in(es, c.ssq_f, 0);
     AttnArgs aa{};
     aa.q = c.Q; aa.o = c.O; aa.block_table = c.d_block_table; aa.max_pages = c.max_pages; aa.seq_ids = c.d_seq_ids;
     aa.seq_len = c.d_seq_len; aa.T = T; aa.hq = hq; aa.hkv = hkv; aa.hd = hd; aa.scale = 1.0f / sqrtf((float)hd);
     aa.n_chunks = c.n_chunks; aa.part_o = c.part_o; aa.part_ml = c.part_ml;
     aa.split_keys = c.split_keys; aa.att_cnt = c.att_cnt;
+    aa.q_lo_off = qlo; aa.o_lo_off = qlo;
 
     int rc;
     if (fused && !last_only && logits_out != nullptr && pf_usable(c, M)) {
@@ -300,7 +306,7 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         }
         eq.k_layer = layer_pool(c, c.k_pool, l);
         eq.v_layer = layer_pool(c, c.v_pool, l);
-        if ((rc = gemm(c, GEMM_QKV, l, L.wq, L.wk, L.wv, d, (hq + 2 * hkv) * hd / 2, c.Xn, eq)) != SPEC_OK) return rc;
+        if ((rc = gemm(c, GEMM_QKV, l, L.wq, L.wk, L.wv, d, (hq + 2 * hkv) * hd / 2, c.Xn, eq, M)) != SPEC_OK) return rc;
         aa.k_layer = eq.k_layer;
         aa.v_layer = eq.v_layer;
         {
@@ -308,14 +314,14 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
             c.launches += launch_attention(c, aa, B, max_after, st);
         }
         norm_out(er, c.ssq_f, L.ffn_norm);
-        if ((rc = gemm(c, GEMM_O, l, L.wo, nullptr, nullptr, hq * hd, d / 2, c.O, er)) != SPEC_OK) return rc;
+        if ((rc = gemm(c, GEMM_O, l, L.wo, nullptr, nullptr, hq * hd, d / 2, c.O, er, M)) != SPEC_OK) return rc;
         if (!fused) {
             launch_rmsnorm(c, c.X, L.ffn_norm, c.Xn, M, st);
             c.launches += 1;
         }
-        if ((rc = gemm(c, GEMM_GU, l, L.wg, L.wu, nullptr, d, F, c.Xn, es)) != SPEC_OK) return rc;
+        if ((rc = gemm(c, GEMM_GU, l, L.wg, L.wu, nullptr, d, F, c.Xn, es, M)) != SPEC_OK) return rc;
         norm_out(er, c.ssq_a, l + 1 < m.n_layers ? c.w.layers[l + 1].attn_norm : c.w.final_norm);
-        if ((rc = gemm(c, GEMM_DOWN, l, L.wd, nullptr, nullptr, F, d / 2, c.H, er)) != SPEC_OK) return rc;
+        if ((rc = gemm(c, GEMM_DOWN, l, L.wd, nullptr, nullptr, F, d / 2, c.H, er, M)) != SPEC_OK) return rc;
     }
     if (logits_out != nullptr) {
         const int rows = last_only ? 1 : M;
@@ -328,7 +334,7 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         el.kind = EPI_STORE; el.M = rows; el.x = logits_out; el.ldx = m.vocab;
         norm_in(el, c.ssq_a, (int)off);
         if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2,
-                       static_cast<uint8_t*>(c.Xn) + off * d * c.esize, el)) != SPEC_OK)
+                       static_cast<uint8_t*>(c.Xn) + off * d * c.esize, el, M)) != SPEC_OK)
             return rc;
     }
     cudaError_t e = cudaGetLastError();
@@ -418,16 +424,17 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
     c->layer_pool_elems = (size_t)lim.num_pages * m.n_kv_heads * SPEC_PAGE_TOKENS * m.head_dim;
     int rc = SPEC_OK;
     auto ok = [&](int r) { rc = r; return r == SPEC_OK; };
+    const size_t halves = c->esize == 2 ? 2 : 1;    // bf16: hi and lo halves of the GEMM inputs
     if (!(ok(dalloc(*c, &c->k_pool, c->layer_pool_elems * m.n_layers * c->esize, true)) &&
           ok(dalloc(*c, &c->v_pool, c->layer_pool_elems * m.n_layers * c->esize, true)) &&
           ok(dalloc(*c, &c->d_block_table, sizeof(int) * (size_t)lim.max_batch * max_pages, true)) &&
           ok(dalloc(*c, &c->d_seq_len, sizeof(int) * lim.max_batch, true)) &&
           ok(dalloc(*c, &c->d_rope, sizeof(float2) * (size_t)lim.max_ctx * (m.head_dim / 2))) &&
           ok(dalloc(*c, &c->X, sizeof(float) * (size_t)c->Mmax * m.d_model, true)) &&
-          ok(dalloc(*c, &c->Xn, (size_t)c->esize * c->Mmax * m.d_model, true)) &&
-          ok(dalloc(*c, &c->Q, (size_t)c->esize * c->Mmax * qd, true)) &&
-          ok(dalloc(*c, &c->O, (size_t)c->esize * c->Mmax * qd, true)) &&
-          ok(dalloc(*c, &c->H, (size_t)c->esize * c->Mmax * m.ffn_dim, true)) &&
+          ok(dalloc(*c, &c->Xn, halves * c->esize * c->Mmax * m.d_model, true)) &&
+          ok(dalloc(*c, &c->Q, halves * c->esize * c->Mmax * qd, true)) &&
+          ok(dalloc(*c, &c->O, halves * c->esize * c->Mmax * qd, true)) &&
+          ok(dalloc(*c, &c->H, halves * c->esize * c->Mmax * m.ffn_dim, true)) &&
           ok(dalloc(*c, &c->ssq_a, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&
           ok(dalloc(*c, &c->ssq_f, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&
           ok(dalloc(*c, &c->logits, sizeof(float) * (size_t)c->Mmax * m.vocab)) &&

@@ -17,7 +17,8 @@ constexpr int TC_THREADS = 192;
 constexpr int TC_BM = 128;
 constexpr int TC_ATOM = 64;                          // K elements per atom = accumulation unit
 constexpr int TC_ATOM_A = TC_BM * TC_ATOM * 2;       // 16 KB: one 128-row x 64 A atom
-constexpr int TC_MAX_NTOK = 256;
+constexpr int TC_MAX_NTOK = 256;                    // tokens of one launch (more: several launches)
+constexpr int TC_MMA_NMAX = 256;                    // N of one tcgen05.mma (M = 128)
 constexpr int TC_MAX_STAGES = 8;
 constexpr int TC_CW = 16;                           // epilogue column chunk
 constexpr int TC_XPITCH = TC_CW + 1;
@@ -59,6 +60,24 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
+// The four MMAs of one 64-column K atom (K = 16 each; descriptors advance by 32 bytes = 2
+// units), in one asm block so that the issuing thread spends as few instructions as
+// possible between them: the weight stream waits on this thread.  acc = 0 starts a new
+// accumulation with the first of them.
+__device__ __forceinline__ void mma_bf16_atom(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n\t}"
+        :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc), "l"(a + 2), "l"(b + 2), "l"(a + 4), "l"(b + 4),
+           "l"(a + 6), "l"(b + 6)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
@@ -76,6 +95,56 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Accumulator values of tokens c0 .. c0 + 15 in this thread's TMEM lane.  With split
+// activations the token's W x_lo product sits lo_col columns after its W x_hi product and
+// the two are added (hi + lo, in that order):
+//  * lo_col = 0: not split;
+//  * lo_col >= 16 (a multiple of 16): hi and lo in separate 16-column groups;
+//  * 1 <= lo_col <= 8 (packed, at most 8 tokens, c0 = 0): hi in columns [0, lo_col), lo in
+//    [lo_col, 2 lo_col) of the one 16-column group.
+__device__ __forceinline__ void acc_ld16(uint32_t taddr, int c0, int lo_col, float (&v)[16]) {
+    tmem_ld16(taddr + (uint32_t)c0, v);
+    if (lo_col >= 16) {
+        float w[16];
+        tmem_ld16(taddr + (uint32_t)(c0 + lo_col), w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += w[j];
+    } else if (lo_col > 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float lo = 0.0f;
+#pragma unroll
+            for (int k = 1; k <= 8; ++k)
+                if (k == lo_col) lo = v[j + k];
+            v[j] += lo;
+        }
+    }
+}
+
+// Rows of the activation operand B of one launch over tokens [x_row0, x_row0 + M) of a pass
+// of pass_M tokens whose split activations hold hi rows [0, pass_M) and lo rows
+// [pass_M, 2 pass_M).
+struct BRows {
+    int nb;       // rows of B (the MMA N)
+    int nr0;      // rows of the first range, from row b_row0
+    int b_row0, b_row1;   // second range (nb - nr0 rows) from b_row1, or -1
+    int lo_col;   // see acc_ld16
+    int acc_stride;       // TMEM columns per accumulator buffer
+};
+__host__ __device__ inline BRows b_rows(bool split, int M, int x_row0, int pass_M) {
+    const int ntok = (M + 15) & ~15;
+    BRows r;
+    if (!split) {
+        r.nb = r.nr0 = ntok; r.b_row0 = x_row0; r.b_row1 = -1; r.lo_col = 0; r.acc_stride = ntok;
+    } else if (M <= 8 && x_row0 == 0 && M == pass_M) {
+        r.nb = r.nr0 = 16; r.b_row0 = 0; r.b_row1 = -1; r.lo_col = M; r.acc_stride = 16;
+    } else {
+        r.nr0 = ntok; r.nb = 2 * ntok; r.b_row0 = x_row0; r.b_row1 = pass_M + x_row0; r.lo_col = ntok;
+        r.acc_stride = 2 * ntok;
+    }
+    return r;
+}
 
 // 1 if any of the 128 epilogue threads passes pred != 0 (and a barrier among them).
 __device__ __forceinline__ int epi_any(int pred) {
@@ -168,20 +237,26 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
         for (int cc = half; cc < TC_CW; cc += 2) {
             const int m = c0 + cc;
             if (m >= M) break;        // uniform over a warp: a warp holds one half
-            float2* x = reinterpret_cast<float2*>(e.x + (size_t)m * e.ldx + n0);
+            float2* x = reinterpret_cast<float2*>(e.x + (size_t)(m + e.m0) * e.ldx + n0);
             float2 xv = __ldcg(x);        // written by other CTAs of a persistent pass: not from L1
             xv.x += xs[r0 * TC_XPITCH + cc];
             xv.y += xs[r1 * TC_XPITCH + cc];
             *x = xv;
-            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(e.xg_out) + (size_t)m * e.ldx + n0) =
-                __floats2bfloat162_rn(xv.x * g.x, xv.y * g.y);
+            const float y0 = xv.x * g.x, y1 = xv.y * g.y;
+            __nv_bfloat16* xg = static_cast<__nv_bfloat16*>(e.xg_out) + (size_t)(m + e.m0) * e.ldx + n0;
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(y0, y1);
+            *reinterpret_cast<__nv_bfloat162*>(xg) = hi;
+            if (e.lo_off) {
+                const float2 hf = __bfloat1622float2(hi);
+                *reinterpret_cast<__nv_bfloat162*>(xg + e.lo_off) = __floats2bfloat162_rn(y0 - hf.x, y1 - hf.y);
+            }
             const float sq = warp_sum(fmaf(xv.x, xv.x, xv.y * xv.y));
             if ((etid & 31) == 0) red[half * 2 + wq][cc] = sq;
         }
         epi_bar();
         if (etid < TC_CW && c0 + etid < M) {
             const int h = etid & 1;
-            e.ssq_out[(size_t)tile * e.ssq_ld + c0 + etid] = red[2 * h][etid] + red[2 * h + 1][etid];
+            e.ssq_out[(size_t)tile * e.ssq_ld + e.m0 + c0 + etid] = red[2 * h][etid] + red[2 * h + 1][etid];
         }
         return;
     }

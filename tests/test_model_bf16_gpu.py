@@ -58,11 +58,11 @@ def test_prefill_logits_match_oracle(lib, w):
     m.close()
 
 
-@pytest.mark.parametrize("B,K", [(1, 4), (3, 7), (8, 15), (16, 15)])
+@pytest.mark.parametrize("B,K", [(1, 4), (3, 7), (8, 15), (16, 15), (32, 8), (20, 15)])
 def test_verify_rows_match_oracle_and_decode_bitwise(lib, w, B, K):
     V = synth.SMALL_BF16.vocab
-    m = make(lib, w, max_batch=B, max_ctx=256, max_k=K)
-    dec = make(lib, w, max_batch=B, max_ctx=256, max_k=K)
+    m = make(lib, w, max_batch=B, max_ctx=512, max_k=K)
+    dec = make(lib, w, max_batch=B, max_ctx=512, max_k=K)
     prompts = [synth.prompt_tokens(20 + b, 17 + 9 * b, V) for b in range(B)]
     for b, p in enumerate(prompts):
         m.prefill(b, torch.from_numpy(p[:-1]).cuda())

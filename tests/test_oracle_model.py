@@ -101,3 +101,32 @@ def test_generator_reproducible_and_distribution():
     small_chunks = synth.normal_tensor(synth.tensor_key(0, "x", "y"), (1 << 12,), 1.0,
                                        dtype=torch.float32, chunk=1000)
     assert torch.equal(small_chunks, big[:1 << 12])
+
+
+def test_round_bf16_ties_and_library():
+    """Nearest bfloat16 with ties to even: hand-worked cases at 1 (spacing 2^-7), then the
+    same rounding as torch's float32 -> bfloat16 conversion on float32 values."""
+    r = om.round_bf16
+    assert r(1.0 + 2.0 ** -8) == 1.0                               # tie, even mantissa below
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6               # tie, even mantissa above
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -20) == 1.0 + 2.0 ** -7      # just above the tie
+    assert r(-(1.0 + 3 * 2.0 ** -8)) == -(1.0 + 2.0 ** -6)
+    assert r(0.0) == 0.0 and r(3.0) == 3.0 and r(1.0 / 3.0) == 0.333984375
+    x = np.random.default_rng(5).standard_normal(100000).astype(np.float32) * 7.0
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(r(x.astype(np.float64)), ref)
+
+
+def test_bf16_shape_caches_rounded_keys():
+    """A bf16 model's cache holds bf16 keys and values; the float32 model's does not."""
+    s = synth.SMALL_BF16
+    w = {n: synth.model_weight(s, n) for n in synth.weight_names(s)}
+    o = om.Decoder(s, w)
+    c = o.new_cache()
+    o.forward([1, 2, 3], c, logits_rows=np.zeros(0, dtype=np.int64))
+    assert np.array_equal(c.k[0], om.round_bf16(c.k[0])) and np.array_equal(c.v[1], om.round_bf16(c.v[1]))
+    t = synth.TINY_TARGET
+    o32 = om.Decoder(t, synth.model_weights(t))
+    c32 = o32.new_cache()
+    o32.forward([1, 2, 3], c32)
+    assert not np.array_equal(c32.k[0], om.round_bf16(c32.k[0]))
