@@ -592,8 +592,10 @@ def main():
     wl = WORKLOADS[args.workload](n_gen=args.gen, layers=args.layers) if args.workload == DenseVerifyWorkload.name \
         else WORKLOADS[args.workload]()
     n_total = args.warmup + args.steps
+    # a created stream: the legacy default stream serialises programmatic dependent launches
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
     wl.setup(dev, max(n_total, args.profile_steps))
-    stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
         wl.step(i)

@@ -8,25 +8,26 @@
 // of "What is Speculative Decoding and How Does a Draft Model Work?" ("#2": keep drafts
 // while they equal the target's choice, replace the first mismatch).
 //
-// GB300 design:
-//  * persistent grid of 3 CTAs x 8 warps per SM; every warp streams one (row, chunk) work
-//    item at a time with coalesced 16-byte streaming loads, 8 in flight per lane (about
-//    100 KB of HBM reads in flight per SM), handed out by a global atomic counter so the
-//    warps stay balanced whatever B, K and V are (the index of the next item is fetched
-//    one item ahead);
-//  * each warp keeps an exact running top-k of its item as a warp-wide sorted list (one
-//    entry per lane); the common path per 1024 elements is a lane maximum and one vote
-//    against the running cut, which is the larger of the list's k-th value and a lower
-//    bound of the row's k-th value shared by all chunks of the row (atomicMax on an
-//    order-preserving integer key); the rare candidates go to a shared-memory buffer and
-//    through a bitonic sort + merge 32 at a time;
-//  * the last warp to finish a row (atomic arrival count, no spin-wait) merges the chunk
-//    lists and builds the row's truncated distribution; the last row of a sequence runs
-//    the acceptance scan and the final inverse-CDF draw on one warp.
+// GB300 design, two kernels:
+//  * pass 1 streams every needed row once, with coalesced 16-byte streaming loads (two
+//    blocks of 4 KB in flight per warp, 16 warps per SM), and writes for each 256-element
+//    fine block its largest element with that element's id and its second largest element
+//    (12 bytes per KB read); eight lanes own a fine block, so the reductions are 3-step
+//    shuffles within the group;
+//  * pass 2 (one warp per row, launched programmatically dependent on pass 1) ranks the
+//    fine blocks' maxima: tau, the k-th largest of the 32 lanes' maxima, bounds the row's
+//    k-th largest element from below, the maxima >= tau are sorted and merged 32 at a time
+//    into the row's top list, and only the blocks whose second largest element reaches
+//    that list's k-th value can hold a further top-k element -- on random rows about one
+//    row in five re-reads one fine block (1 KB).  Ties and adversarial rows stay exact;
+//  * the row's truncated distribution is built from that list, and the last row of a
+//    sequence to finish (atomic arrival count, no spin-wait) runs the acceptance scan and
+//    the final inverse-CDF draw on one warp.
 #include <cstdio>
 #include <cstring>
 #include <cmath>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -34,18 +35,39 @@
 
 namespace sv {
 
-constexpr int VT_WARPS = 8;
-constexpr int VT_THREADS = VT_WARPS * 32;
-constexpr int VT_BLOCKS_PER_SM = 2;
-constexpr int VS_UNROLL = 8;                         // 16-byte loads per lane per iteration (x2 in flight)
-constexpr int VT_CHUNK_QUANTUM = 1024;               // chunk sizes are multiples of this
 constexpr int LISTN = 32;
-constexpr int VT_TARGET_ITEMS = 4096;
-constexpr int VT_MAX_CHUNKS = 128;
 constexpr int VT_MAX_K = 64;
-// per-warp candidate buffer: a flush leaves < 32 entries and one iteration adds at most
-// 32 * 4 * VS_UNROLL, so it never overflows
-constexpr int VT_CAND_CAP = 32 + 32 * 4 * 8;
+constexpr int VB = 1024;                             // elements per block (the pass-1 unit, coarse maxima)
+constexpr int VB4 = VB / 4;                          // float4 per block
+constexpr int VF = 256;                              // elements per fine block (fine maxima, pass-2 reads)
+constexpr int NF = VB / VF;                          // fine blocks per block
+constexpr int BM_THREADS = 256;                      // pass 1 CTA
+#ifndef BM_CTAS_PER_SM
+#define BM_CTAS_PER_SM 2                             // 16 warps per SM
+#endif
+constexpr int BM_INFLIGHT = 2;                       // blocks loaded at once per warp
+// registers per pass-1 thread: 16 warps of pass 1 leave room for one pass-2 CTA per SM
+#ifndef BM_MAXNREG
+#define BM_MAXNREG 96
+#endif
+#ifndef BM_SMEM_CARVEOUT
+#define BM_SMEM_CARVEOUT 13                         // per cent of L1 kept as shared memory
+#endif
+#ifndef BM_STATIC_PCT
+#define BM_STATIC_PCT 75                             // share of pass-1 blocks in static sweeps
+#endif
+constexpr int RF_WARPS = 4;                          // pass 2: one warp per row, 4 rows per CTA
+constexpr int RF_THREADS = RF_WARPS * 32;
+constexpr int RF_BPL = 5;                            // blocks' second values a lane holds per round
+constexpr int RF_KPL = 2 * RF_BPL;                   // float4 of (maximum, id) pairs a lane holds per round
+constexpr int RF_BATCH = 8;                          // fine blocks loaded at once per warp
+constexpr int RF_SEL_CAP = 64;                       // fine blocks listed before they are read again
+// per-warp candidate buffer, merged into the warp's list of 32 before an append could
+// overflow it (appends come 64 or 128 at a time)
+constexpr int RF_CAND_CAP = 192;
+// pass-2 CTAs per SM the register budget must allow: one beside pass 1's 16 warps of 96
+// registers (49152 of 65536) leaves 128 a thread
+constexpr int RF_MIN_CTAS = 4;
 
 enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
 
@@ -62,9 +84,7 @@ struct VerifyParams {
     int mode;
     int n_target_rows;          // B*(K+1) (verify) or R (sample)
     int n_rows;                 // + B*K draft rows when draft logits are given
-    int chunks;                 // chunks per row
-    int chunk_elems;            // body elements per chunk (multiple of VT_CHUNK_QUANTUM)
-    int n_items;                // n_rows * chunks
+    int nbb;                    // blocks per row (ceil(V / VB)); fine blocks NF * nbb
     int* accepted_len;
     int* next_token;
     int* out_ids;
@@ -72,12 +92,10 @@ struct VerifyParams {
     int* seq_status;
     int* out_tokens;
     // workspace
-    int* work;                  // [1] item counter
-    int* row_cnt;               // [n_rows]
-    int* seq_cnt;               // [B]
-    unsigned* row_bound;        // [n_rows] order-preserving key of a lower bound of the row's k-th best
-    float* cl_v;                // [n_rows][chunks][LISTN]
-    int* cl_id;
+    int* seq_cnt;               // [B] rows of the sequence finished
+    int* blk_next;              // pass-1 dynamic block counter
+    float2* fk;                 // [n_rows][NF * nbb] fine block (maximum, id of an element at it)
+    float* fm2;                 // [n_rows][NF * nbb] fine block second largest element
     int* rd_n;                  // [n_rows]
     int* rd_id;                 // [n_rows][LISTN]
     float* rd_p;
@@ -237,20 +255,40 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
         bool reject = false;
         a = kb;
         int d = -1;
-        for (int i = 0; i < kb; ++i) {
-            d = p.draft_tokens[(size_t)b * p.K + i];
-            const int pid = __ldcg(p.rd_id + (size_t)trow(p, b, i) * LISTN + lane);
-            const float pp = __ldcg(p.rd_p + (size_t)trow(p, b, i) * LISTN + lane);
-            const float pd = warp_max(pid == d ? pp : 0.0f);
-            float qd = 1.0f;
-            if (has_q) {
-                const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, i) * LISTN + lane);
-                const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, i) * LISTN + lane);
-                qd = warp_max(qid == d ? qp : 0.0f);
+        // the positions' P(d) and Q(d), 8 positions per round with their loads and warp
+        // reductions issued together; the scan stops at the first reject
+        constexpr int SB = 8;
+        bool done = false;
+        for (int i0 = 0; i0 < kb && !done; i0 += SB) {
+            float pd[SB], qd[SB];
+            int dt[SB];
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                const int i = i0 + j;
+                pd[j] = 0.0f; qd[j] = 1.0f; dt[j] = -1;
+                if (i < kb) {
+                    dt[j] = p.draft_tokens[(size_t)b * p.K + i];
+                    const int pid = __ldcg(p.rd_id + (size_t)trow(p, b, i) * LISTN + lane);
+                    const float pp = __ldcg(p.rd_p + (size_t)trow(p, b, i) * LISTN + lane);
+                    pd[j] = pid == dt[j] ? pp : 0.0f;
+                    if (has_q) {
+                        const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, i) * LISTN + lane);
+                        const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, i) * LISTN + lane);
+                        qd[j] = qid == dt[j] ? qp : 0.0f;
+                    }
+                }
             }
-            if (qd == 0.0f) { status = SPEC_E_DRAFT; a = i; break; }
-            const float ratio = pd / qd;
-            if (!(ub[i] < ratio)) { a = i; reject = true; break; }
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                pd[j] = warp_max(pd[j]);
+                if (has_q) qd[j] = warp_max(qd[j]);
+            }
+            for (int j = 0; j < SB && i0 + j < kb; ++j) {
+                d = dt[j];
+                if (qd[j] == 0.0f) { status = SPEC_E_DRAFT; a = i0 + j; done = true; break; }
+                const float ratio = pd[j] / qd[j];
+                if (!(ub[i0 + j] < ratio)) { a = i0 + j; reject = true; done = true; break; }
+            }
         }
         if (status == SPEC_OK) {
             const int prow = trow(p, b, a);
@@ -262,6 +300,7 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
                 if (has_q) {
                     const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, a) * LISTN + lane);
                     const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, a) * LISTN + lane);
+#pragma unroll
                     for (int t = 0; t < LISTN; ++t) {
                         const int tid = __shfl_sync(FULL, qid, t);
                         const float tp = __shfl_sync(FULL, qp, t);
@@ -291,30 +330,9 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
     }
 }
 
-// The last chunk of a row: merge the chunk lists, build the distribution, then either
-// sample (sample mode) or arrive on the sequence.
-__device__ void finish_row(const VerifyParams& p, int row, int lane) {
-    float lv = -INFINITY;
-    int lid = SENT_ID;
-    const size_t base = (size_t)row * p.chunks * LISTN;
-    constexpr int BATCH = 8;
-    for (int c0 = 0; c0 < p.chunks; c0 += BATCH) {
-        float bv[BATCH];
-        int bi[BATCH];
-#pragma unroll
-        for (int j = 0; j < BATCH; ++j) {
-            const int c = c0 + j;
-            if (c < p.chunks) {
-                bv[j] = __ldcg(p.cl_v + base + (size_t)c * LISTN + lane);
-                bi[j] = __ldcg(p.cl_id + base + (size_t)c * LISTN + lane);
-            } else {
-                bv[j] = -INFINITY; bi[j] = SENT_ID;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < BATCH; ++j)
-            if (c0 + j < p.chunks) warp_merge_desc(lv, lid, bv[j], bi[j], lane);
-    }
+// A row's exact top list (lane j = j-th best): build the distribution, then either sample
+// (sample mode) or arrive on the sequence; the sequence's last row runs the scan.
+__device__ void finish_row(const VerifyParams& p, int row, float lv, int lid, int lane) {
     build_row_dist(p, row, lv, lid, lane);
 
     if (p.mode == MODE_SAMPLE) {
@@ -330,181 +348,406 @@ __device__ void finish_row(const VerifyParams& p, int row, int lane) {
     const int b = ri.seq;
     const int kb = draft_count(p, b);
     const int expected = (kb + 1) + (p.draft != nullptr && p.temperature != 0.0f ? kb : 0);
-    __threadfence();
+    // arrival: releases this row's distribution, and the last row acquires the others'
     __syncwarp();
     int prev = 0;
-    if (lane == 0) prev = atomicAdd(p.seq_cnt + b, 1);
+    if (lane == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.seq_cnt + b) : "memory");
     prev = __shfl_sync(FULL, prev, 0);
-    if (prev == expected - 1) {
-        __threadfence();
-        finish_sequence(p, b, lane);
-    }
+    __syncwarp();
+    if (prev == expected - 1) finish_sequence(p, b, lane);
 }
 
 
-// One warp streams one (row, chunk) work item at a time: coalesced 16-byte streaming loads,
-// two register tiles of VS_UNROLL float4 per lane so that the next 4 KB of the row is in
-// flight while the current 4 KB is examined, 2 CTAs of 8 warps per SM.  Per 1024 elements
-// the common path is a lane maximum (per float4 first) and one vote against the running
-// cut; only the float4s whose maximum reaches the cut are looked at element by element.
-struct TopkState {
-    float lv, lb, published;
-    int lid, ccount;
-};
+__device__ __forceinline__ float max4(const float4& x) { return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)); }
 
-__device__ __forceinline__ void examine_tile(const VerifyParams& p, const float4 (&x)[VS_UNROLL], int i0, int s0,
-                                             bool first, unsigned rb_key, unsigned* rb_ptr, TopkState& st,
-                                             float* cbuf_v, int* cbuf_id, int* ccnt, int lane) {
-    const int k = p.top_k;
-    float mu[VS_UNROLL];
+__device__ __forceinline__ float comp4(const float4& x, int c) {
+    return c == 0 ? x.x : c == 1 ? x.y : c == 2 ? x.z : x.w;
+}
+
+// Fine blocks: fine block 4 b + g of block b is the 64 float4 of the block's lanes
+// [8 g, 8 g + 8) in pass 1 -- body float4 b * VB4 + l + 32 u for l in that range and u in
+// [0, 8).  A warp reading it again takes two of them per lane: l = 8 g + (lane & 7),
+// u = (lane >> 3) + 4 h.
+__device__ __forceinline__ int fine_float4(int fb, int lane, int h) {
+    const int b = fb >> 2, g = fb & 3;
+    return b * VB4 + 8 * g + (lane & 7) + 32 * ((lane >> 3) + 4 * h);
+}
+
+// Largest and second largest of four values (as a multiset: equal values count twice).
+__device__ __forceinline__ void top2_4(const float4& v, float& t1, float& t2) {
+    const float h1 = fmaxf(v.x, v.y), l1 = fminf(v.x, v.y);
+    const float h2 = fmaxf(v.z, v.w), l2 = fminf(v.z, v.w);
+    t1 = fmaxf(h1, h2);
+    t2 = fmaxf(fminf(h1, h2), fmaxf(l1, l2));
+}
+
+// Maximum over the 8-lane group of the calling lane.
+__device__ __forceinline__ float group8_max(float x) {
 #pragma unroll
-    for (int u = 0; u < VS_UNROLL; ++u) mu[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
-    float mx = mu[0];
+    for (int o = 1; o < 8; o <<= 1) x = fmaxf(x, __shfl_xor_sync(FULL, x, o));
+    return x;
+}
+
+// (a1, a2) <- the top two of the multiset union of (a1, a2) and (b1, b2).
+__device__ __forceinline__ void top2_merge(float& a1, float& a2, float b1, float b2) {
+    a2 = fmaxf(fminf(a1, b1), fmaxf(a2, b2));
+    a1 = fmaxf(a1, b1);
+}
+
+#ifdef VT_TRACE
+// Per-row timeline of the last refine launch (profiling builds only): [row][0, 1 start,
+// 2 tau, 3 candidates merged, 4 blocks read again, 5 row finished]
+__device__ unsigned long long g_vt_trace[4096][6];
+#define VT_STAMP(r, i) if (lane == 0 && (r) < 4096) g_vt_trace[r][i] = globaltimer_ns()
+// pass 1: [CTA][0 start, 1 end]
+__device__ unsigned long long g_vt_p1[1024][2];
+#define VT_P1_STAMP(i) if (threadIdx.x == 0 && blockIdx.x < 1024) g_vt_p1[blockIdx.x][i] = globaltimer_ns()
+extern "C" int spec_debug_vt_trace(unsigned long long* out) {
+    if (cudaMemcpyFromSymbol(out, g_vt_trace, sizeof(g_vt_trace)) != cudaSuccess) return -6;
+    return cudaMemcpyFromSymbol(out + 4096 * 6, g_vt_p1, sizeof(g_vt_p1)) == cudaSuccess ? 0 : -6;
+}
+#else
+#define VT_STAMP(r, i) ((void)0)
+#define VT_P1_STAMP(i) ((void)0)
+#endif
+
+// Pass 1: for every VF-element fine block of each needed row, its largest element with the
+// id of one element at that value, and its second largest element (fine block 0 also covers
+// the row's unaligned head and tail, at most 3 + 3 scalars).  A warp reads VB elements
+// (four fine blocks) at a time, BM_INFLIGHT such blocks before reducing any of them; the
+// last (100 - BM_STATIC_PCT) per cent of the blocks are handed out by a counter.
+__global__ void __maxnreg__(BM_MAXNREG) vt_stats_kernel(const VerifyParams p) {
+    pdl_launch_dependents();     // pass 2 may be scheduled now; it waits per row
+    const int lane = threadIdx.x & 31;
+    const long long nw = (long long)gridDim.x * (BM_THREADS / 32);
+    const long long total = (long long)p.n_rows * p.nbb;
+    const long long gw = (long long)blockIdx.x * (BM_THREADS / 32) + (threadIdx.x >> 5);
+    // BM_STATIC_PCT per cent of the blocks in static sweeps over all warps, the rest in
+    // pairs of consecutive blocks from a counter (SMs do not stream at the same rate)
+    const long long sweep = nw * BM_INFLIGHT;
+    const long long n_static = (total * BM_STATIC_PCT / 100) / sweep;
+    const long long dyn0 = n_static * sweep;
+    int nextb = 0;               // lane 0: the next dynamic grab, fetched one iteration ahead
+    if (n_static == 0 && lane == 0) nextb = atomicAdd(p.blk_next, BM_INFLIGHT);
+    VT_P1_STAMP(0);
+    for (long long it = 0;; ++it) {
+        long long w0, wstep;
+        if (it < n_static) {
+            w0 = gw + it * sweep;
+            wstep = nw;
+        } else {
+            w0 = dyn0 + __shfl_sync(FULL, nextb, 0);
+            wstep = 1;
+            if (w0 >= total) break;
+        }
+        float4 x[BM_INFLIGHT][VB4 / 32];
+        int row[BM_INFLIGHT], blk[BM_INFLIGHT];
+        bool act[BM_INFLIGHT];
+        const float* ptr[BM_INFLIGHT];
+        int head[BM_INFLIGHT], body[BM_INFLIGHT];
 #pragma unroll
-    for (int u = 1; u < VS_UNROLL; ++u) mx = fmaxf(mx, mu[u]);
-    if (first) {
-        // k distinct elements reach the k-th largest lane maximum: a lower bound of the
-        // chunk's (and the row's) k-th best.
-        float m = mx;
-        int dummy = lane;
-        warp_sort_desc(m, dummy, lane);
-        st.lb = __shfl_sync(FULL, m, k - 1);
-        if (lane == 0 && st.lb > -INFINITY) atomicMax(rb_ptr, float_key(st.lb));
-        st.published = st.lb;
-    }
-    st.lb = fmaxf(st.lb, key_float(rb_key));
-    const float cut = fmaxf(st.lb, __shfl_sync(FULL, st.lv, k - 1));
-    if (__any_sync(FULL, mx >= cut)) {
-        // value test only: an entry equal to the k-th value with a larger id is a harmless
-        // extra for the exact merge
-        if (mx >= cut) {
+        for (int j = 0; j < BM_INFLIGHT; ++j) {
+            const long long w = w0 + j * wstep;
+            act[j] = false;
+            row[j] = 0; blk[j] = 0; ptr[j] = nullptr; head[j] = 0; body[j] = 0;
+            if (w < total) {
+                row[j] = (int)(w / p.nbb);
+                blk[j] = (int)(w - (long long)row[j] * p.nbb);
+                const RowInfo ri = row_info(p, row[j]);
+                act[j] = row_needed(p, ri);
+                ptr[j] = ri.ptr;
+                row_split(ri.ptr, p.V, head[j], body[j]);
+            }
+            const int n4 = act[j] ? min(VB4, (body[j] >> 2) - blk[j] * VB4) : 0;
+            const float4* src = reinterpret_cast<const float4*>(ptr[j] + head[j]) + (size_t)blk[j] * VB4;
 #pragma unroll
-            for (int u = 0; u < VS_UNROLL; ++u) {
-                if (mu[u] >= cut) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float xc = pick4(x[u], q);
-                        if (xc >= cut) {
-                            const int pos = atomicAdd(ccnt, 1);
-                            cbuf_v[pos] = xc;
-                            cbuf_id[pos] = s0 + 4 * (i0 + lane + 32 * u) + q;
-                        }
-                    }
-                }
+            for (int u = 0; u < VB4 / 32; ++u) {
+                const int idx = lane + 32 * u;
+                x[j][u] = idx < n4 ? __ldcs(src + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
         }
-        __syncwarp();
-        st.ccount = *reinterpret_cast<volatile int*>(ccnt);
-    }
-    if (st.ccount >= 32 || (st.ccount > 0 && __shfl_sync(FULL, st.lid, k - 1) == SENT_ID)) {
-        flush_candidates(st.lv, st.lid, cbuf_v, cbuf_id, st.ccount, lane);
-        st.ccount = 0;
-        if (lane == 0) *ccnt = 0;
-        __syncwarp();
-    }
-    const float kth = __shfl_sync(FULL, st.lv, k - 1);
-    if (kth > st.published) {
-        if (lane == 0) atomicMax(rb_ptr, float_key(kth));
-        st.published = kth;
-        st.lb = fmaxf(st.lb, kth);
-    }
-}
-
-__device__ __forceinline__ void load_tile(float4 (&x)[VS_UNROLL], const float4* src, int i0, int n4, int lane) {
+        if (lane == 0 && it + 1 >= n_static) nextb = atomicAdd(p.blk_next, BM_INFLIGHT);
 #pragma unroll
-    for (int u = 0; u < VS_UNROLL; ++u) {
-        const int idx = i0 + lane + 32 * u;
-        x[u] = idx < n4 ? __ldcs(src + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int j = 0; j < BM_INFLIGHT; ++j) {
+            if (!act[j]) continue;      // uniform over the warp
+            // fine block g = lanes [8 g, 8 g + 8), all eight of their float4 (fine_block_lanes)
+            const int n4 = min(VB4, (body[j] >> 2) - blk[j] * VB4);
+            const int g = lane >> 3;
+            float a1 = -INFINITY, a2 = -INFINITY, hm[VB4 / 32];
+#pragma unroll
+            for (int u = 0; u < VB4 / 32; ++u) {
+                float t1, t2;
+                top2_4(x[j][u], t1, t2);
+                hm[u] = t1;
+                top2_merge(a1, a2, t1, t2);
+            }
+            float sh = -INFINITY, st = -INFINITY;               // block 0: head and tail scalars
+            int tail0 = 0;
+            if (blk[j] == 0) {
+                tail0 = head[j] + body[j];
+                if (lane < head[j]) sh = ptr[j][lane];
+                if (lane < p.V - tail0) st = ptr[j][tail0 + lane];
+                top2_merge(a1, a2, sh, -INFINITY);
+                top2_merge(a1, a2, st, -INFINITY);
+            }
+            const float M1 = group8_max(a1);
+            const unsigned eq = (__ballot_sync(FULL, a1 == M1) >> (8 * g)) & 0xffu;
+            const int L = 8 * g + __ffs(eq) - 1;
+            // the block's second largest: the other lanes' maxima and lane L's second
+            const float M2 = group8_max(lane == L ? a2 : a1);
+            // lane's first element (in id order: head, body, tail) equal to its maximum
+            int id = SENT_ID;
+            if (blk[j] == 0 && lane < p.V - tail0 && st == a1) id = tail0 + lane;
+            {
+                int uf = -1;
+#pragma unroll
+                for (int u = VB4 / 32 - 1; u >= 0; --u) uf = hm[u] == a1 ? u : uf;
+                if (uf >= 0 && lane + 32 * uf < n4) {
+                    float4 xv = x[j][0];
+#pragma unroll
+                    for (int u = 1; u < VB4 / 32; ++u) xv = uf == u ? x[j][u] : xv;
+                    const int c = xv.x == a1 ? 0 : xv.y == a1 ? 1 : xv.z == a1 ? 2 : 3;
+                    id = head[j] + 4 * (blk[j] * VB4 + lane + 32 * uf) + c;
+                }
+            }
+            if (blk[j] == 0 && lane < head[j] && sh == a1) id = lane;
+            const int idL = __shfl_sync(FULL, id, L);
+            // lane 0 stores the four blocks' statistics (group leaders 0, 8, 16, 24)
+            float r1[NF], r2[NF], rid[NF];
+#pragma unroll
+            for (int f = 0; f < NF; ++f) {
+                r1[f] = __shfl_sync(FULL, M1, 8 * f);
+                r2[f] = __shfl_sync(FULL, M2, 8 * f);
+                rid[f] = __int_as_float(__shfl_sync(FULL, idL, 8 * f));
+            }
+            if (lane == 0) {
+                static_assert(NF == 4, "a block's fine statistics are stored as float4s");
+                const size_t fi = (size_t)row[j] * p.nbb * NF + (size_t)blk[j] * NF;
+                float4* k4 = reinterpret_cast<float4*>(p.fk + fi);
+                k4[0] = make_float4(r1[0], rid[0], r1[1], rid[1]);
+                k4[1] = make_float4(r1[2], rid[2], r1[3], rid[3]);
+                *reinterpret_cast<float4*>(p.fm2 + fi) = make_float4(r2[0], r2[1], r2[2], r2[3]);
+            }
+        }
     }
+    VT_P1_STAMP(1);
 }
 
-__global__ void __launch_bounds__(VT_THREADS, VT_BLOCKS_PER_SM) verify_kernel(const VerifyParams p) {
-    __shared__ float cand_v[VT_WARPS][VT_CAND_CAP];
-    __shared__ int cand_id[VT_WARPS][VT_CAND_CAP];
-    __shared__ int ccnt_s[VT_WARPS];
+// Append each lane's (v, id) for which c holds to the warp's buffer, in lane order (ballot
+// + prefix count).
+__device__ __forceinline__ void append_if(bool c, float v, int id, float* cv, int* ci, int& cnt, int lane) {
+    const unsigned m = __ballot_sync(FULL, c);
+    if (c) {
+        const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+        cv[pos] = v;
+        ci[pos] = id;
+    }
+    cnt += __popc(m);
+}
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    float* cbuf_v = cand_v[warp];
-    int* cbuf_id = cand_id[warp];
-    int* ccnt = &ccnt_s[warp];
-    if (lane == 0) *ccnt = 0;
-    __syncwarp();
-    int pref = 0;
-    if (lane == 0) pref = atomicAdd(p.work, 1);
-    constexpr int STEP = 32 * VS_UNROLL;
+// Append each lane's index x for which c holds to the warp's list, in lane order.
+__device__ __forceinline__ void append_index(bool c, int x, int* list, int& n, int lane) {
+    const unsigned m = __ballot_sync(FULL, c);
+    if (c) list[n + __popc(m & ((1u << lane) - 1u))] = x;
+    n += __popc(m);
+}
 
-    while (true) {
-        // next needed work item (the index after it is fetched now and used next time)
-        int it = 0;
-        if (lane == 0) {
-            it = pref;
-            while (it < p.n_items && !row_needed(p, row_info(p, it / p.chunks))) it = atomicAdd(p.work, 1);
-            if (it < p.n_items) pref = atomicAdd(p.work, 1);
+// Read the n listed fine blocks of the row again, RF_BATCH at a time, and merge their
+// elements >= tau2 -- all but the block's recorded maximum (already listed) -- into the
+// warp's list (lv, lid).  cv/ci: the warp's candidate buffer (empty on entry and exit).
+__device__ __forceinline__ void reread_blocks(const VerifyParams& p, const RowInfo& ri, int row, const int* sel,
+                                              int n, float tau2, int head, int body, float& lv, int& lid, float* cv,
+                                              int* ci, int lane) {
+    const int n4_row = body >> 2;
+    const float4* src = reinterpret_cast<const float4*>(ri.ptr + head);
+    const size_t krow = (size_t)row * NF * p.nbb;
+    int cnt = 0;
+    for (int i0 = 0; i0 < n; i0 += RF_BATCH) {
+        int fb[RF_BATCH], skip[RF_BATCH];
+        float4 x[RF_BATCH][2];
+#pragma unroll
+        for (int j = 0; j < RF_BATCH; ++j) {
+            fb[j] = i0 + j < n ? sel[i0 + j] : -1;
+            skip[j] = fb[j] >= 0 ? __float_as_int(__ldcg(&p.fk[krow + fb[j]].y)) : SENT_ID;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int idx = fine_float4(fb[j], lane, h);
+                x[j][h] = (fb[j] >= 0 && idx < n4_row)
+                              ? __ldcs(src + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
         }
-        it = __shfl_sync(FULL, it, 0);
-        if (it >= p.n_items) break;
-        const int row = it / p.chunks, c = it % p.chunks;
-        const RowInfo ri = row_info(p, row);
-        int head, body;
-        row_split(ri.ptr, p.V, head, body);
-        const int s0 = head + min(c * p.chunk_elems, body);
-        const int s1 = head + min(body, (c + 1) * p.chunk_elems);
-        const float4* src = reinterpret_cast<const float4*>(ri.ptr + s0);
-        const int n4 = s1 > s0 ? (s1 - s0) >> 2 : 0;
-        unsigned* rb_ptr = p.row_bound + row;
-
-        TopkState st;
-        st.lv = -INFINITY; st.lb = -INFINITY; st.published = -INFINITY; st.lid = SENT_ID; st.ccount = 0;
-        float4 xa[VS_UNROLL], xb[VS_UNROLL];
-        if (n4 > 0) load_tile(xa, src, 0, n4, lane);
-        for (int i0 = 0; i0 < n4; i0 += 2 * STEP) {
-            unsigned rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
-            if (i0 + STEP < n4) load_tile(xb, src, i0 + STEP, n4, lane);
-            examine_tile(p, xa, i0, s0, i0 == 0, rb_key, rb_ptr, st, cbuf_v, cbuf_id, ccnt, lane);
-            if (i0 + STEP >= n4) break;
-            rb_key = *reinterpret_cast<volatile unsigned*>(rb_ptr);
-            if (i0 + 2 * STEP < n4) load_tile(xa, src, i0 + 2 * STEP, n4, lane);
-            examine_tile(p, xb, i0 + STEP, s0, false, rb_key, rb_ptr, st, cbuf_v, cbuf_id, ccnt, lane);
-        }
-        float lv = st.lv;
-        int lid = st.lid;
-        if (st.ccount > 0) {
-            flush_candidates(lv, lid, cbuf_v, cbuf_id, st.ccount, lane);
-            if (lane == 0) *ccnt = 0;
-            __syncwarp();
-        }
-        // scalar head / tail of the row
-        const int tail0 = head + body, tail = p.V - tail0;
-        if (c == 0 && head > 0) {
-            const bool has = lane < head;
-            offer_round(lv, lid, has, has ? ri.ptr[lane] : 0.0f, lane, lane);
-        }
-        if (c == p.chunks - 1 && tail > 0) {
-            const bool has = lane < tail;
-            offer_round(lv, lid, has, has ? ri.ptr[tail0 + lane] : 0.0f, tail0 + lane, lane);
-        }
-        // publish the chunk list; the last chunk of the row finishes it
-        const size_t o = ((size_t)row * p.chunks + c) * LISTN + lane;
-        p.cl_v[o] = lv;
-        p.cl_id[o] = lid;
-        __threadfence();
-        __syncwarp();
-        int prev = 0;
-        if (lane == 0) prev = atomicAdd(p.row_cnt + row, 1);
-        prev = __shfl_sync(FULL, prev, 0);
-        if (prev == p.chunks - 1) {
-            __threadfence();
-            finish_row(p, row, lane);
+#pragma unroll
+        for (int j = 0; j < RF_BATCH; ++j) {
+            if (fb[j] < 0) continue;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (cnt > RF_CAND_CAP - 128) {
+                    flush_candidates(lv, lid, cv, ci, cnt, lane);
+                    cnt = 0;
+                }
+                const int idx = fine_float4(fb[j], lane, h);
+                const int e = head + 4 * idx;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float v = comp4(x[j][h], c);
+                    append_if(idx < n4_row && e + c != skip[j] && v >= tau2, v, e + c, cv, ci, cnt, lane);
+                }
+            }
+            if (fb[j] == 0) {      // the unaligned head and tail belong to fine block 0
+                if (cnt > RF_CAND_CAP - 64) {
+                    flush_candidates(lv, lid, cv, ci, cnt, lane);
+                    cnt = 0;
+                }
+                const int tail0 = head + body;
+                const bool hok = lane < head, tok = lane < p.V - tail0;
+                const float hv = hok ? ri.ptr[lane] : -INFINITY;
+                const float tv = tok ? ri.ptr[tail0 + lane] : -INFINITY;
+                append_if(hok && lane != skip[j] && hv >= tau2, hv, lane, cv, ci, cnt, lane);
+                append_if(tok && tail0 + lane != skip[j] && tv >= tau2, tv, tail0 + lane, cv, ci, cnt, lane);
+            }
         }
     }
+    flush_candidates(lv, lid, cv, ci, cnt, lane);
+}
+
+// One row of pass 2 on one warp.  Candidates are the fine blocks' maxima:
+// tau, the k-th largest of the 32 lanes' maxima over their shares of them, is at most the
+// row's k-th largest element, so only blocks with a maximum >= tau can hold a top-k element
+// at their maximum.  The top list of those candidates has k-th value tau2; any element other
+// than a block's recorded maximum is at most the block's second largest value, so a block
+// whose second value is below tau2 holds nothing else of the top k.  The few blocks whose
+// second value reaches tau2 are read again and their other elements >= tau2 merged in.
+__device__ __forceinline__ void refine_row(const VerifyParams& p, int row, int lane, float* cv, int* ci, int* sel) {
+    const RowInfo ri = row_info(p, row);
+    if (!row_needed(p, ri)) return;
+    VT_STAMP(row, 0);
+    VT_STAMP(row, 1);
+    const int k = p.top_k;
+    const int nbb = p.nbb, nfb = NF * nbb;
+    const int nq = nfb / 2;                                  // float4 = two (maximum, id) pairs
+    const float4* kq = reinterpret_cast<const float4*>(p.fk + (size_t)row * nfb);
+    const float4* m2q = reinterpret_cast<const float4*>(p.fm2 + (size_t)row * nfb);
+    const float4 NEG = make_float4(-INFINITY, __int_as_float(SENT_ID), -INFINITY, __int_as_float(SENT_ID));
+    // the first round of (maximum, id) pairs and second values, loaded together
+    float4 kv[RF_KPL], mv[RF_BPL];
+#pragma unroll
+    for (int i = 0; i < RF_KPL; ++i) {
+        const int q = lane + 32 * i;
+        kv[i] = q < nq ? __ldcg(kq + q) : NEG;
+    }
+#pragma unroll
+    for (int i = 0; i < RF_BPL; ++i) {
+        const int b = lane + 32 * i;
+        mv[i] = b < nbb ? __ldcg(m2q + b) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    float lm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < RF_KPL; ++i) lm = fmaxf(lm, fmaxf(kv[i].x, kv[i].z));
+    for (int q = lane + 32 * RF_KPL; q < nq; q += 32) {
+        const float4 t = __ldcg(kq + q);
+        lm = fmaxf(lm, fmaxf(t.x, t.z));
+    }
+    int dummy = lane;
+    warp_sort_desc(lm, dummy, lane);
+    const float tau = __shfl_sync(FULL, lm, k - 1);
+    VT_STAMP(row, 2);
+
+    // candidates: the maxima >= tau
+    float lv = -INFINITY;
+    int lid = SENT_ID;
+    int cnt = 0;
+    for (int q0 = 0; q0 < nq; q0 += 32 * RF_KPL) {
+        if (q0 > 0) {
+#pragma unroll
+            for (int i = 0; i < RF_KPL; ++i) {
+                const int q = q0 + lane + 32 * i;
+                kv[i] = q < nq ? __ldcg(kq + q) : NEG;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RF_KPL; ++i) {
+            if (cnt > RF_CAND_CAP - 64) {
+                flush_candidates(lv, lid, cv, ci, cnt, lane);
+                cnt = 0;
+            }
+            const int id0 = __float_as_int(kv[i].y), id1 = __float_as_int(kv[i].w);
+            append_if(id0 != SENT_ID && kv[i].x >= tau, kv[i].x, id0, cv, ci, cnt, lane);
+            append_if(id1 != SENT_ID && kv[i].z >= tau, kv[i].z, id1, cv, ci, cnt, lane);
+        }
+    }
+    flush_candidates(lv, lid, cv, ci, cnt, lane);
+    cnt = 0;
+    const float tau2 = __shfl_sync(FULL, lv, k - 1);
+    VT_STAMP(row, 3);
+
+    // blocks whose second value reaches tau2: read again, every element >= tau2 but the
+    // recorded maximum joins the list.  Each lane keeps a bit per fine block of its share
+    // (RF_BPL blocks of 4) and hands them out one per step into the warp's list.
+    int head, body;
+    row_split(ri.ptr, p.V, head, body);
+    int n = 0;
+    for (int b0 = 0; b0 < nbb; b0 += 32 * RF_BPL) {
+        if (b0 > 0) {
+#pragma unroll
+            for (int i = 0; i < RF_BPL; ++i) {
+                const int b = b0 + lane + 32 * i;
+                mv[i] = b < nbb ? __ldcg(m2q + b) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+        }
+        unsigned bits = 0;
+#pragma unroll
+        for (int i = 0; i < RF_BPL; ++i) {
+            if (b0 + lane + 32 * i < nbb) {
+                bits |= (mv[i].x >= tau2 ? 1u : 0u) << (4 * i);
+                bits |= (mv[i].y >= tau2 ? 2u : 0u) << (4 * i);
+                bits |= (mv[i].z >= tau2 ? 4u : 0u) << (4 * i);
+                bits |= (mv[i].w >= tau2 ? 8u : 0u) << (4 * i);
+            }
+        }
+        while (true) {
+            const bool more = __any_sync(FULL, bits != 0);
+            if (more) {
+                int fbi = -1;
+                if (bits) {
+                    const int t = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    fbi = 4 * (b0 + lane + 32 * (t >> 2)) + (t & 3);
+                }
+                append_index(fbi >= 0, fbi, sel, n, lane);
+            }
+            const bool last = !more && b0 + 32 * RF_BPL >= nbb;
+            if (n > RF_SEL_CAP - 32 || (last && n > 0)) {
+                __syncwarp();
+                reread_blocks(p, ri, row, sel, n, tau2, head, body, lv, lid, cv, ci, lane);
+                n = 0;
+            }
+            if (!more) break;
+        }
+    }
+    VT_STAMP(row, 4);
+    finish_row(p, row, lv, lid, lane);
+    VT_STAMP(row, 5);
+}
+
+// Pass 2: one warp per row (refine_row), RF_WARPS rows per CTA.
+__global__ void __launch_bounds__(RF_THREADS, RF_MIN_CTAS) vt_refine_kernel(const VerifyParams p) {
+    __shared__ float cand_v[RF_WARPS][RF_CAND_CAP];
+    __shared__ int cand_id[RF_WARPS][RF_CAND_CAP];
+    __shared__ int sel_list[RF_WARPS][RF_SEL_CAP];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * RF_WARPS + warp;
+    // the grid is launched programmatically dependent on pass 1: its CTAs may be resident
+    // early (pass 1 keeps room for one per SM); the statistics are read after pass 1 is done
+    pdl_wait();
+    if (row < p.n_rows) refine_row(p, row, lane, cand_v[warp], cand_id[warp], sel_list[warp]);
 }
 
 // ---- host side ---------------------------------------------------------------------------
 
 struct Plan {
-    int n_rows, chunks, chunk_elems;
-    size_t off_work, off_row, off_seq, off_rb, off_clv, off_clid, off_rdn, off_rdid, off_rdp, total, counters_bytes;
+    int n_rows, nbb;
+    size_t off_seq, off_blk, off_fk, off_fm2, off_rdn, off_rdid, off_rdp, total, counters_bytes;
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -512,28 +755,14 @@ static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static Plan make_plan(int n_rows_max, int n_seq, int V) {
     Plan pl{};
     pl.n_rows = n_rows_max;
-    const int per_row = std::max(1, (VT_TARGET_ITEMS + n_rows_max - 1) / n_rows_max);
-    long long ch = ((long long)V + per_row - 1) / per_row;
-    ch = ((ch + VT_CHUNK_QUANTUM - 1) / VT_CHUNK_QUANTUM) * VT_CHUNK_QUANTUM;
-    if (ch < VT_CHUNK_QUANTUM) ch = VT_CHUNK_QUANTUM;
-    long long chunks = ((long long)V + ch - 1) / ch;
-    if (chunks > VT_MAX_CHUNKS) {
-        chunks = VT_MAX_CHUNKS;
-        ch = (((long long)V + chunks - 1) / chunks + VT_CHUNK_QUANTUM - 1) / VT_CHUNK_QUANTUM * VT_CHUNK_QUANTUM;
-        chunks = ((long long)V + ch - 1) / ch;
-    }
-    pl.chunks = (int)chunks;
-    pl.chunk_elems = (int)ch;
+    pl.nbb = (V + VB - 1) / VB;
     size_t o = 0;
-    pl.off_work = o; o += 4;
-    pl.off_row = o; o += (size_t)n_rows_max * 4;
     pl.off_seq = o; o += (size_t)n_seq * 4;
-    pl.off_rb = o; o += (size_t)n_rows_max * 4;
+    pl.off_blk = o; o += 4;
     pl.counters_bytes = o;
     o = align256(o);
-    const size_t lists = (size_t)n_rows_max * pl.chunks * LISTN;
-    pl.off_clv = o; o = align256(o + lists * 4);
-    pl.off_clid = o; o = align256(o + lists * 4);
+    pl.off_fk = o; o = align256(o + (size_t)n_rows_max * pl.nbb * NF * 8);
+    pl.off_fm2 = o; o = align256(o + (size_t)n_rows_max * pl.nbb * NF * 4);
     pl.off_rdn = o; o = align256(o + (size_t)n_rows_max * 4);
     pl.off_rdid = o; o = align256(o + (size_t)n_rows_max * LISTN * 4);
     pl.off_rdp = o; o = align256(o + (size_t)n_rows_max * LISTN * 4);
@@ -541,36 +770,58 @@ static Plan make_plan(int n_rows_max, int n_seq, int V) {
     return pl;
 }
 
-static int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+// SM count of the current device; the first call on a device also asks for pass 1's SMs to
+// keep shared memory configured (pass 1 uses none, and an SM whose carveout was sized for
+// it cannot take a pass-2 CTA until pass 1 leaves).
+static int device_setup() {
+    constexpr int MAX_DEV = 64;
+    static std::atomic<int> sms[MAX_DEV];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+    if (dev < MAX_DEV && sms[dev].load() > 0) return sms[dev].load();
+    std::lock_guard<std::mutex> lock(mu);
+    int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (cudaFuncSetAttribute(vt_stats_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             BM_SMEM_CARVEOUT) != cudaSuccess)
+        return -1;
+    if (dev < MAX_DEV) sms[dev].store(n);
     return n;
 }
 
 static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream_t st) {
     uint8_t* w = static_cast<uint8_t*>(ws);
-    prm.work = reinterpret_cast<int*>(w + pl.off_work);
-    prm.row_cnt = reinterpret_cast<int*>(w + pl.off_row);
     prm.seq_cnt = reinterpret_cast<int*>(w + pl.off_seq);
-    prm.row_bound = reinterpret_cast<unsigned*>(w + pl.off_rb);
-    prm.cl_v = reinterpret_cast<float*>(w + pl.off_clv);
-    prm.cl_id = reinterpret_cast<int*>(w + pl.off_clid);
+    prm.blk_next = reinterpret_cast<int*>(w + pl.off_blk);
+    prm.fk = reinterpret_cast<float2*>(w + pl.off_fk);
+    prm.fm2 = reinterpret_cast<float*>(w + pl.off_fm2);
     prm.rd_n = reinterpret_cast<int*>(w + pl.off_rdn);
     prm.rd_id = reinterpret_cast<int*>(w + pl.off_rdid);
     prm.rd_p = reinterpret_cast<float*>(w + pl.off_rdp);
-    prm.chunks = pl.chunks;
-    prm.chunk_elems = pl.chunk_elems;
-    prm.n_items = prm.n_rows * pl.chunks;
+    prm.nbb = pl.nbb;
 
     cudaError_t e = cudaMemsetAsync(ws, 0, pl.counters_bytes, st);
     if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
-    const int nsm = sm_count();
-    if (nsm <= 0) return set_error(SPEC_E_CUDA, "no CUDA device");
-    const int grid = std::max(1, std::min(nsm * VT_BLOCKS_PER_SM, (prm.n_items + VT_WARPS - 1) / VT_WARPS));
-    verify_kernel<<<grid, VT_THREADS, 0, st>>>(prm);
+    const int nsm = device_setup();
+    if (nsm <= 0) return set_error(SPEC_E_CUDA, "no CUDA device, or its verify kernel attributes could not be set");
+    const long long blocks = (long long)prm.n_rows * pl.nbb;
+    const long long warps_needed = (blocks + BM_INFLIGHT - 1) / BM_INFLIGHT;
+    const int grid1 = (int)std::max(1LL, std::min((long long)nsm * BM_CTAS_PER_SM, (warps_needed + 7) / 8));
+    vt_stats_kernel<<<grid1, BM_THREADS, 0, st>>>(prm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((prm.n_rows + RF_WARPS - 1) / RF_WARPS);
+    cfg.blockDim = dim3(RF_THREADS);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, vt_refine_kernel, prm);
+    if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "vt_refine_kernel launch: %s", cudaGetErrorString(e));
     e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "verify_kernel launch: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return set_error(SPEC_E_CUDA, "verify kernel launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
 }
 

@@ -4,6 +4,10 @@ the CPU oracle, on seeded synthetic logits.
 Bar: accepted lengths and emitted tokens bit-exact (a sequence whose oracle decision lies
 within 1e-6 of a boundary -- acceptance ratio, top-p cut or inverse-CDF step -- is
 excused), final-distribution ids exact and probabilities within 1e-5 absolute.
+
+The module runs on a created stream, where the per-row pass of the kernel starts while the
+streaming pass still runs (programmatic dependent launch); the full-size case also runs on
+the legacy default stream, where the two passes serialise.
 """
 import numpy as np
 import pytest
@@ -22,7 +26,11 @@ def sv():
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_verify_token_gb300 import verify
-    return verify
+    prev = torch.cuda.current_stream()
+    torch.cuda.set_stream(torch.cuda.Stream())
+    yield verify
+    torch.cuda.synchronize()
+    torch.cuda.set_stream(prev)
 
 
 def oracle_drafts(draft, u_draft, T, k, p):
@@ -149,9 +157,18 @@ def test_illegal_draft_status(sv):
     assert out["accepted_len"][1].item() == 0
 
 
-def test_full_size_standalone_verify_config(sv):
+@pytest.mark.parametrize("default_stream", [False, True])
+def test_full_size_standalone_verify_config(sv, default_stream):
     """The standalone-verify workload at full size: B=64, K=4, V=151936, T=1, k=20, p=0.95."""
-    res, out = run_case(sv, 3, 64, 4, 151936)
+    side = torch.cuda.current_stream()
+    if default_stream:
+        torch.cuda.synchronize()
+        torch.cuda.set_stream(torch.cuda.default_stream())
+    try:
+        res, out = run_case(sv, 3, 64, 4, 151936)
+    finally:
+        torch.cuda.synchronize()
+        torch.cuda.set_stream(side)
     assert compare(res, out) <= 2
     a = out["accepted_len"].cpu().numpy()
     assert a.min() >= 0 and a.max() <= 4
