@@ -14,15 +14,15 @@
 //    fine block its largest element with that element's id and its second largest element
 //    (12 bytes per KB read); eight lanes own a fine block, so the reductions are 3-step
 //    shuffles within the group;
-//  * pass 2 (one warp per row, launched programmatically dependent on pass 1) ranks the
-//    fine blocks' maxima: tau, the k-th largest of the 32 lanes' maxima, bounds the row's
-//    k-th largest element from below, the maxima >= tau are sorted and merged 32 at a time
-//    into the row's top list, and only the blocks whose second largest element reaches
-//    that list's k-th value can hold a further top-k element -- on random rows about one
-//    row in five re-reads one fine block (1 KB).  Ties and adversarial rows stay exact;
-//  * the row's truncated distribution is built from that list, and the last row of a
-//    sequence to finish (atomic arrival count, no spin-wait) runs the acceptance scan and
-//    the final inverse-CDF draw on one warp.
+//  * pass 2 (one CTA per sequence, one warp per row, launched programmatically dependent
+//    on pass 1) ranks the fine blocks' maxima: tau, the k-th largest of the 32 lanes'
+//    maxima, bounds the row's k-th largest element from below, the maxima >= tau are
+//    sorted and merged 32 at a time into the row's top list, and only the blocks whose
+//    second largest element reaches that list's k-th value can hold a further top-k
+//    element -- on random rows about one row in four re-reads one fine block (1 KB).  Ties
+//    and adversarial rows stay exact;
+//  * each row's truncated distribution is built from its list in shared memory, and warp 0
+//    runs the sequence's acceptance scan and the final inverse-CDF draw.
 #include <cstdio>
 #include <cstring>
 #include <cmath>
@@ -46,7 +46,7 @@ constexpr int BM_THREADS = 256;                      // pass 1 CTA
 #define BM_CTAS_PER_SM 2                             // 16 warps per SM
 #endif
 constexpr int BM_INFLIGHT = 2;                       // blocks loaded at once per warp
-// registers per pass-1 thread: 16 warps of pass 1 leave room for one pass-2 CTA per SM
+// registers per pass-1 thread (two CTAs of 256 threads per SM)
 #ifndef BM_MAXNREG
 #define BM_MAXNREG 96
 #endif
@@ -56,8 +56,8 @@ constexpr int BM_INFLIGHT = 2;                       // blocks loaded at once pe
 #ifndef BM_STATIC_PCT
 #define BM_STATIC_PCT 75                             // share of pass-1 blocks in static sweeps
 #endif
-constexpr int RF_WARPS = 4;                          // pass 2: one warp per row, 4 rows per CTA
-constexpr int RF_THREADS = RF_WARPS * 32;
+constexpr int RF_MAX_WARPS = 16;                     // pass 2: warps (rows in flight) per CTA
+constexpr int RF_SAMPLE_WARPS = 4;                   // sample mode: rows per CTA
 constexpr int RF_BPL = 5;                            // blocks' second values a lane holds per round
 constexpr int RF_KPL = 2 * RF_BPL;                   // float4 of (maximum, id) pairs a lane holds per round
 constexpr int RF_BATCH = 8;                          // fine blocks loaded at once per warp
@@ -65,9 +65,7 @@ constexpr int RF_SEL_CAP = 64;                       // fine blocks listed befor
 // per-warp candidate buffer, merged into the warp's list of 32 before an append could
 // overflow it (appends come 64 or 128 at a time)
 constexpr int RF_CAND_CAP = 192;
-// pass-2 CTAs per SM the register budget must allow: one beside pass 1's 16 warps of 96
-// registers (49152 of 65536) leaves 128 a thread
-constexpr int RF_MIN_CTAS = 4;
+constexpr int RF_WARP_WORDS = 2 * RF_CAND_CAP + RF_SEL_CAP;   // 4-byte words of shared memory per warp
 
 enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
 
@@ -92,13 +90,9 @@ struct VerifyParams {
     int* seq_status;
     int* out_tokens;
     // workspace
-    int* seq_cnt;               // [B] rows of the sequence finished
     int* blk_next;              // pass-1 dynamic block counter
     float2* fk;                 // [n_rows][NF * nbb] fine block (maximum, id of an element at it)
     float* fm2;                 // [n_rows][NF * nbb] fine block second largest element
-    int* rd_n;                  // [n_rows]
-    int* rd_id;                 // [n_rows][LISTN]
-    float* rd_p;
 };
 
 struct RowInfo {
@@ -166,9 +160,12 @@ __device__ __forceinline__ float key_float(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Sort + merge the warp's buffered candidates into its running list, 32 at a time.
-__device__ __forceinline__ void flush_candidates(float& lv, int& lid, const float* cv, const int* ci, int n,
-                                                 int lane) {
+// Sort + merge the warp's buffered candidates into its running list, 32 at a time.  Not
+// inlined: it is reached from many unrolled sites, and one copy keeps the code in the
+// instruction cache.
+struct ListEntry { float v; int id; };
+__device__ __noinline__ ListEntry merge_candidates(float lv, int lid, const float* cv, const int* ci, int n,
+                                                   int lane) {
     __syncwarp();
     for (int base = 0; base < n; base += 32) {
         const bool has = base + lane < n;
@@ -178,16 +175,21 @@ __device__ __forceinline__ void flush_candidates(float& lv, int& lid, const floa
         warp_merge_desc(lv, lid, v, id, lane);
     }
     __syncwarp();
+    return ListEntry{lv, lid};
 }
 
-// Truncated distribution of a merged row list (lane j = j-th best), written to rd_*.
-__device__ void build_row_dist(const VerifyParams& p, int row, float lv, int lid, int lane) {
+__device__ __forceinline__ void flush_candidates(float& lv, int& lid, const float* cv, const int* ci, int n,
+                                                 int lane) {
+    const ListEntry e = merge_candidates(lv, lid, cv, ci, n, lane);
+    lv = e.v;
+    lid = e.id;
+}
+
+// Truncated distribution of a merged row list (lane j = j-th best): lane j's (id, probability),
+// id -1 where the entry is cut.
+__device__ void row_dist(const VerifyParams& p, float lv, int lid, int lane, int& oid, float& op) {
     const int k = p.top_k;
-    int n;
-    int oid;
-    float op;
     if (p.temperature == 0.0f) {
-        n = 1;
         oid = lane == 0 ? lid : -1;
         op = lane == 0 ? 1.0f : 0.0f;
     } else {
@@ -205,14 +207,10 @@ __device__ void build_row_dist(const VerifyParams& p, int row, float lv, int lid
         }
         const float before = incl - pr;
         const bool kept = valid && (lane == 0 || p.top_p >= 1.0f || before < p.top_p);
-        n = __popc(__ballot_sync(FULL, kept));
         const float S2 = warp_sum(kept ? e : 0.0f);
         oid = kept ? lid : -1;
         op = kept ? e / S2 : 0.0f;
     }
-    p.rd_id[(size_t)row * LISTN + lane] = oid;
-    p.rd_p[(size_t)row * LISTN + lane] = op;
-    if (lane == 0) p.rd_n[row] = n;
 }
 
 // Inverse CDF over ascending token id: (key, w) per lane, key = SENT_ID for empty lanes.
@@ -235,19 +233,19 @@ __device__ int inverse_cdf_draw(int& key, float& w, float u, int lane, float& Z)
     return __shfl_sync(FULL, key, src);
 }
 
-__device__ __forceinline__ int trow(const VerifyParams& p, int b, int i) { return b * (p.K + 1) + i; }
-__device__ __forceinline__ int drow(const VerifyParams& p, int b, int i) { return p.n_target_rows + b * p.K + i; }
-
-// Acceptance scan of one sequence on one warp.
-__device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
+// Acceptance scan of one sequence on one warp, over its rows' truncated distributions in
+// shared memory: target position i at list i, draft position i at list kb + 1 + i.
+__device__ void finish_sequence(const VerifyParams& p, int b, int lane, const int* rid, const float* rp) {
     const int kb = draft_count(p, b);
+    auto tl = [&](int i) { return i * LISTN + lane; };
+    auto dl = [&](int i) { return (kb + 1 + i) * LISTN + lane; };
     const float* ub = p.u + (size_t)b * (p.K + 1);
     int a = 0, next = -1, status = SPEC_OK;
     int okey = SENT_ID;
     float ow = 0.0f, oZ = 1.0f;
     if (p.temperature == 0.0f) {
-        while (a < kb && p.draft_tokens[(size_t)b * p.K + a] == __ldcg(p.rd_id + (size_t)trow(p, b, a) * LISTN)) ++a;
-        next = __ldcg(p.rd_id + (size_t)trow(p, b, a) * LISTN);
+        while (a < kb && p.draft_tokens[(size_t)b * p.K + a] == rid[a * LISTN]) ++a;
+        next = rid[a * LISTN];
         okey = lane == 0 ? next : SENT_ID;
         ow = lane == 0 ? 1.0f : 0.0f;
     } else {
@@ -268,12 +266,12 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
                 pd[j] = 0.0f; qd[j] = 1.0f; dt[j] = -1;
                 if (i < kb) {
                     dt[j] = p.draft_tokens[(size_t)b * p.K + i];
-                    const int pid = __ldcg(p.rd_id + (size_t)trow(p, b, i) * LISTN + lane);
-                    const float pp = __ldcg(p.rd_p + (size_t)trow(p, b, i) * LISTN + lane);
+                    const int pid = rid[tl(i)];
+                    const float pp = rp[tl(i)];
                     pd[j] = pid == dt[j] ? pp : 0.0f;
                     if (has_q) {
-                        const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, i) * LISTN + lane);
-                        const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, i) * LISTN + lane);
+                        const int qid = rid[dl(i)];
+                        const float qp = rp[dl(i)];
                         qd[j] = qid == dt[j] ? qp : 0.0f;
                     }
                 }
@@ -291,15 +289,14 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
             }
         }
         if (status == SPEC_OK) {
-            const int prow = trow(p, b, a);
-            const int pid = __ldcg(p.rd_id + (size_t)prow * LISTN + lane);
-            const float pp = __ldcg(p.rd_p + (size_t)prow * LISTN + lane);
+            const int pid = rid[tl(a)];
+            const float pp = rp[tl(a)];
             float w = pid >= 0 ? pp : 0.0f;
             if (reject) {
                 float qx = 0.0f;
                 if (has_q) {
-                    const int qid = __ldcg(p.rd_id + (size_t)drow(p, b, a) * LISTN + lane);
-                    const float qp = __ldcg(p.rd_p + (size_t)drow(p, b, a) * LISTN + lane);
+                    const int qid = rid[dl(a)];
+                    const float qp = rp[dl(a)];
 #pragma unroll
                     for (int t = 0; t < LISTN; ++t) {
                         const int tid = __shfl_sync(FULL, qid, t);
@@ -330,33 +327,6 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane) {
     }
 }
 
-// A row's exact top list (lane j = j-th best): build the distribution, then either sample
-// (sample mode) or arrive on the sequence; the sequence's last row runs the scan.
-__device__ void finish_row(const VerifyParams& p, int row, float lv, int lid, int lane) {
-    build_row_dist(p, row, lv, lid, lane);
-
-    if (p.mode == MODE_SAMPLE) {
-        int key = __ldcg(p.rd_id + (size_t)row * LISTN + lane);
-        float w = __ldcg(p.rd_p + (size_t)row * LISTN + lane);
-        if (key < 0) { key = SENT_ID; w = 0.0f; }
-        float Z;
-        const int tok = inverse_cdf_draw(key, w, p.u[row], lane, Z);
-        if (lane == 0) p.out_tokens[row] = tok;
-        return;
-    }
-    const RowInfo ri = row_info(p, row);
-    const int b = ri.seq;
-    const int kb = draft_count(p, b);
-    const int expected = (kb + 1) + (p.draft != nullptr && p.temperature != 0.0f ? kb : 0);
-    // arrival: releases this row's distribution, and the last row acquires the others'
-    __syncwarp();
-    int prev = 0;
-    if (lane == 0)
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.seq_cnt + b) : "memory");
-    prev = __shfl_sync(FULL, prev, 0);
-    __syncwarp();
-    if (prev == expected - 1) finish_sequence(p, b, lane);
-}
 
 
 __device__ __forceinline__ float max4(const float4& x) { return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)); }
@@ -437,9 +407,10 @@ __global__ void __maxnreg__(BM_MAXNREG) vt_stats_kernel(const VerifyParams p) {
             w0 = gw + it * sweep;
             wstep = nw;
         } else {
-            w0 = dyn0 + __shfl_sync(FULL, nextb, 0);
+            const int nb = __shfl_sync(FULL, nextb, 0);
+            w0 = dyn0 + nb;
             wstep = 1;
-            if (w0 >= total) break;
+            if (nb < 0 || w0 >= total) break;     // the counter starts at 0 (cleared by the host)
         }
         float4 x[BM_INFLIGHT][VB4 / 32];
         int row[BM_INFLIGHT], blk[BM_INFLIGHT];
@@ -618,9 +589,10 @@ __device__ __forceinline__ void reread_blocks(const VerifyParams& p, const RowIn
 // than a block's recorded maximum is at most the block's second largest value, so a block
 // whose second value is below tau2 holds nothing else of the top k.  The few blocks whose
 // second value reaches tau2 are read again and their other elements >= tau2 merged in.
-__device__ __forceinline__ void refine_row(const VerifyParams& p, int row, int lane, float* cv, int* ci, int* sel) {
+// Returns lane j's entry of the row's top list (j-th best).
+__device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, int lane, float* cv, int* ci,
+                                                int* sel) {
     const RowInfo ri = row_info(p, row);
-    if (!row_needed(p, ri)) return;
     VT_STAMP(row, 0);
     VT_STAMP(row, 1);
     const int k = p.top_k;
@@ -726,53 +698,83 @@ __device__ __forceinline__ void refine_row(const VerifyParams& p, int row, int l
         }
     }
     VT_STAMP(row, 4);
-    finish_row(p, row, lv, lid, lane);
-    VT_STAMP(row, 5);
+    return ListEntry{lv, lid};
 }
 
-// Pass 2: one warp per row (refine_row), RF_WARPS rows per CTA.
-__global__ void __launch_bounds__(RF_THREADS, RF_MIN_CTAS) vt_refine_kernel(const VerifyParams p) {
-    __shared__ float cand_v[RF_WARPS][RF_CAND_CAP];
-    __shared__ int cand_id[RF_WARPS][RF_CAND_CAP];
-    __shared__ int sel_list[RF_WARPS][RF_SEL_CAP];
+// Pass 2.  Verify: one CTA per sequence, one warp per row of the sequence (rows beyond the
+// CTA's warps are taken in turn); each row's truncated distribution goes to shared memory
+// and warp 0 runs the sequence's acceptance scan there.  Sample: one warp per row, which
+// draws its token itself.  Launched programmatically dependent on pass 1: the CTAs may be
+// resident early, the statistics are read after pass 1 is done.
+// Dynamic shared memory: per warp RF_CAND_CAP candidates (value, id) and RF_SEL_CAP fine
+// block indices, then (verify) the sequence's lists, ids then probabilities.
+__global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const VerifyParams p) {
+    extern __shared__ __align__(16) unsigned char rf_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * RF_WARPS + warp;
-    // the grid is launched programmatically dependent on pass 1: its CTAs may be resident
-    // early (pass 1 keeps room for one per SM); the statistics are read after pass 1 is done
+    const int nwarps = blockDim.x >> 5;
+    float* cv = reinterpret_cast<float*>(rf_smem) + warp * RF_WARP_WORDS;
+    int* ci = reinterpret_cast<int*>(cv + RF_CAND_CAP);
+    int* sel = ci + RF_CAND_CAP;
     pdl_wait();
-    if (row < p.n_rows) refine_row(p, row, lane, cand_v[warp], cand_id[warp], sel_list[warp]);
+    if (p.mode == MODE_SAMPLE) {
+        const int row = blockIdx.x * nwarps + warp;
+        if (row >= p.n_rows) return;
+        const ListEntry e = refine_row(p, row, lane, cv, ci, sel);
+        int key;
+        float w;
+        row_dist(p, e.v, e.id, lane, key, w);
+        if (key < 0) { key = SENT_ID; w = 0.0f; }
+        float Z;
+        const int tok = inverse_cdf_draw(key, w, p.u[row], lane, Z);
+        if (lane == 0) p.out_tokens[row] = tok;
+        VT_STAMP(row, 5);
+        return;
+    }
+    const int b = blockIdx.x;
+    const int kb = draft_count(p, b);
+    const int nr = (kb + 1) + (p.draft != nullptr ? kb : 0);
+    int* rid = reinterpret_cast<int*>(rf_smem) + nwarps * RF_WARP_WORDS;
+    float* rp = reinterpret_cast<float*>(rid + nr * LISTN);
+    for (int r = warp; r < nr; r += nwarps) {
+        const int row = r <= kb ? b * (p.K + 1) + r : p.n_target_rows + b * p.K + (r - kb - 1);
+        const ListEntry e = refine_row(p, row, lane, cv, ci, sel);
+        row_dist(p, e.v, e.id, lane, rid[r * LISTN + lane], rp[r * LISTN + lane]);
+        VT_STAMP(row, 5);
+    }
+    __syncthreads();
+    if (warp == 0) finish_sequence(p, b, lane, rid, rp);
 }
 
 // ---- host side ---------------------------------------------------------------------------
 
 struct Plan {
     int n_rows, nbb;
-    size_t off_seq, off_blk, off_fk, off_fm2, off_rdn, off_rdid, off_rdp, total, counters_bytes;
+    size_t off_blk, off_fk, off_fm2, total, counters_bytes;
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static Plan make_plan(int n_rows_max, int n_seq, int V) {
+// largest pass-2 shared memory: RF_MAX_WARPS warps and the lists of 2 VT_MAX_K + 1 rows
+constexpr int RF_SMEM_MAX = (RF_MAX_WARPS * RF_WARP_WORDS + 2 * (2 * VT_MAX_K + 1) * LISTN) * 4;
+
+static Plan make_plan(int n_rows_max, int V) {
     Plan pl{};
     pl.n_rows = n_rows_max;
     pl.nbb = (V + VB - 1) / VB;
     size_t o = 0;
-    pl.off_seq = o; o += (size_t)n_seq * 4;
     pl.off_blk = o; o += 4;
     pl.counters_bytes = o;
     o = align256(o);
     pl.off_fk = o; o = align256(o + (size_t)n_rows_max * pl.nbb * NF * 8);
     pl.off_fm2 = o; o = align256(o + (size_t)n_rows_max * pl.nbb * NF * 4);
-    pl.off_rdn = o; o = align256(o + (size_t)n_rows_max * 4);
-    pl.off_rdid = o; o = align256(o + (size_t)n_rows_max * LISTN * 4);
-    pl.off_rdp = o; o = align256(o + (size_t)n_rows_max * LISTN * 4);
     pl.total = o;
     return pl;
 }
 
-// SM count of the current device; the first call on a device also asks for pass 1's SMs to
-// keep shared memory configured (pass 1 uses none, and an SM whose carveout was sized for
-// it cannot take a pass-2 CTA until pass 1 leaves).
+// SM count of the current device; the first call on a device also sets pass 1's shared
+// memory carveout (pass 1 uses none: a small carveout leaves L1, which holds its loads in
+// flight, large -- a 100% carveout measured 15% slower) and pass 2's dynamic shared memory
+// limit.
 static int device_setup() {
     constexpr int MAX_DEV = 64;
     static std::atomic<int> sms[MAX_DEV];
@@ -784,7 +786,9 @@ static int device_setup() {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
     if (cudaFuncSetAttribute(vt_stats_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             BM_SMEM_CARVEOUT) != cudaSuccess)
+                             BM_SMEM_CARVEOUT) != cudaSuccess ||
+        cudaFuncSetAttribute(vt_refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RF_SMEM_MAX) !=
+            cudaSuccess)
         return -1;
     if (dev < MAX_DEV) sms[dev].store(n);
     return n;
@@ -792,13 +796,9 @@ static int device_setup() {
 
 static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream_t st) {
     uint8_t* w = static_cast<uint8_t*>(ws);
-    prm.seq_cnt = reinterpret_cast<int*>(w + pl.off_seq);
     prm.blk_next = reinterpret_cast<int*>(w + pl.off_blk);
     prm.fk = reinterpret_cast<float2*>(w + pl.off_fk);
     prm.fm2 = reinterpret_cast<float*>(w + pl.off_fm2);
-    prm.rd_n = reinterpret_cast<int*>(w + pl.off_rdn);
-    prm.rd_id = reinterpret_cast<int*>(w + pl.off_rdid);
-    prm.rd_p = reinterpret_cast<float*>(w + pl.off_rdp);
     prm.nbb = pl.nbb;
 
     cudaError_t e = cudaMemsetAsync(ws, 0, pl.counters_bytes, st);
@@ -810,8 +810,17 @@ static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream
     const int grid1 = (int)std::max(1LL, std::min((long long)nsm * BM_CTAS_PER_SM, (warps_needed + 7) / 8));
     vt_stats_kernel<<<grid1, BM_THREADS, 0, st>>>(prm);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((prm.n_rows + RF_WARPS - 1) / RF_WARPS);
-    cfg.blockDim = dim3(RF_THREADS);
+    if (prm.mode == MODE_SAMPLE) {
+        cfg.gridDim = dim3((prm.n_rows + RF_SAMPLE_WARPS - 1) / RF_SAMPLE_WARPS);
+        cfg.blockDim = dim3(RF_SAMPLE_WARPS * 32);
+        cfg.dynamicSmemBytes = (size_t)RF_SAMPLE_WARPS * RF_WARP_WORDS * 4;
+    } else {
+        const int nr_max = (prm.K + 1) + (prm.draft != nullptr ? prm.K : 0);
+        const int nw = std::min(nr_max, RF_MAX_WARPS);
+        cfg.gridDim = dim3(prm.B);
+        cfg.blockDim = dim3(nw * 32);
+        cfg.dynamicSmemBytes = ((size_t)nw * RF_WARP_WORDS + (size_t)2 * nr_max * LISTN) * 4;
+    }
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -858,7 +867,7 @@ int verify_into(int B, int K, int V, const float* target_logits, const float* dr
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return set_error(SPEC_E_INVAL, "workspace not 256-byte aligned");
     if ((reinterpret_cast<uintptr_t>(target_logits) & 3) || (reinterpret_cast<uintptr_t>(draft_logits) & 3))
         return set_error(SPEC_E_INVAL, "logits must be 4-byte aligned");
-    const Plan pl = make_plan(B * (2 * K + 1), B, V);
+    const Plan pl = make_plan(B * (2 * K + 1), V);
     if (workspace_bytes < pl.total)
         return set_error(SPEC_E_NOMEM, "workspace %zu bytes < required %zu", workspace_bytes, pl.total);
 
@@ -891,7 +900,7 @@ using namespace sv;
 
 extern "C" size_t spec_verify_logits_workspace_bytes(int B, int K, int V) {
     if (B < 1 || K < 0 || V < 2 || K > VT_MAX_K) return 0;
-    return make_plan(B * (2 * K + 1), B, V).total;
+    return make_plan(B * (2 * K + 1), V).total;
 }
 
 extern "C" int spec_verify_logits(int B, int K, int V, const float* target_logits, const float* draft_logits,
@@ -907,7 +916,7 @@ extern "C" int spec_verify_logits(int B, int K, int V, const float* target_logit
 
 extern "C" size_t spec_sample_logits_workspace_bytes(int R, int V) {
     if (R < 1 || V < 2) return 0;
-    return make_plan(R, R, V).total;
+    return make_plan(R, V).total;
 }
 
 extern "C" int spec_sample_logits(int R, int V, const float* logits, const float* uniforms,
@@ -921,7 +930,7 @@ extern "C" int spec_sample_logits(int R, int V, const float* logits, const float
     if (!logits || !uniforms || !out_tokens || !workspace) return set_error(SPEC_E_INVAL, "NULL required pointer");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return set_error(SPEC_E_INVAL, "workspace not 256-byte aligned");
     if (reinterpret_cast<uintptr_t>(logits) & 3) return set_error(SPEC_E_INVAL, "logits must be 4-byte aligned");
-    const Plan pl = make_plan(R, R, V);
+    const Plan pl = make_plan(R, V);
     if (workspace_bytes < pl.total)
         return set_error(SPEC_E_NOMEM, "workspace %zu bytes < required %zu", workspace_bytes, pl.total);
     VerifyParams prm{};
