@@ -373,6 +373,203 @@ class DenseVerifyWorkload:
                                            f"{emitted_per_step:.4f} emitted tokens per step (closed form)")
 
 
+# ---- workload: batched serving with an n-gram drafter -----------------------------------
+
+class ServingWorkload:
+    """Batched serving verify on the 8B shape: B sequences with ragged prompt lengths
+    U[len_lo, len_hi] built from spans of which 40% copy an earlier window of the same
+    sequence; drafts from the native n-gram drafter (longest suffix match of 8 down to 3
+    tokens, at most K tokens, draft_len per sequence); greedy verify with auto trim.  A step
+    is one serving round: host drafting, the drafts' upload, spec_verify and the download of
+    accepted lengths and next tokens.  The verify itself is timed with CUDA events on the
+    stream (value, ms_per_step); the whole round is the end-to-end number."""
+    name = "serving-8b-b32-k8"
+    dtype = "bf16"
+    device_timed = True
+
+    def __init__(self, B=32, K=8, len_lo=2048, len_hi=16384, layers=None, **_):
+        import dataclasses
+        import synth
+        self.shape = synth.QWEN_8B
+        if layers is not None and layers != self.shape.n_layers:
+            self.shape = dataclasses.replace(self.shape, n_layers=layers, name=f"dense-8b-{layers}l")
+        self.B, self.K, self.len_lo, self.len_hi = B, K, len_lo, len_hi
+
+    def config(self):
+        s = self.shape
+        return {"workload": self.name,
+                "model_shape": f"{s.n_layers} layers, d {s.d_model}, {s.n_q_heads}/{s.n_kv_heads} heads, head_dim "
+                               f"{s.head_dim}, SwiGLU {s.ffn_dim}, vocab {s.vocab}, bf16, random init N(0,0.02^2)",
+                "B": self.B, "K": self.K, "prompt_len": f"U[{self.len_lo}, {self.len_hi}] per sequence (seed 5)",
+                "kv_tokens_at_start": int(self.lens.sum()) if hasattr(self, "lens") else None,
+                "prompts": "spans of U[8,64] tokens, 40% copying an earlier window of the same sequence",
+                "decoding": "greedy", "drafter": "native n-gram lookup, suffix match 8..3 tokens, <= K drafted",
+                "kv_cache": "paged bf16, 16-token pages",
+                "l2": "inputs larger than L2 (15.1 GB of weights + the KV cache streamed per step)"}
+
+    def setup(self, device, n_steps):
+        import torch
+        import synth
+        from speculative_decoding_verify_token_gb300 import model as M, ngram as NG
+        s, B, K = self.shape, self.B, self.K
+        g = np.random.Generator(np.random.PCG64(5))
+        self.lens = g.integers(self.len_lo, self.len_hi + 1, size=B)
+        self.weights = synth.model_weights(s, seed=0, device=device)
+        max_ctx = int(self.lens.max()) + (K + 1) * (n_steps + 64) + 64
+        self.m = M.SpecModel(s, self.weights, max_batch=B, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
+        self.ctx = []
+        self.drafters = []
+        for b in range(B):
+            prompt = synth.ngram_prompt(5 + b, int(self.lens[b]), s.vocab)
+            self.m.prefill(b, torch.from_numpy(prompt[:-1]).to(device))
+            d = NG.NgramDrafter(3, 8)
+            d.append(prompt)
+            self.drafters.append(d)
+            self.ctx.append(prompt)
+        self.pending = torch.tensor([int(c[-1]) for c in self.ctx], dtype=torch.int32).pin_memory()
+        self.h_drafts = torch.zeros(B, K, dtype=torch.int32).pin_memory()
+        self.h_len = torch.zeros(B, dtype=torch.int32).pin_memory()
+        self.h_out = torch.zeros(2, B, dtype=torch.int32).pin_memory()
+        self.d_last = torch.empty(B, dtype=torch.int32, device=device)
+        self.d_drafts = torch.empty(B, K, dtype=torch.int32, device=device)
+        self.d_len = torch.empty(B, dtype=torch.int32, device=device)
+        self.d_u = torch.zeros(B, K + 1, dtype=torch.float32, device=device)
+        self.out = {"accepted_len": torch.empty(B, dtype=torch.int32, device=device),
+                    "next_token": torch.empty(B, dtype=torch.int32, device=device),
+                    "out_ids": torch.empty(B, 32, dtype=torch.int32, device=device),
+                    "out_probs": torch.empty(B, 32, dtype=torch.float32, device=device),
+                    "status": torch.empty(B, dtype=torch.int32, device=device)}
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+        self.log = []              # per step: (emitted, drafted, accepted, status ok, kv tokens read)
+        self.dev_ms = []
+        self.seq_ids = list(range(B))
+        torch.cuda.synchronize()
+
+    def _round(self, timed_events=True):
+        import torch
+        from speculative_decoding_verify_token_gb300 import ngram as NG
+        B, K = self.B, self.K
+        toks, lens = NG.draft_batch(self.drafters, K)
+        self.h_drafts.numpy()[:] = toks
+        self.h_len.numpy()[:] = lens
+        kv_read = int(sum(len(c) - 1 for c in self.ctx))
+        self.d_last.copy_(self.pending, non_blocking=True)
+        self.d_drafts.copy_(self.h_drafts, non_blocking=True)
+        self.d_len.copy_(self.h_len, non_blocking=True)
+        a, b = self.ev[len(self.dev_ms) % len(self.ev)]
+        a.record()
+        self.m.verify(self.seq_ids, self.d_last, self.d_drafts, self.d_u, 0.0, draft_len=self.d_len, out=self.out)
+        b.record()
+        self.h_out[0].copy_(self.out["accepted_len"], non_blocking=True)
+        self.h_out[1].copy_(self.out["next_token"], non_blocking=True)
+        st_ok = True
+        torch.cuda.current_stream().synchronize()
+        self.dev_ms.append(a.elapsed_time(b))
+        acc = self.h_out[0].numpy().copy()
+        nxt = self.h_out[1].numpy().copy()
+        emitted = 0
+        for i in range(B):
+            a_i = int(acc[i])
+            if not (0 <= a_i <= int(lens[i])) or not (0 <= int(nxt[i]) < self.shape.vocab):
+                st_ok = False
+                a_i = max(0, min(a_i, int(lens[i])))
+            new = np.concatenate([toks[i, :a_i], [int(nxt[i])]]).astype(np.int32)
+            self.drafters[i].append(new)
+            self.ctx[i] = np.concatenate([self.ctx[i], new])
+            self.pending[i] = int(nxt[i])
+            emitted += a_i + 1
+        self.log.append((emitted, int(lens.sum()), int(acc.sum()), st_ok, kv_read))
+
+    def step(self, i):
+        self._round()
+
+    def launches(self):
+        return self.m.launches()
+
+    def check(self, i0, n):
+        rows = self.log[i0:i0 + n]
+        ok = all(r[3] for r in rows) and int(self.out["status"].abs().sum().item()) == 0
+        return ok, int(sum(r[0] for r in rows))
+
+    def timed_ms(self, i0, n):
+        return float(sum(self.dev_ms[i0:i0 + n]))
+
+    def stats(self, i0, n):
+        rows = self.log[i0:i0 + n]
+        drafted = sum(r[1] for r in rows)
+        accepted = sum(r[2] for r in rows)
+        kv = sum(r[4] for r in rows) / max(len(rows), 1)
+        return {"acceptance": accepted / max(drafted, 1), "drafted_per_step": drafted / max(len(rows), 1),
+                "emitted_per_step": sum(r[0] for r in rows) / max(len(rows), 1), "kv_tokens_per_step": kv}
+
+    def profile(self, n):
+        self.m.profile(True)
+        for _ in range(n):
+            self._round()
+        prof = self.m.profile_read()
+        self.m.profile(False)
+        return prof
+
+    def roofline(self, prof, peaks):
+        # the kernel class with the largest time share (attention at these context lengths)
+        cls = max((k for k in prof if prof[k]["launches"] and k != "other"), key=lambda k: prof[k]["ms"])
+        x = prof[cls]
+        kernel = {"attention": "attn_mma_kernel", "verify": "verify_kernel"}.get(cls, "tc_gemm_kernel")
+        achieved = (x["bytes"] / x["launches"]) / (x["ms"] / x["launches"] / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": kernel, "class": cls,
+                "algorithmic_bytes_per_launch": x["bytes"] / x["launches"], "launches_measured": x["launches"],
+                "avg_launch_us": x["ms"] / x["launches"] * 1e3, "peak_source": peaks["source"]}
+
+    def e2e(self, n):
+        """Serving rounds through the C ABI with host buffers: host drafting, the drafts'
+        upload, spec_verify, the download of the accepted lengths and next tokens."""
+        import torch
+        torch.cuda.synchronize()
+        i0 = len(self.log)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            self._round()
+        dt = time.perf_counter() - t0
+        emitted = sum(r[0] for r in self.log[i0:])
+        B, K = self.B, self.K
+        return emitted / dt, 4 * B + 4 * B * K + 4 * B, 8 * B
+
+    def oracle_sample(self, budget_s):
+        """The float64 oracle on a bounded sample: the verify pass of K+1 tokens of one
+        sequence through 1 of the 36 layers at a context of 255 tokens, plus final norm and
+        a 4096-row slice of lm_head; scaled to 36 layers, the full lm_head and B sequences,
+        at the measured emitted tokens per step.  Attention over the real 2k-16k contexts is
+        not scaled, so the oracle's rate is an upper bound."""
+        import dataclasses
+        import synth
+        from oracle import model as om
+        from oracle import verify as ov
+        s = self.shape
+        sub = dataclasses.replace(s, n_layers=1, vocab=4096)
+        names = [n for n in synth.weight_names(sub) if n.startswith("layers.0.")]
+        w = {n: om.to_f64(synth.model_weight(s, n, seed=0)) for n in names}
+        w["embed"] = om.to_f64(synth.model_weight(sub, "embed", seed=0))
+        w["final_norm"] = np.ones(s.d_model)
+        w["lm_head"] = om.to_f64(synth.model_weight(sub, "lm_head", seed=0))
+        dec = om.Decoder(sub, w)
+        prompt = synth.ngram_prompt(5, 255, sub.vocab)
+        toks = [int(t) for t in synth.prompt_tokens(2, self.K + 1, sub.vocab)]
+        cache = dec.new_cache()
+        dec.forward(prompt, cache)
+        t0 = time.perf_counter()
+        rows = dec.forward(toks, cache)
+        ov.verify_greedy(rows, toks[1:])
+        t_pass = time.perf_counter() - t0
+        per_step = t_pass * s.n_layers * s.vocab / sub.vocab * self.B
+        st = self.stats(0, len(self.log))
+        return st["emitted_per_step"] / per_step, (
+            f"float64 verify pass of {self.K + 1} tokens of 1 sequence through 1 of {s.n_layers} layers (context "
+            f"255) + a 4096-row lm_head slice, scaled to {s.n_layers} layers, the full lm_head and {self.B} "
+            f"sequences at {st['emitted_per_step']:.2f} emitted tokens per step; attention over the 2k-16k "
+            f"contexts not scaled")
+
+
 # ---- workload: standalone verify on logits ----------------------------------------------
 
 class VerifyLogitsWorkload:
@@ -491,7 +688,8 @@ class VerifyLogitsWorkload:
                               "float64 numpy, one process")
 
 
-WORKLOADS = {DenseVerifyWorkload.name: DenseVerifyWorkload, VerifyLogitsWorkload.name: VerifyLogitsWorkload}
+WORKLOADS = {DenseVerifyWorkload.name: DenseVerifyWorkload, VerifyLogitsWorkload.name: VerifyLogitsWorkload,
+             ServingWorkload.name: ServingWorkload}
 DEFAULT_WORKLOAD = DenseVerifyWorkload.name
 
 
@@ -517,6 +715,8 @@ def run_reference(args):
             return em
         sample = f"{n_per_step} of the {wl.B} sequences per step"
         unit_per_step = None
+    elif isinstance(wl, ServingWorkload):
+        step, sample = reference_serving_step(wl)
     else:
         step, sample = reference_dense_step(wl)
     for _ in range(args.warmup):
@@ -535,6 +735,44 @@ def run_reference(args):
                              "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def reference_serving_step(wl):
+    """One bounded oracle step of the serving workload: one sequence's verify pass (the last
+    committed token and its n-gram drafts, K <= 8) through one layer of the 8B shape at a
+    context of 255 tokens (float64, weights drawn on the CPU from the same seeded generator,
+    a 4096-row lm_head), greedy rule on its rows; counted as 1/36 of that sequence's share
+    of a verify step, emitting (a + 1) / 36 tokens."""
+    import dataclasses
+    import synth
+    from oracle import generate as og
+    from oracle import model as om
+    from oracle import verify as ov
+    s = wl.shape
+    sub = dataclasses.replace(s, n_layers=1, vocab=4096)
+    names = [n for n in synth.weight_names(sub) if n.startswith("layers.0.")]
+    w = {n: om.to_f64(synth.model_weight(s, n, seed=0)) for n in names}
+    w["embed"] = om.to_f64(synth.model_weight(sub, "embed", seed=0))
+    w["final_norm"] = np.ones(s.d_model)
+    w["lm_head"] = om.to_f64(synth.model_weight(sub, "lm_head", seed=0))
+    dec = om.Decoder(sub, w)
+    ctx = [int(t) for t in synth.ngram_prompt(5, 256, sub.vocab)]
+    drafts = og.ngram_draft(ctx, n_draft=wl.K)
+    toks = [ctx[-1]] + drafts
+
+    import copy
+    cache0 = dec.new_cache()
+    dec.forward(ctx[:-1], cache0, logits_rows=np.zeros(0, dtype=np.int64))
+
+    def step():
+        cache = copy.deepcopy(cache0)
+        rows = dec.forward(toks, cache)
+        r = ov.verify_greedy(rows, drafts)
+        return (r["a"] + 1) / s.n_layers
+
+    return step, (f"one sequence's verify pass ({len(toks)} tokens: last + n-gram drafts) through 1 of "
+                  f"{s.n_layers} layers at context 255 + a 4096-row lm_head, counted as 1/{s.n_layers} of its "
+                  f"share of a step")
 
 
 def reference_dense_step(wl):
@@ -592,8 +830,12 @@ def main():
     rank, world, local = dist_setup()
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
-    wl = WORKLOADS[args.workload](n_gen=args.gen, layers=args.layers) if args.workload == DenseVerifyWorkload.name \
-        else WORKLOADS[args.workload]()
+    if args.workload == DenseVerifyWorkload.name:
+        wl = WORKLOADS[args.workload](n_gen=args.gen, layers=args.layers)
+    elif args.workload == ServingWorkload.name:
+        wl = WORKLOADS[args.workload](layers=args.layers)
+    else:
+        wl = WORKLOADS[args.workload]()
     n_total = args.warmup + args.steps
     # a created stream: the legacy default stream serialises programmatic dependent launches
     stream = torch.cuda.Stream()
@@ -621,9 +863,15 @@ def main():
         barrier(world)
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ok, emitted = wl.check(args.warmup, args.steps)
+    extra = {}
+    if getattr(wl, "device_timed", False):
+        # each step also does host work (drafting, the round's download); the value counts
+        # the verify calls' own CUDA-event time, the loop's span goes beside it
+        extra["round_ms_per_step"] = total_ms / args.steps
+        extra.update(wl.stats(args.warmup, args.steps))
+        total_ms = max_over_ranks(wl.timed_ms(args.warmup, args.steps), world)
     value = emitted * world / (total_ms / 1e3)
 
-    extra = {}
     if isinstance(wl, DenseVerifyWorkload):
         dec_ms = wl.decode_ms(20)
         extra["decode_ms_per_step"] = dec_ms

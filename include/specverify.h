@@ -19,6 +19,8 @@
  *              has to match on both sides" (top-k 20 / top-p 0.95 on both p and q).
  *  [Draft]     "What is Speculative Decoding and How Does a Draft Model Work?", "#2"
  *              and "#3" (greedy acceptance; one target pass always emits >= 1 token).
+ *  [OptiQ]     "Speculative decoding on Apple Silicon" (mlx-optiq docs), "N-gram lookup:
+ *              any model" (draft what followed an earlier occurrence of the last tokens).
  *
  * Readings of what the pages leave open (the same in the CPU oracle):
  *  - a full acceptance emits a bonus token from the last target row;
@@ -273,6 +275,38 @@ int spec_profile(spec_ctx* ctx, int enable);
  * GEMMs, KV pages read + written for attention, logits for the verify), accumulated since
  * the previous read; then reset.  Arrays of SPEC_PROF_CLASSES entries (host). */
 int spec_profile_read(spec_ctx* ctx, double* ms, long long* launches, double* bytes);
+
+/* ------------------------------------------------------------------------------------
+ * Host-side n-gram drafter ([OptiQ] "Speculative decoding on Apple Silicon" (mlx-optiq
+ * docs), "N-gram lookup: any model").  One object per sequence holds the sequence's
+ * committed tokens (host memory) and an index of their m-grams for
+ * m in [min_match, max_match].  A draft takes the longest m (max_match down to min_match,
+ * at most length - 1) whose last-m-token suffix occurred earlier, and returns the tokens
+ * that followed its most recent earlier occurrence, at most n_draft of them; no match
+ * drafts nothing.  Host-only: no CUDA calls, no stream.
+ *
+ * spec_ngram_create: 1 <= min_match <= max_match <= SPEC_NGRAM_MAX_MATCH, else
+ *   SPEC_E_INVAL; SPEC_E_NOMEM if the object cannot be allocated.  Destroy with
+ *   spec_ngram_destroy (NULL is ignored).
+ * spec_ngram_append: append n committed tokens (host array); SPEC_E_NOMEM when the index
+ *   cannot grow (the object then holds a prefix of the tokens).
+ * spec_ngram_draft: writes the draft to out (host, room for n_draft) and returns its
+ *   length (>= 0), or a negative SPEC_E_* code.
+ * spec_ngram_draft_batch: drafts for B objects at once into out_tokens (host [B][K],
+ *   entries past out_len[b] set to 0) and out_len (host [B]) -- the draft_tokens/draft_len
+ *   of one spec_verify call.
+ * spec_ngram_length: number of tokens held, or SPEC_E_INVAL for NULL.
+ * ---------------------------------------------------------------------------------- */
+#define SPEC_NGRAM_MAX_MATCH 8
+
+typedef struct spec_ngram spec_ngram;
+
+int spec_ngram_create(int min_match, int max_match, spec_ngram** out);
+int spec_ngram_append(spec_ngram* g, const int32_t* tokens, int n);
+int spec_ngram_draft(const spec_ngram* g, int n_draft, int32_t* out);
+int spec_ngram_draft_batch(spec_ngram* const* g, int B, int K, int32_t* out_tokens, int32_t* out_len);
+int spec_ngram_length(const spec_ngram* g);
+void spec_ngram_destroy(spec_ngram* g);
 
 /* Number of kernels the context launched since creation (for launch accounting). */
 long long spec_kernel_launches(const spec_ctx* ctx);

@@ -23,6 +23,7 @@ SPEC_E_TIMEOUT = -5
 SPEC_E_CUDA = -6
 SPEC_E_DRAFT = -7
 SPEC_TOPK_MAX = 32
+SPEC_NGRAM_MAX_MATCH = 8
 
 STATUS_NAMES = {0: "SPEC_OK", -1: "SPEC_E_INVAL", -2: "SPEC_E_NOMEM", -3: "SPEC_E_RANGE",
                 -4: "SPEC_E_STATE", -5: "SPEC_E_TIMEOUT", -6: "SPEC_E_CUDA", -7: "SPEC_E_DRAFT"}
@@ -93,6 +94,13 @@ SIGNATURES = {
     "spec_profile_read": (c_int, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong),
                                   ctypes.POINTER(ctypes.c_double)]),
     "spec_destroy": (None, [c_vp]),
+    "spec_ngram_create": (c_int, [c_int, c_int, ctypes.POINTER(c_vp)]),
+    "spec_ngram_append": (c_int, [c_vp, ctypes.POINTER(ctypes.c_int32), c_int]),
+    "spec_ngram_draft": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32)]),
+    "spec_ngram_draft_batch": (c_int, [ctypes.POINTER(c_vp), c_int, c_int, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int32)]),
+    "spec_ngram_length": (c_int, [c_vp]),
+    "spec_ngram_destroy": (None, [c_vp]),
 }
 
 _lib = None
