@@ -20,6 +20,9 @@ namespace sv {
 constexpr int ATT_THREADS = 256;
 constexpr int ATT_RT = 32;                     // query rows per tile
 constexpr int ATT_KV_SMEM = 128 * 1024;        // K + V bytes of one split
+#ifndef ATT_MULTI_MIN
+#define ATT_MULTI_MIN 4                        // fewest splits per CTA worth the multi-split kernel
+#endif
 
 
 static bool use_mma_path(int hd, int esize) { return hd == 128 && esize == 2; }
@@ -190,6 +193,96 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnArgs a) {
                   [] { return true; });
 }
 
+// Long contexts: one CTA of 4 warps per run of `spc` consecutive 64-key splits of a (kv head,
+// sequence), for items whose T*G query rows fit one 64-row tile.  The queries are loaded
+// once; K and V of the next split stream into the other half of a double buffer while the
+// current split is computed by the same per-tile code as attn_mma_kernel, so every split's
+// partial (and hence every output bit) is the same as with one CTA per split -- only the
+// number of CTAs, and the per-CTA overhead, change.  Rows a split fully masks (positions
+// below its first key) are not written; the combine never reads them.
+constexpr size_t MMA_MULTI_SMEM =
+    sizeof(__nv_bfloat16) * ((size_t)4 * MMA_SPLIT * MMA_PITCH + (size_t)2 * MMA_RT * MMA_PITCH +
+                             (size_t)MMA_RT * MMA_PPITCH);
+
+__device__ __forceinline__ void attn_load_split(const AttnArgs& a, int slot, int g, int k0, int nk,
+                                                __nv_bfloat16* Ks, __nv_bfloat16* Vs, int tid) {
+    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_layer);
+    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_layer);
+    for (int i = tid; i < MMA_SPLIT * 16; i += 128) {
+        const int key = i >> 4, ch = i & 15;
+        if (key < nk) {
+            const int pos = k0 + key;
+            const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
+            const size_t off = (((size_t)page * a.hkv + g) * 16 + (pos & 15)) * 128 + ch * 8;
+            cp_async16(smem_u32(Ks + key * MMA_PITCH + ch * 8), kp + off);
+            cp_async16(smem_u32(Vs + key * MMA_PITCH + ch * 8), vp + off);
+        } else {
+            *reinterpret_cast<uint4*>(Ks + key * MMA_PITCH + ch * 8) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(Vs + key * MMA_PITCH + ch * 8) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(128) attn_mma_multi_kernel(const AttnArgs a, int spc) {
+    extern __shared__ __align__(128) uint8_t sm_raw[];
+    __shared__ float wmax[4][MMA_RT], wsum[4][MMA_RT];
+    pdl_launch_dependents();
+    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(sm_raw);          // [2][K, V][64][PITCH]
+    __nv_bfloat16* Qs = Kb + 4 * MMA_SPLIT * MMA_PITCH;
+    __nv_bfloat16* Qlo = Qs + MMA_RT * MMA_PITCH;
+    __nv_bfloat16* Ps = Qlo + MMA_RT * MMA_PITCH;
+    const int tid = threadIdx.x;
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int slot = a.seq_ids[b];
+    const int L0 = a.seq_len[slot];
+    const int Ltot = L0 + a.T;
+    const int s_begin = blockIdx.x * spc;
+    const int s_end = min(s_begin + spc, (Ltot + MMA_SPLIT - 1) / MMA_SPLIT);
+    if (s_begin >= s_end) return;
+    const int G = a.hq / a.hkv;
+    const int R = a.T * G;            // <= MMA_RT (checked by the host)
+    const bool qsplit = a.q_lo_off != 0;
+    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q);
+    for (int i = tid; i < MMA_RT * 16; i += 128) {
+        const int ri = i >> 4, ch = i & 15;
+        if (ri < R) {
+            const int t = ri / G, hh = ri - t * G;
+            const size_t m = (size_t)b * a.T + t;
+            const __nv_bfloat16* src = Q + (m * a.hq + (size_t)g * G + hh) * 128 + ch * 8;
+            cp_async16(smem_u32(Qs + ri * MMA_PITCH + ch * 8), src);
+            if (qsplit) cp_async16(smem_u32(Qlo + ri * MMA_PITCH + ch * 8), src + a.q_lo_off);
+        } else {
+            *reinterpret_cast<uint4*>(Qs + ri * MMA_PITCH + ch * 8) = make_uint4(0, 0, 0, 0);
+            if (qsplit) *reinterpret_cast<uint4*>(Qlo + ri * MMA_PITCH + ch * 8) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    auto kbuf = [&](int s) { return Kb + (size_t)(s & 1) * 2 * MMA_SPLIT * MMA_PITCH; };
+    {
+        const int k0 = s_begin * MMA_SPLIT;
+        attn_load_split(a, slot, g, k0, min(MMA_SPLIT, Ltot - k0), kbuf(s_begin), kbuf(s_begin) + MMA_SPLIT * MMA_PITCH,
+                        tid);        // commits the queries too
+    }
+    const float sl2 = a.scale * 1.4426950408889634f;
+    for (int s = s_begin; s < s_end; ++s) {
+        if (s + 1 < s_end) {
+            const int k1 = (s + 1) * MMA_SPLIT;
+            attn_load_split(a, slot, g, k1, min(MMA_SPLIT, Ltot - k1), kbuf(s + 1),
+                            kbuf(s + 1) + MMA_SPLIT * MMA_PITCH, tid);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const int k0 = s * MMA_SPLIT;
+        const int nk = min(MMA_SPLIT, Ltot - k0);
+        const size_t pbase = (((size_t)b * a.hkv + g) * a.n_chunks + s) * R;
+        attn_mma_tile(a, kbuf(s), kbuf(s) + MMA_SPLIT * MMA_PITCH, Qs, Qlo, Ps, wmax, wsum, qsplit, 0, R,
+                      max(0, k0 - L0) * G, k0, nk, L0, G, pbase, sl2, tid, [] { __syncthreads(); });
+        __syncthreads();             // this half of the buffer is refilled two splits on
+    }
+}
+
 // One warp per query row.
 template <typename T>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
@@ -208,7 +301,17 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
     const int G = a.hq / a.hkv;
     const dim3 cgrid((a.T * G + 3) / 4, a.hkv, B);
     if (use_mma_path(a.hd, c.esize)) {
-        attn_mma_kernel<<<dim3(nsplit, a.hkv, B), 128, MMA_SMEM, st>>>(a);
+        // splits per CTA: one while the items fill about four waves of the GPU, more for
+        // long contexts (at least ATT_MULTI_MIN), so that each CTA streams a run of keys
+        const long long items = (long long)nsplit * a.hkv * B;
+        const long long target = 4LL * 2 * (c.num_sms > 0 ? c.num_sms : 152);
+        int spc = (int)std::min<long long>(nsplit, (items + target - 1) / target);
+        if (a.T * G > MMA_RT || spc < ATT_MULTI_MIN) spc = 1;
+        if (spc == 1) {
+            attn_mma_kernel<<<dim3(nsplit, a.hkv, B), 128, MMA_SMEM, st>>>(a);
+        } else {
+            attn_mma_multi_kernel<<<dim3((nsplit + spc - 1) / spc, a.hkv, B), 128, MMA_MULTI_SMEM, st>>>(a, spc);
+        }
         attn_combine_kernel<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a);
         return 2;
     }
@@ -226,7 +329,9 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
 
 int attention_set_smem_limits(int hd) {
     if (cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MMA_SMEM) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_mma_multi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)MMA_MULTI_SMEM) != cudaSuccess)
         return -1;
     if (cudaFuncSetAttribute(attn_split_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)attn_smem(hd, 2)) != cudaSuccess ||

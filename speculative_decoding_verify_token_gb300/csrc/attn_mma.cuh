@@ -52,6 +52,152 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// The scores, softmax and P V of one tile of up to 64 query rows (rows rt .. rt + nr of the
+// item, in Qs / Qlo rows 0 .. nr) against the nk keys in Ks / Vs starting at key k0, and the
+// tile's per-split (max, sum, unnormalised output) for rows >= row_lo.  Each row's bits
+// depend only on the row, the keys and the split, not on the other rows of the tile.
+template <class Sync>
+__device__ __forceinline__ void attn_mma_tile(const AttnArgs& a, const __nv_bfloat16* Ks, const __nv_bfloat16* Vs,
+                                              const __nv_bfloat16* Qs, const __nv_bfloat16* Qlo, __nv_bfloat16* Ps,
+                                              float (*wmax)[MMA_RT], float (*wsum)[MMA_RT], bool qsplit, int rt,
+                                              int nr, int row_lo, int k0, int nk, int L0, int G, size_t pbase,
+                                              float sl2, int tid, Sync sync) {
+    const int warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int mtiles = (nr + 15) >> 4;
+    // ---- S = Q K^T for this warp's 16 keys ----
+    float sacc[4][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        {
+            const int key = warp * 16 + (lane & 7) + (lane >> 4) * 8;
+            const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
+            ldsm_x4(smem_u32(Ks + key * MMA_PITCH + dim), b0, b1, b2, b3);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            if (mt < mtiles) {
+                uint32_t a0, a1, a2, a3;
+                const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int col = ks * 16 + (lane >> 4) * 8;
+                ldsm_x4(smem_u32(Qs + row * MMA_PITCH + col), a0, a1, a2, a3);
+                mma16816(sacc[mt][0], a0, a1, a2, a3, b0, b1);
+                mma16816(sacc[mt][1], a0, a1, a2, a3, b2, b3);
+                if (qsplit) {      // q_lo K^T into the same scores
+                    ldsm_x4(smem_u32(Qlo + row * MMA_PITCH + col), a0, a1, a2, a3);
+                    mma16816(sacc[mt][0], a0, a1, a2, a3, b0, b1);
+                    mma16816(sacc[mt][1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+        }
+    }
+    // mask, per-warp row max
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        if (mt >= mtiles) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = mt * 16 + gq + h * 8;
+            const int pos = (row < nr) ? L0 + (rt + row) / G : -1;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = warp * 16 + nt * 8 + 2 * tq + e;
+                    float v = sacc[mt][nt][h * 2 + e] * sl2;
+                    if (key >= nk || k0 + key > pos) v = -INFINITY;
+                    sacc[mt][nt][h * 2 + e] = v;
+                    mx = fmaxf(mx, v);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+            if (tq == 0) wmax[warp][row] = mx;
+        }
+    }
+    sync();
+    // p = 2^(s - m), per-warp row sums, P to smem (bf16)
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        if (mt >= mtiles) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = mt * 16 + gq + h * 8;
+            float m = fmaxf(fmaxf(wmax[0][row], wmax[1][row]), fmaxf(wmax[2][row], wmax[3][row]));
+            if (m == -INFINITY) m = 0.0f;
+            float sum = 0.0f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float p0 = exp2f(sacc[mt][nt][h * 2] - m);
+                const float p1 = exp2f(sacc[mt][nt][h * 2 + 1] - m);
+                sum += p0;
+                sum += p1;
+                *reinterpret_cast<uint32_t*>(Ps + row * MMA_PPITCH + warp * 16 + nt * 8 + 2 * tq) = pack_bf16(p0, p1);
+            }
+            sum += __shfl_xor_sync(FULL, sum, 1);
+            sum += __shfl_xor_sync(FULL, sum, 2);
+            if (tq == 0) wsum[warp][row] = sum;
+        }
+    }
+    sync();
+    // ---- O = P V for this warp's 32 dims ----
+    float oacc[4][4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[mt][nt][e] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t v[8];
+        {
+            const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int dim = warp * 32 + (lane >> 4) * 8;
+            ldsm_x4_t(smem_u32(Vs + key * MMA_PITCH + dim), v[0], v[1], v[2], v[3]);
+            ldsm_x4_t(smem_u32(Vs + key * MMA_PITCH + dim + 16), v[4], v[5], v[6], v[7]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            if (mt < mtiles) {
+                uint32_t a0, a1, a2, a3;
+                const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int col = ks * 16 + (lane >> 4) * 8;
+                ldsm_x4(smem_u32(Ps + row * MMA_PPITCH + col), a0, a1, a2, a3);
+                mma16816(oacc[mt][0], a0, a1, a2, a3, v[0], v[1]);
+                mma16816(oacc[mt][1], a0, a1, a2, a3, v[2], v[3]);
+                mma16816(oacc[mt][2], a0, a1, a2, a3, v[4], v[5]);
+                mma16816(oacc[mt][3], a0, a1, a2, a3, v[6], v[7]);
+            }
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        if (mt >= mtiles) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = mt * 16 + gq + h * 8;
+            if (row >= nr) continue;
+            float* dst = a.part_o + (pbase + rt + row) * 128 + warp * 32 + 2 * tq;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                *reinterpret_cast<float2*>(dst + nt * 8) = make_float2(oacc[mt][nt][h * 2], oacc[mt][nt][h * 2 + 1]);
+            if (warp == 0 && tq == 0) {
+                const float m = fmaxf(fmaxf(wmax[0][row], wmax[1][row]), fmaxf(wmax[2][row], wmax[3][row]));
+                const float l = ((wsum[0][row] + wsum[1][row]) + wsum[2][row]) + wsum[3][row];
+                a.part_ml[pbase + rt + row] = make_float2(m, l);
+            }
+        }
+    }
+}
+
 // One attention item: the 64-key split s of kv head g of sequence b, for all T*G query
 // rows, by 128 threads (4 warps; tid in [0, 128)).  S = Q K^T with warp w owning keys
 // [16w, 16w + 16); softmax statistics reduced in a fixed order; O = P V with warp w owning
@@ -78,8 +224,6 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
     const int nk = min(MMA_SPLIT, Ltot - k0);
     const int G = a.hq / a.hkv;
     const int R = a.T * G;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int gq = lane >> 2, tq = lane & 3;
 
     // K and V rows of the split (zero past the sequence end)
     const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_layer);
@@ -138,137 +282,7 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
         cp_async_wait_all();
         sync();
 
-        // ---- S = Q K^T for this warp's 16 keys ----
-        float sacc[4][2][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            {
-                const int key = warp * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
-                ldsm_x4(smem_u32(Ks + key * MMA_PITCH + dim), b0, b1, b2, b3);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                if (mt < mtiles) {
-                    uint32_t a0, a1, a2, a3;
-                    const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int col = ks * 16 + (lane >> 4) * 8;
-                    ldsm_x4(smem_u32(Qs + row * MMA_PITCH + col), a0, a1, a2, a3);
-                    mma16816(sacc[mt][0], a0, a1, a2, a3, b0, b1);
-                    mma16816(sacc[mt][1], a0, a1, a2, a3, b2, b3);
-                    if (qsplit) {      // q_lo K^T into the same scores
-                        ldsm_x4(smem_u32(Qlo + row * MMA_PITCH + col), a0, a1, a2, a3);
-                        mma16816(sacc[mt][0], a0, a1, a2, a3, b0, b1);
-                        mma16816(sacc[mt][1], a0, a1, a2, a3, b2, b3);
-                    }
-                }
-            }
-        }
-        // mask, per-warp row max
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            if (mt >= mtiles) continue;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = mt * 16 + gq + h * 8;
-                const int pos = (row < nr) ? L0 + (rt + row) / G : -1;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int key = warp * 16 + nt * 8 + 2 * tq + e;
-                        float v = sacc[mt][nt][h * 2 + e] * sl2;
-                        if (key >= nk || k0 + key > pos) v = -INFINITY;
-                        sacc[mt][nt][h * 2 + e] = v;
-                        mx = fmaxf(mx, v);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-                if (tq == 0) wmax[warp][row] = mx;
-            }
-        }
-        sync();
-        // p = 2^(s - m), per-warp row sums, P to smem (bf16)
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            if (mt >= mtiles) continue;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = mt * 16 + gq + h * 8;
-                float m = fmaxf(fmaxf(wmax[0][row], wmax[1][row]), fmaxf(wmax[2][row], wmax[3][row]));
-                if (m == -INFINITY) m = 0.0f;
-                float sum = 0.0f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const float p0 = exp2f(sacc[mt][nt][h * 2] - m);
-                    const float p1 = exp2f(sacc[mt][nt][h * 2 + 1] - m);
-                    sum += p0;
-                    sum += p1;
-                    *reinterpret_cast<uint32_t*>(Ps + row * MMA_PPITCH + warp * 16 + nt * 8 + 2 * tq) = pack_bf16(p0, p1);
-                }
-                sum += __shfl_xor_sync(FULL, sum, 1);
-                sum += __shfl_xor_sync(FULL, sum, 2);
-                if (tq == 0) wsum[warp][row] = sum;
-            }
-        }
-        sync();
-        // ---- O = P V for this warp's 32 dims ----
-        float oacc[4][4][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) oacc[mt][nt][e] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t v[8];
-            {
-                const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int dim = warp * 32 + (lane >> 4) * 8;
-                ldsm_x4_t(smem_u32(Vs + key * MMA_PITCH + dim), v[0], v[1], v[2], v[3]);
-                ldsm_x4_t(smem_u32(Vs + key * MMA_PITCH + dim + 16), v[4], v[5], v[6], v[7]);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                if (mt < mtiles) {
-                    uint32_t a0, a1, a2, a3;
-                    const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int col = ks * 16 + (lane >> 4) * 8;
-                    ldsm_x4(smem_u32(Ps + row * MMA_PPITCH + col), a0, a1, a2, a3);
-                    mma16816(oacc[mt][0], a0, a1, a2, a3, v[0], v[1]);
-                    mma16816(oacc[mt][1], a0, a1, a2, a3, v[2], v[3]);
-                    mma16816(oacc[mt][2], a0, a1, a2, a3, v[4], v[5]);
-                    mma16816(oacc[mt][3], a0, a1, a2, a3, v[6], v[7]);
-                }
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            if (mt >= mtiles) continue;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = mt * 16 + gq + h * 8;
-                if (row >= nr) continue;
-                float* dst = a.part_o + (pbase + rt + row) * 128 + warp * 32 + 2 * tq;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-                    *reinterpret_cast<float2*>(dst + nt * 8) = make_float2(oacc[mt][nt][h * 2], oacc[mt][nt][h * 2 + 1]);
-                if (warp == 0 && tq == 0) {
-                    const float m = fmaxf(fmaxf(wmax[0][row], wmax[1][row]), fmaxf(wmax[2][row], wmax[3][row]));
-                    const float l = ((wsum[0][row] + wsum[1][row]) + wsum[2][row]) + wsum[3][row];
-                    a.part_ml[pbase + rt + row] = make_float2(m, l);
-                }
-            }
-        }
+        attn_mma_tile(a, Ks, Vs, Qs, Qlo, Ps, wmax, wsum, qsplit, rt, nr, 0, k0, nk, L0, G, pbase, sl2, tid, sync);
     }
     return true;
 }

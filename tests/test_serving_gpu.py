@@ -95,3 +95,32 @@ def test_serving_rounds(lib):
             ctx[b] += new
     assert matched > 0          # the prompts' copied spans give n-gram matches
     m.close()
+
+
+def test_long_context_attention_bitwise(lib):
+    """32 sequences of ~1300 tokens take the multi-split attention kernel (runs of splits per
+    CTA); the same sequences alone (B=1) take one CTA per split.  Every split's arithmetic
+    is the same, as is every other stage's per-token arithmetic, so the verify rows agree
+    bit for bit."""
+    model, _ = lib
+    shape = dataclasses.replace(synth.QWEN_8B, n_layers=2, name="dense-8b-2l")
+    w = synth.model_weights(shape, seed=0, device="cuda")
+    B, K = 32, 8
+    g = np.random.Generator(np.random.PCG64(11))
+    lens = g.integers(1200, 1400, size=B)
+    prompts = [synth.prompt_tokens(20 + b, int(lens[b]), shape.vocab) for b in range(B)]
+    drafts = torch.from_numpy(g.integers(0, shape.vocab, size=(B, K)).astype(np.int32)).cuda()
+    u = torch.zeros(B, K + 1, dtype=torch.float32, device="cuda")
+    m = model.SpecModel(shape, w, max_batch=B, max_ctx=1400 + K + 8, max_k=K, prefill_chunk=256)
+    for b in range(B):
+        m.prefill(b, torch.from_numpy(prompts[b][:-1]).cuda())
+    last = torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32, device="cuda")
+    big = m.verify(list(range(B)), last, drafts, u, 0.0, want_logits=True)["logits"].cpu()
+    m.close()
+    for b in (0, 17):
+        one = model.SpecModel(shape, w, max_batch=1, max_ctx=1400 + K + 8, max_k=K, prefill_chunk=256)
+        one.prefill(0, torch.from_numpy(prompts[b][:-1]).cuda())
+        r = one.verify([0], last[b:b + 1].clone(), drafts[b:b + 1].clone(), u[b:b + 1].clone(), 0.0,
+                       want_logits=True)["logits"].cpu()
+        assert torch.equal(r[0], big[b]), b
+        one.close()
