@@ -373,6 +373,199 @@ class DenseVerifyWorkload:
                                            f"{emitted_per_step:.4f} emitted tokens per step (closed form)")
 
 
+# ---- workload: 27B target + 0.8B draft under sampling -------------------------------------
+
+class SamplingWorkload:
+    """A 27B-class bf16 target with a 0.8B-class bf16 draft, B = 1, a 2048-token prompt,
+    temperature 1, top-k 20, top-p 0.95 on both sides.  A step is one speculative round at
+    K = 4: the draft decodes K tokens one at a time, each sampled from its truncated q with
+    a seeded uniform, then the target verifies them in one pass against the draft logits
+    (rejection sampling with the same truncation), and both caches are trimmed.  The round
+    reads the accepted length back (the next round's draft input depends on it), so the
+    value is emitted tokens over the rounds' span, drafting included.  `k_sweep` repeats
+    the generation of 512 tokens for K in {1, 2, 4, 8, 16} from the same prefilled prompt."""
+    name = "sampling-27b-0p8b"
+    dtype = "bf16"
+
+    def __init__(self, K=4, prompt_len=2048, n_sweep=512, sweep=(1, 2, 4, 8, 16), layers=None, **_):
+        import dataclasses
+        import synth
+        self.shape, self.dshape = synth.QWEN_27B, synth.DRAFT_0P8B
+        if layers is not None and layers != self.shape.n_layers:
+            self.shape = dataclasses.replace(self.shape, n_layers=layers, name=f"dense-27b-{layers}l")
+        self.K, self.prompt_len, self.n_sweep, self.sweep = K, prompt_len, n_sweep, tuple(sweep)
+        self.T, self.k, self.p = 1.0, 20, 0.95
+
+    def config(self):
+        s, d = self.shape, self.dshape
+        return {"workload": self.name,
+                "model_shape": f"target {s.n_layers} layers, d {s.d_model}, {s.n_q_heads}/{s.n_kv_heads} heads, "
+                               f"head_dim {s.head_dim}, SwiGLU {s.ffn_dim}; draft {d.n_layers} layers, d {d.d_model}, "
+                               f"{d.n_q_heads}/{d.n_kv_heads} heads, SwiGLU {d.ffn_dim}; vocab {s.vocab}, bf16, "
+                               "random init N(0,0.02^2)",
+                "B": 1, "K": self.K, "prompt_len": self.prompt_len, "decoding": "sampling T 1.0, top-k 20, top-p 0.95",
+                "uniforms": "verify PCG64 seed 2, draft PCG64 seed 4",
+                "l2": "inputs larger than L2 (target weights streamed per verify, draft weights per draft token)"}
+
+    def setup(self, device, n_steps):
+        import torch
+        import synth
+        from speculative_decoding_verify_token_gb300 import model as M
+        self.dev = device
+        self.wt = synth.model_weights(self.shape, seed=0, device=device)
+        self.wd = synth.model_weights(self.dshape, seed=0, device=device)
+        kmax = max((self.K,) + self.sweep)
+        max_ctx = self.prompt_len + max(self.n_sweep, (self.K + 1) * n_steps) + 8 * (kmax + 1) + 64
+        self.t = M.SpecModel(self.shape, self.wt, max_ctx=max_ctx, max_k=kmax, prefill_chunk=256)
+        self.d = M.SpecModel(self.dshape, self.wd, max_ctx=max_ctx, max_k=kmax, prefill_chunk=256)
+        self.prompt = torch.from_numpy(synth.prompt_tokens(1, self.prompt_len, self.shape.vocab)).to(device)
+        self.log = []
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        self.reset()
+        torch.cuda.synchronize()
+
+    def reset(self):
+        self.t.reset(0)
+        self.d.reset(0)
+        self.t.prefill(0, self.prompt[:-1])
+        self.d.prefill(0, self.prompt[:-1])
+        self.pending = self.prompt[-1:].clone()
+        self.extra = None
+        self.g = np.random.Generator(np.random.PCG64(2))
+        self.gd = np.random.Generator(np.random.PCG64(4))
+
+    def _round(self, K, u=None, ud=None):
+        import torch
+        dev = self.dev
+        e0, e1, e2 = self.ev
+        e0.record()
+        if self.extra is not None:
+            self.d.prefill(0, self.extra)
+        toks, rows = [], []
+        tok = self.pending
+        if ud is None:
+            ud = torch.from_numpy(self.gd.random(K, dtype=np.float32)).to(dev, non_blocking=True)
+        for i in range(K):
+            tok, lg = self.d.decode([0], tok, ud[i:i + 1], self.T, self.k, self.p, want_logits=True)
+            toks.append(tok)
+            rows.append(lg)
+        drafts = torch.stack(toks, dim=1)
+        dl = torch.stack(rows, dim=1)
+        if u is None:
+            u = torch.from_numpy(self.g.random((1, K + 1), dtype=np.float32)).to(dev, non_blocking=True)
+        e1.record()
+        r = self.t.verify([0], self.pending, drafts, u, self.T, self.k, self.p, draft_logits=dl)
+        e2.record()
+        a = int(r["accepted_len"].item())
+        self.d.kv_trim([0], K - 1, torch.clamp(r["accepted_len"], max=K - 1))
+        self.extra = drafts[0, K - 1:K].clone() if a == K else None
+        self.pending = r["next_token"].clone()
+        ok = int(r["status"].item()) == 0
+        self.log.append((a + 1, K, a, ok, e0.elapsed_time(e1), e1.elapsed_time(e2)))
+
+    def step(self, i):
+        self._round(self.K)
+
+    def launches(self):
+        return self.t.launches() + self.d.launches()
+
+    def check(self, i0, n):
+        rows = self.log[i0:i0 + n]
+        return all(r[3] for r in rows), int(sum(r[0] for r in rows))
+
+    def stats(self, i0, n):
+        rows = self.log[i0:i0 + n]
+        return {"acceptance": sum(r[2] for r in rows) / max(1, sum(r[1] for r in rows)),
+                "emitted_per_step": sum(r[0] for r in rows) / max(1, len(rows)),
+                "draft_ms_per_step": sum(r[4] for r in rows) / max(1, len(rows)),
+                "verify_ms_per_step": sum(r[5] for r in rows) / max(1, len(rows))}
+
+    def k_sweep(self):
+        """512 new tokens per K from the same prompt: accepted tokens/s over the decode wall
+        time (drafting included), the verify pass's and the drafting's event times."""
+        import torch
+        out = {}
+        for K in self.sweep:
+            self.reset()
+            torch.cuda.synchronize()
+            i0 = len(self.log)
+            emitted = 0
+            t0 = time.perf_counter()
+            while emitted < self.n_sweep:
+                self._round(K)
+                emitted += self.log[-1][0]
+            dt = time.perf_counter() - t0
+            st = self.stats(i0, len(self.log) - i0)
+            out[str(K)] = {"tokens_per_s": emitted / dt, "rounds": len(self.log) - i0, **st}
+        return out
+
+    def profile(self, n):
+        self.t.profile(True)
+        for _ in range(n):
+            self._round(self.K)
+        prof = self.t.profile_read()
+        self.t.profile(False)
+        return prof
+
+    def roofline(self, prof, peaks):
+        g = [prof[k] for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head")]
+        ms = sum(x["ms"] for x in g)
+        n = sum(x["launches"] for x in g)
+        by = sum(x["bytes"] for x in g)
+        achieved = (by / n) / (ms / n / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "tc_gemm_kernel",
+                "model": "target", "algorithmic_bytes_per_launch": by / n, "launches_measured": n,
+                "avg_launch_us": ms / n * 1e3, "peak_source": peaks["source"]}
+
+    def e2e(self, n):
+        """The same rounds with the verify uniforms, the draft uniforms and the pending token
+        taken from pinned host memory every round and the round's outputs read back."""
+        import torch
+        h_u = torch.from_numpy(self.g.random((n, self.K + 1), dtype=np.float32)).pin_memory()
+        h_ud = torch.from_numpy(self.gd.random((n, self.K), dtype=np.float32)).pin_memory()
+        torch.cuda.synchronize()
+        emitted = 0
+        t0 = time.perf_counter()
+        for i in range(n):
+            self._round(self.K, u=h_u[i:i + 1].to(self.dev, non_blocking=True),
+                        ud=h_ud[i].to(self.dev, non_blocking=True))
+            emitted += self.log[-1][0]
+        dt = time.perf_counter() - t0
+        return emitted / dt, 4 * (self.K + 1) + 4 * self.K, 8
+
+    def oracle_sample(self, budget_s):
+        """The float64 oracle on a bounded sample of one round: the target's verify pass of
+        K + 1 tokens and the draft's K single-token passes, each through 1 layer (context 63)
+        with a 4096-row lm_head slice, scaled to 64 and 28 layers and the full vocabulary, at
+        the measured emitted tokens per round."""
+        import dataclasses
+        import synth
+        from oracle import model as om
+        out_t = []
+        for shp, n_tok, passes in ((self.shape, self.K + 1, 1), (self.dshape, 1, self.K)):
+            sub = dataclasses.replace(shp, n_layers=1, vocab=4096)
+            names = [n for n in synth.weight_names(sub) if n.startswith("layers.0.")]
+            w = {n: om.to_f64(synth.model_weight(shp, n, seed=0)) for n in names}
+            w["embed"] = om.to_f64(synth.model_weight(sub, "embed", seed=0))
+            w["final_norm"] = np.ones(shp.d_model)
+            w["lm_head"] = om.to_f64(synth.model_weight(sub, "lm_head", seed=0))
+            dec = om.Decoder(sub, w)
+            cache = dec.new_cache()
+            dec.forward(synth.prompt_tokens(1, 63, sub.vocab), cache)
+            toks = [int(t) for t in synth.prompt_tokens(2, n_tok, sub.vocab)]
+            t0 = time.perf_counter()
+            dec.forward(toks, cache)
+            dt = time.perf_counter() - t0
+            out_t.append(dt * shp.n_layers * shp.vocab / sub.vocab * passes)
+        st = self.stats(0, len(self.log))
+        return st["emitted_per_step"] / sum(out_t), (
+            f"float64 target pass of {self.K + 1} tokens and {self.K} draft single-token passes, each through 1 "
+            f"layer (context 63) with a 4096-row lm_head slice, scaled to {self.shape.n_layers}/"
+            f"{self.dshape.n_layers} layers and the full vocabulary, at {st['emitted_per_step']:.3f} emitted tokens "
+            "per round")
+
+
 # ---- workload: batched serving with an n-gram drafter -----------------------------------
 
 class ServingWorkload:
@@ -689,7 +882,7 @@ class VerifyLogitsWorkload:
 
 
 WORKLOADS = {DenseVerifyWorkload.name: DenseVerifyWorkload, VerifyLogitsWorkload.name: VerifyLogitsWorkload,
-             ServingWorkload.name: ServingWorkload}
+             ServingWorkload.name: ServingWorkload, SamplingWorkload.name: SamplingWorkload}
 DEFAULT_WORKLOAD = DenseVerifyWorkload.name
 
 
@@ -717,6 +910,8 @@ def run_reference(args):
         unit_per_step = None
     elif isinstance(wl, ServingWorkload):
         step, sample = reference_serving_step(wl)
+    elif isinstance(wl, SamplingWorkload):
+        step, sample = reference_sampling_step(wl)
     else:
         step, sample = reference_dense_step(wl)
     for _ in range(args.warmup):
@@ -735,6 +930,54 @@ def run_reference(args):
                              "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def reference_sampling_step(wl):
+    """One bounded oracle round of the sampling workload on 1-layer slices (float64, weights
+    drawn on the CPU from the same seeded generators, 4096-row vocabulary): the draft
+    samples K = 4 tokens from its truncated q (context 63), the target's verify pass of the
+    K + 1 tokens and the oracle's rejection-sampling rule; counted as 1/64 of a round
+    (the target's 64 layers dominate), emitting (a + 1) / 64 tokens."""
+    import copy
+    import dataclasses
+    import synth
+    from oracle import model as om
+    from oracle import verify as ov
+    decs = []
+    for shp in (wl.shape, wl.dshape):
+        sub = dataclasses.replace(shp, n_layers=1, vocab=4096)
+        names = [n for n in synth.weight_names(sub) if n.startswith("layers.0.")]
+        w = {n: om.to_f64(synth.model_weight(shp, n, seed=0)) for n in names}
+        w["embed"] = om.to_f64(synth.model_weight(sub, "embed", seed=0))
+        w["final_norm"] = np.ones(shp.d_model)
+        w["lm_head"] = om.to_f64(synth.model_weight(sub, "lm_head", seed=0))
+        decs.append(om.Decoder(sub, w))
+    tgt, dft = decs
+    prompt = [int(t) for t in synth.prompt_tokens(1, 64, 4096)]
+    caches = []
+    for dec in decs:
+        c = dec.new_cache()
+        dec.forward(prompt[:-1], c, logits_rows=np.zeros(0, dtype=np.int64))
+        caches.append(c)
+    g = np.random.Generator(np.random.PCG64(2))
+    K = wl.K
+
+    def step():
+        ct, cd = copy.deepcopy(caches[0]), copy.deepcopy(caches[1])
+        tok = prompt[-1]
+        drafts, qrows = [], []
+        for _ in range(K):
+            row = dft.forward([tok], cd)[0]
+            tok, _ = ov.sample_token(row, float(g.random()), wl.T, wl.k, wl.p)
+            drafts.append(tok)
+            qrows.append(row)
+        rows = tgt.forward([prompt[-1]] + drafts, ct)
+        r = ov.verify(rows, np.array(qrows), np.array(drafts), list(g.random(K + 1)), wl.T, wl.k, wl.p)
+        return (r["a"] + 1) / wl.shape.n_layers
+
+    return step, (f"one round on 1-layer slices of the target and the draft (4096-row vocabulary, context 63): "
+                  f"{K} sampled draft tokens, the target pass of {K + 1} tokens and the rejection rule; counted as "
+                  f"1/{wl.shape.n_layers} of a round")
 
 
 def reference_serving_step(wl):
@@ -832,7 +1075,7 @@ def main():
     peaks = load_peaks()
     if args.workload == DenseVerifyWorkload.name:
         wl = WORKLOADS[args.workload](n_gen=args.gen, layers=args.layers)
-    elif args.workload == ServingWorkload.name:
+    elif args.workload in (ServingWorkload.name, SamplingWorkload.name):
         wl = WORKLOADS[args.workload](layers=args.layers)
     else:
         wl = WORKLOADS[args.workload]()
@@ -890,6 +1133,9 @@ def main():
         extra["step_frac_of_8tbs"] = extra["step_hbm_gbs"] / 8000.0
     e2e_val, h2d, d2h = wl.e2e(max(5, min(args.steps, 20)))
     e2e_val = e2e_val * world
+    if isinstance(wl, SamplingWorkload):
+        extra.update(wl.stats(args.warmup, args.steps))
+        extra["k_sweep"] = wl.k_sweep()
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
