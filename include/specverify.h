@@ -260,6 +260,11 @@ int spec_seq_reset(spec_ctx* ctx, int seq_id);
 #define SPEC_OPT_PERSISTENT 4
 #define SPEC_OPT_PF_ATOMS 5
 #define SPEC_OPT_PF_L2_AHEAD 6
+/* SPEC_OPT_ATTN_L2_AHEAD (0..64, default 0 = off): on long contexts, where one attention CTA
+ * walks a run of 64-key splits, the K and V pages of the split this many splits ahead are
+ * prefetched into L2 (bulk prefetch, no shared memory) while the current one is computed.
+ * Changes no result bit (measured neutral on 2k-16k contexts). */
+#define SPEC_OPT_ATTN_L2_AHEAD 7
 int spec_set_option(spec_ctx* ctx, int option, int value);
 
 /* Per-kernel-class timing of the context's passes with CUDA events recorded on its

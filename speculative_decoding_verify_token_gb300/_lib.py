@@ -51,6 +51,7 @@ class SpecCtxLimits(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("prefill_chunk", ctypes.c_int32)]
 
 
+SPEC_OPT_ATTN_L2_AHEAD = 7
 SPEC_OPT_GRAPHS = 1
 SPEC_OPT_PDL = 2
 SPEC_OPT_L2_PREFETCH = 3

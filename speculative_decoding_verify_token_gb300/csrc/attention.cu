@@ -224,6 +224,18 @@ __device__ __forceinline__ void attn_load_split(const AttnArgs& a, int slot, int
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// Warm L2 with the K and V pages of split s (four 16-token pages of each, 4 KB apiece).
+__device__ __forceinline__ void attn_prefetch_split(const AttnArgs& a, int slot, int g, int s, int Ltot) {
+    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_layer);
+    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_layer);
+    for (int pos = s * MMA_SPLIT; pos < min(Ltot, (s + 1) * MMA_SPLIT); pos += 16) {
+        const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
+        const size_t off = ((size_t)page * a.hkv + g) * 16 * 128;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 4096;" :: "l"(kp + off) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 4096;" :: "l"(vp + off) : "memory");
+    }
+}
+
 __global__ void __launch_bounds__(128) attn_mma_multi_kernel(const AttnArgs a, int spc) {
     extern __shared__ __align__(128) uint8_t sm_raw[];
     __shared__ float wmax[4][MMA_RT], wsum[4][MMA_RT];
@@ -258,6 +270,9 @@ __global__ void __launch_bounds__(128) attn_mma_multi_kernel(const AttnArgs a, i
         }
     }
     auto kbuf = [&](int s) { return Kb + (size_t)(s & 1) * 2 * MMA_SPLIT * MMA_PITCH; };
+    const int ahead = a.l2_ahead;
+    if (tid == 0)
+        for (int s = s_begin + 1; s < min(s_end, s_begin + 1 + ahead); ++s) attn_prefetch_split(a, slot, g, s, Ltot);
     {
         const int k0 = s_begin * MMA_SPLIT;
         attn_load_split(a, slot, g, k0, min(MMA_SPLIT, Ltot - k0), kbuf(s_begin), kbuf(s_begin) + MMA_SPLIT * MMA_PITCH,
@@ -265,6 +280,7 @@ __global__ void __launch_bounds__(128) attn_mma_multi_kernel(const AttnArgs a, i
     }
     const float sl2 = a.scale * 1.4426950408889634f;
     for (int s = s_begin; s < s_end; ++s) {
+        if (tid == 0 && ahead > 0 && s + 1 + ahead < s_end) attn_prefetch_split(a, slot, g, s + 1 + ahead, Ltot);
         if (s + 1 < s_end) {
             const int k1 = (s + 1) * MMA_SPLIT;
             attn_load_split(a, slot, g, k1, min(MMA_SPLIT, Ltot - k1), kbuf(s + 1),
@@ -291,6 +307,19 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
     attn_combine_row<T>(a, blockIdx.x * 4 + (threadIdx.x >> 5), blockIdx.y, blockIdx.z, threadIdx.x & 31);
 }
 
+// head_dim 128 with at most COMB_MAXC splits: the vectorised combine (same bits), with few
+// enough registers for six CTAs (24 warps) per SM.
+template <typename T>
+__global__ void __launch_bounds__(128, 6) attn_combine128_kernel(const AttnArgs a) {
+    __shared__ float2 mls[4][COMB_MAXC];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * 4 + warp;
+    if (r >= a.T * (a.hq / a.hkv)) return;
+    attn_combine_row_128<T>(a, r, blockIdx.y, blockIdx.z, threadIdx.x & 31, mls[warp]);
+}
+
 size_t attn_smem(int hd, int esize) {
     const int split = attention_split_keys(hd, esize);
     return (size_t)2 * split * hd * esize + sizeof(float) * ((size_t)ATT_RT * hd + (size_t)ATT_RT * split);
@@ -312,7 +341,10 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
         } else {
             attn_mma_multi_kernel<<<dim3((nsplit + spc - 1) / spc, a.hkv, B), 128, MMA_MULTI_SMEM, st>>>(a, spc);
         }
-        attn_combine_kernel<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a);
+        if (a.n_chunks <= COMB_MAXC)
+            attn_combine128_kernel<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a);
+        else
+            attn_combine_kernel<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a);
         return 2;
     }
     const size_t smem = attn_smem(a.hd, c.esize);

@@ -341,6 +341,58 @@ __device__ __forceinline__ void attn_combine_row_dpl(const AttnArgs& a, int r, i
     for (int e = 0; e < DPL; ++e) store_split<T>(dst + e, a.o_lo_off, o[e] / l);
 }
 
+// head_dim 128 with the row's (max, sum) pairs staged in shared memory (mls: room for
+// COMB_MAXC splits, per warp): the same arithmetic, in the same order, as the general
+// version -- lanes over splits for the max and the sum, then the output in split order --
+// with one 16-byte load per lane and split and CG splits' loads in flight.
+constexpr int COMB_MAXC = 512;
+template <typename T>
+__device__ __forceinline__ void attn_combine_row_128(const AttnArgs& a, int r, int g, int b, int lane, float2* mls) {
+    const int G = a.hq / a.hkv;
+    const int R = a.T * G;
+    const int slot = a.seq_ids[b];
+    const int t = r / G, hh = r - t * G;
+    const int ns = (a.seq_len[slot] + t) / a.split_keys + 1;
+    const size_t cbase = ((size_t)b * a.hkv + g) * a.n_chunks;
+    for (int c = lane; c < ns; c += 32) mls[c] = __ldcg(a.part_ml + (cbase + c) * R + r);
+    __syncwarp();
+    float mloc = -INFINITY;
+    for (int c = lane; c < ns; c += 32) mloc = fmaxf(mloc, mls[c].x);
+    const float mt = warp_max(mloc);
+    float lloc = 0.0f;
+    for (int c = lane; c < ns; c += 32) lloc = fmaf(exp2f(mls[c].x - mt), mls[c].y, lloc);
+    const float l = warp_sum(lloc);
+    __syncwarp();
+    for (int c = lane; c < ns; c += 32) mls[c].x = exp2f(mls[c].x - mt);
+    __syncwarp();
+    float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
+    constexpr int CG = 16;
+    const float4* src = reinterpret_cast<const float4*>(a.part_o + (cbase * R + r) * 128) + lane;
+    const size_t cstride = (size_t)R * 128 / 4;      // float4 per split
+    for (int c0 = 0; c0 < ns; c0 += CG) {
+        float4 v[CG];
+#pragma unroll
+        for (int u = 0; u < CG; ++u)
+            v[u] = c0 + u < ns ? __ldcg(src + (size_t)(c0 + u) * cstride) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int u = 0; u < CG; ++u)
+            if (c0 + u < ns) {        // uniform over the warp
+                const float w = mls[c0 + u].x;
+                o0 = fmaf(w, v[u].x, o0);
+                o1 = fmaf(w, v[u].y, o1);
+                o2 = fmaf(w, v[u].z, o2);
+                o3 = fmaf(w, v[u].w, o3);
+            }
+    }
+    __syncwarp();
+    const size_t m = (size_t)b * a.T + t;
+    T* dst = static_cast<T*>(a.o) + (m * a.hq + (size_t)g * G + hh) * 128 + lane * 4;
+    store_split<T>(dst + 0, a.o_lo_off, o0 / l);
+    store_split<T>(dst + 1, a.o_lo_off, o1 / l);
+    store_split<T>(dst + 2, a.o_lo_off, o2 / l);
+    store_split<T>(dst + 3, a.o_lo_off, o3 / l);
+}
+
 // Combine of the splits of one query row r of kv head g of sequence b, by one warp (lane =
 // lane index): the row's splits 0..pos/SPLIT are reduced in a fixed order (lanes over
 // splits for the max and the sum, then the output in split order), so the result depends

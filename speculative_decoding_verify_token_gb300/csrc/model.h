@@ -40,6 +40,7 @@ struct AttnArgs {
     int* att_cnt;             // [slots * hkv] arrival counters, zero between passes
     size_t q_lo_off;          // split activations: elements from a query (output) value to
     size_t o_lo_off;          // its bf16 lo half; 0 = not split
+    int l2_ahead;             // multi-split kernel: splits prefetched into L2 ahead of the copies
 };
 
 struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
@@ -125,6 +126,7 @@ struct Ctx {
     bool use_pf = false;
     int pf_atoms = 4;
     int pf_l2_ahead = 0;
+    int attn_l2_ahead = 0;                 // splits of K/V warmed in L2 ahead (long contexts)
     std::vector<void*> allocs;
 };
 

@@ -277,6 +277,7 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     aa.n_chunks = c.n_chunks; aa.part_o = c.part_o; aa.part_ml = c.part_ml;
     aa.split_keys = c.split_keys; aa.att_cnt = c.att_cnt;
     aa.q_lo_off = qlo; aa.o_lo_off = qlo;
+    aa.l2_ahead = c.attn_l2_ahead;
 
     int rc;
     if (fused && !last_only && logits_out != nullptr && pf_usable(c, M)) {
@@ -676,6 +677,10 @@ extern "C" int spec_set_option(spec_ctx* c, int option, int value) {
     } else if (option == SPEC_OPT_PF_L2_AHEAD) {
         if (value < 0 || value > 256) return set_error(SPEC_E_INVAL, "L2 prefetch distance must be in [0, 256]");
         c->pf_l2_ahead = value;
+    } else if (option == SPEC_OPT_ATTN_L2_AHEAD) {
+        if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "attention L2 prefetch distance must be in [0, 64]");
+        c->attn_l2_ahead = value;
+        drop_graphs(*c);
     } else if (option == SPEC_OPT_L2_PREFETCH) {
         if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "L2 prefetch atoms must be in [0, 64]");
         c->l2_prefetch_atoms = value;
