@@ -54,13 +54,13 @@ constexpr int BM_INFLIGHT = 2;                       // blocks loaded at once pe
 #define BM_SMEM_CARVEOUT 13                         // per cent of L1 kept as shared memory
 #endif
 #ifndef BM_STATIC_PCT
-#define BM_STATIC_PCT 75                             // share of pass-1 blocks in static sweeps
+#define BM_STATIC_PCT 90                             // share of pass-1 blocks in static sweeps
 #endif
 constexpr int RF_MAX_WARPS = 16;                     // pass 2: warps (rows in flight) per CTA
 constexpr int RF_SAMPLE_WARPS = 4;                   // sample mode: rows per CTA
 constexpr int RF_BPL = 5;                            // blocks' second values a lane holds per round
 constexpr int RF_KPL = 2 * RF_BPL;                   // float4 of (maximum, id) pairs a lane holds per round
-constexpr int RF_BATCH = 8;                          // fine blocks loaded at once per warp
+constexpr int RF_BATCH = 4;                          // fine blocks read again at once per warp
 constexpr int RF_SEL_CAP = 64;                       // fine blocks listed before they are read again
 // per-warp candidate buffer, merged into the warp's list of 32 before an append could
 // overflow it (appends come 64 or 128 at a time)
@@ -253,9 +253,9 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
         bool reject = false;
         a = kb;
         int d = -1;
-        // the positions' P(d) and Q(d), 8 positions per round with their loads and warp
+        // the positions' P(d) and Q(d), SB positions per round with their loads and warp
         // reductions issued together; the scan stops at the first reject
-        constexpr int SB = 8;
+        constexpr int SB = 4;
         bool done = false;
         for (int i0 = 0; i0 < kb && !done; i0 += SB) {
             float pd[SB], qd[SB];
@@ -297,7 +297,7 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
                 if (has_q) {
                     const int qid = rid[dl(a)];
                     const float qp = rp[dl(a)];
-#pragma unroll
+#pragma unroll 1
                     for (int t = 0; t < LISTN; ++t) {
                         const int tid = __shfl_sync(FULL, qid, t);
                         const float tp = __shfl_sync(FULL, qp, t);
