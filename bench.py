@@ -1062,6 +1062,8 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=10)
     ap.add_argument("--gen", type=int, default=512, help="tokens of the recorded greedy trajectory (8B workload)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the 8B shape (profiler captures only)")
+    ap.add_argument("--profiler-range", action="store_true",
+                    help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -1097,11 +1099,15 @@ def main():
         l0 = wl.launches()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        if args.profiler_range:
+            torch.cuda.profiler.start()
         t0.record(stream)
         for i in range(args.warmup, n_total):
             wl.step(i)
         t1.record(stream)
         torch.cuda.synchronize()
+        if args.profiler_range:
+            torch.cuda.profiler.stop()
         launches = wl.launches() - l0
         barrier(world)
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
