@@ -87,6 +87,32 @@ __device__ __forceinline__ void qkv_pair_rows(int p, int hd, int& hs, int& j) {
     j = p - hs * half;
 }
 
+// QKV epilogue of one token m (pass-wide index) and one rotate-half pair (j, j + hd/2) of
+// head row hs: RoPE with (cos, sin) = cs for q and k heads, then the query store (hi/lo
+// split) or the K/V append at position pos of KV page `page`.
+template <typename T>
+__device__ __forceinline__ void qkv_store(const EpiArgs& e, int m, int hs, int j, int pos, float2 cs, int page,
+                                          float a0, float a1) {
+    const int half = e.hd >> 1;
+    if (hs < e.hq + e.hkv) {
+        const float r0 = a0 * cs.x - a1 * cs.y;
+        const float r1 = a1 * cs.x + a0 * cs.y;
+        a0 = r0; a1 = r1;
+    }
+    if (hs < e.hq) {
+        T* q = static_cast<T*>(e.q_out) + (size_t)m * e.hq * e.hd + (size_t)hs * e.hd;
+        store_split<T>(q + j, e.lo_off, a0);
+        store_split<T>(q + j + half, e.lo_off, a1);
+    } else {
+        const bool is_k = hs < e.hq + e.hkv;
+        const int kvh = is_k ? hs - e.hq : hs - e.hq - e.hkv;
+        T* base = static_cast<T*>(is_k ? e.k_layer : e.v_layer) +
+                  (((size_t)page * e.hkv + kvh) * 16 + (pos & 15)) * e.hd;
+        base[j] = from_f32<T>(a0);
+        base[j + half] = from_f32<T>(a1);
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ void epi_pair(const EpiArgs& e, int m_local, int p, float a0, float a1) {
     const int m = m_local + e.m0;
@@ -94,27 +120,10 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& e, int m_local, int p, f
     case EPI_QKV: {
         int hs, j;
         qkv_pair_rows(p, e.hd, hs, j);
-        const int half = e.hd >> 1;
         const int pos = e.tok_pos[m];
-        if (hs < e.hq + e.hkv) {
-            const float2 cs = e.rope[(size_t)pos * half + j];
-            const float r0 = a0 * cs.x - a1 * cs.y;
-            const float r1 = a1 * cs.x + a0 * cs.y;
-            a0 = r0; a1 = r1;
-        }
-        if (hs < e.hq) {
-            T* q = static_cast<T*>(e.q_out) + (size_t)m * e.hq * e.hd + (size_t)hs * e.hd;
-            store_split<T>(q + j, e.lo_off, a0);
-            store_split<T>(q + j + half, e.lo_off, a1);
-        } else {
-            const bool is_k = hs < e.hq + e.hkv;
-            const int kvh = is_k ? hs - e.hq : hs - e.hq - e.hkv;
-            const int page = e.block_table[(size_t)e.tok_seq[m] * e.max_pages + (pos >> 4)];
-            T* base = static_cast<T*>(is_k ? e.k_layer : e.v_layer) +
-                      (((size_t)page * e.hkv + kvh) * 16 + (pos & 15)) * e.hd;
-            base[j] = from_f32<T>(a0);
-            base[j + half] = from_f32<T>(a1);
-        }
+        const float2 cs = hs < e.hq + e.hkv ? e.rope[(size_t)pos * (e.hd >> 1) + j] : make_float2(1.0f, 0.0f);
+        const int page = hs >= e.hq ? e.block_table[(size_t)e.tok_seq[m] * e.max_pages + (pos >> 4)] : 0;
+        qkv_store<T>(e, m, hs, j, pos, cs, page, a0, a1);
         break;
     }
     case EPI_SWIGLU:

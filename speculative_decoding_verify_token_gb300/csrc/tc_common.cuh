@@ -234,11 +234,22 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
             static_cast<const __nv_bfloat16*>(e.g_next) + n0);
         const float2 g = __bfloat1622float2(g2);
         const int wq = (etid >> 5) & 1;
-        for (int cc = half; cc < TC_CW; cc += 2) {
+        // this thread's residual pairs of the chunk's tokens, loaded together (written by
+        // other CTAs of a persistent pass: not from L1)
+        float2 xin[TC_CW / 2];
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int m = c0 + half + 2 * j;
+            xin[j] = m < M ? __ldcg(reinterpret_cast<const float2*>(e.x + (size_t)(m + e.m0) * e.ldx + n0))
+                           : make_float2(0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int cc = half + 2 * j;
             const int m = c0 + cc;
             if (m >= M) break;        // uniform over a warp: a warp holds one half
             float2* x = reinterpret_cast<float2*>(e.x + (size_t)(m + e.m0) * e.ldx + n0);
-            float2 xv = __ldcg(x);        // written by other CTAs of a persistent pass: not from L1
+            float2 xv = xin[j];
             xv.x += xs[r0 * TC_XPITCH + cc];
             xv.y += xs[r1 * TC_XPITCH + cc];
             *x = xv;
@@ -261,6 +272,39 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
         return;
     }
     const bool scaled = e.ssq_in != nullptr;
+    if (e.kind == EPI_QKV) {
+        // the chunk's per-token inputs (position, RoPE pair, KV page) loaded together first
+        int hs, jq;
+        qkv_pair_rows(pidx, e.hd, hs, jq);
+        int pos[TC_CW / 2], page[TC_CW / 2];
+        float2 cs[TC_CW / 2];
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int m = c0 + half + 2 * j;
+            pos[j] = m < M ? e.tok_pos[m + e.m0] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int m = c0 + half + 2 * j;
+            cs[j] = (m < M && hs < e.hq + e.hkv) ? e.rope[(size_t)pos[j] * (e.hd >> 1) + jq] : make_float2(1.0f, 0.0f);
+            page[j] = (m < M && hs >= e.hq)
+                          ? e.block_table[(size_t)e.tok_seq[m + e.m0] * e.max_pages + (pos[j] >> 4)] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int cc = half + 2 * j;
+            const int m = c0 + cc;
+            if (m >= M) break;
+            float a0 = xs[r0 * TC_XPITCH + cc], a1 = xs[r1 * TC_XPITCH + cc];
+            if (scaled) {
+                const float s = inv_s[m];
+                a0 *= s;
+                a1 *= s;
+            }
+            qkv_store<__nv_bfloat16>(e, m + e.m0, hs, jq, pos[j], cs[j], page[j], a0, a1);
+        }
+        return;
+    }
     for (int cc = half; cc < TC_CW; cc += 2) {
         const int m = c0 + cc;
         if (m >= M) break;
