@@ -86,7 +86,7 @@ struct PfParams {
     // [hkv QKV head groups][B x hkv attention splits][combined rows][O][gate/up][down] tiles
     unsigned* ctr;
     int ctr_stride, ctr_count;
-    float* partial;             // [grid][2][128][ntok] stream-K partial sums
+    float* partial;             // [grid][2] x ntok/16 chunks of [4][128] float4 stream-K partial sums
     int* tile_cnt;              // [n_tile_cnt] fixup tickets, zero between launches
     int n_tile_cnt;
     int* err;
@@ -515,13 +515,13 @@ __device__ __noinline__ bool pf_gemm_epilogue(const PfParams& P, const PfShared&
             finished = true;
         } else {
             const int which = (s0 >= tile_k0) ? 0 : 1;
-            float* dst = P.partial + (((size_t)cta * 2 + which) * TC_BM + row) * P.ntok;
             for (int c0 = 0; c0 < P.ntok; c0 += TC_CW) {
                 float v[16];
                 acc_ld16(taddr, c0, P.br.lo_col, v);
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < 4; ++j)
+                    *partial_f4(P.partial, cta, which, P.ntok, c0, j, row) =
+                        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&sh.acce[buf]));
@@ -547,10 +547,9 @@ __device__ __noinline__ bool pf_gemm_epilogue(const PfParams& P, const PfShared&
                             const int cc = cb + u;
                             if (cc <= c_hi) {
                                 const int wc = cc == c_lo ? wc_lo : 0;
-                                const float* src = P.partial + (((size_t)cc * 2 + wc) * TC_BM + row) * P.ntok + c0;
 #pragma unroll
                                 for (int j = 0; j < 4; ++j)
-                                    part[u][j] = __ldcg(reinterpret_cast<const float4*>(src + 4 * j));
+                                    part[u][j] = __ldcg(partial_f4(P.partial, cc, wc, P.ntok, c0, j, row));
                             }
                         }
 #pragma unroll

@@ -56,7 +56,7 @@ struct TcParams {
     // producer once its own loads are all issued)
     CUtensorMap nwmap[3];
     int ngid, n_ntiles, n_KB, n_atoms;       // n_atoms = 0: no prefetch
-    float* partial;          // [grid][2][128][ntok]
+    float* partial;          // [grid][2] x ntok/16 chunks of [4][128] float4 (partial_f4)
     int* tile_cnt;           // [n_tiles], zero between launches
     int* err;
     EpiArgs e;
@@ -331,13 +331,13 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 }
             } else {
                 const int which = (s0 >= tile_k0) ? 0 : 1;
-                float* dst = p.partial + (((size_t)cta * 2 + which) * TC_BM + row) * p.ntok;
                 for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
                     float v[16];
                     acc_ld16(taddr, c0, p.br.lo_col, v);
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    for (int j = 0; j < 4; ++j)
+                        *partial_f4(p.partial, cta, which, p.ntok, c0, j, row) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&acce[buf]));
@@ -366,10 +366,9 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                                 const int cc = cb + u;
                                 if (cc <= c_hi) {
                                     const int wc = cc == c_lo ? wc_lo : 0;
-                                    const float* src = p.partial + (((size_t)cc * 2 + wc) * TC_BM + row) * p.ntok + c0;
 #pragma unroll
                                     for (int j = 0; j < 4; ++j)
-                                        part[u][j] = __ldcg(reinterpret_cast<const float4*>(src + 4 * j));
+                                        part[u][j] = __ldcg(partial_f4(p.partial, cc, wc, p.ntok, c0, j, row));
                                 }
                             }
 #pragma unroll

@@ -215,6 +215,13 @@ struct StageWalk {
     }
 };
 
+// Stream-K partial sums of one (CTA, slot): ntok / 16 chunks of 16 token columns, each
+// stored as [4 float4 columns][TC_BM rows], so that a warp's stores and loads of one float4
+// column of a chunk (32 consecutive rows) are contiguous.  ntok is a multiple of 16.
+__device__ __forceinline__ float4* partial_f4(float* base, int cta, int which, int ntok, int c0, int j, int row) {
+    return reinterpret_cast<float4*>(base + (((size_t)cta * 2 + which) * ntok + c0) * TC_BM) + (size_t)j * TC_BM + row;
+}
+
 // Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
 // inv_s[m] = 1/rms of token m when the GEMM consumes a normed row; red = [4 warps][16]
 // scratch of the sums of squares when it produces one.
