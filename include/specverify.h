@@ -313,6 +313,29 @@ int spec_ngram_draft_batch(spec_ngram* const* g, int B, int K, int32_t* out_toke
 int spec_ngram_length(const spec_ngram* g);
 void spec_ngram_destroy(spec_ngram* g);
 
+/* Draft-length gate ([OptiQ] "N-gram lookup: any model": the draft length follows how often
+ * recent drafts were accepted, against a timed verification pass).  Reading: acceptance
+ * alpha = (S + 1) / (S + F + 2) from decayed counts of accepted draft tokens S and first
+ * rejections F (both multiplied by `decay` every round, drafts or not); a round drafts the
+ * n <= min(n_max, available) maximising (1 + alpha + ... + alpha^n) / cost[n], the
+ * smaller n on ties.  cost [n_max + 1] (host): the timed cost of a verify pass with n
+ * drafted tokens, any positive unit.  Host-only.
+ *
+ * spec_ngram_gate_create: SPEC_E_INVAL for n_max outside [0, 1024], decay outside [0, 1]
+ *   or a cost that is not finite and positive; SPEC_E_NOMEM if allocation fails.
+ * spec_ngram_gate_choose: the draft length for a round whose drafter offers `available`
+ *   tokens (>= 0), or SPEC_E_INVAL.
+ * spec_ngram_gate_update: after the round: `drafted` tokens were verified and `accepted`
+ *   of them kept (0 <= accepted <= drafted, else SPEC_E_INVAL).
+ * spec_ngram_gate_acceptance: the current alpha (-1 for NULL). */
+typedef struct spec_ngram_gate spec_ngram_gate;
+
+int spec_ngram_gate_create(int n_max, const double* cost, double decay, spec_ngram_gate** out);
+int spec_ngram_gate_choose(const spec_ngram_gate* g, int available);
+int spec_ngram_gate_update(spec_ngram_gate* g, int drafted, int accepted);
+double spec_ngram_gate_acceptance(const spec_ngram_gate* g);
+void spec_ngram_gate_destroy(spec_ngram_gate* g);
+
 /* Number of kernels the context launched since creation (for launch accounting). */
 long long spec_kernel_launches(const spec_ctx* ctx);
 

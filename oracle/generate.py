@@ -13,10 +13,13 @@ Drafters defined here (inputs to the verify step, not part of it):
   * n-gram -- [OptiQ] "N-gram lookup": when the last >= 3 tokens match earlier in the
     context, draft the tokens that followed (longest match of 8 down to 3 tokens, most
     recent occurrence, at most n_draft tokens).
+A draft-length gate (DraftGate) picks how many of those tokens to verify each step.
 
 Parity status: pinned -- greedy speculative output equals plain greedy output
 ([SD-Apple] "Why this needed a patch", [OptiQ] "In float32 the output is identical"),
-and the scripted drafter's mean emitted tokens per step against its closed form.
+and the scripted drafter's mean emitted tokens per step against its closed form; the draft
+gate's expected tokens against the geometric closed form and brute-force enumeration, and
+its decisions on hand-worked cost tables.
 """
 import numpy as np
 
@@ -109,3 +112,60 @@ def ngram_draft(context, n_draft=8, min_match=3, max_match=8):
                 if follow:
                     return follow
     return []
+
+
+class DraftGate:
+    """[OptiQ] "N-gram lookup": the draft length of a step follows how often recent drafts
+    were accepted, set against the timed cost of a verify pass; long drafts while text is
+    copied, none during new prose.
+
+    Reading (the pages give no formula): a drafted token is accepted with probability
+    alpha = (S + 1) / (S + F + 2) -- a uniform prior over alpha updated with S accepted draft
+    tokens and F first rejections -- where every round first multiplies S and F by `decay`
+    (so that alpha drifts back to 1/2 while nothing is drafted, and drafting is retried).
+    With acceptance alpha a verify pass over n drafts emits j + 1 tokens when the first j
+    drafts are accepted, so its mean is expected_tokens(alpha, n); the gate drafts the
+    n <= min(n_max, available) with the largest expected_tokens / cost[n], the smaller n on
+    ties."""
+
+    def __init__(self, cost, decay=0.9):
+        self.cost = [float(c) for c in cost]
+        self.n_max = len(self.cost) - 1
+        self.decay = float(decay)
+        self.S = 0.0
+        self.F = 0.0
+
+    def acceptance(self):
+        return (self.S + 1.0) / (self.S + self.F + 2.0)
+
+    @staticmethod
+    def expected_tokens(alpha, n):
+        """Mean tokens emitted by a verify pass with n drafts: the j accepted drafts plus the
+        target's own token, j = n with probability alpha^n, else j < n with probability
+        alpha^j (1 - alpha)."""
+        total = 0.0
+        for j in range(n + 1):
+            p = alpha ** j * ((1.0 - alpha) if j < n else 1.0)
+            total += p * (j + 1)
+        return total
+
+    def scores(self, available):
+        lim = max(0, min(self.n_max, int(available)))
+        a = self.acceptance()
+        return [self.expected_tokens(a, n) / self.cost[n] for n in range(lim + 1)]
+
+    def choose(self, available):
+        s = self.scores(available)
+        best = 0
+        for n in range(1, len(s)):
+            if s[n] > s[best]:
+                best = n
+        return best
+
+    def update(self, drafted, accepted):
+        self.S *= self.decay
+        self.F *= self.decay
+        if drafted > 0:
+            self.S += accepted
+            if accepted < drafted:
+                self.F += 1.0

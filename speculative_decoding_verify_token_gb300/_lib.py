@@ -102,6 +102,11 @@ SIGNATURES = {
                                        ctypes.POINTER(ctypes.c_int32)]),
     "spec_ngram_length": (c_int, [c_vp]),
     "spec_ngram_destroy": (None, [c_vp]),
+    "spec_ngram_gate_create": (c_int, [c_int, ctypes.POINTER(ctypes.c_double), ctypes.c_double, ctypes.POINTER(c_vp)]),
+    "spec_ngram_gate_choose": (c_int, [c_vp, c_int]),
+    "spec_ngram_gate_update": (c_int, [c_vp, c_int, c_int]),
+    "spec_ngram_gate_acceptance": (ctypes.c_double, [c_vp]),
+    "spec_ngram_gate_destroy": (None, [c_vp]),
 }
 
 _lib = None

@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <array>
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <unordered_map>
@@ -142,3 +143,87 @@ extern "C" int spec_ngram_length(const spec_ngram* g) {
 }
 
 extern "C" void spec_ngram_destroy(spec_ngram* g) { delete g; }
+
+// ---- draft-length gate ------------------------------------------------------------------
+//
+// [OptiQ] "N-gram lookup: any model": the server times a verification pass per model, then
+// picks how many tokens to draft each step from how often recent drafts were accepted,
+// drafting long while text is copied and not at all during new prose.  Reading: the
+// acceptance of a drafted token is alpha = (S + 1) / (S + F + 2), with S the accepted draft
+// tokens and F the first rejections of recent rounds, both decayed by `decay` every round
+// (so that after rounds without drafts alpha drifts back to 1/2 and drafting is tried
+// again); a round with n drafts is expected to emit E(n) = 1 + alpha + ... + alpha^n tokens
+// at the timed cost cost[n], and the gate drafts the n <= min(n_max, available) that
+// maximises E(n) / cost[n] (the smaller n on ties).
+
+struct spec_ngram_gate {
+    int n_max = 0;
+    std::vector<double> cost;
+    double decay = 0.9;
+    double S = 0.0, F = 0.0;
+
+    double alpha() const { return (S + 1.0) / (S + F + 2.0); }
+
+    int choose(int available) const {
+        const int lim = std::max(0, std::min(n_max, available));
+        const double a = alpha();
+        double e = 1.0, pw = 1.0;
+        int best = 0;
+        double best_v = e / cost[0];
+        for (int n = 1; n <= lim; ++n) {
+            pw *= a;
+            e += pw;
+            const double v = e / cost[n];
+            if (v > best_v) {
+                best_v = v;
+                best = n;
+            }
+        }
+        return best;
+    }
+
+    void update(int drafted, int accepted) {
+        S *= decay;
+        F *= decay;
+        if (drafted > 0) {
+            S += accepted;
+            if (accepted < drafted) F += 1.0;
+        }
+    }
+};
+
+extern "C" int spec_ngram_gate_create(int n_max, const double* cost, double decay, spec_ngram_gate** out) {
+    sv::clear_error();
+    if (out == nullptr || cost == nullptr) return set_error(SPEC_E_INVAL, "NULL argument");
+    *out = nullptr;
+    if (n_max < 0 || n_max > 1024) return set_error(SPEC_E_INVAL, "n_max = %d outside [0, 1024]", n_max);
+    if (!(decay >= 0.0 && decay <= 1.0)) return set_error(SPEC_E_INVAL, "decay must be in [0, 1]");
+    for (int n = 0; n <= n_max; ++n)
+        if (!(cost[n] > 0.0) || std::isinf(cost[n])) return set_error(SPEC_E_INVAL, "cost[%d] must be finite and > 0", n);
+    spec_ngram_gate* g = new (std::nothrow) spec_ngram_gate();
+    if (g == nullptr) return set_error(SPEC_E_NOMEM, "spec_ngram_gate allocation failed");
+    g->n_max = n_max;
+    g->cost.assign(cost, cost + n_max + 1);
+    g->decay = decay;
+    *out = g;
+    return SPEC_OK;
+}
+
+extern "C" int spec_ngram_gate_choose(const spec_ngram_gate* g, int available) {
+    sv::clear_error();
+    if (g == nullptr) return set_error(SPEC_E_INVAL, "gate is NULL");
+    return g->choose(available);
+}
+
+extern "C" int spec_ngram_gate_update(spec_ngram_gate* g, int drafted, int accepted) {
+    sv::clear_error();
+    if (g == nullptr) return set_error(SPEC_E_INVAL, "gate is NULL");
+    if (drafted < 0 || accepted < 0 || accepted > drafted)
+        return set_error(SPEC_E_INVAL, "need 0 <= accepted (%d) <= drafted (%d)", accepted, drafted);
+    g->update(drafted, accepted);
+    return SPEC_OK;
+}
+
+extern "C" double spec_ngram_gate_acceptance(const spec_ngram_gate* g) { return g ? g->alpha() : -1.0; }
+
+extern "C" void spec_ngram_gate_destroy(spec_ngram_gate* g) { delete g; }

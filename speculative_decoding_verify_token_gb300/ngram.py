@@ -57,3 +57,39 @@ def draft_batch(drafters, K):
     _lib.check(lib.spec_ngram_draft_batch(arr, B, int(K), toks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                           lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
     return toks, lens
+
+
+class DraftGate:
+    """Draft-length gate of one sequence (spec_ngram_gate_*): `cost[n]` is the timed cost of
+    a verify pass with n drafted tokens (n = 0 .. n_max)."""
+
+    def __init__(self, cost, decay=0.9):
+        self.lib = _lib.load()
+        c = np.ascontiguousarray(np.asarray(cost, dtype=np.float64))
+        h = ctypes.c_void_p()
+        _lib.check(self.lib.spec_ngram_gate_create(int(c.size - 1), c.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                                   float(decay), ctypes.byref(h)))
+        self.h = h
+
+    def choose(self, available):
+        n = self.lib.spec_ngram_gate_choose(self.h, int(available))
+        if n < 0:
+            _lib.check(n)
+        return n
+
+    def update(self, drafted, accepted):
+        _lib.check(self.lib.spec_ngram_gate_update(self.h, int(drafted), int(accepted)))
+
+    def acceptance(self):
+        return float(self.lib.spec_ngram_gate_acceptance(self.h))
+
+    def close(self):
+        if self.h:
+            self.lib.spec_ngram_gate_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -70,3 +70,43 @@ def test_bad_arguments(ng):
         ng.NgramDrafter(4, 3)
     with pytest.raises(_lib.SpecError):
         ng.NgramDrafter(3, 9)
+
+
+@pytest.mark.parametrize("seed,decay", [(0, 0.9), (1, 0.5), (2, 1.0), (3, 0.0)])
+def test_gate_matches_oracle(ng, seed, decay):
+    """The native draft-length gate (spec_ngram_gate_*) against the oracle's DraftGate over
+    random rounds: same acceptance estimate, same draft length (where the oracle's two best
+    scores are within rounding of each other, either of them)."""
+    rng = np.random.default_rng(seed)
+    n_max = 8
+    cost = np.cumsum(np.concatenate([[1.0], rng.uniform(0.02, 0.4, n_max)]))
+    nat = ng.DraftGate(cost, decay=decay)
+    ref = og.DraftGate(cost, decay=decay)
+    for r in range(300):
+        avail = int(rng.integers(0, n_max + 3))
+        n = nat.choose(avail)
+        e = ref.choose(avail)
+        if n != e:
+            sc = ref.scores(avail)
+            assert abs(sc[n] - sc[e]) <= 1e-12 * sc[e], (r, n, e)
+        assert nat.acceptance() == pytest.approx(ref.acceptance(), rel=1e-12)
+        # copied spans are accepted whole, new prose mostly rejected
+        acc = n if rng.random() < 0.5 else int(rng.integers(0, n + 1))
+        nat.update(n, acc)
+        ref.update(n, acc)
+    nat.close()
+
+
+def test_gate_argument_errors(ng):
+    from speculative_decoding_verify_token_gb300._lib import SpecError
+    with pytest.raises(SpecError):
+        ng.DraftGate([1.0, 0.0, 2.0])
+    with pytest.raises(SpecError):
+        ng.DraftGate([1.0, 2.0], decay=1.5)
+    g = ng.DraftGate([1.0, 1.25])
+    with pytest.raises(SpecError):
+        g.update(2, 3)
+    with pytest.raises(SpecError):
+        g.update(-1, 0)
+    assert g.choose(-4) == 0
+    g.close()

@@ -4,6 +4,8 @@
 all": greedy speculative output is byte-identical to greedy non-speculative output; the
 OptiQ docs ("N-gram lookup") say the same in float32.
 """
+import itertools
+
 import numpy as np
 import pytest
 
@@ -75,3 +77,72 @@ def test_ngram_draft_definition():
     # the longest match wins over a more recent shorter one
     ctx2 = [7, 1, 2, 3, 50, 8, 2, 3, 60, 9, 7, 1, 2, 3]
     assert og.ngram_draft(ctx2, n_draft=3) == [50, 8, 2]
+
+
+# ---- draft-length gate ------------------------------------------------------------------
+
+@pytest.mark.parametrize("alpha", [0.0, 0.1, 0.5, 0.9, 1.0])
+@pytest.mark.parametrize("n", [0, 1, 4, 8])
+def test_gate_expected_tokens(alpha, n):
+    """Mean emitted tokens against the geometric series in closed form and against a
+    brute-force enumeration of every accept/reject pattern of the n drafts (a pass emits
+    the accepted prefix plus one target token)."""
+    e = og.DraftGate.expected_tokens(alpha, n)
+    closed = n + 1.0 if alpha == 1.0 else (1.0 - alpha ** (n + 1)) / (1.0 - alpha)
+    assert e == pytest.approx(closed, rel=1e-12, abs=1e-12)
+    brute = 0.0
+    for pattern in itertools.product((0, 1), repeat=n):
+        p = 1.0
+        for ok in pattern:
+            p *= alpha if ok else 1.0 - alpha
+        j = next((i for i, ok in enumerate(pattern) if not ok), n)
+        brute += p * (j + 1)
+    assert e == pytest.approx(brute, rel=1e-12, abs=1e-12)
+
+
+def test_gate_hand_worked_decisions():
+    # no history: alpha = 1/2.  cost grows by 1/4 of a pass per drafted token:
+    # E/cost = 1/1, 1.5/1.25 = 1.2, 1.75/1.5 = 1.1667, 1.875/1.75 = 1.0714 -> 1 draft
+    g = og.DraftGate([1.0, 1.25, 1.5, 1.75, 2.0])
+    assert g.acceptance() == 0.5
+    assert g.choose(4) == 1
+    assert g.choose(0) == 0                 # nothing offered, nothing drafted
+    # an exact tie (1.5 / 1.5 = 1 / 1) goes to the shorter draft
+    assert og.DraftGate([1.0, 1.5, 2.0]).choose(2) == 0
+    # free drafts: any alpha > 0 takes the longest draft offered
+    h = og.DraftGate([1.0] * 9)
+    assert h.choose(8) == 8 and h.choose(3) == 3
+    # one accepted token of one (S = 1, F = 0): alpha = 2/3; with cost 1 + n/4:
+    # E = 1, 1.6667, 2.1111, 2.4074, 2.6049; E/cost = 1, 1.3333, 1.4074, 1.3757, 1.3025
+    # -> 2 drafts
+    g.update(1, 1)
+    assert g.acceptance() == pytest.approx(2.0 / 3.0)
+    assert g.choose(4) == 2
+
+
+def test_gate_new_prose_then_retry():
+    """Rejection after rejection (decay 0.9): F tends to 1 / (1 - 0.9) = 10 and alpha to
+    1/12, below the 1/4 that a first draft at cost 1.25 needs ((1 + alpha) / 1.25 > 1), so
+    the gate stops drafting.  Rounds without drafts then only decay F: drafting resumes once
+    10 * 0.9^r < 2, at r = 16."""
+    g = og.DraftGate([1.0, 1.25, 1.5, 1.75, 2.0], decay=0.9)
+    for _ in range(200):
+        g.update(1, 0)
+    assert g.acceptance() == pytest.approx(1.0 / 12.0, rel=1e-6)
+    assert g.choose(4) == 0
+    for r in range(1, 40):
+        g.update(0, 0)
+        if g.choose(4) > 0:
+            break
+    assert r == 16
+
+
+def test_gate_copying_drafts_long():
+    """All 8 drafts accepted every round: S tends to 8 / (1 - 0.9) = 80, alpha to 81/82, and
+    with cost 1 + n/4 the full draft wins (E(8) / 3 = 2.86 against E(1) / 1.25 = 1.59)."""
+    g = og.DraftGate([1.0 + n / 4 for n in range(9)])
+    for _ in range(200):
+        g.update(8, 8)
+    assert g.acceptance() == pytest.approx(81.0 / 82.0, rel=1e-6)
+    assert g.choose(8) == 8
+    assert g.choose(5) == 5
