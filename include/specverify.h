@@ -86,6 +86,8 @@ const char* spec_version(void);
  * (may be NULL): SPEC_OK, SPEC_E_DRAFT (then accepted_len[b] = number accepted before the
  * illegal draft and next_token[b] = -1) or SPEC_E_TIMEOUT (outputs of b undefined).
  *
+ * Logits are finite or -inf; a NaN entry makes that sequence's outputs unspecified (its
+ * ids still lie in [0, V) or are -1).
  * workspace: device scratch of at least spec_verify_logits_workspace_bytes(B, K, V)
  * bytes, 256-byte aligned, owned by the caller; its contents need no initialisation (the
  * call clears what must start at zero with cudaMemsetAsync on `stream`).  Two calls that

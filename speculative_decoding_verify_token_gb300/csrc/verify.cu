@@ -62,10 +62,13 @@ constexpr int RF_BPL = 5;                            // blocks' second values a 
 constexpr int RF_KPL = 2 * RF_BPL;                   // float4 of (maximum, id) pairs a lane holds per round
 constexpr int RF_BATCH = 4;                          // fine blocks read again at once per warp
 constexpr int RF_SEL_CAP = 64;                       // fine blocks listed before they are read again
-// per-warp candidate buffer, merged into the warp's list of 32 before an append could
-// overflow it (appends come 64 or 128 at a time)
+// per-warp pool of (value, id) entries: the buffered candidates and, during a merge, the
+// warp's list of LISTN behind them; merged before an append could overflow it (appends come
+// 64 or 128 at a time)
 constexpr int RF_CAND_CAP = 192;
-constexpr int RF_WARP_WORDS = 2 * RF_CAND_CAP + RF_SEL_CAP;   // 4-byte words of shared memory per warp
+// 4-byte words of shared memory per warp: the pool, the merge's output list, the fine
+// blocks to read again
+constexpr int RF_WARP_WORDS = 2 * RF_CAND_CAP + 2 * LISTN + RF_SEL_CAP;
 
 enum { MODE_VERIFY = 0, MODE_SAMPLE = 1 };
 
@@ -143,13 +146,6 @@ __device__ __forceinline__ float pick4(const float4& x, int c) {
     return r;
 }
 
-// One round: every lane offers at most one candidate; sort them and merge into the list.
-__device__ __forceinline__ void offer_round(float& lv, int& lid, bool has, float cv, int cid, int lane) {
-    if (!has) { cv = -INFINITY; cid = SENT_ID; }
-    warp_sort_desc(cv, cid, lane);
-    warp_merge_desc(lv, lid, cv, cid, lane);
-}
-
 // Order-preserving map of floats to unsigned ints (for atomicMax); 0 means "no bound".
 __device__ __forceinline__ unsigned float_key(float f) {
     const unsigned b = __float_as_uint(f);
@@ -160,27 +156,47 @@ __device__ __forceinline__ float key_float(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Sort + merge the warp's buffered candidates into its running list, 32 at a time.  Not
-// inlined: it is reached from many unrolled sites, and one copy keeps the code in the
-// instruction cache.
+// The warp's running list (lane j = j-th best under better(), padded with (-inf, SENT_ID))
+// and the n candidates buffered in pool[0, n) become the best LISTN entries of their union.
+// Each entry's place is the number of entries of the union that beat it: better() orders
+// entries with distinct ids strictly, and every real entry has its own id (one element of
+// the row), so the places are those of a sort of the union.  Padding is never placed; the
+// output starts as padding, so no id can come from anywhere but the pool.  The counts read
+// the pool as broadcast shared-memory loads with no dependence between them, where a
+// bitonic sort is a chain of dependent shuffles.  Not inlined: it is reached from many
+// unrolled sites, and one copy keeps the code in the instruction cache.
 struct ListEntry { float v; int id; };
-__device__ __noinline__ ListEntry merge_candidates(float lv, int lid, const float* cv, const int* ci, int n,
-                                                   int lane) {
+__device__ __noinline__ ListEntry merge_candidates(float lv, int lid, float2* pool, float2* outl, int n, int lane) {
+    const unsigned real = __ballot_sync(FULL, lid != SENT_ID);
+    if (lid != SENT_ID) pool[n + __popc(real & ((1u << lane) - 1u))] = make_float2(lv, __int_as_float(lid));
+    outl[lane] = make_float2(-INFINITY, __int_as_float(SENT_ID));
     __syncwarp();
-    for (int base = 0; base < n; base += 32) {
-        const bool has = base + lane < n;
-        float v = has ? cv[base + lane] : -INFINITY;
-        int id = has ? ci[base + lane] : SENT_ID;
-        warp_sort_desc(v, id, lane);
-        warp_merge_desc(lv, lid, v, id, lane);
+    const int P = n + __popc(real);
+    const float2 PAD = make_float2(-INFINITY, __int_as_float(SENT_ID));
+    for (int e0 = 0; e0 < P; e0 += 64) {
+        const int ea = e0 + lane, eb = ea + 32;
+        const float2 A = ea < P ? pool[ea] : PAD;
+        const float2 Bq = eb < P ? pool[eb] : PAD;
+        const int ia = __float_as_int(A.y), ib = __float_as_int(Bq.y);
+        int ra = 0, rb = 0;
+#pragma unroll 4
+        for (int j = 0; j < P; ++j) {
+            const float2 c = pool[j];
+            const int ic = __float_as_int(c.y);
+            ra += better(c.x, ic, A.x, ia) ? 1 : 0;
+            rb += better(c.x, ic, Bq.x, ib) ? 1 : 0;
+        }
+        if (ia != SENT_ID && ra < LISTN) outl[ra] = A;
+        if (ib != SENT_ID && rb < LISTN) outl[rb] = Bq;
     }
     __syncwarp();
-    return ListEntry{lv, lid};
+    const float2 r = outl[lane];
+    __syncwarp();
+    return ListEntry{r.x, __float_as_int(r.y)};
 }
 
-__device__ __forceinline__ void flush_candidates(float& lv, int& lid, const float* cv, const int* ci, int n,
-                                                 int lane) {
-    const ListEntry e = merge_candidates(lv, lid, cv, ci, n, lane);
+__device__ __forceinline__ void flush_candidates(float& lv, int& lid, float2* pool, float2* outl, int n, int lane) {
+    const ListEntry e = merge_candidates(lv, lid, pool, outl, n, lane);
     lv = e.v;
     lid = e.id;
 }
@@ -213,10 +229,25 @@ __device__ void row_dist(const VerifyParams& p, float lv, int lid, int lane, int
     }
 }
 
-// Inverse CDF over ascending token id: (key, w) per lane, key = SENT_ID for empty lanes.
-// Returns the chosen token; sorts (key, w) ascending in place.
-__device__ int inverse_cdf_draw(int& key, float& w, float u, int lane, float& Z) {
-    warp_sort_asc_key(key, w, lane);
+// Inverse CDF over ascending token id: (key, w) per lane, key = SENT_ID (weight 0) for
+// empty lanes.  Returns the chosen token; sorts (key, w) ascending in place -- each entry
+// goes to the number of entries before it (smaller key, or equal key on a lower lane), a
+// permutation -- through the 64 entries of scratch.
+__device__ int inverse_cdf_draw(int& key, float& w, float u, int lane, float& Z, float2* scratch) {
+    scratch[lane] = make_float2(__int_as_float(key), w);
+    __syncwarp();
+    int rk = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int o = __float_as_int(scratch[j].x);
+        rk += (o < key || (o == key && j < lane)) ? 1 : 0;
+    }
+    scratch[32 + rk] = make_float2(__int_as_float(key), w);
+    __syncwarp();
+    const float2 srt = scratch[32 + lane];
+    __syncwarp();
+    key = __float_as_int(srt.x);
+    w = srt.y;
     Z = warp_sum(key != SENT_ID ? w : 0.0f);
     float cum = key != SENT_ID ? w : 0.0f;
 #pragma unroll
@@ -235,7 +266,8 @@ __device__ int inverse_cdf_draw(int& key, float& w, float u, int lane, float& Z)
 
 // Acceptance scan of one sequence on one warp, over its rows' truncated distributions in
 // shared memory: target position i at list i, draft position i at list kb + 1 + i.
-__device__ void finish_sequence(const VerifyParams& p, int b, int lane, const int* rid, const float* rp) {
+__device__ void finish_sequence(const VerifyParams& p, int b, int lane, const int* rid, const float* rp,
+                                float2* scratch) {
     const int kb = draft_count(p, b);
     auto tl = [&](int i) { return i * LISTN + lane; };
     auto dl = [&](int i) { return (kb + 1 + i) * LISTN + lane; };
@@ -253,8 +285,9 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
         bool reject = false;
         a = kb;
         int d = -1;
-        // the positions' P(d) and Q(d), SB positions per round with their loads and warp
-        // reductions issued together; the scan stops at the first reject
+        // the positions' P(d) and Q(d), SB positions per round with their loads issued
+        // together; a list holds each id at most once, so the lane whose id is d (if any)
+        // holds its probability.  The scan stops at the first reject.
         constexpr int SB = 4;
         bool done = false;
         for (int i0 = 0; i0 < kb && !done; i0 += SB) {
@@ -266,20 +299,13 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
                 pd[j] = 0.0f; qd[j] = 1.0f; dt[j] = -1;
                 if (i < kb) {
                     dt[j] = p.draft_tokens[(size_t)b * p.K + i];
-                    const int pid = rid[tl(i)];
-                    const float pp = rp[tl(i)];
-                    pd[j] = pid == dt[j] ? pp : 0.0f;
+                    const unsigned mp = __ballot_sync(FULL, rid[tl(i)] == dt[j]);
+                    pd[j] = mp ? rp[i * LISTN + __ffs(mp) - 1] : 0.0f;
                     if (has_q) {
-                        const int qid = rid[dl(i)];
-                        const float qp = rp[dl(i)];
-                        qd[j] = qid == dt[j] ? qp : 0.0f;
+                        const unsigned mq = __ballot_sync(FULL, rid[dl(i)] == dt[j]);
+                        qd[j] = mq ? rp[(kb + 1 + i) * LISTN + __ffs(mq) - 1] : 0.0f;
                     }
                 }
-            }
-#pragma unroll
-            for (int j = 0; j < SB; ++j) {
-                pd[j] = warp_max(pd[j]);
-                if (has_q) qd[j] = warp_max(qd[j]);
             }
             for (int j = 0; j < SB && i0 + j < kb; ++j) {
                 d = dt[j];
@@ -295,13 +321,11 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
             if (reject) {
                 float qx = 0.0f;
                 if (has_q) {
-                    const int qid = rid[dl(a)];
-                    const float qp = rp[dl(a)];
-#pragma unroll 1
+                    const int q0 = (kb + 1 + a) * LISTN;
+#pragma unroll 8
                     for (int t = 0; t < LISTN; ++t) {
-                        const int tid = __shfl_sync(FULL, qid, t);
-                        const float tp = __shfl_sync(FULL, qp, t);
-                        if (tid >= 0 && tid == pid) qx = tp;
+                        const int tid = rid[q0 + t];
+                        if (tid >= 0 && tid == pid) qx = rp[q0 + t];
                     }
                 } else {
                     qx = (pid == d) ? 1.0f : 0.0f;
@@ -312,7 +336,7 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
             }
             okey = (pid >= 0 && w > 0.0f) ? pid : SENT_ID;
             ow = okey != SENT_ID ? w : 0.0f;
-            next = inverse_cdf_draw(okey, ow, ub[p.K], lane, oZ);
+            next = inverse_cdf_draw(okey, ow, ub[p.K], lane, oZ, scratch);
         }
     }
     if (p.out_ids != nullptr) {
@@ -507,13 +531,9 @@ __global__ void __maxnreg__(BM_MAXNREG) vt_stats_kernel(const VerifyParams p) {
 
 // Append each lane's (v, id) for which c holds to the warp's buffer, in lane order (ballot
 // + prefix count).
-__device__ __forceinline__ void append_if(bool c, float v, int id, float* cv, int* ci, int& cnt, int lane) {
+__device__ __forceinline__ void append_if(bool c, float v, int id, float2* pool, int& cnt, int lane) {
     const unsigned m = __ballot_sync(FULL, c);
-    if (c) {
-        const int pos = cnt + __popc(m & ((1u << lane) - 1u));
-        cv[pos] = v;
-        ci[pos] = id;
-    }
+    if (c) pool[cnt + __popc(m & ((1u << lane) - 1u))] = make_float2(v, __int_as_float(id));
     cnt += __popc(m);
 }
 
@@ -526,10 +546,11 @@ __device__ __forceinline__ void append_index(bool c, int x, int* list, int& n, i
 
 // Read the n listed fine blocks of the row again, RF_BATCH at a time, and merge their
 // elements >= tau2 -- all but the block's recorded maximum (already listed) -- into the
-// warp's list (lv, lid).  cv/ci: the warp's candidate buffer (empty on entry and exit).
+// warp's list (lv, lid).  pool/outl: the warp's candidate pool (empty on entry and exit)
+// and merge output.
 __device__ __forceinline__ void reread_blocks(const VerifyParams& p, const RowInfo& ri, int row, const int* sel,
-                                              int n, float tau2, int head, int body, float& lv, int& lid, float* cv,
-                                              int* ci, int lane) {
+                                              int n, float tau2, int head, int body, float& lv, int& lid,
+                                              float2* pool, float2* outl, int lane) {
     const int n4_row = body >> 2;
     const float4* src = reinterpret_cast<const float4*>(ri.ptr + head);
     const size_t krow = (size_t)row * NF * p.nbb;
@@ -553,8 +574,8 @@ __device__ __forceinline__ void reread_blocks(const VerifyParams& p, const RowIn
             if (fb[j] < 0) continue;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                if (cnt > RF_CAND_CAP - 128) {
-                    flush_candidates(lv, lid, cv, ci, cnt, lane);
+                if (cnt > RF_CAND_CAP - LISTN - 128) {
+                    flush_candidates(lv, lid, pool, outl, cnt, lane);
                     cnt = 0;
                 }
                 const int idx = fine_float4(fb[j], lane, h);
@@ -562,24 +583,24 @@ __device__ __forceinline__ void reread_blocks(const VerifyParams& p, const RowIn
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float v = comp4(x[j][h], c);
-                    append_if(idx < n4_row && e + c != skip[j] && v >= tau2, v, e + c, cv, ci, cnt, lane);
+                    append_if(idx < n4_row && e + c != skip[j] && v >= tau2, v, e + c, pool, cnt, lane);
                 }
             }
             if (fb[j] == 0) {      // the unaligned head and tail belong to fine block 0
-                if (cnt > RF_CAND_CAP - 64) {
-                    flush_candidates(lv, lid, cv, ci, cnt, lane);
+                if (cnt > RF_CAND_CAP - LISTN - 64) {
+                    flush_candidates(lv, lid, pool, outl, cnt, lane);
                     cnt = 0;
                 }
                 const int tail0 = head + body;
                 const bool hok = lane < head, tok = lane < p.V - tail0;
                 const float hv = hok ? ri.ptr[lane] : -INFINITY;
                 const float tv = tok ? ri.ptr[tail0 + lane] : -INFINITY;
-                append_if(hok && lane != skip[j] && hv >= tau2, hv, lane, cv, ci, cnt, lane);
-                append_if(tok && tail0 + lane != skip[j] && tv >= tau2, tv, tail0 + lane, cv, ci, cnt, lane);
+                append_if(hok && lane != skip[j] && hv >= tau2, hv, lane, pool, cnt, lane);
+                append_if(tok && tail0 + lane != skip[j] && tv >= tau2, tv, tail0 + lane, pool, cnt, lane);
             }
         }
     }
-    flush_candidates(lv, lid, cv, ci, cnt, lane);
+    flush_candidates(lv, lid, pool, outl, cnt, lane);
 }
 
 // One row of pass 2 on one warp.  Candidates are the fine blocks' maxima:
@@ -590,8 +611,8 @@ __device__ __forceinline__ void reread_blocks(const VerifyParams& p, const RowIn
 // whose second value is below tau2 holds nothing else of the top k.  The few blocks whose
 // second value reaches tau2 are read again and their other elements >= tau2 merged in.
 // Returns lane j's entry of the row's top list (j-th best).
-__device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, int lane, float* cv, int* ci,
-                                                int* sel) {
+__device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, int lane, float2* pool,
+                                                float2* outl, int* sel) {
     const RowInfo ri = row_info(p, row);
     VT_STAMP(row, 0);
     VT_STAMP(row, 1);
@@ -620,9 +641,20 @@ __device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, 
         const float4 t = __ldcg(kq + q);
         lm = fmaxf(lm, fmaxf(t.x, t.z));
     }
-    int dummy = lane;
-    warp_sort_desc(lm, dummy, lane);
-    const float tau = __shfl_sync(FULL, lm, k - 1);
+    // tau: the k-th best lane maximum, from each lane's rank among the 32 (ties to the lower
+    // lane, so the ranks are 0..31 once each)
+    float* lmx = reinterpret_cast<float*>(outl);
+    lmx[lane] = lm;
+    __syncwarp();
+    int rk = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float o = lmx[j];
+        rk += (o > lm || (o == lm && j < lane)) ? 1 : 0;
+    }
+    const unsigned at = __ballot_sync(FULL, rk == k - 1);
+    const float tau = at ? lmx[__ffs(at) - 1] : -INFINITY;
+    __syncwarp();
     VT_STAMP(row, 2);
 
     // candidates: the maxima >= tau
@@ -639,16 +671,16 @@ __device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, 
         }
 #pragma unroll
         for (int i = 0; i < RF_KPL; ++i) {
-            if (cnt > RF_CAND_CAP - 64) {
-                flush_candidates(lv, lid, cv, ci, cnt, lane);
+            if (cnt > RF_CAND_CAP - LISTN - 64) {
+                flush_candidates(lv, lid, pool, outl, cnt, lane);
                 cnt = 0;
             }
             const int id0 = __float_as_int(kv[i].y), id1 = __float_as_int(kv[i].w);
-            append_if(id0 != SENT_ID && kv[i].x >= tau, kv[i].x, id0, cv, ci, cnt, lane);
-            append_if(id1 != SENT_ID && kv[i].z >= tau, kv[i].z, id1, cv, ci, cnt, lane);
+            append_if(id0 != SENT_ID && kv[i].x >= tau, kv[i].x, id0, pool, cnt, lane);
+            append_if(id1 != SENT_ID && kv[i].z >= tau, kv[i].z, id1, pool, cnt, lane);
         }
     }
-    flush_candidates(lv, lid, cv, ci, cnt, lane);
+    flush_candidates(lv, lid, pool, outl, cnt, lane);
     cnt = 0;
     const float tau2 = __shfl_sync(FULL, lv, k - 1);
     VT_STAMP(row, 3);
@@ -691,7 +723,7 @@ __device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, 
             const bool last = !more && b0 + 32 * RF_BPL >= nbb;
             if (n > RF_SEL_CAP - 32 || (last && n > 0)) {
                 __syncwarp();
-                reread_blocks(p, ri, row, sel, n, tau2, head, body, lv, lid, cv, ci, lane);
+                reread_blocks(p, ri, row, sel, n, tau2, head, body, lv, lid, pool, outl, lane);
                 n = 0;
             }
             if (!more) break;
@@ -706,26 +738,27 @@ __device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, 
 // and warp 0 runs the sequence's acceptance scan there.  Sample: one warp per row, which
 // draws its token itself.  Launched programmatically dependent on pass 1: the CTAs may be
 // resident early, the statistics are read after pass 1 is done.
-// Dynamic shared memory: per warp RF_CAND_CAP candidates (value, id) and RF_SEL_CAP fine
-// block indices, then (verify) the sequence's lists, ids then probabilities.
+// Dynamic shared memory: per warp a pool of RF_CAND_CAP (value, id) entries, a merge output
+// of LISTN and RF_SEL_CAP fine block indices, then (verify) the sequence's lists, ids then
+// probabilities.
 __global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) unsigned char rf_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
-    float* cv = reinterpret_cast<float*>(rf_smem) + warp * RF_WARP_WORDS;
-    int* ci = reinterpret_cast<int*>(cv + RF_CAND_CAP);
-    int* sel = ci + RF_CAND_CAP;
+    float2* pool = reinterpret_cast<float2*>(reinterpret_cast<float*>(rf_smem) + warp * RF_WARP_WORDS);
+    float2* outl = pool + RF_CAND_CAP;
+    int* sel = reinterpret_cast<int*>(outl + LISTN);
     pdl_wait();
     if (p.mode == MODE_SAMPLE) {
         const int row = blockIdx.x * nwarps + warp;
         if (row >= p.n_rows) return;
-        const ListEntry e = refine_row(p, row, lane, cv, ci, sel);
+        const ListEntry e = refine_row(p, row, lane, pool, outl, sel);
         int key;
         float w;
         row_dist(p, e.v, e.id, lane, key, w);
         if (key < 0) { key = SENT_ID; w = 0.0f; }
         float Z;
-        const int tok = inverse_cdf_draw(key, w, p.u[row], lane, Z);
+        const int tok = inverse_cdf_draw(key, w, p.u[row], lane, Z, pool);
         if (lane == 0) p.out_tokens[row] = tok;
         VT_STAMP(row, 5);
         return;
@@ -737,12 +770,12 @@ __global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const Veri
     float* rp = reinterpret_cast<float*>(rid + nr * LISTN);
     for (int r = warp; r < nr; r += nwarps) {
         const int row = r <= kb ? b * (p.K + 1) + r : p.n_target_rows + b * p.K + (r - kb - 1);
-        const ListEntry e = refine_row(p, row, lane, cv, ci, sel);
+        const ListEntry e = refine_row(p, row, lane, pool, outl, sel);
         row_dist(p, e.v, e.id, lane, rid[r * LISTN + lane], rp[r * LISTN + lane]);
         VT_STAMP(row, 5);
     }
     __syncthreads();
-    if (warp == 0) finish_sequence(p, b, lane, rid, rp);
+    if (warp == 0) finish_sequence(p, b, lane, rid, rp, pool);
 }
 
 // ---- host side ---------------------------------------------------------------------------
