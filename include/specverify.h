@@ -84,10 +84,14 @@ const char* spec_version(void);
  * token; out_ids/out_probs [B][SPEC_TOPK_MAX] (may be NULL): the distribution the final
  * token was drawn from, ascending token id, padded with id -1 / prob 0; seq_status[b]
  * (may be NULL): SPEC_OK, SPEC_E_DRAFT (then accepted_len[b] = number accepted before the
- * illegal draft and next_token[b] = -1) or SPEC_E_TIMEOUT (outputs of b undefined).
+ * illegal draft and next_token[b] = -1), SPEC_E_INVAL (the row the final token comes from
+ * has nothing to draw from -- sampling from a row without a finite logit; next_token[b]
+ * = -1, out_ids of b all -1) or SPEC_E_TIMEOUT (outputs of b undefined).
  *
- * Logits are finite or -inf; a NaN entry makes that sequence's outputs unspecified (its
- * ids still lie in [0, V) or are -1).
+ * Logits are finite or -inf.  A row of -inf only: greedy takes its lowest id (the
+ * argmax tie order); sampling has no distribution there (SPEC_E_INVAL above).  A NaN
+ * entry makes that sequence's outputs unspecified, but its ids still lie in [0, V) or
+ * are -1.
  * workspace: device scratch of at least spec_verify_logits_workspace_bytes(B, K, V)
  * bytes, 256-byte aligned, owned by the caller; its contents need no initialisation (the
  * call clears what must start at zero with cudaMemsetAsync on `stream`).  Two calls that
@@ -111,7 +115,8 @@ int spec_verify_logits(int B, int K, int V,
  * truncation, by inverse CDF over ascending token id with uniforms[r]; greedy (argmax)
  * when temperature == 0.  This is how a draft model's token is drawn from its truncated
  * distribution q ([MTP-fixes] "Truncation has to match on both sides").
- * out_tokens [R] (device).  Workspace rules as for spec_verify_logits.
+ * out_tokens [R] (device); -1 for a row without a finite logit when sampling.  Workspace
+ * rules as for spec_verify_logits.
  * ---------------------------------------------------------------------------------- */
 /* ------------------------------------------------------------------------------------
  * spec_verify_logits without a caller workspace, for callers that cannot allocate

@@ -258,25 +258,25 @@ __device__ int inverse_cdf_draw(int& key, float& w, float u, int lane, float& Z,
     const float target = u * Z;
     const unsigned sel = __ballot_sync(FULL, key != SENT_ID && cum > target);
     const unsigned valid = __ballot_sync(FULL, key != SENT_ID);
-    int src;
-    if (sel) src = __ffs(sel) - 1;
-    else src = valid ? 31 - __clz(valid) : 0;
+    if (valid == 0u) return -1;           // nothing to draw from: no finite logit in the row
+    const int src = sel ? __ffs(sel) - 1 : 31 - __clz(valid);
     return __shfl_sync(FULL, key, src);
 }
 
 // Acceptance scan of one sequence on one warp, over its rows' truncated distributions in
 // shared memory: target position i at list i, draft position i at list kb + 1 + i.
+// sdt [K]: the sequence's draft tokens, su [K + 1]: its uniforms (copies in shared memory).
 __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const int* rid, const float* rp,
-                                float2* scratch) {
+                                const int* sdt, const float* su, float2* scratch) {
     const int kb = draft_count(p, b);
     auto tl = [&](int i) { return i * LISTN + lane; };
     auto dl = [&](int i) { return (kb + 1 + i) * LISTN + lane; };
-    const float* ub = p.u + (size_t)b * (p.K + 1);
+    const float* ub = su;
     int a = 0, next = -1, status = SPEC_OK;
     int okey = SENT_ID;
     float ow = 0.0f, oZ = 1.0f;
     if (p.temperature == 0.0f) {
-        while (a < kb && p.draft_tokens[(size_t)b * p.K + a] == rid[a * LISTN]) ++a;
+        while (a < kb && sdt[a] == rid[a * LISTN]) ++a;
         next = rid[a * LISTN];
         okey = lane == 0 ? next : SENT_ID;
         ow = lane == 0 ? 1.0f : 0.0f;
@@ -298,7 +298,7 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
                 const int i = i0 + j;
                 pd[j] = 0.0f; qd[j] = 1.0f; dt[j] = -1;
                 if (i < kb) {
-                    dt[j] = p.draft_tokens[(size_t)b * p.K + i];
+                    dt[j] = sdt[i];
                     const unsigned mp = __ballot_sync(FULL, rid[tl(i)] == dt[j]);
                     pd[j] = mp ? rp[i * LISTN + __ffs(mp) - 1] : 0.0f;
                     if (has_q) {
@@ -331,7 +331,8 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
                     qx = (pid == d) ? 1.0f : 0.0f;
                 }
                 float r = pid >= 0 ? fmaxf(pp - qx, 0.0f) : 0.0f;
-                if (warp_sum(r) == 0.0f) r = w;      // residual empty: fall back to P
+                // residual empty (r >= 0, so a zero sum is no positive lane): fall back to P
+                if (__ballot_sync(FULL, r > 0.0f) == 0u) r = w;
                 w = r;
             }
             okey = (pid >= 0 && w > 0.0f) ? pid : SENT_ID;
@@ -339,6 +340,7 @@ __device__ void finish_sequence(const VerifyParams& p, int b, int lane, const in
             next = inverse_cdf_draw(okey, ow, ub[p.K], lane, oZ, scratch);
         }
     }
+    if (status == SPEC_OK && (next < 0 || next == SENT_ID)) status = SPEC_E_INVAL;
     if (p.out_ids != nullptr) {
         const bool v = okey != SENT_ID && status == SPEC_OK;
         p.out_ids[(size_t)b * SPEC_TOPK_MAX + lane] = v ? okey : -1;
@@ -669,15 +671,46 @@ __device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, 
                 kv[i] = q < nq ? __ldcg(kq + q) : NEG;
             }
         }
+        // bit 2i / 2i+1: the lane's pair i.x / i.z is a candidate; each lane's place in the
+        // pool is the candidates of the lanes below it, from ballots of the count's bits
+        unsigned mb = 0;
 #pragma unroll
         for (int i = 0; i < RF_KPL; ++i) {
-            if (cnt > RF_CAND_CAP - LISTN - 64) {
-                flush_candidates(lv, lid, pool, outl, cnt, lane);
-                cnt = 0;
+            mb |= (__float_as_int(kv[i].y) != SENT_ID && kv[i].x >= tau ? 1u : 0u) << (2 * i);
+            mb |= (__float_as_int(kv[i].w) != SENT_ID && kv[i].z >= tau ? 1u : 0u) << (2 * i + 1);
+        }
+        const int c = __popc(mb);
+        const unsigned lt = (1u << lane) - 1u;
+        int before = 0, total = 0;
+#pragma unroll
+        for (int bit = 0; bit < 5; ++bit) {                  // c <= 2 RF_KPL < 32
+            const unsigned bm = __ballot_sync(FULL, (c >> bit) & 1);
+            before += __popc(bm & lt) << bit;
+            total += __popc(bm) << bit;
+        }
+        if (cnt > 0 && cnt + total > RF_CAND_CAP - LISTN) {
+            flush_candidates(lv, lid, pool, outl, cnt, lane);
+            cnt = 0;
+        }
+        if (total <= RF_CAND_CAP - LISTN) {
+            int pos = cnt + before;
+#pragma unroll
+            for (int i = 0; i < RF_KPL; ++i) {
+                if ((mb >> (2 * i)) & 1u) pool[pos++] = make_float2(kv[i].x, kv[i].y);
+                if ((mb >> (2 * i + 1)) & 1u) pool[pos++] = make_float2(kv[i].z, kv[i].w);
             }
-            const int id0 = __float_as_int(kv[i].y), id1 = __float_as_int(kv[i].w);
-            append_if(id0 != SENT_ID && kv[i].x >= tau, kv[i].x, id0, pool, cnt, lane);
-            append_if(id1 != SENT_ID && kv[i].z >= tau, kv[i].z, id1, pool, cnt, lane);
+            cnt += total;
+        } else {
+            // more than a pool of candidates in one round (rows of many equal maxima): in turns
+#pragma unroll
+            for (int i = 0; i < RF_KPL; ++i) {
+                if (cnt > RF_CAND_CAP - LISTN - 64) {
+                    flush_candidates(lv, lid, pool, outl, cnt, lane);
+                    cnt = 0;
+                }
+                append_if((mb >> (2 * i)) & 1u, kv[i].x, __float_as_int(kv[i].y), pool, cnt, lane);
+                append_if((mb >> (2 * i + 1)) & 1u, kv[i].z, __float_as_int(kv[i].w), pool, cnt, lane);
+            }
         }
     }
     flush_candidates(lv, lid, pool, outl, cnt, lane);
@@ -740,7 +773,7 @@ __device__ __forceinline__ ListEntry refine_row(const VerifyParams& p, int row, 
 // resident early, the statistics are read after pass 1 is done.
 // Dynamic shared memory: per warp a pool of RF_CAND_CAP (value, id) entries, a merge output
 // of LISTN and RF_SEL_CAP fine block indices, then (verify) the sequence's lists, ids then
-// probabilities.
+// probabilities (room for 2K + 1 rows), its K draft tokens and K + 1 uniforms.
 __global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const VerifyParams p) {
     extern __shared__ __align__(16) unsigned char rf_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -748,17 +781,20 @@ __global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const Veri
     float2* pool = reinterpret_cast<float2*>(reinterpret_cast<float*>(rf_smem) + warp * RF_WARP_WORDS);
     float2* outl = pool + RF_CAND_CAP;
     int* sel = reinterpret_cast<int*>(outl + LISTN);
-    pdl_wait();
+    // inputs (draft tokens, uniforms, draft lengths) are complete before pass 1 starts, so
+    // they are read while it runs; pass 1's statistics only after pdl_wait()
     if (p.mode == MODE_SAMPLE) {
         const int row = blockIdx.x * nwarps + warp;
+        const float ur = row < p.n_rows ? p.u[row] : 0.0f;
+        pdl_wait();
         if (row >= p.n_rows) return;
         const ListEntry e = refine_row(p, row, lane, pool, outl, sel);
         int key;
         float w;
         row_dist(p, e.v, e.id, lane, key, w);
-        if (key < 0) { key = SENT_ID; w = 0.0f; }
+        if (key < 0 || !(w > 0.0f)) { key = SENT_ID; w = 0.0f; }     // as the verify scan: weight > 0
         float Z;
-        const int tok = inverse_cdf_draw(key, w, p.u[row], lane, Z, pool);
+        const int tok = inverse_cdf_draw(key, w, ur, lane, Z, pool);
         if (lane == 0) p.out_tokens[row] = tok;
         VT_STAMP(row, 5);
         return;
@@ -766,8 +802,16 @@ __global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const Veri
     const int b = blockIdx.x;
     const int kb = draft_count(p, b);
     const int nr = (kb + 1) + (p.draft != nullptr ? kb : 0);
+    const int nr_max = (p.K + 1) + (p.draft != nullptr ? p.K : 0);
     int* rid = reinterpret_cast<int*>(rf_smem) + nwarps * RF_WARP_WORDS;
     float* rp = reinterpret_cast<float*>(rid + nr * LISTN);
+    int* sdt = rid + 2 * nr_max * LISTN;
+    float* su = reinterpret_cast<float*>(sdt + p.K);
+    for (int t = threadIdx.x; t < 2 * p.K + 1; t += blockDim.x) {
+        if (t < p.K) sdt[t] = t < kb ? p.draft_tokens[(size_t)b * p.K + t] : -1;
+        else su[t - p.K] = p.u[(size_t)b * (p.K + 1) + (t - p.K)];
+    }
+    pdl_wait();
     for (int r = warp; r < nr; r += nwarps) {
         const int row = r <= kb ? b * (p.K + 1) + r : p.n_target_rows + b * p.K + (r - kb - 1);
         const ListEntry e = refine_row(p, row, lane, pool, outl, sel);
@@ -775,7 +819,7 @@ __global__ void __launch_bounds__(RF_MAX_WARPS * 32) vt_refine_kernel(const Veri
         VT_STAMP(row, 5);
     }
     __syncthreads();
-    if (warp == 0) finish_sequence(p, b, lane, rid, rp, pool);
+    if (warp == 0) finish_sequence(p, b, lane, rid, rp, sdt, su, pool);
 }
 
 // ---- host side ---------------------------------------------------------------------------
@@ -787,8 +831,9 @@ struct Plan {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// largest pass-2 shared memory: RF_MAX_WARPS warps and the lists of 2 VT_MAX_K + 1 rows
-constexpr int RF_SMEM_MAX = (RF_MAX_WARPS * RF_WARP_WORDS + 2 * (2 * VT_MAX_K + 1) * LISTN) * 4;
+// largest pass-2 shared memory: RF_MAX_WARPS warps, the lists of 2 VT_MAX_K + 1 rows, the
+// draft tokens and uniforms
+constexpr int RF_SMEM_MAX = (RF_MAX_WARPS * RF_WARP_WORDS + 2 * (2 * VT_MAX_K + 1) * LISTN + 2 * VT_MAX_K + 1) * 4;
 
 static Plan make_plan(int n_rows_max, int V) {
     Plan pl{};
@@ -852,7 +897,7 @@ static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream
         const int nw = std::min(nr_max, RF_MAX_WARPS);
         cfg.gridDim = dim3(prm.B);
         cfg.blockDim = dim3(nw * 32);
-        cfg.dynamicSmemBytes = ((size_t)nw * RF_WARP_WORDS + (size_t)2 * nr_max * LISTN) * 4;
+        cfg.dynamicSmemBytes = ((size_t)nw * RF_WARP_WORDS + (size_t)2 * nr_max * LISTN + 2 * (size_t)prm.K + 1) * 4;
     }
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -232,3 +232,38 @@ def test_chi_square_gpu_emitted_law():
     alpha = sum(min(P1.get(x, 0.0), q) for x, q in Q1.items())
     rate = (out["accepted_len"] > 0).float().mean().item()
     assert abs(rate - alpha) < 5 * np.sqrt(alpha * (1 - alpha) / n) + 1e-4
+
+
+def test_row_without_finite_logit(sv):
+    """A sequence whose target rows are all -inf: sampling has nothing to draw the final
+    token from (status SPEC_E_INVAL, next token -1, no final distribution); greedy takes
+    the lowest id (argmax ties go to the lower id).  The other sequences keep their oracle
+    results, and the sampler does the same per row."""
+    B, K, V = 3, 3, 5000
+    case = synth.verify_logits_case(21, B, K, V)
+    tgt, dft = case["target"].copy(), case["draft"]
+    tgt[1] = -np.inf
+    drafts = oracle_drafts(dft, case["u_draft"], 1.0, 20, 0.95)
+    args = [torch.from_numpy(x).cuda() for x in (tgt, dft, drafts, case["u"])]
+    out = sv.verify_logits(*args, 1.0, 20, 0.95)
+    torch.cuda.synchronize()
+    assert out["status"][1].item() == -1 and out["next_token"][1].item() == -1
+    assert torch.all(out["out_ids"][1] == -1)
+    keep = [0, 2]
+    res = oracle_batch(tgt[keep], dft[keep], drafts[keep], case["u"][keep], 1.0, 20, 0.95)
+    compare(res, {k: v[keep] for k, v in out.items()})
+    g = sv.verify_logits(*args, 0.0, 20, 0.95)
+    torch.cuda.synchronize()
+    a1 = int(np.argmax(drafts[1] != 0)) if np.any(drafts[1] != 0) else K
+    assert g["status"][1].item() == 0 and g["next_token"][1].item() == 0
+    assert g["accepted_len"][1].item() == a1
+    x = synth.verify_logits_case(22, 1, 3, 3000)["target"][0]
+    x[1] = -np.inf
+    u = synth.uniforms(23, (4,))
+    tok = sv.sample_logits(torch.from_numpy(x).cuda(), torch.from_numpy(u).cuda(), 1.0, 20, 0.95).cpu().numpy()
+    assert tok[1] == -1
+    for r in (0, 2, 3):
+        exp, margin = ov.sample_token(x[r], u[r], 1.0, 20, 0.95)
+        assert margin < EDGE or tok[r] == exp
+    tok0 = sv.sample_logits(torch.from_numpy(x).cuda(), torch.from_numpy(u).cuda(), 0.0, 20, 0.95).cpu().numpy()
+    assert tok0[1] == 0
