@@ -161,18 +161,47 @@ __device__ __forceinline__ float key_float(unsigned k) {
 // Each entry's place is the number of entries of the union that beat it: better() orders
 // entries with distinct ids strictly, and every real entry has its own id (one element of
 // the row), so the places are those of a sort of the union.  Padding is never placed; the
-// output starts as padding, so no id can come from anywhere but the pool.  The counts read
-// the pool as broadcast shared-memory loads with no dependence between them, where a
-// bitonic sort is a chain of dependent shuffles.  Not inlined: it is reached from many
-// unrolled sites, and one copy keeps the code in the instruction cache.
+// output starts as padding, so no id can come from the list or the pool alone.  The counts
+// read the pool as broadcast shared-memory loads with no dependence between them, where a
+// bitonic sort is a chain of dependent shuffles.  A list that already holds entries (the
+// merges after blocks are read again: a few candidates) is sorted, so entry j has j
+// entries above it in the list; only the candidates are counted against it, and a
+// candidate counts the list with one ballot.  Not inlined: it is reached from many unrolled
+// sites, and one copy keeps the code in the instruction cache.
 struct ListEntry { float v; int id; };
 __device__ __noinline__ ListEntry merge_candidates(float lv, int lid, float2* pool, float2* outl, int n, int lane) {
+    const float2 PAD = make_float2(-INFINITY, __int_as_float(SENT_ID));
     const unsigned real = __ballot_sync(FULL, lid != SENT_ID);
+    outl[lane] = PAD;
+    if (real != 0u && n <= 32) {
+        __syncwarp();
+        int cl = 0, lrank = 0;
+        for (int i = 0; i < n; ++i) {
+            const float2 c = pool[i];
+            const int ic = __float_as_int(c.y);
+            cl += better(c.x, ic, lv, lid) ? 1 : 0;
+            const unsigned lb = __ballot_sync(FULL, lid != SENT_ID && better(lv, lid, c.x, ic));
+            if (lane == i) lrank = __popc(lb);
+        }
+        const float2 me = lane < n ? pool[lane] : PAD;
+        const int im = __float_as_int(me.y);
+        int crank = lrank;
+        if (lane < n) {
+            for (int i = 0; i < n; ++i) {
+                const float2 c = pool[i];
+                crank += better(c.x, __float_as_int(c.y), me.x, im) ? 1 : 0;
+            }
+        }
+        if (lid != SENT_ID && lane + cl < LISTN) outl[lane + cl] = make_float2(lv, __int_as_float(lid));
+        if (lane < n && im != SENT_ID && crank < LISTN) outl[crank] = me;
+        __syncwarp();
+        const float2 r = outl[lane];
+        __syncwarp();
+        return ListEntry{r.x, __float_as_int(r.y)};
+    }
     if (lid != SENT_ID) pool[n + __popc(real & ((1u << lane) - 1u))] = make_float2(lv, __int_as_float(lid));
-    outl[lane] = make_float2(-INFINITY, __int_as_float(SENT_ID));
     __syncwarp();
     const int P = n + __popc(real);
-    const float2 PAD = make_float2(-INFINITY, __int_as_float(SENT_ID));
     for (int e0 = 0; e0 < P; e0 += 64) {
         const int ea = e0 + lane, eb = ea + 32;
         const float2 A = ea < P ? pool[ea] : PAD;
