@@ -88,58 +88,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ---- warp-wide sorted (value, id) lists -------------------------------------------------
+// ---- warp reductions and the (value, id) order -------------------------------------------
 
+// (a, ia) ranks above (b, ib): larger value, then lower id (ties to the lower token id)
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
     return (a > b) || (a == b && ia < ib);
-}
-
-// Bitonic sort of one entry per lane into descending order (lane 0 best).
-__device__ __forceinline__ void warp_sort_desc(float& v, int& id, int lane) {
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float ov = __shfl_xor_sync(FULL, v, stride);
-            const int oi = __shfl_xor_sync(FULL, id, stride);
-            const bool desc_block = (lane & size) == 0 || size == 32;
-            const bool lower = (lane & stride) == 0;
-            const bool take = (lower == desc_block) ? better(ov, oi, v, id) : better(v, id, ov, oi);
-            if (take) { v = ov; id = oi; }
-        }
-    }
-}
-
-// Merge a descending list (cv, cid) into the running descending list (v, id): the result
-// is the best 32 of the 64 entries, still descending.
-__device__ __forceinline__ void warp_merge_desc(float& v, int& id, float cv, int cid, int lane) {
-    const float rv = __shfl_sync(FULL, cv, 31 - lane);
-    const int ri = __shfl_sync(FULL, cid, 31 - lane);
-    if (better(rv, ri, v, id)) { v = rv; id = ri; }          // bitonic now
-#pragma unroll
-    for (int stride = 16; stride > 0; stride >>= 1) {
-        const float ov = __shfl_xor_sync(FULL, v, stride);
-        const int oi = __shfl_xor_sync(FULL, id, stride);
-        const bool lower = (lane & stride) == 0;
-        const bool take = lower ? better(ov, oi, v, id) : better(v, id, ov, oi);
-        if (take) { v = ov; id = oi; }
-    }
-}
-
-// Ascending sort by integer key, carrying a float payload.
-__device__ __forceinline__ void warp_sort_asc_key(int& key, float& val, int lane) {
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int ok = __shfl_xor_sync(FULL, key, stride);
-            const float ov = __shfl_xor_sync(FULL, val, stride);
-            const bool asc_block = (lane & size) == 0 || size == 32;
-            const bool lower = (lane & stride) == 0;
-            const bool take = (lower == asc_block) ? (ok < key) : (ok > key);
-            if (take) { key = ok; val = ov; }
-        }
-    }
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

@@ -146,16 +146,6 @@ __device__ __forceinline__ float pick4(const float4& x, int c) {
     return r;
 }
 
-// Order-preserving map of floats to unsigned ints (for atomicMax); 0 means "no bound".
-__device__ __forceinline__ unsigned float_key(float f) {
-    const unsigned b = __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_float(unsigned k) {
-    if (k == 0u) return -INFINITY;
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // The warp's running list (lane j = j-th best under better(), padded with (-inf, SENT_ID))
 // and the n candidates buffered in pool[0, n) become the best LISTN entries of their union.
 // Each entry's place is the number of entries of the union that beat it: better() orders
