@@ -266,8 +266,19 @@ class DenseVerifyWorkload:
         n = sum(x["launches"] for x in g)
         by = sum(x["bytes"] for x in g)
         achieved = (by / n) / (ms / n / 1e3) / 1e9
+        traffic = None
+        if kernel == "tc_gemm_kernel":
+            # DRAM bytes (read + write) of the current tc_gemm_kernel from one ncu capture of
+            # a 2-layer slice of this shape (profiles/tc_gemm_kernel-dense-8b-2layer-slice.md,
+            # --cache-control none, so that each GEMM's L2 prefetch of the next one's first
+            # weight atoms counts once): 402.1 MB per layer (QKV, O, gate/up, down) and
+            # 1227.6 MB for lm_head, scaled to the layers run; re-take it when the kernel
+            # changes
+            L = self.shape.n_layers
+            traffic = (L * 402.1e6 + 1227.6e6) / (4 * L + 1)
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": kernel,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": kernel,
+                "traffic_unit": "bytes per launch",
                 "algorithmic_bytes_per_launch": by / n, "launches_measured": n,
                 "avg_launch_us": ms / n * 1e3, "peak_source": peaks["source"]}
 
@@ -839,8 +850,13 @@ class VerifyLogitsWorkload:
     def roofline(self, prof, peaks):
         avg = sum(prof) / len(prof)
         achieved = self.bytes_per_step() / (avg / 1e3) / 1e9
+        # DRAM bytes (read + write) of both verify kernels from one ncu capture of this
+        # workload (profiles/verify_kernel-verify-logits-b64-k4.md; caches flushed per
+        # kernel): pass 1 350.09 + 5.36 MB, pass 2 4.41 MB; re-take it when they change
+        traffic = 350.09e6 + 5.36e6 + 4.41e6 if (self.B, self.K, self.V) == (64, 4, 151936) else None
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "verify_kernel",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "verify_kernel",
+                "traffic_unit": "bytes per launch",
                 "algorithmic_bytes_per_launch": self.bytes_per_step(), "avg_launch_us": avg * 1e3,
                 "peak_source": peaks["source"]}
 
