@@ -17,10 +17,12 @@
 //  * pass 2 (one CTA per sequence, one warp per row, launched programmatically dependent
 //    on pass 1) ranks the fine blocks' maxima: tau, the k-th largest of the 32 lanes'
 //    maxima, bounds the row's k-th largest element from below, the maxima >= tau are
-//    sorted and merged 32 at a time into the row's top list, and only the blocks whose
-//    second largest element reaches that list's k-th value can hold a further top-k
-//    element -- on random rows about one row in four re-reads one fine block (1 KB).  Ties
-//    and adversarial rows stay exact;
+//    merged into the row's top list, and only the blocks whose second largest element
+//    reaches that list's k-th value can hold a further top-k element -- on random rows
+//    about one row in four re-reads one fine block (1 KB).  Ties and adversarial rows stay
+//    exact.  Pass 2 is a latency chain, so its orderings are rank selections (each entry
+//    counts the entries that beat it over shared memory and goes to that place) rather
+//    than bitonic sorts, whose 15 dependent shuffle stages cost about 1.5 us a sort;
 //  * each row's truncated distribution is built from its list in shared memory, and warp 0
 //    runs the sequence's acceptance scan and the final inverse-CDF draw.
 #include <cstdio>
