@@ -22,9 +22,12 @@ inverse frequency theta^(-2j/hd).
 
 Parity status: pinned -- attention against torch's scaled_dot_product_attention
 (float64, CPU), RMSNorm and RoPE against closed forms and invariants (norm
-preservation, relative-position dependence), incremental decoding against a full
-forward, the trim invariant, and the bfloat16 rounding against hand-worked ties and
-torch's conversion -- see tests/test_oracle_model.py.
+preservation, relative-position dependence, the pairing and frequencies of head_dim 4),
+hand-worked closed forms of a two-token attention layer and a one-token layer through
+SwiGLU and the lm_head, incremental decoding against a full forward, the trim invariant,
+and the bfloat16 rounding against hand-worked ties and torch's conversion -- see
+tests/test_oracle_model.py; tests/test_oracle_mutations.py checks that planted mistakes
+fail these pins.
 """
 import numpy as np
 

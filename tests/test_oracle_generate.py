@@ -77,6 +77,13 @@ def test_ngram_draft_definition():
     # the longest match wins over a more recent shorter one
     ctx2 = [7, 1, 2, 3, 50, 8, 2, 3, 60, 9, 7, 1, 2, 3]
     assert og.ngram_draft(ctx2, n_draft=3) == [50, 8, 2]
+    # the 4-token suffix (7, 1, 2, 3) matches at 0 and is continued, although the 3-token
+    # suffix (1, 2, 3) also occurs later, at 6 (it would continue with 60)
+    ctx4 = [7, 1, 2, 3, 50, 9, 1, 2, 3, 60, 7, 1, 2, 3]
+    assert og.ngram_draft(ctx4, n_draft=3) == [50, 9, 1]
+    # of several earlier occurrences the most recent one is continued
+    ctx3 = [1, 2, 3, 10, 1, 2, 3, 20, 1, 2, 3]
+    assert og.ngram_draft(ctx3, n_draft=4) == [20, 1, 2, 3]
 
 
 # ---- draft-length gate ------------------------------------------------------------------

@@ -130,3 +130,79 @@ def test_bf16_shape_caches_rounded_keys():
     c32 = o32.new_cache()
     o32.forward([1, 2, 3], c32)
     assert not np.array_equal(c32.k[0], om.round_bf16(c32.k[0]))
+
+
+# ---- hand-worked closed forms of the layer ----------------------------------------------
+
+def test_rope_pairs_and_frequencies():
+    """head_dim 4, theta 1e4: dimension j pairs with j + 2 (rotate-half), pair 0 turns by
+    the position in radians, pair 1 by position * theta^(-2/4) = position / 100."""
+    p = 3.0
+    e = np.eye(4).reshape(4, 1, 4)                                   # the four basis vectors
+    got = om.rope(e, [p] * 4, 1e4)[:, 0, :]
+    c0, s0, c1, s1 = np.cos(p), np.sin(p), np.cos(p / 100), np.sin(p / 100)
+    ref = np.array([[c0, 0, s0, 0],
+                    [0, c1, 0, s1],
+                    [-s0, 0, c0, 0],
+                    [0, -s1, 0, c1]])
+    np.testing.assert_allclose(got, ref, atol=1e-15)
+
+
+def test_rmsnorm_epsilon_inside_the_root_and_gains():
+    x = np.array([[3.0, 4.0]])                                      # mean square 12.5
+    np.testing.assert_allclose(om.rmsnorm(x, np.array([2.0, -1.0]), 0.5), [[6 / np.sqrt(13), -4 / np.sqrt(13)]],
+                               rtol=1e-15)
+
+
+def _layer_shape(d, hq, hkv, hd, f, v):
+    return synth.ModelShape("closed-form", 1, d, hq, hkv, hd, f, v, rope_theta=1e4, rms_eps=0.0, dtype="f32")
+
+
+def test_two_token_attention_closed_form():
+    """d = 2, one head of dimension 2 (one RoPE pair turning 1 rad per position), identity
+    projections, no FFN.  Token 0 = (1, 0) at position 0, token 1 = (0, 1) at position 1.
+    Normed: h0 = (sqrt2, 0), h1 = (0, sqrt2).  Token 0 sees itself: x0 = (1 + sqrt2, 0).
+    Token 1: q1 = k1 = R(1) h1 = sqrt2 (-sin 1, cos 1), v1 = h1 (values are not rotated);
+    scores (scale 1/sqrt2) are q1.k0 = -sqrt2 sin 1 and q1.k1 = sqrt2, so the weight on
+    key 1 is w = 1 / (1 + exp(-sqrt2 (1 + sin 1))) and x1 = (sqrt2 (1 - w), 1 + sqrt2 w).
+    The logits (final norm, identity head) are x / rms(x)."""
+    s = _layer_shape(2, 1, 1, 2, 2, 2)
+    I2 = np.eye(2)
+    z = np.zeros((2, 2))
+    w = {"embed": I2, "lm_head": I2, "final_norm": np.ones(2), "layers.0.attn_norm": np.ones(2),
+         "layers.0.ffn_norm": np.ones(2), "layers.0.wq": I2, "layers.0.wk": I2, "layers.0.wv": I2,
+         "layers.0.wo": I2, "layers.0.wg": z, "layers.0.wu": z, "layers.0.wd": z}
+    m = om.Decoder(s, w)
+    got = m.forward([0, 1], m.new_cache())
+    r2 = np.sqrt(2.0)
+    wk1 = 1.0 / (1.0 + np.exp(-r2 * (1.0 + np.sin(1.0))))
+    x0 = np.array([1.0 + r2, 0.0])
+    x1 = np.array([r2 * (1.0 - wk1), 1.0 + r2 * wk1])
+    ref = np.stack([x / np.sqrt(np.mean(x * x)) for x in (x0, x1)])
+    np.testing.assert_allclose(got, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_single_token_layer_closed_form():
+    """One token at position 0 (attention over one key returns its value, whatever W_q and
+    W_k are).  d = 4, two q heads sharing one kv head of dimension 2, F = 4, vocabulary 3.
+    e = (1, -1, 1, -1) has mean square 1, so h = e; v = (h_0, h_2) = (1, 1), both q heads
+    read it, and W_o = diag(-2, 2, 0, 0) adds (-2, 2, 0, 0): x1 = (-1, 1, 1, -1) = h2 (its
+    mean square is 1).  Gate W_g = ln3 I, up W_u = I: silu(+ln3) = (3/4) ln3 and
+    silu(-ln3) = -(1/4) ln3, so silu(gate) * up = ln3 (1/4, 3/4, 3/4, 1/4).  W_d is the
+    cyclic shift (row i reads column i + 1): x2 = x1 + ln3 (3/4, 3/4, 1/4, 1/4).  The head
+    sums dimensions 1 and 2 into the middle logit."""
+    s = _layer_shape(4, 2, 1, 2, 4, 3)
+    rng = np.random.default_rng(9)
+    L = np.log(3.0)
+    wd = np.roll(np.eye(4), 1, axis=1)                    # wd[i, (i + 1) % 4] = 1
+    lm = np.array([[1.0, 0, 0, 0], [0, 1, 1, 0], [0, 0, 0, 1]])
+    w = {"embed": np.array([[1.0, -1, 1, -1], [0.0, 0, 0, 0], [0.0, 0, 0, 0]]), "lm_head": lm,
+         "final_norm": np.ones(4), "layers.0.attn_norm": np.ones(4), "layers.0.ffn_norm": np.ones(4),
+         "layers.0.wq": rng.normal(size=(4, 4)), "layers.0.wk": rng.normal(size=(2, 4)),
+         "layers.0.wv": np.array([[1.0, 0, 0, 0], [0, 0, 1, 0]]), "layers.0.wo": np.diag([-2.0, 2, 0, 0]),
+         "layers.0.wg": L * np.eye(4), "layers.0.wu": np.eye(4), "layers.0.wd": wd}
+    m = om.Decoder(s, w)
+    got = m.forward([0], m.new_cache())[0]
+    x2 = np.array([-1.0, 1, 1, -1]) + L * np.array([0.75, 0.75, 0.25, 0.25])
+    y = x2 / np.sqrt(np.mean(x2 * x2))
+    np.testing.assert_allclose(got, [y[0], y[1] + y[2], y[3]], rtol=1e-14, atol=1e-15)

@@ -228,3 +228,27 @@ def test_chi_square_emitted_law_1e6():
         assert counts[~m].sum() == 0
         p = stats.chisquare(counts[m], exp[m]).pvalue
         assert p > 1e-4, p
+
+
+def test_acceptance_is_strict():
+    """Reading R5: accept iff u < P(d)/Q(d).  P(0) = 1/4, Q(0) = 1/2: u = 1/2 sits on the
+    boundary and rejects; the residual max(0, P - Q) is all on token 1."""
+    P = [{0: 0.25, 1: 0.75}, {2: 1.0}]
+    Q = [{0: 0.5, 1: 0.5}]
+    r = ov.accept_and_resample(P, Q, [0], [0.5, 0.0])
+    assert r["a"] == 0 and r["next"] == 1 and r["final"] == {1: 1.0}
+    assert ov.accept_and_resample(P, Q, [0], [0.4999, 0.0])["a"] == 1
+
+
+def test_ratio_uses_the_truncated_draft_distribution():
+    """[MTP-fixes] "Truncation has to match on both sides", top-k 2: the target row
+    (ln 3, 0, -30) gives P = (3/4, 1/4, 0) and the draft row (0, ln 3, ln 3) gives
+    Q = (0, 1/2, 1/2) (its untruncated softmax would be (1, 3, 3) / 7).  Draft token 1 has
+    ratio (1/4) / (1/2) = 1/2 (untruncated: 7/12): u = 0.55 rejects, and the residual
+    max(0, P - Q) is all on token 0; u = 0.45 accepts."""
+    L = math.log(3.0)
+    rows = np.array([[L, 0.0, -30.0], [0.0, 0.0, 5.0]])
+    drows = np.array([[0.0, L, L]])
+    r = ov.verify_sampling(rows, drows, [1], [0.55, 0.5], 1.0, 2, 1.0)
+    assert r["a"] == 0 and r["next"] == 0 and r["final"] == {0: 1.0}
+    assert ov.verify_sampling(rows, drows, [1], [0.45, 0.5], 1.0, 2, 1.0)["a"] == 1
