@@ -1,0 +1,164 @@
+"""8B-class dense bf16 target, greedy, K = 4, with the scripted drafter: the drafts copy
+j ~ Geometric (P(j = n) = 0.3 * 0.7^n, capped at K) tokens of the target's own greedy
+trajectory, then one wrong token.  Greedy speculative output must equal plain greedy
+output ("Speculative Decoding on Apple Silicon: 119% Faster on Qwen3.8", section "Why
+this needed a patch to mlx_lm at all"; "What is Speculative Decoding and How Does a
+Draft Model Work?", section "#3").
+
+* a 2-layer slice at full width and vocabulary: plain greedy decoding teacher-forced
+  against the float64 oracle (logits within 3e-2 max-abs; every token the oracle's
+  argmax unless its top-2 gap is below 1e-2), and scripted verify steps whose logits
+  match the oracle's verify pass within 3e-2;
+* the full shape (36 layers, 1024-token prompt) in the configuration the benchmark times:
+  every scripted verify step accepts exactly j and emits the trajectory's next token
+  (speculative = plain, token for token), its decision is the greedy rule on its own
+  logits, and the first pass's rows equal single-token decode rows bit for bit.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import model as om
+from oracle import verify as ov
+
+pytestmark = pytest.mark.gpu
+LOGIT_TOL = 3e-2
+GAP_EXCUSE = 1e-2
+K = 4
+ALPHA = 0.7
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_verify_token_gb300 import generate, model
+    return model, generate
+
+
+class EmbedRows:
+    """Embedding table for the oracle, converted to float64 one gathered row set at a time."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, idx):
+        return self.t[torch.as_tensor(np.asarray(idx))].double().numpy()
+
+
+def oracle_of(shape, w):
+    host = {k: v.cpu() for k, v in w.items()}
+    host["embed"] = EmbedRows(host["embed"])
+    return om.Decoder(shape, host)
+
+
+def scripted_drafts(seq, pos, g, V):
+    """Drafts for the verify step whose pending token is seq[pos]: j true tokens, then
+    tokens that differ from the true ones.  Returns (j, drafts)."""
+    j = min(int(g.geometric(1.0 - ALPHA)) - 1, K)
+    d = [int(seq[pos + 1 + i]) for i in range(j)]
+    while len(d) < K:
+        true = int(seq[pos + 1 + len(d)])
+        d.append(int((true + 1 + g.integers(0, V - 1)) % V))
+    return j, d
+
+
+def scripted_steps(m, seq, prompt_len, V, on_step=None):
+    """Verify steps over the recorded trajectory seq (prompt + plain greedy tokens), starting
+    from a context that holds the prompt except its last token.  Every step must accept
+    exactly j and emit seq[pos + j + 1]; on_step(step, pos, drafts, result) sees each."""
+    dev = m.device
+    g = np.random.Generator(np.random.PCG64(4))
+    u = torch.full((1, K + 1), 0.5, dtype=torch.float32, device=dev)
+    pos = prompt_len - 1
+    step = 0
+    while pos + K + 1 < len(seq):
+        j, d = scripted_drafts(seq, pos, g, V)
+        last = torch.tensor([int(seq[pos])], dtype=torch.int32, device=dev)
+        r = m.verify([0], last, torch.tensor([d], dtype=torch.int32, device=dev), u, 0.0, want_logits=True)
+        a, nxt = int(r["accepted_len"].item()), int(r["next_token"].item())
+        assert (a, nxt) == (j, int(seq[pos + j + 1])), (step, pos, a, nxt, j)
+        rule = ov.verify_greedy(r["logits"][0].double().cpu().numpy(), d)
+        assert (a, nxt) == (rule["a"], rule["next"]), (step, rule["a"], rule["next"])
+        if on_step is not None:
+            on_step(step, pos, d, r)
+        pos += j + 1
+        step += 1
+    return step
+
+
+def test_8b_slice_matches_oracle(lib):
+    M, G = lib
+    s = dataclasses.replace(synth.QWEN_8B, n_layers=2, name="dense-8b-2l")
+    w = synth.model_weights(s, seed=0, device="cuda")
+    V, n_new = s.vocab, 40
+    prompt = torch.from_numpy(synth.prompt_tokens(1, 40, V)).cuda()
+    m = M.SpecModel(s, w, max_ctx=256, max_k=K)
+    # plain greedy decoding with its logits
+    m.prefill(0, prompt[:-1])
+    tok = prompt[-1:].clone()
+    toks, rows = [], []
+    for _ in range(n_new):
+        tok, lg = m.decode([0], tok, want_logits=True)
+        toks.append(int(tok.item()))
+        rows.append(lg[0].double().cpu().numpy())
+    o = oracle_of(s, w)
+    p = [int(x) for x in prompt.cpu()]
+    ref = o.forward(p + toks[:-1], o.new_cache(), logits_rows=np.arange(len(p) - 1, len(p) - 1 + n_new))
+    assert np.max(np.abs(np.stack(rows) - ref)) < LOGIT_TOL
+    for t in range(n_new):          # teacher-forced: the oracle's choice given the GPU's prefix
+        g_tok, gap = ov.argmax_with_gap(ref[t])
+        if g_tok != toks[t]:
+            assert gap < GAP_EXCUSE, (t, g_tok, toks[t], gap)
+    # scripted verify steps over that trajectory; the first three against the oracle's pass
+    seq = np.array(p + toks)
+    m.reset(0)
+    m.prefill(0, prompt[:-1])
+
+    def against_oracle(step, pos, d, r):
+        if step < 3:
+            c = o.new_cache()
+            o.forward([int(x) for x in seq[:pos]], c, logits_rows=np.zeros(0, dtype=np.int64))
+            ref_v = o.forward([int(seq[pos])] + d, c)
+            assert np.max(np.abs(r["logits"][0].double().cpu().numpy() - ref_v)) < LOGIT_TOL, step
+
+    assert scripted_steps(m, seq, len(p), V, against_oracle) >= 3
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def full_weights(lib):
+    w = synth.model_weights(synth.QWEN_8B, seed=0, device="cuda")
+    yield w
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_8b_full_scripted_steps_equal_plain_greedy(lib, full_weights):
+    M, G = lib
+    s = synth.QWEN_8B
+    V, n_new = s.vocab, 64
+    prompt = torch.from_numpy(synth.prompt_tokens(1, 1024, V)).cuda()
+    m = M.SpecModel(s, full_weights, max_ctx=1024 + 128, max_k=K, prefill_chunk=256)
+    traj = G.plain_generate(m, prompt, n_new).cpu().numpy()
+    seq = np.concatenate([prompt.cpu().numpy(), traj])
+    m.reset(0)
+    m.prefill(0, prompt[:-1])
+    first = {}
+
+    def keep_first(step, pos, d, r):
+        if step == 0:
+            first.update(pending=int(seq[pos]), drafts=d, logits=r["logits"].clone())
+
+    assert scripted_steps(m, seq, prompt.numel(), V, keep_first) >= 10
+    # the first verify pass's rows against single-token decode steps of the same tokens
+    m.reset(0)
+    m.prefill(0, prompt[:-1])
+    toks = torch.tensor([first["pending"]] + first["drafts"], dtype=torch.int32, device=m.device)
+    for i in range(K + 1):
+        _, lg = m.decode([0], toks[i:i + 1].contiguous(), want_logits=True)
+        assert torch.equal(lg[0], first["logits"][0, i]), i
+    m.close()
