@@ -98,7 +98,9 @@ const char* spec_version(void);
  * share a workspace must not overlap on the GPU.
  * Errors: SPEC_E_INVAL for NULL required pointers, B < 1, K < 0, V < 2, K > 64,
  * temperature < 0 or NaN, top_k outside [1, SPEC_TOPK_MAX] with temperature > 0;
+ * SPEC_E_RANGE when the B (2K + 1) rows reach 2^30 or their logits 2^40 elements;
  * SPEC_E_NOMEM if workspace_bytes is too small; SPEC_E_CUDA on a launch failure.
+ * spec_verify_logits_workspace_bytes returns 0 for sizes the call would reject.
  * ---------------------------------------------------------------------------------- */
 size_t spec_verify_logits_workspace_bytes(int B, int K, int V);
 

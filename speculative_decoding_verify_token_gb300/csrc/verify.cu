@@ -946,6 +946,13 @@ static int check_sampling(const spec_sampling* s, int V, int& k_eff) {
 }
 
 
+// The B (2K + 1) rows of a call (target and draft) are counted in int and their logits
+// addressed with 40-bit offsets: both limits hold for any size the library is meant for.
+static bool rows_fit(int B, int K, int V) {
+    const long long rows = (long long)B * (2 * K + 1);
+    return rows < (1LL << 30) && rows * (long long)V < (1LL << 40);
+}
+
 // Validation + launch of the fused verify (used by spec_verify_logits and spec_verify).
 int verify_into(int B, int K, int V, const float* target_logits, const float* draft_logits,
                 const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
@@ -953,8 +960,7 @@ int verify_into(int B, int K, int V, const float* target_logits, const float* dr
                 float* out_probs, int32_t* seq_status, void* workspace, size_t workspace_bytes, cudaStream_t st) {
     if (B < 1 || K < 0 || V < 2) return set_error(SPEC_E_INVAL, "bad sizes B=%d K=%d V=%d", B, K, V);
     if (K > VT_MAX_K) return set_error(SPEC_E_INVAL, "K=%d above the maximum %d", K, VT_MAX_K);
-    if ((long long)B * (2 * K + 1) * (long long)V >= (1LL << 40))
-        return set_error(SPEC_E_RANGE, "logits too large");
+    if (!rows_fit(B, K, V)) return set_error(SPEC_E_RANGE, "logits too large");
     int k_eff = 1;
     int rc = check_sampling(sampling, V, k_eff);
     if (rc != SPEC_OK) return rc;
@@ -998,7 +1004,7 @@ int verify_into(int B, int K, int V, const float* target_logits, const float* dr
 using namespace sv;
 
 extern "C" size_t spec_verify_logits_workspace_bytes(int B, int K, int V) {
-    if (B < 1 || K < 0 || V < 2 || K > VT_MAX_K) return 0;
+    if (B < 1 || K < 0 || V < 2 || K > VT_MAX_K || !rows_fit(B, K, V)) return 0;
     return make_plan(B * (2 * K + 1), V).total;
 }
 
@@ -1085,7 +1091,11 @@ extern "C" int spec_verify_logits_noalloc(int B, int K, int V, const float* targ
                                           int32_t* out_ids, float* out_probs, int32_t* seq_status, void* stream) {
     clear_error();
     const size_t need = spec_verify_logits_workspace_bytes(B, K, V);
-    if (need == 0) return set_error(SPEC_E_INVAL, "bad sizes B=%d K=%d V=%d", B, K, V);
+    if (need == 0) {
+        if (B < 1 || K < 0 || V < 2 || K > sv::VT_MAX_K) return set_error(SPEC_E_INVAL, "bad sizes B=%d K=%d V=%d", B, K, V);
+        return set_error(SPEC_E_RANGE, "B=%d K=%d V=%d is above the built-in scratch of %zu bytes", B, K, V,
+                         sv::NOALLOC_SCRATCH_BYTES);
+    }
     if (need > sv::NOALLOC_SCRATCH_BYTES)
         return set_error(SPEC_E_RANGE, "B=%d K=%d V=%d needs %zu bytes of scratch, above the built-in %zu", B, K, V,
                          need, sv::NOALLOC_SCRATCH_BYTES);

@@ -79,3 +79,54 @@ def test_workspace_sizes_monotone(lib):
     b = lib.spec_verify_logits_workspace_bytes(64, 8, 151936)
     assert 0 < a < b < 64 << 20
     assert lib.spec_sample_logits_workspace_bytes(8, 1000) > 0
+
+
+def test_row_count_limits(lib):
+    """Sizes whose row count or logits overflow the library's 32-bit row and 40-bit element
+    counts are rejected (SPEC_E_RANGE) before anything is launched; the workspace query
+    returns 0 for them."""
+    from speculative_decoding_verify_token_gb300 import _lib
+    s = _lib.SpecSampling(0.0, 1, 1.0)
+    fake = ctypes.c_void_p(256)
+    for B, K, V in ((1 << 29, 1, 2), (2**31 - 1, 64, 2), (1 << 20, 4, 1 << 20)):
+        assert lib.spec_verify_logits_workspace_bytes(B, K, V) == 0
+        rc = lib.spec_verify_logits(B, K, V, fake, None, fake, None, fake, ctypes.byref(s), fake, fake,
+                                    None, None, None, fake, 1 << 62, None)
+        assert rc == _lib.SPEC_E_RANGE and b"too large" in lib.spec_last_error()
+        rc = lib.spec_verify_logits_noalloc(B, K, V, fake, None, fake, None, fake, ctypes.byref(s), fake, fake,
+                                            None, None, None, None)
+        assert rc == _lib.SPEC_E_RANGE
+    assert lib.spec_verify_logits_workspace_bytes((1 << 30) // 3 - 1, 1, 2) > 0
+
+
+def test_context_argument_validation(lib):
+    """spec_create rejects shapes and limits the kernels do not support before it allocates
+    anything; calls on a NULL context fail with SPEC_E_INVAL."""
+    from speculative_decoding_verify_token_gb300 import _lib
+    good = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=768, vocab=1024,
+                rope_theta=1e6, rms_eps=1e-6, dtype=_lib.SPEC_F32)
+    lim = _lib.SpecCtxLimits(1, 128, 4, 0, 0)
+    h = ctypes.c_void_p()
+    for change in (dict(d_model=260), dict(n_kv_heads=3), dict(head_dim=48), dict(head_dim=512),
+                   dict(vocab=1023), dict(vocab=1), dict(d_model=16384), dict(rope_theta=0.0),
+                   dict(rms_eps=-1.0), dict(dtype=7), dict(n_layers=0), dict(ffn_dim=100)):
+        cfg = _lib.SpecModelCfg(**dict(good, **change))
+        assert lib.spec_create(ctypes.byref(cfg), ctypes.byref(lim), None, ctypes.byref(h)) == _lib.SPEC_E_INVAL, change
+        assert b"bad model shape" in lib.spec_last_error()
+    cfg = _lib.SpecModelCfg(**good)
+    for bad in (_lib.SpecCtxLimits(0, 128, 4, 0, 0), _lib.SpecCtxLimits(1, 1, 4, 0, 0),
+                _lib.SpecCtxLimits(1, 128, 65, 0, 0), _lib.SpecCtxLimits(1, 128, -1, 0, 0)):
+        assert lib.spec_create(ctypes.byref(cfg), ctypes.byref(bad), None, ctypes.byref(h)) == _lib.SPEC_E_INVAL
+        assert b"bad limits" in lib.spec_last_error()
+    assert lib.spec_create(None, ctypes.byref(lim), None, ctypes.byref(h)) == _lib.SPEC_E_INVAL
+    ids = (ctypes.c_int32 * 1)(0)
+    s = _lib.SpecSampling(0.0, 1, 1.0)
+    fake = ctypes.c_void_p(256)
+    assert lib.spec_prefill(None, 0, fake, 4, None) == _lib.SPEC_E_INVAL
+    assert lib.spec_verify(None, 1, ids, 4, fake, fake, None, None, fake, ctypes.byref(s), fake, fake,
+                           None, None, None, None, 1) == _lib.SPEC_E_INVAL
+    assert lib.spec_kv_trim(None, 1, ids, 4, fake) == _lib.SPEC_E_INVAL
+    assert lib.spec_set_option(None, _lib.SPEC_OPT_GRAPHS, 1) == _lib.SPEC_E_INVAL
+    assert lib.spec_load_weights(None, None, None, 0) == _lib.SPEC_E_INVAL
+    assert lib.spec_kernel_launches(None) == 0
+    lib.spec_destroy(None)
