@@ -14,6 +14,13 @@ Prints one JSON line (rank 0).  Workloads:
       residual), final norm, lm_head, fused verify, KV trim.
   verify-logits-b64-k4: the fused verify kernel alone on fp32 logits, B = 64, K = 4,
       vocab 151936, temperature 1.0, top-k 20, top-p 0.95.
+  sampling-27b-0p8b: a 27B-class bf16 target with a 0.8B-class bf16 draft, B = 1, a
+      2048-token prompt, temperature 1.0, top-k 20, top-p 0.95; a step is one round of K = 4
+      sampled drafts and the target's verify against the draft logits; a K sweep over
+      {1, 2, 4, 8, 16} goes beside it.
+  serving-8b-b32-k8: batched verify on the 8B-class shape, B = 32 sequences with KV
+      lengths uniform in [2048, 16384], n-gram drafts (K = 8 with per-sequence draft
+      lengths) from the host drafter, a KV trim after every step.
 
 The metric is emitted tokens per second of verify steps (accepted drafts plus the
 correction or bonus token); ms_per_step is the verify-step latency; `roofline` is the
