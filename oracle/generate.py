@@ -27,6 +27,9 @@ from .verify import verify, sample_token
 
 
 def plain_generate(model, prompt, n_new, temperature=0.0, top_k=0, top_p=1.0, uniforms=None):
+    """Token-by-token decoding of the target alone, the output speculative decoding must
+    reproduce under greedy decoding ([SD-Apple] "Why this needed a patch to mlx_lm at all").
+    Sampling draws token t from the truncated row with uniforms[t]."""
     cache = model.new_cache()
     logits = model.forward(prompt, cache, logits_rows=[len(prompt) - 1])[0]
     out = []

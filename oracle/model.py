@@ -40,12 +40,15 @@ def to_f64(t):
 
 
 def rmsnorm(x, g, eps):
+    """g * x / sqrt(mean(x^2) + eps) over the last axis.  The pages name Llama/Qwen-style
+    models without printing their layers; this is the plain reading of their norm."""
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * g
 
 
 def rope(x, positions, theta):
-    """Rotate-half RoPE on x [T, H, hd] at absolute positions [T]."""
+    """Rotate-half RoPE on x [T, H, hd] at absolute positions [T] (the plain Llama/Qwen
+    reading: dimension j pairs with j + hd/2 and turns by position * theta^(-2j/hd))."""
     hd = x.shape[-1]
     half = hd // 2
     inv_freq = theta ** (-2.0 * np.arange(half, dtype=np.float64) / hd)
@@ -59,7 +62,10 @@ def rope(x, positions, theta):
 def causal_gqa_attention(q, k, v, q_pos):
     """q [T, Hq, hd] at absolute positions q_pos; k, v [S, Hkv, hd] for positions 0..S-1.
 
-    Query t attends keys 0..q_pos[t].  Returns [T, Hq, hd].
+    Query t attends keys 0..q_pos[t] with weights softmax(q.k / sqrt(hd)); q head h reads kv
+    head h // (Hq / Hkv).  The K+1 rows of a verify pass are such queries at consecutive
+    positions ([Draft] "#2": the target checks the drafts the way it reads a prompt).
+    Returns [T, Hq, hd].
     """
     T, Hq, hd = q.shape
     S, Hkv, _ = k.shape
@@ -79,6 +85,7 @@ def causal_gqa_attention(q, k, v, q_pos):
 
 
 def silu(x):
+    """x * sigmoid(x), the gate of the SwiGLU feed-forward of the Llama/Qwen reading."""
     return x / (1.0 + np.exp(-x))
 
 
