@@ -57,6 +57,12 @@ def test_definition_cases(ng):
     g = ng.NgramDrafter()
     g.append([7, 1, 2, 3, 50, 8, 2, 3, 60, 9, 7, 1, 2, 3])     # longest match beats a later shorter one
     assert list(g.draft(3)) == [50, 8, 2]
+    h = ng.NgramDrafter()
+    h.append([7, 1, 2, 3, 50, 9, 1, 2, 3, 60, 7, 1, 2, 3])     # 4-token match at 0, 3-token also at 6
+    assert list(h.draft(3)) == [50, 9, 1]
+    m = ng.NgramDrafter()
+    m.append([1, 2, 3, 10, 1, 2, 3, 20, 1, 2, 3])              # the most recent occurrence is continued
+    assert list(m.draft(4)) == [20, 1, 2, 3]
     f = ng.NgramDrafter()
     f.append([])
     assert list(f.draft(4)) == [] and len(f) == 0
