@@ -130,3 +130,18 @@ def test_context_argument_validation(lib):
     assert lib.spec_load_weights(None, None, None, 0) == _lib.SPEC_E_INVAL
     assert lib.spec_kernel_launches(None) == 0
     lib.spec_destroy(None)
+
+
+def test_workspace_layout_matches_its_description(lib):
+    """The verify workspace is a 4-byte work counter, then per row and 256-element fine block
+    a (largest, id) pair of 8 bytes and a second-largest float, each region 256-byte aligned:
+    7,152 bytes per row of 151,936 logits (149 blocks of 1,024, four fine blocks each)."""
+    a = lambda x: (x + 255) // 256 * 256
+    for B, K, V in ((64, 4, 151936), (1, 0, 2), (3, 7, 1025), (16, 15, 4096)):
+        rows = B * (2 * K + 1)
+        nfb = 4 * ((V + 1023) // 1024)
+        assert lib.spec_verify_logits_workspace_bytes(B, K, V) == a(4) + a(rows * nfb * 8) + a(rows * nfb * 4)
+    assert 4 * ((151936 + 1023) // 1024) * 12 == 7152
+    for R, V in ((1, 2), (8, 151936)):
+        assert lib.spec_sample_logits_workspace_bytes(R, V) == a(4) + a(R * 4 * ((V + 1023) // 1024) * 8) \
+            + a(R * 4 * ((V + 1023) // 1024) * 4)
