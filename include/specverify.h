@@ -213,7 +213,8 @@ int spec_load_weights(spec_ctx* ctx, const char* const* names, const void* const
  * (chunks of prefill_chunk tokens, the same kernels as the verify pass).  When
  * out_last_logits (device fp32 [V]) is given it receives the logits after the last token.
  * Note the KV convention above: to start a generation, prefill the prompt without its
- * last token and pass that token as the pending one. */
+ * last token and pass that token as the pending one.  Token ids outside [0, V) are
+ * embedded as token 0 (the ids are device data, so they are not checked on the host). */
 int spec_prefill(spec_ctx* ctx, int seq_id, const int32_t* tokens, int n, float* out_last_logits);
 
 /* The verify pass ([SD-Apple] "How speculative decoding works"; [Draft] "#2"):
@@ -223,8 +224,8 @@ int spec_prefill(spec_ctx* ctx, int seq_id, const int32_t* tokens, int n, float*
  * NULL = deterministic drafts), then, when auto_trim != 0, the trim to len + a + 1.
  * With auto_trim == 0 the K+1 entries stay and spec_kv_trim does the trim later.
  * Outputs as spec_verify_logits; out_logits (device fp32 [B][K+1][V], may be NULL)
- * receives the target logits.  Draft ids outside [0, V) are embedded as token 0 and can
- * never be accepted.  SPEC_E_RANGE when a sequence would exceed max_ctx, SPEC_E_NOMEM
+ * receives the target logits.  Ids outside [0, V) are embedded as token 0: a pending token
+ * then reads as token 0, and such a draft can never be accepted.  SPEC_E_RANGE when a sequence would exceed max_ctx, SPEC_E_NOMEM
  * when the page pool is exhausted. */
 int spec_verify(spec_ctx* ctx, int B, const int32_t* seq_ids, int K,
                 const int32_t* last_tokens, const int32_t* draft_tokens, const int32_t* draft_len,
@@ -239,7 +240,8 @@ int spec_decode(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* tok
                 float* out_logits);
 
 /* Trim after a verify pass run with auto_trim == 0: keep accepted_len[b] + 1 of the
- * K + 1 entries it appended (device O(1) length update). */
+ * K + 1 entries it appended (device O(1) length update).  accepted_len (device int32 [B])
+ * is clamped to [0, K], so a trim never reaches below the entries the pass appended. */
 int spec_kv_trim(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len);
 
 /* Exact length of a slot (synchronises the context stream; reclaims pages past it). */
