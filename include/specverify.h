@@ -244,8 +244,17 @@ int spec_decode(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* tok
  * is clamped to [0, K], so a trim never reaches below the entries the pass appended. */
 int spec_kv_trim(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len);
 
-/* Exact length of a slot (synchronises the context stream; reclaims pages past it). */
+/* Exact length of a slot (synchronises the context stream; reclaims pages past it).
+ * Fails with SPEC_E_TIMEOUT as spec_sync does. */
 int spec_seq_len(spec_ctx* ctx, int seq_id, int32_t* out_len);
+
+/* Wait for the context's stream, then report the device-side status: SPEC_E_TIMEOUT when
+ * a bounded wait inside a kernel (a tensor-core GEMM's pipeline barriers, the persistent
+ * pass's hand-offs; each gives up after 2 s) gave up since the context was created.  The
+ * kernel then skipped the rest of its work, so results since then are unreliable; the
+ * status is sticky and the context must be destroyed.  SPEC_E_CUDA on a stream error.
+ * (No counterpart on the pages: the library's own failure reporting.) */
+int spec_sync(spec_ctx* ctx);
 
 /* Empty a slot and return its pages to the pool. */
 int spec_seq_reset(spec_ctx* ctx, int seq_id);

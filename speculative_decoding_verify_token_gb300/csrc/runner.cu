@@ -635,11 +635,34 @@ extern "C" int spec_kv_trim(spec_ctx* c, int B, const int32_t* seq_ids, int K, c
     return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_kv_trim", e);
 }
 
+// After the stream has been synchronised: SPEC_E_TIMEOUT when a bounded wait inside a
+// tensor-core GEMM or the persistent pass gave up since the context was created.  The
+// device word stays set: the passes since then may hold wrong values, and so may the
+// GEMMs' tile counters, so the context is not to be used again.
+static int device_status(Ctx& c) {
+    int word = 0;
+    if (tc_error_word(c, &word) != SPEC_OK) return set_error(SPEC_E_CUDA, "reading the device error word failed");
+    if (word != 0)
+        return set_error(SPEC_E_TIMEOUT,
+                         "a bounded wait on the device gave up (status %d); results since then are unreliable, "
+                         "destroy the context", word);
+    return SPEC_OK;
+}
+
+extern "C" int spec_sync(spec_ctx* c) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    const cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    return device_status(*c);
+}
+
 extern "C" int spec_seq_len(spec_ctx* c, int seq_id, int32_t* out_len) {
     clear_error();
     if (!c || !out_len || seq_id < 0 || seq_id >= c->lim.max_batch) return set_error(SPEC_E_INVAL, "bad argument");
-    const int rc = reclaim(*c);
+    int rc = reclaim(*c);
     if (rc != SPEC_OK) return rc;
+    if ((rc = device_status(*c)) != SPEC_OK) return rc;
     *out_len = c->len_hi[seq_id];
     return SPEC_OK;
 }

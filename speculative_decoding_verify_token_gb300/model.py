@@ -119,6 +119,11 @@ class SpecModel:
     def reset(self, seq_id):
         _lib.check(self.lib.spec_seq_reset(self.h, int(seq_id)))
 
+    def sync(self):
+        """Wait for the context's stream; raises SpecError (SPEC_E_TIMEOUT) if a device-side
+        wait gave up since the context was created."""
+        _lib.check(self.lib.spec_sync(self.h))
+
     def launches(self):
         return int(self.lib.spec_kernel_launches(self.h))
 

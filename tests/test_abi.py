@@ -128,6 +128,7 @@ def test_context_argument_validation(lib):
     assert lib.spec_kv_trim(None, 1, ids, 4, fake) == _lib.SPEC_E_INVAL
     assert lib.spec_set_option(None, _lib.SPEC_OPT_GRAPHS, 1) == _lib.SPEC_E_INVAL
     assert lib.spec_load_weights(None, None, None, 0) == _lib.SPEC_E_INVAL
+    assert lib.spec_sync(None) == _lib.SPEC_E_INVAL
     assert lib.spec_kernel_launches(None) == 0
     lib.spec_destroy(None)
 

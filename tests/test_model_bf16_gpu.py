@@ -131,6 +131,7 @@ def test_graphs_and_pdl_change_no_bits(lib, w):
         for rep in range(3):        # replays of the same graph along a growing context
             r = m.verify([0], last, drafts, u, 0.0, auto_trim=False, want_logits=True)
             outs.append(r["logits"].clone())
+        m.sync()                    # no device-side wait gave up
         res.append(outs)
         m.close()
     for outs in res[1:]:

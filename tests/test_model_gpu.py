@@ -203,4 +203,5 @@ def test_errors_are_reported(lib, weights):
     with pytest.raises(_lib.SpecError) as e:
         m.prefill(0, torch.zeros(41, dtype=torch.int32, device="cuda"))
     assert e.value.code == _lib.SPEC_E_RANGE
+    m.sync()                        # host-side rejections leave the device status clean
     m.close()
