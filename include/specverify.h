@@ -234,7 +234,10 @@ int spec_verify(spec_ctx* ctx, int B, const int32_t* seq_ids, int K,
                 int32_t* seq_status, float* out_logits, int auto_trim);
 
 /* Single-token decode of B slots: spec_verify with K = 0 (the token is appended and the
- * next one is drawn from its logits with uniforms[b]).  The comparator of the verify pass. */
+ * next one is drawn from its logits with uniforms[b]).  The comparator of the verify pass.
+ * uniforms (device fp32 [B]) is required, also when greedy (then unread).  A row without
+ * a finite logit has no distribution to draw from: sampling then writes next_token[b] = -1
+ * (no per-sequence status here; spec_verify with K = 0 reports it in seq_status). */
 int spec_decode(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* tokens,
                 const spec_sampling* sampling, const float* uniforms, int32_t* next_token,
                 float* out_logits);
