@@ -125,62 +125,3 @@ def test_long_context_attention_bitwise(lib):
         assert torch.equal(r[0], big[b]), b
         one.close()
 
-
-def test_serving_full_shape(lib):
-    """The serving configuration at its full size, set up as the benchmark sets it up: the
-    36-layer 8B shape, B = 32 sequences with KV lengths U[2048, 16384] (PCG64 seed 5), prompts
-    with 40% copied spans, K = 8, greedy, three rounds:
-      * drafts equal the oracle's n-gram lookup (four sequences checked per round);
-      * every sequence's decision follows the greedy rule on its own verify rows;
-      * every KV length grows by exactly accepted + 1;
-      * the first round's rows of a short and a long sequence equal, bit for bit, the rows of
-        the same sequence verified alone (B = 1)."""
-    model, ngram = lib
-    shape = synth.QWEN_8B
-    w = synth.model_weights(shape, seed=0, device="cuda")
-    B, K, rounds = 32, 8, 3
-    lens = np.random.Generator(np.random.PCG64(5)).integers(2048, 16384 + 1, size=B)
-    max_ctx = int(lens.max()) + (K + 1) * (rounds + 2) + 64
-    m = model.SpecModel(shape, w, max_batch=B, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
-    prompts = [synth.ngram_prompt(5 + b, int(lens[b]), shape.vocab) for b in range(B)]
-    ctx, drafters = [], []
-    for b in range(B):
-        m.prefill(b, torch.from_numpy(prompts[b][:-1]).cuda())
-        d = ngram.NgramDrafter(3, 8)
-        d.append(prompts[b])
-        drafters.append(d)
-        ctx.append([int(t) for t in prompts[b]])
-    u = torch.zeros(B, K + 1, dtype=torch.float32, device="cuda")
-    first = None
-    for r in range(rounds):
-        toks, dl = ngram.draft_batch(drafters, K)
-        for b in range(r, B, 8):
-            assert list(toks[b, :dl[b]]) == og.ngram_draft(ctx[b], n_draft=K), (r, b)
-        last = torch.tensor([c[-1] for c in ctx], dtype=torch.int32, device="cuda")
-        d_toks, d_len = torch.from_numpy(toks).cuda(), torch.from_numpy(dl).cuda()
-        before = [m.seq_len(b) for b in range(B)]
-        out = m.verify(list(range(B)), last, d_toks, u, 0.0, draft_len=d_len, want_logits=True)
-        a = out["accepted_len"].cpu().numpy()
-        nx = out["next_token"].cpu().numpy()
-        assert np.all(out["status"].cpu().numpy() == 0)
-        for b in range(B):
-            rows = out["logits"][b, :dl[b] + 1].double().cpu().numpy()
-            ref = ov.verify_greedy(rows, toks[b, :dl[b]])
-            assert (int(a[b]), int(nx[b])) == (ref["a"], ref["next"]), (r, b)
-            assert m.seq_len(b) == before[b] + int(a[b]) + 1, (r, b)
-        if r == 0:
-            first = (last.clone(), d_toks.clone(), d_len.clone(), out["logits"].clone())
-        for b in range(B):
-            new = [int(t) for t in toks[b, :a[b]]] + [int(nx[b])]
-            drafters[b].append(np.array(new, dtype=np.int32))
-            ctx[b] += new
-    m.close()
-    del m, out
-    last0, toks0, dl0, lg0 = first
-    for b in (int(np.argmin(lens)), int(np.argmax(lens))):
-        one = model.SpecModel(shape, w, max_batch=1, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
-        one.prefill(0, torch.from_numpy(prompts[b][:-1]).cuda())
-        r1 = one.verify([0], last0[b:b + 1].clone(), toks0[b:b + 1].clone(), u[:1].clone(), 0.0,
-                        draft_len=dl0[b:b + 1].clone(), want_logits=True)
-        assert torch.equal(r1["logits"][0], lg0[b]), b
-        one.close()

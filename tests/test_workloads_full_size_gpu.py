@@ -1,4 +1,6 @@
-"""8B-class dense bf16 target, greedy, K = 4, with the scripted drafter: the drafts copy
+"""Full-size workloads on the GPU, in the configurations the benchmark times.
+
+8B-class dense bf16 target, greedy, K = 4, with the scripted drafter: the drafts copy
 j ~ Geometric (P(j = n) = 0.3 * 0.7^n, capped at K) tokens of the target's own greedy
 trajectory, then one wrong token.  Greedy speculative output must equal plain greedy
 output ("Speculative Decoding on Apple Silicon: 119% Faster on Qwen3.8", section "Why
@@ -9,10 +11,17 @@ Draft Model Work?", section "#3").
   against the float64 oracle (logits within 3e-2 max-abs; every token the oracle's
   argmax unless its top-2 gap is below 1e-2), and scripted verify steps whose logits
   match the oracle's verify pass within 3e-2;
-* the full shape (36 layers, 1024-token prompt) in the configuration the benchmark times:
-  every scripted verify step accepts exactly j and emits the trajectory's next token
-  (speculative = plain, token for token), its decision is the greedy rule on its own
-  logits, and the first pass's rows equal single-token decode rows bit for bit.
+* the full shape (36 layers, 1024-token prompt): every scripted verify step accepts
+  exactly j and emits the trajectory's next token (speculative = plain, token for
+  token), its decision is the greedy rule on its own logits, and the first pass's rows
+  equal single-token decode rows bit for bit.
+
+Batched serving on the 8B-class shape ("Speculative decoding on Apple Silicon" (mlx-optiq
+docs), section "N-gram lookup: any model"): B = 32 sequences with KV lengths
+U[2048, 16384], n-gram drafts, K = 8, a trim after every verify pass.
+
+Kept in a file collected after the other GPU tests (before the allocation-free entry
+point's), so that a run that stops at its first failure has run those first.
 """
 import dataclasses
 
@@ -21,6 +30,7 @@ import pytest
 import torch
 
 import synth
+from oracle import generate as og
 from oracle import model as om
 from oracle import verify as ov
 
@@ -35,8 +45,8 @@ ALPHA = 0.7
 def lib():
     import __graft_entry__
     __graft_entry__.build()
-    from speculative_decoding_verify_token_gb300 import generate, model
-    return model, generate
+    from speculative_decoding_verify_token_gb300 import generate, model, ngram
+    return model, generate, ngram
 
 
 class EmbedRows:
@@ -91,7 +101,7 @@ def scripted_steps(m, seq, prompt_len, V, on_step=None):
 
 
 def test_8b_slice_matches_oracle(lib):
-    M, G = lib
+    M, G, _ = lib
     s = dataclasses.replace(synth.QWEN_8B, n_layers=2, name="dense-8b-2l")
     w = synth.model_weights(s, seed=0, device="cuda")
     V, n_new = s.vocab, 40
@@ -138,7 +148,7 @@ def full_weights(lib):
 
 
 def test_8b_full_scripted_steps_equal_plain_greedy(lib, full_weights):
-    M, G = lib
+    M, G, _ = lib
     s = synth.QWEN_8B
     V, n_new = s.vocab, 64
     prompt = torch.from_numpy(synth.prompt_tokens(1, 1024, V)).cuda()
@@ -162,3 +172,63 @@ def test_8b_full_scripted_steps_equal_plain_greedy(lib, full_weights):
         _, lg = m.decode([0], toks[i:i + 1].contiguous(), want_logits=True)
         assert torch.equal(lg[0], first["logits"][0, i]), i
     m.close()
+
+
+def test_serving_full_shape(lib, full_weights):
+    """The serving configuration at its full size, set up as the benchmark sets it up: the
+    36-layer 8B shape, B = 32 sequences with KV lengths U[2048, 16384] (PCG64 seed 5), prompts
+    with 40% copied spans, K = 8, greedy, three rounds:
+      * drafts equal the oracle's n-gram lookup (four sequences checked per round);
+      * every sequence's decision follows the greedy rule on its own verify rows;
+      * every KV length grows by exactly accepted + 1;
+      * the first round's rows of a short and a long sequence equal, bit for bit, the rows of
+        the same sequence verified alone (B = 1)."""
+    model, _, ngram = lib
+    shape = synth.QWEN_8B
+    w = full_weights
+    B, K, rounds = 32, 8, 3
+    lens = np.random.Generator(np.random.PCG64(5)).integers(2048, 16384 + 1, size=B)
+    max_ctx = int(lens.max()) + (K + 1) * (rounds + 2) + 64
+    m = model.SpecModel(shape, w, max_batch=B, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
+    prompts = [synth.ngram_prompt(5 + b, int(lens[b]), shape.vocab) for b in range(B)]
+    ctx, drafters = [], []
+    for b in range(B):
+        m.prefill(b, torch.from_numpy(prompts[b][:-1]).cuda())
+        d = ngram.NgramDrafter(3, 8)
+        d.append(prompts[b])
+        drafters.append(d)
+        ctx.append([int(t) for t in prompts[b]])
+    u = torch.zeros(B, K + 1, dtype=torch.float32, device="cuda")
+    first = None
+    for r in range(rounds):
+        toks, dl = ngram.draft_batch(drafters, K)
+        for b in range(r, B, 8):
+            assert list(toks[b, :dl[b]]) == og.ngram_draft(ctx[b], n_draft=K), (r, b)
+        last = torch.tensor([c[-1] for c in ctx], dtype=torch.int32, device="cuda")
+        d_toks, d_len = torch.from_numpy(toks).cuda(), torch.from_numpy(dl).cuda()
+        before = [m.seq_len(b) for b in range(B)]
+        out = m.verify(list(range(B)), last, d_toks, u, 0.0, draft_len=d_len, want_logits=True)
+        a = out["accepted_len"].cpu().numpy()
+        nx = out["next_token"].cpu().numpy()
+        assert np.all(out["status"].cpu().numpy() == 0)
+        for b in range(B):
+            rows = out["logits"][b, :dl[b] + 1].double().cpu().numpy()
+            ref = ov.verify_greedy(rows, toks[b, :dl[b]])
+            assert (int(a[b]), int(nx[b])) == (ref["a"], ref["next"]), (r, b)
+            assert m.seq_len(b) == before[b] + int(a[b]) + 1, (r, b)
+        if r == 0:
+            first = (last.clone(), d_toks.clone(), d_len.clone(), out["logits"].clone())
+        for b in range(B):
+            new = [int(t) for t in toks[b, :a[b]]] + [int(nx[b])]
+            drafters[b].append(np.array(new, dtype=np.int32))
+            ctx[b] += new
+    m.close()
+    del m, out
+    last0, toks0, dl0, lg0 = first
+    for b in (int(np.argmin(lens)), int(np.argmax(lens))):
+        one = model.SpecModel(shape, w, max_batch=1, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
+        one.prefill(0, torch.from_numpy(prompts[b][:-1]).cuda())
+        r1 = one.verify([0], last0[b:b + 1].clone(), toks0[b:b + 1].clone(), u[:1].clone(), 0.0,
+                        draft_len=dl0[b:b + 1].clone(), want_logits=True)
+        assert torch.equal(r1["logits"][0], lg0[b]), b
+        one.close()
