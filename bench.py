@@ -262,13 +262,8 @@ class DenseVerifyWorkload:
         return prof
 
     def roofline(self, prof, peaks):
-        if prof["persistent_pass"]["launches"] > 0:
-            # the whole decoder pass is one persistent kernel: its bytes are the weights of
-            # every GEMM, the KV pages read and written and the logits written
-            g, kernel = [prof["persistent_pass"]], "pf_kernel"
-        else:
-            g = [prof[k] for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head")]
-            kernel = "tc_gemm_kernel"
+        g = [prof[k] for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head")]
+        kernel = "tc_gemm_kernel"
         ms = sum(x["ms"] for x in g)
         n = sum(x["launches"] for x in g)
         by = sum(x["bytes"] for x in g)
@@ -288,31 +283,6 @@ class DenseVerifyWorkload:
                 "traffic_unit": "bytes per launch",
                 "algorithmic_bytes_per_launch": by / n, "launches_measured": n,
                 "avg_launch_us": ms / n * 1e3, "peak_source": peaks["source"]}
-
-    def persistent_pass(self, n):
-        """The same steps as one persistent kernel per pass (SPEC_OPT_PERSISTENT): step time
-        and per-class breakdown, reported beside the default per-kernel pass."""
-        import torch
-        from speculative_decoding_verify_token_gb300 import _lib
-        self.m.set_option(_lib.SPEC_OPT_PERSISTENT, 1)
-        try:
-            self.reset()
-            for i in range(3):
-                self.step(i)
-            self.reset()
-            torch.cuda.synchronize()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            for i in range(n):
-                self.step(i)
-            b.record()
-            torch.cuda.synchronize()
-            ms = a.elapsed_time(b) / n
-            prof = self.profile(n)
-        finally:
-            self.m.set_option(_lib.SPEC_OPT_PERSISTENT, 0)
-        return ms, {k: v["ms"] / n for k, v in prof.items() if v["launches"]}
 
     # end to end through the C ABI with host buffers
     def e2e(self, n):
@@ -1151,10 +1121,6 @@ def main():
         extra["verify_over_decode"] = (total_ms / args.steps) / dec_ms
     prof = wl.profile(args.profile_steps)
     roof = wl.roofline(prof, peaks)
-    if isinstance(wl, DenseVerifyWorkload):
-        pk_ms, pk_break = wl.persistent_pass(args.profile_steps)
-        extra["persistent_pass_ms_per_step"] = pk_ms
-        extra["persistent_pass_breakdown_ms_per_step"] = pk_break
     if isinstance(prof, dict):
         extra["kernel_breakdown_ms_per_step"] = {k: v["ms"] / args.profile_steps for k, v in prof.items()}
         step_bytes = sum(v["bytes"] for v in prof.values()) / args.profile_steps

@@ -252,8 +252,8 @@ int spec_kv_trim(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int3
 int spec_seq_len(spec_ctx* ctx, int seq_id, int32_t* out_len);
 
 /* Wait for the context's stream, then report the device-side status: SPEC_E_TIMEOUT when
- * a bounded wait inside a kernel (a tensor-core GEMM's pipeline barriers, the persistent
- * pass's hand-offs; each gives up after 2 s) gave up since the context was created.  The
+ * a bounded wait inside a kernel (a tensor-core GEMM's pipeline barriers; each gives up
+ * after 2 s) gave up since the context was created.  The
  * kernel then skipped the rest of its work, so results since then are unreliable; the
  * status is sticky and the context must be destroyed.  SPEC_E_CUDA on a stream error.
  * (No counterpart on the pages: the library's own failure reporting.) */
@@ -268,34 +268,28 @@ int spec_seq_reset(spec_ctx* ctx, int seq_id);
  * changes any result bit. */
 #define SPEC_OPT_GRAPHS 1
 #define SPEC_OPT_PDL    2
-/* SPEC_OPT_L2_PREFETCH (value 0..64, default 12): once a GEMM has issued all its loads, each
- * of its CTAs warms L2 with this many 64-column atoms (16 KB each) of the weights it will
- * stream first in the next GEMM of the pass; 0 disables.  Changes no result bit. */
+/* SPEC_OPT_L2_PREFETCH (value 0..64, default 0 = off): once a GEMM has issued all its loads,
+ * each of its CTAs warms L2 with this many 64-column atoms (16 KB each) of the weights it
+ * will stream first in the next GEMM of the pass.  Changes no result bit. */
 #define SPEC_OPT_L2_PREFETCH 3
-/* SPEC_OPT_PERSISTENT (default 0): 1 runs a verify or decode pass of at most 32 tokens
- * (B*(K+1)) of a bf16 model on the tensor-core path as one persistent cooperative kernel
- * (one CTA per SM) in which the phases of the pass hand off through counters in global
- * memory instead of kernel boundaries; 0 launches one kernel per step.  Same result bits
- * either way.  SPEC_OPT_PF_ATOMS (1, 2 or 4; default 4): 64-column K atoms per shared-memory
- * stage of that kernel's weight ring.  SPEC_OPT_PF_L2_AHEAD (0..256, default 0): weight
- * atoms (16 KB each) per CTA prefetched into L2 ahead of that ring, so that HBM keeps
- * streaming while a phase waits for its inputs. */
-#define SPEC_OPT_PERSISTENT 4
-#define SPEC_OPT_PF_ATOMS 5
-#define SPEC_OPT_PF_L2_AHEAD 6
 /* SPEC_OPT_ATTN_L2_AHEAD (0..64, default 0 = off): on long contexts, where one attention CTA
  * walks a run of 64-key splits, the K and V pages of the split this many splits ahead are
  * prefetched into L2 (bulk prefetch, no shared memory) while the current one is computed.
  * Changes no result bit (measured neutral on 2k-16k contexts). */
 #define SPEC_OPT_ATTN_L2_AHEAD 7
+/* SPEC_OPT_GEMM_MIN_FILL (percent, 0..101, default 80): a tensor-core GEMM with fewer output
+ * tiles than SMs runs as a whole number of CTAs per tile when that keeps at least this share
+ * of the SMs busy, else one CTA per SM over equal ranges that cross tile boundaries (101:
+ * always the latter).  The split sets the order of the K sums, so it changes result bits
+ * (within the rounding of fp32 accumulation), the same way for every token count. */
+#define SPEC_OPT_GEMM_MIN_FILL 8
 int spec_set_option(spec_ctx* ctx, int option, int value);
 
 /* Per-kernel-class timing of the context's passes with CUDA events recorded on its
  * stream around each launch (off by default; meant for a measurement pass).  Classes:
  * 0 QKV GEMM, 1 O GEMM, 2 gate/up GEMM, 3 down GEMM, 4 lm_head GEMM, 5 attention,
- * 6 fused verify, 7 other small kernels, 8 persistent decoder pass (SPEC_OPT_PERSISTENT;
- * bytes = weights + KV pages + logits of the pass). */
-#define SPEC_PROF_CLASSES 9
+ * 6 fused verify, 7 other small kernels. */
+#define SPEC_PROF_CLASSES 8
 int spec_profile(spec_ctx* ctx, int enable);
 
 /* Synchronise the context stream and return, per class, the summed event time (ms), the

@@ -55,12 +55,10 @@ SPEC_OPT_ATTN_L2_AHEAD = 7
 SPEC_OPT_GRAPHS = 1
 SPEC_OPT_PDL = 2
 SPEC_OPT_L2_PREFETCH = 3
-SPEC_OPT_PERSISTENT = 4
-SPEC_OPT_PF_ATOMS = 5
-SPEC_OPT_PF_L2_AHEAD = 6
-SPEC_PROF_CLASSES = 9
+SPEC_OPT_GEMM_MIN_FILL = 8
+SPEC_PROF_CLASSES = 8
 PROF_CLASS_NAMES = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head", "attention",
-                    "verify", "other", "persistent_pass"]
+                    "verify", "other"]
 SPEC_F32 = 0
 SPEC_BF16 = 1
 

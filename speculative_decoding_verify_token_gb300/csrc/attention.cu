@@ -189,8 +189,9 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnArgs a) {
     sm.Ps = sm.Qlo + MMA_RT * MMA_PITCH;
     sm.wmax = wmax;
     sm.wsum = wsum;
+    // keys of earlier passes load before the wait for the QKV GEMM (programmatic launch)
     attn_mma_item(a, blockIdx.x, blockIdx.y, blockIdx.z, sm, threadIdx.x, [] { __syncthreads(); },
-                  [] { return true; });
+                  [] { pdl_wait(); return true; });
 }
 
 // Long contexts: one CTA of 4 warps per run of `spc` consecutive 64-key splits of a (kv head,
@@ -325,6 +326,25 @@ size_t attn_smem(int hd, int esize) {
     return (size_t)2 * split * hd * esize + sizeof(float) * ((size_t)ATT_RT * hd + (size_t)ATT_RT * split);
 }
 
+// Launch with programmatic stream serialization when pdl is set: the kernel may start
+// while the previous one finishes and waits for it (griddepcontrol.wait) where it first
+// reads that kernel's outputs.
+template <typename... Args>
+static void launch_pdl(bool pdl, void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, cudaStream_t st) {
     const int nsplit = (max_len_after + a.split_keys - 1) / a.split_keys;
     const int G = a.hq / a.hkv;
@@ -337,7 +357,7 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
         int spc = (int)std::min<long long>(nsplit, (items + target - 1) / target);
         if (a.T * G > MMA_RT || spc < ATT_MULTI_MIN) spc = 1;
         if (spc == 1) {
-            attn_mma_kernel<<<dim3(nsplit, a.hkv, B), 128, MMA_SMEM, st>>>(a);
+            launch_pdl(c.use_pdl, attn_mma_kernel, dim3(nsplit, a.hkv, B), dim3(128), MMA_SMEM, st, a);
         } else {
             attn_mma_multi_kernel<<<dim3((nsplit + spc - 1) / spc, a.hkv, B), 128, MMA_MULTI_SMEM, st>>>(a, spc);
         }

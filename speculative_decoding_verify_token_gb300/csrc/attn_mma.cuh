@@ -1,6 +1,6 @@
-// Device pieces of the tensor-core attention (bf16, head_dim 128, mma.sync m16n8k16) shared
-// by the attention kernels and the persistent decoder kernel: one (split, kv head,
-// sequence) item over the paged KV cache, and the combine of one query row's splits.
+// Device pieces of the tensor-core attention (bf16, head_dim 128, mma.sync m16n8k16): one
+// (split, kv head, sequence) item over the paged KV cache, and the combine of one query
+// row's splits.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -6,9 +6,16 @@
 // "How speculative decoding works").  Design:
 //  * swap-AB: a 128-row weight tile is the A operand, the tokens are the N dimension
 //    (16..256); the fp32 accumulator [128 x N] lives in tensor memory;
-//  * operands arrive by TMA (cp.async.bulk.tensor, 128-byte swizzle) into an mbarrier ring
-//    of up to 8 stages of 64 k-elements; weights are loaded evict-first, activations
-//    evict-last (every CTA re-reads them);
+//  * the weights are re-laid out once, when they are loaded, tile-major: every (tile, K
+//    atom) is the 16 KB A operand of one MMA atom, already in the 128-byte-swizzled order
+//    the tensor cores read, so a ring stage of n consecutive atoms of a tile is ONE
+//    contiguous bulk copy (cp.async.bulk) of n x 16 KB; a tensor-map box of 64 rows
+//    instead makes 64 separate 128-byte row requests, and issuing the boxes of a stage
+//    costs microseconds at the start of every GEMM;
+//  * the activations (the B operand, a few rows) arrive by TMA tensor loads with the
+//    128-byte swizzle; stages go into an mbarrier ring of up to 8 stages of up to four
+//    64-column K atoms; weights are loaded evict-first, activations evict-last (every CTA
+//    re-reads them);
 //  * warp roles: warp 0 = TMA producer, warp 1 = tcgen05.mma issuer (one thread) and TMEM
 //    owner, warps 2-5 = epilogue (tcgen05.ld of the 4 lane quarters);
 //  * persistent stream-K: the (tile, k-block) space is cut into one contiguous range per
@@ -43,7 +50,7 @@ namespace sv {
 constexpr int TC_SMEM_MAX = TC_CTAS_PER_SM == 1 ? 230912 : 110 * 1024;
 
 struct TcParams {
-    CUtensorMap wmap[3];
+    const uint8_t* wt;        // this GEMM's tile-major weights: [n_tiles][KB] atoms of TC_ATOM_A bytes
     CUtensorMap xmap;
     int gid;
     int n_tiles, KB;          // tiles; K atoms per tile (the stream-K unit)
@@ -54,8 +61,8 @@ struct TcParams {
     int hq, hkv;
     // L2 prefetch of the next GEMM's first weight atoms of this CTA's range (issued by the
     // producer once its own loads are all issued)
-    CUtensorMap nwmap[3];
-    int ngid, n_ntiles, n_KB, n_atoms;       // n_atoms = 0: no prefetch
+    const uint8_t* nwt;
+    int n_ntiles, n_KB, n_atoms;       // n_atoms = 0: no prefetch
     float* partial;          // [grid][2] x ntok/16 chunks of [4][128] float4 (partial_f4)
     int* tile_cnt;           // [n_tiles], zero between launches
     int* err;
@@ -67,26 +74,18 @@ struct TcParams {
 // [gid][cta][0 entry, 1 set-up done, 2 first stage ready, 3 last MMA issued,
 //            4 last accumulator ready, 5 exit]
 __device__ unsigned long long g_tc_trace[5][1024][6];
-#define TC_STAMP(i) g_tc_trace[p.gid][blockIdx.x][i] = globaltimer_ns()
+#define TC_STAMP(i) do { if (blockIdx.x < 1024) g_tc_trace[p.gid][blockIdx.x][i] = globaltimer_ns(); } while (0)
 #else
 #define TC_STAMP(i) ((void)0)
 #endif
 
-__device__ __forceinline__ void tile_rows(const TcParams& p, int tile, const CUtensorMap*& m0, int& r0,
-                                          const CUtensorMap*& m1, int& r1) {
-    tile_rows_of(p.gid, p.wmap, p.hq, p.hkv, tile, m0, r0, m1, r1);
+// The weights (A) of n consecutive K atoms kt .. kt + n - 1 of a tile: one bulk copy.
+__device__ __forceinline__ void load_stage_a(const TcParams& p, int tile, int kt, int n, uint32_t a_dst, uint32_t fb,
+                                             uint64_t pol) {
+    bulk_g2s(a_dst, p.wt + ((size_t)tile * p.KB + kt) * TC_ATOM_A, (uint32_t)(n * TC_ATOM_A), fb, pol);
 }
 
-// One K atom of a stage: the tile's 128 weight rows as two 64-row boxes (A) and the token
-// rows in boxes of 16 (B), at K coordinate kc.
-__device__ __forceinline__ void load_atom_a(const TcParams& p, int tile, int kc, uint32_t a_dst, uint32_t fb,
-                                            uint64_t pol) {
-    const CUtensorMap *m0, *m1;
-    int r0, r1;
-    tile_rows(p, tile, m0, r0, m1, r1);
-    tma_load_2d(a_dst, m0, kc, r0, fb, pol);
-    tma_load_2d(a_dst + TC_ATOM_A / 2, m1, kc, r1, fb, pol);
-}
+// The token rows (B) of one K atom at K coordinate kc, in boxes of 16 rows.
 
 __device__ __forceinline__ void load_atom_b(const TcParams& p, int kc, uint32_t b_dst, uint32_t fb, uint64_t pol) {
     for (int t = 0; t < p.br.nr0 / 16; ++t) tma_load_2d(b_dst + t * 2048, &p.xmap, kc, p.br.b_row0 + t * 16, fb, pol);
@@ -128,7 +127,6 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
         }
         mbar_init(smem_u32(&done_bar), 1);
         fence_barrier_init();
-        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&p.wmap[0])) : "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
     }
     if (warp == 1) {
@@ -161,7 +159,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 const uint32_t fb = smem_u32(&full_bar[i]);
                 mbar_arrive_expect_tx(fb, per_atom_tx * n);
                 const uint32_t a_dst = base + (uint32_t)i * p.stage_bytes;
-                for (int at = 0; at < n; ++at) load_atom_a(p, tile, (kt + at) * TC_ATOM, a_dst + at * TC_ATOM_A, fb, pw);
+                load_stage_a(p, tile, kt, n, a_dst, fb, pw);
                 w.g += n;
                 if (sl) seg0 = w.g;
             }
@@ -193,27 +191,20 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 const uint32_t fb = smem_u32(&full_bar[s]);
                 mbar_arrive_expect_tx(fb, per_atom_tx * n);
                 const uint32_t a_dst = base + (uint32_t)s * p.stage_bytes;
-                for (int at = 0; at < n; ++at) {
-                    load_atom_a(p, tile, (kt + at) * TC_ATOM, a_dst + at * TC_ATOM_A, fb, pw);
+                load_stage_a(p, tile, kt, n, a_dst, fb, pw);
+                for (int at = 0; at < n; ++at)
                     load_atom_b(p, (kt + at) * TC_ATOM, a_dst + b_off + at * p.br.nb * TC_ATOM * 2, fb, px);
-                }
                 w.g += n;
                 if (sl) seg0 = w.g;
             }
             if (p.n_atoms > 0) {
                 // warm L2 with the first atoms this CTA index will stream in the next GEMM,
                 // so HBM keeps working while the kernels in between run
+                // (the atoms of a range are contiguous in the tile-major layout)
                 const long long T2 = (long long)p.n_ntiles * p.n_KB;
                 const long long a0 = range_start(T2, G, cta);
                 const long long a1 = min(range_start(T2, G, cta + 1), a0 + p.n_atoms);
-                for (long long g = a0; g < a1; ++g) {
-                    const int tile = (int)(g / p.n_KB), kt = (int)(g % p.n_KB);
-                    const CUtensorMap *m0, *m1;
-                    int r0, r1;
-                    tile_rows_of(p.ngid, p.nwmap, p.hq, p.hkv, tile, m0, r0, m1, r1);
-                    tma_prefetch_l2(m0, kt * TC_ATOM, r0);
-                    tma_prefetch_l2(m1, kt * TC_ATOM, r1);
-                }
+                if (a1 > a0) bulk_prefetch_l2(p.nwt + (size_t)a0 * TC_ATOM_A, (uint32_t)((a1 - a0) * TC_ATOM_A));
             }
         }
     } else if (warp == 1) {
@@ -307,6 +298,15 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
             const long long seg_end = min(s1, tile_k0 + p.KB);
             const bool full_tile = (g == tile_k0) && (seg_end == tile_k0 + p.KB);
             const int buf = si % nbuf;
+            EpiPre pre;
+            epi_preload(p.M, p.e, tile, etid, pre);
+            // contributors of a split tile (CTA order), found before the accumulator is ready
+            int c_lo = cta, c_hi = cta, wc_lo = 0;
+            if (!full_tile) {
+                c_lo = owner_cta(T, G, tile_k0);
+                c_hi = owner_cta(T, G, tile_k0 + p.KB - 1);
+                wc_lo = (range_start(T, G, c_lo) >= tile_k0) ? 0 : 1;
+            }
             const bool okw = mbar_wait(smem_u32(&accf[buf]), (uint32_t)((si / nbuf) & 1));
             if (epi_any(okw ? 0 : 1)) {
                 if (etid == 0) atomicExch(p.err, SPEC_E_TIMEOUT);
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 #pragma unroll
                     for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = v[j];
                     epi_bar();
-                    epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid);
+                    epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid, c0 == 0 ? &pre : nullptr);
                     epi_bar();
                 }
             } else {
@@ -341,8 +341,6 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&acce[buf]));
-                const int c_lo = owner_cta(T, G, tile_k0);
-                const int c_hi = owner_cta(T, G, tile_k0 + p.KB - 1);
                 __threadfence();
                 epi_bar();
                 if (etid == 0) {
@@ -354,7 +352,6 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                     __threadfence();
                     // contributors in CTA order; the first one's slot is 1 unless its range
                     // starts exactly at the tile, every later one starts inside the tile
-                    const int wc_lo = (range_start(T, G, c_lo) >= tile_k0) ? 0 : 1;
                     for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
                         float acc[16];
 #pragma unroll
@@ -385,7 +382,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 #pragma unroll
                         for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = acc[j];
                         epi_bar();
-                        epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid);
+                        epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid, c0 == 0 ? &pre : nullptr);
                         epi_bar();
                     }
                     if (etid == 0) p.tile_cnt[tile] = 0;
@@ -409,13 +406,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-struct TcLayerMaps {
-    CUtensorMap q, k, v, o, g, u, d;
-};
-
 struct TcGemm {
-    std::vector<TcLayerMaps> layers;
-    CUtensorMap lm;
+    uint8_t* wt = nullptr;                 // tile-major weights of every GEMM
+    std::vector<size_t> off;               // byte offset of GEMM (layer, gid) at 4 * layer + gid; lm_head last
     CUtensorMap xn, xo, xh;
     float* partial = nullptr;
     int* tile_cnt = nullptr;
@@ -460,6 +453,43 @@ bool tc_supported(const Ctx& c) {
            m.ffn_dim % 64 == 0 && (m.n_q_heads * m.head_dim) % 64 == 0 && encode_fn();
 }
 
+// Weight bytes, tiles and K atoms per tile of GEMM `gid` (one layer; lm_head for GEMM_LM).
+static void gemm_shape(const spec_model_cfg& m, int gid, int& n_tiles, int& KB) {
+    const int d = m.d_model, qd = m.n_q_heads * m.head_dim, F = m.ffn_dim;
+    switch (gid) {
+    case GEMM_QKV: n_tiles = m.n_q_heads + 2 * m.n_kv_heads; KB = d / TC_ATOM; break;
+    case GEMM_O: n_tiles = d / TC_BM; KB = qd / TC_ATOM; break;
+    case GEMM_GU: n_tiles = F / 64; KB = d / TC_ATOM; break;
+    case GEMM_DOWN: n_tiles = d / TC_BM; KB = F / TC_ATOM; break;
+    default: n_tiles = m.vocab / TC_BM; KB = d / TC_ATOM; break;
+    }
+}
+
+// Tile-major copy of one weight GEMM (see the file header): destination 16-byte chunk i =
+// ((atom * 2 + half) * 64 + row) * 8 + chunk, atom = tile * KB + k, holds the source chunk
+// chunk ^ (row % 8) of that row (the 128-byte swizzle of a K-major operand row).
+struct RelayoutArgs {
+    const __nv_bfloat16* src[3];   // the GEMM's weight matrices, row-major [rows][ld]
+    int gid, hq, hkv, KB, ld;
+    size_t n_chunks;
+    uint8_t* dst;
+};
+
+__global__ void tc_relayout_kernel(const RelayoutArgs a) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < a.n_chunks; i += (size_t)gridDim.x * blockDim.x) {
+        const int cd = (int)(i & 7);
+        const int r = (int)((i >> 3) & 63);
+        const int h = (int)((i >> 9) & 1);
+        const size_t atom = i >> 10;
+        const int tile = (int)(atom / a.KB), k = (int)(atom - (size_t)tile * a.KB);
+        int mat, row0;
+        tile_half_rows(a.gid, a.hq, a.hkv, tile, h, mat, row0);
+        const int c = cd ^ (r & 7);
+        *reinterpret_cast<uint4*>(a.dst + i * 16) =
+            *reinterpret_cast<const uint4*>(a.src[mat] + (size_t)(row0 + r) * a.ld + (size_t)k * TC_ATOM + c * 8);
+    }
+}
+
 int tc_create(Ctx& c) {
     c.use_tc = false;
     if (!tc_supported(c)) return SPEC_OK;
@@ -468,22 +498,56 @@ int tc_create(Ctx& c) {
     const uint64_t d = m.d_model, qd = (uint64_t)m.n_q_heads * m.head_dim, kvd = (uint64_t)m.n_kv_heads * m.head_dim,
                    F = m.ffn_dim, V = m.vocab;
     int rc = SPEC_OK;
-    t->layers.resize(m.n_layers);
-    for (int l = 0; l < m.n_layers && rc == SPEC_OK; ++l) {
-        const LayerWeights& L = c.w.layers[l];
-        TcLayerMaps& M = t->layers[l];
-        if ((rc = make_map(&M.q, L.wq, qd, d, 64)) || (rc = make_map(&M.k, L.wk, kvd, d, 64)) ||
-            (rc = make_map(&M.v, L.wv, kvd, d, 64)) || (rc = make_map(&M.o, L.wo, d, qd, 64)) ||
-            (rc = make_map(&M.g, L.wg, F, d, 64)) || (rc = make_map(&M.u, L.wu, F, d, 64)) ||
-            (rc = make_map(&M.d, L.wd, d, F, 64)))
-            break;
+    // tile-major weights: offsets of (layer, gid) at 4 * layer + gid, lm_head last
+    const int L = m.n_layers;
+    t->off.resize((size_t)4 * L + 1);
+    size_t total = 0;
+    for (int i = 0; i <= 4 * L; ++i) {
+        int nt, kb;
+        gemm_shape(m, i == 4 * L ? GEMM_LM : i % 4, nt, kb);
+        t->off[i] = total;
+        total += (size_t)nt * kb * TC_ATOM_A;
     }
-    if (rc == SPEC_OK) rc = make_map(&t->lm, c.w.lm_head, V, d, 64);
+    {
+        void* w = nullptr;
+        if (cudaMalloc(&w, total) != cudaSuccess) {
+            delete t;
+            return set_error(SPEC_E_NOMEM, "tile-major weight copy (%zu bytes) allocation failed", total);
+        }
+        t->wt = static_cast<uint8_t*>(w);
+    }
+    for (int i = 0; i <= 4 * L; ++i) {
+        const int gid = i == 4 * L ? GEMM_LM : i % 4;
+        RelayoutArgs a{};
+        int nt, kb;
+        gemm_shape(m, gid, nt, kb);
+        a.gid = gid; a.hq = m.n_q_heads; a.hkv = m.n_kv_heads; a.KB = kb; a.ld = kb * TC_ATOM;
+        a.n_chunks = (size_t)nt * kb * (TC_ATOM_A / 16);
+        a.dst = t->wt + t->off[i];
+        using bf = __nv_bfloat16;
+        if (gid == GEMM_LM) {
+            a.src[0] = static_cast<const bf*>(c.w.lm_head);
+        } else {
+            const LayerWeights& lw = c.w.layers[i / 4];
+            switch (gid) {
+            case GEMM_QKV:
+                a.src[0] = static_cast<const bf*>(lw.wq); a.src[1] = static_cast<const bf*>(lw.wk);
+                a.src[2] = static_cast<const bf*>(lw.wv);
+                break;
+            case GEMM_O: a.src[0] = static_cast<const bf*>(lw.wo); break;
+            case GEMM_GU: a.src[0] = static_cast<const bf*>(lw.wg); a.src[1] = static_cast<const bf*>(lw.wu); break;
+            default: a.src[0] = static_cast<const bf*>(lw.wd); break;
+            }
+        }
+        tc_relayout_kernel<<<4 * c.num_sms, 256, 0, c.stream>>>(a);
+    }
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(c.stream) != cudaSuccess)
+        rc = set_error(SPEC_E_CUDA, "weight re-layout failed");
     // GEMM inputs as [2][Mmax][cols]: bf16 hi rows, then the lo remainders
     if (rc == SPEC_OK) rc = make_map(&t->xn, c.Xn, 2 * (uint64_t)c.Mmax, d, 16);
     if (rc == SPEC_OK) rc = make_map(&t->xo, c.O, 2 * (uint64_t)c.Mmax, qd, 16);
     if (rc == SPEC_OK) rc = make_map(&t->xh, c.H, 2 * (uint64_t)c.Mmax, F, 16);
-    t->grid = c.num_sms * TC_CTAS_PER_SM;
+    t->grid = c.num_sms;
     const int max_tiles = (int)std::max<uint64_t>({V / 128, F / 64, d / 128, qd / 128 + 2 * kvd / 128});
     if (rc == SPEC_OK) {
         void *a = nullptr, *b = nullptr, *e = nullptr;
@@ -504,6 +568,7 @@ int tc_create(Ctx& c) {
         cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX) != cudaSuccess)
         rc = set_error(SPEC_E_CUDA, "cudaFuncSetAttribute(tc_gemm_kernel)");
     if (rc != SPEC_OK) {
+        if (t->wt) cudaFree(t->wt);
         if (t->partial) cudaFree(t->partial);
         if (t->tile_cnt) cudaFree(t->tile_cnt);
         if (t->err) cudaFree(t->err);
@@ -518,6 +583,7 @@ int tc_create(Ctx& c) {
 
 void tc_destroy(Ctx& c) {
     if (!c.tc) return;
+    cudaFree(c.tc->wt);
     cudaFree(c.tc->partial);
     cudaFree(c.tc->tile_cnt);
     cudaFree(c.tc->err);
@@ -533,55 +599,22 @@ extern "C" int spec_debug_tc_trace(unsigned long long* out) {
 }
 #endif
 
-// Tensor maps and workspace of the context's GEMMs for the persistent pass: wmaps [7L + 1]
-// (q k v o g u d per layer, then lm_head) and xmaps [3] (Xn, O, H); either may be null.
-int tc_export(const Ctx& c, CUtensorMap* wmaps, CUtensorMap* xmaps, float** partial, int** tile_cnt, int* n_tile_cnt,
-              int** err) {
-    const TcGemm* t = c.tc;
-    if (!t) return set_error(SPEC_E_STATE, "tensor-core GEMM not planned");
-    const spec_model_cfg& m = c.cfg;
-    if (wmaps) {
-        for (int l = 0; l < m.n_layers; ++l) {
-            const TcLayerMaps& L = t->layers[l];
-            CUtensorMap* w = wmaps + (size_t)7 * l;
-            w[0] = L.q; w[1] = L.k; w[2] = L.v; w[3] = L.o; w[4] = L.g; w[5] = L.u; w[6] = L.d;
-        }
-        wmaps[(size_t)7 * m.n_layers] = t->lm;
-    }
-    if (xmaps) {
-        xmaps[0] = t->xn;
-        xmaps[1] = t->xo;
-        xmaps[2] = t->xh;
-    }
-    *partial = t->partial;
-    *tile_cnt = t->tile_cnt;
-    *n_tile_cnt = t->n_tile_cnt;
-    *err = t->err;
-    return SPEC_OK;
-}
-
 int tc_error_word(Ctx& c, int* out) {
     if (!c.tc) { *out = 0; return SPEC_OK; }
     return cudaMemcpy(out, c.tc->err, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess ? SPEC_OK : SPEC_E_CUDA;
 }
 
-// Weight maps, tile count and K atoms per tile of GEMM `gid` of `layer`.
-static void gemm_geometry(const Ctx& c, int gid, int layer, CUtensorMap* maps, int& n_tiles, int& KB) {
-    const TcGemm* t = c.tc;
-    const spec_model_cfg& m = c.cfg;
-    const int d = m.d_model, qd = m.n_q_heads * m.head_dim, F = m.ffn_dim;
-    switch (gid) {
-    case GEMM_QKV:
-        maps[0] = t->layers[layer].q; maps[1] = t->layers[layer].k; maps[2] = t->layers[layer].v;
-        n_tiles = m.n_q_heads + 2 * m.n_kv_heads; KB = d / TC_ATOM;
-        break;
-    case GEMM_O: maps[0] = t->layers[layer].o; n_tiles = d / TC_BM; KB = qd / TC_ATOM; break;
-    case GEMM_GU:
-        maps[0] = t->layers[layer].g; maps[1] = t->layers[layer].u; n_tiles = F / 64; KB = d / TC_ATOM;
-        break;
-    case GEMM_DOWN: maps[0] = t->layers[layer].d; n_tiles = d / TC_BM; KB = F / TC_ATOM; break;
-    default: maps[0] = t->lm; n_tiles = m.vocab / TC_BM; KB = d / TC_ATOM; break;
-    }
+// CTAs of a GEMM of n_tiles output tiles on `sms` SMs.  With fewer tiles than SMs, the grid
+// is a whole number s of CTAs per tile (each CTA one s-th of a tile's K atoms, every tile
+// finished by exactly s contributors, whose partial sums the last one reads in one batch)
+// as long as that keeps at least min_fill percent of the SMs streaming; otherwise one CTA
+// per SM with the (tile, atom) space cut into equal ranges across tile boundaries.  The
+// choice depends only on the weight shape and the SM count, so a token's result bits do
+// not depend on how many tokens share the launch.
+static int gemm_grid(int n_tiles, int sms, int min_fill) {
+    if (n_tiles >= sms) return sms;
+    const int g = n_tiles * (sms / n_tiles);
+    return 100 * g >= min_fill * sms ? g : sms;
 }
 
 static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int pass_M, const EpiArgs& e,
@@ -594,25 +627,15 @@ static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int 
     int Kdim = d;
     const CUtensorMap* xm = &t->xn;
     const uint8_t* xbase = static_cast<const uint8_t*>(c.Xn);
-    switch (gid) {
-    case GEMM_QKV:
-        p.wmap[0] = t->layers[layer].q; p.wmap[1] = t->layers[layer].k; p.wmap[2] = t->layers[layer].v;
-        p.n_tiles = m.n_q_heads + 2 * m.n_kv_heads;
-        break;
-    case GEMM_O:
-        p.wmap[0] = t->layers[layer].o; p.n_tiles = d / TC_BM; Kdim = qd; xm = &t->xo;
+    int KB = 0;
+    gemm_shape(m, gid, p.n_tiles, KB);
+    p.wt = t->wt + t->off[gid == GEMM_LM ? (size_t)4 * m.n_layers : (size_t)4 * layer + gid];
+    if (gid == GEMM_O) {
+        Kdim = qd; xm = &t->xo;
         xbase = static_cast<const uint8_t*>(c.O);
-        break;
-    case GEMM_GU:
-        p.wmap[0] = t->layers[layer].g; p.wmap[1] = t->layers[layer].u; p.n_tiles = F / 64;
-        break;
-    case GEMM_DOWN:
-        p.wmap[0] = t->layers[layer].d; p.n_tiles = d / TC_BM; Kdim = F; xm = &t->xh;
+    } else if (gid == GEMM_DOWN) {
+        Kdim = F; xm = &t->xh;
         xbase = static_cast<const uint8_t*>(c.H);
-        break;
-    default:
-        p.wmap[0] = t->lm; p.n_tiles = m.vocab / TC_BM;
-        break;
     }
     const size_t off = static_cast<const uint8_t*>(X) - xbase;
     p.x_row0 = (int)(off / ((size_t)Kdim * 2));
@@ -646,12 +669,12 @@ static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int 
             ngid = layer + 1 < m.n_layers ? GEMM_QKV : GEMM_LM;
             nlayer = layer + 1 < m.n_layers ? layer + 1 : -1;
         }
-        gemm_geometry(c, ngid, nlayer, p.nwmap, p.n_ntiles, p.n_KB);
-        p.ngid = ngid;
+        gemm_shape(m, ngid, p.n_ntiles, p.n_KB);
+        p.nwt = t->wt + t->off[ngid == GEMM_LM ? (size_t)4 * m.n_layers : (size_t)4 * nlayer + ngid];
         p.n_atoms = c.l2_prefetch_atoms;
     }
     const long long T = (long long)p.n_tiles * p.KB;
-    const int grid = (int)std::min<long long>(t->grid, T);
+    const int grid = (int)std::min<long long>(gemm_grid(p.n_tiles, t->grid, c.gemm_min_fill), T);
     const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + TC_XBYTES;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -44,7 +44,6 @@ struct AttnArgs {
 };
 
 struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
-struct PfPlan;   // persistent decoder pass (fwd_persistent.cu)
 
 // The five GEMMs of the decoder pass.
 enum GemmId { GEMM_QKV = 0, GEMM_O = 1, GEMM_GU = 2, GEMM_DOWN = 3, GEMM_LM = 4 };
@@ -114,18 +113,14 @@ struct Ctx {
     // CUDA graphs of the decoder pass per (B, T); programmatic dependent launch
     bool use_graphs = true;
     bool use_pdl = true;
-    int l2_prefetch_atoms = 12;            // next-GEMM weight atoms per CTA warmed into L2
+    int l2_prefetch_atoms = 0;             // next-GEMM weight atoms per CTA warmed into L2
+    int gemm_min_fill = 80;                // percent of the SMs a whole-tile GEMM split must keep busy
     cudaStream_t cap_stream = nullptr;     // private stream the graphs are captured on
     struct GraphEntry { int B, T; cudaGraphExec_t exec; long long kernels; };
     std::vector<GraphEntry> graphs;
     // tensor-core GEMM
     TcGemm* tc = nullptr;
     bool use_tc = false;
-    // persistent decoder pass (fwd_persistent.cu)
-    PfPlan* pf = nullptr;
-    bool use_pf = false;
-    int pf_atoms = 4;
-    int pf_l2_ahead = 0;
     int attn_l2_ahead = 0;                 // splits of K/V warmed in L2 ahead (long contexts)
     std::vector<void*> allocs;
 };
@@ -152,14 +147,6 @@ void tc_destroy(Ctx& c);
 int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, int pass_M, const EpiArgs& e, cudaStream_t st);
 bool tc_supported(const Ctx& c);
 int tc_error_word(Ctx& c, int* out);          // device error word of the tensor-core GEMM (synchronous)
-
-// persistent decoder pass (bf16 tensor-core models, M <= 32 tokens)
-int pf_create(Ctx& c);                       // after tc_create; leaves c.pf null if unsupported
-void pf_destroy(Ctx& c);
-bool pf_usable(const Ctx& c, int M);
-// returns kernels launched (1) or a negative SPEC_E_* code
-int pf_launch(Ctx& c, int B, int T, const EpiArgs& eq, const EpiArgs& eo, const EpiArgs& es, const EpiArgs& ed,
-              const EpiArgs& el, const AttnArgs& aa, cudaStream_t st);
 
 }  // namespace sv
 

@@ -54,7 +54,6 @@ static void free_all(Ctx& c) {
     drop_graphs(c);
     if (c.cap_stream) cudaStreamDestroy(c.cap_stream);
     c.cap_stream = nullptr;
-    pf_destroy(c);
     tc_destroy(c);
     for (auto& r : c.prof_recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
     for (auto e : c.prof_pool) cudaEventDestroy(e);
@@ -280,23 +279,6 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     aa.l2_ahead = c.attn_l2_ahead;
 
     int rc;
-    if (fused && !last_only && logits_out != nullptr && pf_usable(c, M)) {
-        // the whole pass as one persistent kernel (same bits as the launches below)
-        EpiArgs eo = er, ed = er;
-        norm_out(eo, c.ssq_f, nullptr);      // gains of the next norm are set per layer
-        norm_out(ed, c.ssq_a, nullptr);
-        EpiArgs el{};
-        el.kind = EPI_STORE; el.M = M; el.x = logits_out; el.ldx = m.vocab;
-        norm_in(el, c.ssq_a, 0);
-        double bytes = (double)M * m.vocab * 4.0 + kv_bytes * m.n_layers;
-        for (int g = GEMM_QKV; g <= GEMM_LM; ++g) bytes += gemm_weight_bytes(c, g) * (g == GEMM_LM ? 1 : m.n_layers);
-        ProfScope ps(c, 8, bytes);
-        const int n = pf_launch(c, B, T, eq, eo, es, ed, el, aa, st);
-        if (n < 0) return n;
-        c.launches += n;
-        cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? SPEC_OK : cuda_fail("persistent pass launch", e);
-    }
     launch_embed(c, M, T, st, fused);
     c.launches += 1;
     for (int l = 0; l < m.n_layers; ++l) {
@@ -346,8 +328,6 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
 // The decoder pass of B x T tokens through a CUDA graph captured once per (B, T) (logits
 // to the internal buffer).  Falls back to eager launches while profiling.
 static int forward_graph(Ctx& c, const int* slots, int B, int T) {
-    // a single persistent launch gains nothing from a graph
-    if (c.use_tc && pf_usable(c, B * T)) return forward(c, slots, B, T, c.logits, false);
     GraphEntryLookup:
     for (auto& g : c.graphs) {
         if (g.B == B && g.T == T) {
@@ -535,7 +515,6 @@ extern "C" int spec_load_weights(spec_ctx* c, const char* const* names, const vo
     if (all && c->cfg.dtype == SPEC_BF16) {
         int rc = tc_create(*c);
         if (rc != SPEC_OK) return rc;
-        if ((rc = pf_create(*c)) != SPEC_OK) return rc;
     }
     return SPEC_OK;
 }
@@ -636,9 +615,9 @@ extern "C" int spec_kv_trim(spec_ctx* c, int B, const int32_t* seq_ids, int K, c
 }
 
 // After the stream has been synchronised: SPEC_E_TIMEOUT when a bounded wait inside a
-// tensor-core GEMM or the persistent pass gave up since the context was created.  The
-// device word stays set: the passes since then may hold wrong values, and so may the
-// GEMMs' tile counters, so the context is not to be used again.
+// tensor-core GEMM gave up since the context was created.  The device word stays set: the
+// passes since then may hold wrong values, and so may the GEMMs' tile counters, so the
+// context is not to be used again.
 static int device_status(Ctx& c) {
     int word = 0;
     if (tc_error_word(c, &word) != SPEC_OK) return set_error(SPEC_E_CUDA, "reading the device error word failed");
@@ -692,17 +671,13 @@ extern "C" int spec_set_option(spec_ctx* c, int option, int value) {
     } else if (option == SPEC_OPT_PDL) {
         c->use_pdl = value != 0;
         drop_graphs(*c);
-    } else if (option == SPEC_OPT_PERSISTENT) {
-        c->use_pf = value != 0;
-    } else if (option == SPEC_OPT_PF_ATOMS) {
-        if (value != 1 && value != 2 && value != 4) return set_error(SPEC_E_INVAL, "atoms per stage must be 1, 2 or 4");
-        c->pf_atoms = value;
-    } else if (option == SPEC_OPT_PF_L2_AHEAD) {
-        if (value < 0 || value > 256) return set_error(SPEC_E_INVAL, "L2 prefetch distance must be in [0, 256]");
-        c->pf_l2_ahead = value;
     } else if (option == SPEC_OPT_ATTN_L2_AHEAD) {
         if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "attention L2 prefetch distance must be in [0, 64]");
         c->attn_l2_ahead = value;
+        drop_graphs(*c);
+    } else if (option == SPEC_OPT_GEMM_MIN_FILL) {
+        if (value < 0 || value > 101) return set_error(SPEC_E_INVAL, "GEMM fill must be in [0, 101] percent");
+        c->gemm_min_fill = value;
         drop_graphs(*c);
     } else if (option == SPEC_OPT_L2_PREFETCH) {
         if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "L2 prefetch atoms must be in [0, 64]");

@@ -1,7 +1,6 @@
-// Device pieces of the tcgen05 skinny GEMM shared by the per-GEMM kernel and the
-// persistent decoder kernel: PTX wrappers (TMA tensor loads, tcgen05 MMA / commit / TMEM
-// loads), the shared-memory and instruction descriptors, the stream-K partition of the
-// (tile, K atom) space and the epilogue of one staged accumulator chunk.
+// Device pieces of the tcgen05 skinny GEMM: PTX wrappers (TMA tensor loads, tcgen05 MMA /
+// commit / TMEM loads), the shared-memory and instruction descriptors, the stream-K
+// partition of the (tile, K atom) space and the epilogue of one staged accumulator chunk.
 #pragma once
 
 #include <cuda.h>
@@ -158,28 +157,23 @@ __device__ __forceinline__ int epi_any(int pred) {
 
 // ---- tile geometry --------------------------------------------------------------------------
 
-__device__ __forceinline__ void tile_rows_of(int gid, const CUtensorMap* maps, int hq, int hkv, int tile,
-                                             const CUtensorMap*& m0, int& r0, const CUtensorMap*& m1, int& r1) {
+// Source of half h (rows 64h .. 64h + 63) of the 128 rows of GEMM tile `tile`: matrix `mat`
+// of the GEMM's weight list, rows row0 .. row0 + 63.  QKV stacks q, k and v (one 128-row
+// head per tile); gate/up puts the 64 gate rows of 64 outputs over the 64 up rows of the
+// same outputs (the SwiGLU epilogue pairs them); the others take 128 consecutive rows.
+__host__ __device__ inline void tile_half_rows(int gid, int hq, int hkv, int tile, int h, int& mat, int& row0) {
     if (gid == GEMM_QKV) {
         int t = tile, w = 0;
         if (t >= hq) { t -= hq; w = 1; if (t >= hkv) { t -= hkv; w = 2; } }
-        m0 = m1 = &maps[w];
-        r0 = t * TC_BM;
-        r1 = r0 + 64;
+        mat = w;
+        row0 = t * TC_BM + 64 * h;
     } else if (gid == GEMM_GU) {
-        m0 = &maps[0];
-        m1 = &maps[1];
-        r0 = r1 = tile * 64;
+        mat = h;
+        row0 = tile * 64;
     } else {
-        m0 = m1 = &maps[0];
-        r0 = tile * TC_BM;
-        r1 = r0 + 64;
+        mat = 0;
+        row0 = tile * TC_BM + 64 * h;
     }
-}
-
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
 }
 
 __device__ __forceinline__ long long range_start(long long T, int G, int c) {
@@ -222,11 +216,55 @@ __device__ __forceinline__ float4* partial_f4(float* base, int cta, int which, i
     return reinterpret_cast<float4*>(base + (((size_t)cta * 2 + which) * ntok + c0) * TC_BM) + (size_t)j * TC_BM + row;
 }
 
+// Inputs of the epilogue of the first 16-column chunk of a tile (residual values and the
+// next norm's gains; or per-token positions, RoPE pairs and KV pages), loaded before the
+// accumulator is ready so that their latency is off the end of the GEMM.
+struct EpiPre {
+    float2 v[TC_CW / 2];    // RESID: x pairs; QKV: (cos, sin)
+    int pos[TC_CW / 2], page[TC_CW / 2];
+    float2 g;               // RESID: gains of the next norm
+};
+
+__device__ __forceinline__ void epi_preload(int M, const EpiArgs& e, int tile, int etid, EpiPre& pre) {
+    const int i = etid & 63;
+    const int half = etid >> 6;
+    const int pidx = tile * 64 + i;
+    if (e.kind == EPI_RESID && e.xg_out != nullptr) {
+        const int n0 = 2 * pidx;
+        pre.g = __bfloat1622float2(
+            *reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(e.g_next) + n0));
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int m = half + 2 * j;
+            pre.v[j] = m < M ? __ldcg(reinterpret_cast<const float2*>(e.x + (size_t)(m + e.m0) * e.ldx + n0))
+                             : make_float2(0.0f, 0.0f);
+        }
+    } else if (e.kind == EPI_QKV) {
+        int hs, jq;
+        qkv_pair_rows(pidx, e.hd, hs, jq);
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int m = half + 2 * j;
+            pre.pos[j] = m < M ? e.tok_pos[m + e.m0] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int m = half + 2 * j;
+            pre.v[j] = (m < M && hs < e.hq + e.hkv) ? e.rope[(size_t)pre.pos[j] * (e.hd >> 1) + jq]
+                                                   : make_float2(1.0f, 0.0f);
+            pre.page[j] = (m < M && hs >= e.hq)
+                              ? e.block_table[(size_t)e.tok_seq[m + e.m0] * e.max_pages + (pre.pos[j] >> 4)] : 0;
+        }
+    }
+}
+
 // Epilogue of one 16-column chunk staged in xs[128][17]: 64 row pairs x 16 tokens.
 // inv_s[m] = 1/rms of token m when the GEMM consumes a normed row; red = [4 warps][16]
-// scratch of the sums of squares when it produces one.
+// scratch of the sums of squares when it produces one; pre = the chunk's inputs already
+// loaded by epi_preload (chunk c0 = 0 only), or nullptr.
 __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, const float* xs, const float* inv_s,
-                                          float (*red)[TC_CW], int tile, int c0, int etid) {
+                                          float (*red)[TC_CW], int tile, int c0, int etid,
+                                          const EpiPre* pre = nullptr) {
     const int i = etid & 63;
     const int half = etid >> 6;
     const bool adjacent = (gid == GEMM_O || gid == GEMM_DOWN || gid == GEMM_LM);
@@ -237,18 +275,24 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
         // x += acc; xg = bf16(x * g_next); per token, the tile's sum of x^2 (each warp's
         // 32 pairs by a butterfly, then the two warps of a half in order)
         const int n0 = 2 * pidx;
-        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(
-            static_cast<const __nv_bfloat16*>(e.g_next) + n0);
-        const float2 g = __bfloat1622float2(g2);
+        float2 g;
         const int wq = (etid >> 5) & 1;
         // this thread's residual pairs of the chunk's tokens, loaded together (written by
-        // other CTAs of a persistent pass: not from L1)
+        // other CTAs: not from L1)
         float2 xin[TC_CW / 2];
+        if (pre != nullptr) {
+            g = pre->g;
 #pragma unroll
-        for (int j = 0; j < TC_CW / 2; ++j) {
-            const int m = c0 + half + 2 * j;
-            xin[j] = m < M ? __ldcg(reinterpret_cast<const float2*>(e.x + (size_t)(m + e.m0) * e.ldx + n0))
-                           : make_float2(0.0f, 0.0f);
+            for (int j = 0; j < TC_CW / 2; ++j) xin[j] = pre->v[j];
+        } else {
+            g = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(e.g_next) + n0));
+#pragma unroll
+            for (int j = 0; j < TC_CW / 2; ++j) {
+                const int m = c0 + half + 2 * j;
+                xin[j] = m < M ? __ldcg(reinterpret_cast<const float2*>(e.x + (size_t)(m + e.m0) * e.ldx + n0))
+                               : make_float2(0.0f, 0.0f);
+            }
         }
 #pragma unroll
         for (int j = 0; j < TC_CW / 2; ++j) {
@@ -285,17 +329,27 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
         qkv_pair_rows(pidx, e.hd, hs, jq);
         int pos[TC_CW / 2], page[TC_CW / 2];
         float2 cs[TC_CW / 2];
+        if (pre != nullptr) {
 #pragma unroll
-        for (int j = 0; j < TC_CW / 2; ++j) {
-            const int m = c0 + half + 2 * j;
-            pos[j] = m < M ? e.tok_pos[m + e.m0] : 0;
-        }
+            for (int j = 0; j < TC_CW / 2; ++j) {
+                pos[j] = pre->pos[j];
+                cs[j] = pre->v[j];
+                page[j] = pre->page[j];
+            }
+        } else {
 #pragma unroll
-        for (int j = 0; j < TC_CW / 2; ++j) {
-            const int m = c0 + half + 2 * j;
-            cs[j] = (m < M && hs < e.hq + e.hkv) ? e.rope[(size_t)pos[j] * (e.hd >> 1) + jq] : make_float2(1.0f, 0.0f);
-            page[j] = (m < M && hs >= e.hq)
-                          ? e.block_table[(size_t)e.tok_seq[m + e.m0] * e.max_pages + (pos[j] >> 4)] : 0;
+            for (int j = 0; j < TC_CW / 2; ++j) {
+                const int m = c0 + half + 2 * j;
+                pos[j] = m < M ? e.tok_pos[m + e.m0] : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < TC_CW / 2; ++j) {
+                const int m = c0 + half + 2 * j;
+                cs[j] = (m < M && hs < e.hq + e.hkv) ? e.rope[(size_t)pos[j] * (e.hd >> 1) + jq]
+                                                     : make_float2(1.0f, 0.0f);
+                page[j] = (m < M && hs >= e.hq)
+                              ? e.block_table[(size_t)e.tok_seq[m + e.m0] * e.max_pages + (pos[j] >> 4)] : 0;
+            }
         }
 #pragma unroll
         for (int j = 0; j < TC_CW / 2; ++j) {

@@ -137,41 +137,3 @@ def test_graphs_and_pdl_change_no_bits(lib, w):
     for outs in res[1:]:
         for a, b in zip(res[0], outs):
             assert torch.equal(a, b)
-
-
-@pytest.mark.parametrize("B,K", [(1, 4), (3, 7), (4, 0), (2, 15)])
-def test_persistent_pass_matches_per_kernel_pass_bitwise(lib, w, B, K):
-    """The one-launch persistent pass (every phase handing off through global counters)
-    gives the logits and verify results of the per-kernel pass bit for bit, along a context
-    that grows and is trimmed, for every ring-stage width."""
-    from speculative_decoding_verify_token_gb300 import _lib
-    V = synth.SMALL_BF16.vocab
-    prompts = [synth.prompt_tokens(40 + b, 30 + 7 * b, V) for b in range(B)]
-    rng = np.random.default_rng(7)
-    steps = [(torch.from_numpy(rng.integers(0, V, size=(B, K)).astype(np.int32)).cuda(),
-              torch.from_numpy(rng.random((B, K + 1), dtype=np.float32)).cuda()) for _ in range(3)]
-    last = torch.tensor([p[-1] for p in prompts], dtype=torch.int32, device="cuda")
-    res = []
-    for pf, atoms in ((0, 2), (1, 2), (1, 1), (1, 4)):
-        m = make(lib, w, max_batch=B, max_ctx=256, max_k=max(K, 1))
-        m.set_option(_lib.SPEC_OPT_PERSISTENT, pf)
-        m.set_option(_lib.SPEC_OPT_PF_ATOMS, atoms)
-        for b, p in enumerate(prompts):
-            m.prefill(b, torch.from_numpy(p[:-1]).cuda())
-        outs = []
-        cur = last.clone()
-        for drafts, u in steps:
-            n0 = m.launches()
-            r = m.verify(list(range(B)), cur, drafts, u, 1.0, top_k=20, top_p=0.95, want_logits=True)
-            if pf:
-                # pass + token layout + fused verify + length update
-                assert m.launches() - n0 == 4
-            outs.append((r["logits"].clone(), r["accepted_len"].clone(), r["next_token"].clone()))
-            cur = r["next_token"].clone()
-        res.append(outs)
-        m.close()
-    for outs in res[1:]:
-        for (la, aa, na), (lb, ab, nb) in zip(res[0], outs):
-            assert torch.equal(la, lb)
-            assert torch.equal(aa, ab)
-            assert torch.equal(na, nb)
