@@ -200,14 +200,27 @@ typedef struct spec_ctx spec_ctx;
  * n_q_heads a multiple of n_kv_heads), SPEC_E_NOMEM when an allocation fails. */
 int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* limits, void* stream, spec_ctx** out);
 
-/* Borrow the weights: never copied, the caller keeps them alive ([MTP-fixes] "Duplicate
- * weights in unified memory": a second resident copy is what to avoid).  names[i] is
- * one of "embed" [V][d], "final_norm" [d], "lm_head" [V][d], and per layer l
- * "layers.<l>.attn_norm" [d], ".wq" [hq*hd][d], ".wk" [hkv*hd][d], ".wv" [hkv*hd][d],
- * ".wo" [d][hq*hd], ".ffn_norm" [d], ".wg" [F][d], ".wu" [F][d], ".wd" [d][F];
- * dev_ptrs[i] a row-major device array of the model dtype, 16-byte aligned.  Missing
- * names are SPEC_E_STATE at the first forward. */
+/* Load the weights.  names[i] is one of "embed" [V][d], "final_norm" [d], "lm_head" [V][d],
+ * and per layer l "layers.<l>.attn_norm" [d], ".wq" [hq*hd][d], ".wk" [hkv*hd][d],
+ * ".wv" [hkv*hd][d], ".wo" [d][hq*hd], ".ffn_norm" [d], ".wg" [F][d], ".wu" [F][d],
+ * ".wd" [d][F]; dev_ptrs[i] a row-major device array of the model dtype, 16-byte aligned.
+ * Missing names are SPEC_E_STATE at the first forward.
+ * Ownership: float32 models borrow every array (never copied; the caller keeps them
+ * alive).  bf16 models on the tensor-core path copy the matrices of the GEMMs (wq, wk, wv,
+ * wo, wg, wu, wd, lm_head) once, when the last weight arrives, into a library-owned
+ * tile-major buffer (the same bytes in the order the tensor cores consume them, so that
+ * a pipeline stage is one contiguous copy) and never read the caller's GEMM matrices
+ * again: the caller may free them after this call (spec_weights_copied returns 1), and
+ * should, since a second resident copy of the weights is what to avoid ([MTP-fixes]
+ * "Duplicate weights in unified memory").  "embed" and the norm gains stay borrowed.
+ * Changes the caller makes to its GEMM matrices later are not seen.  SPEC_E_NOMEM when
+ * the copy cannot be allocated. */
 int spec_load_weights(spec_ctx* ctx, const char* const* names, const void* const* dev_ptrs, int n);
+
+/* 1 when the context holds its own copy of the GEMM matrices (all weights loaded, bf16
+ * tensor-core path), so that the caller's GEMM arrays are no longer read; else 0.
+ * (No counterpart on the pages: weight ownership of this library.) */
+int spec_weights_copied(const spec_ctx* ctx);
 
 /* Ingest tokens[0..n) (device int32) of sequence slot seq_id after what it already holds
  * (chunks of prefill_chunk tokens, the same kernels as the verify pass).  When

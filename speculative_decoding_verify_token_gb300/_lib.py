@@ -79,6 +79,7 @@ SIGNATURES = {
     "spec_create": (c_int, [ctypes.POINTER(SpecModelCfg), ctypes.POINTER(SpecCtxLimits), c_vp,
                             ctypes.POINTER(c_vp)]),
     "spec_load_weights": (c_int, [c_vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(c_vp), c_int]),
+    "spec_weights_copied": (c_int, [c_vp]),
     "spec_prefill": (c_int, [c_vp, c_int, c_vp, c_int, c_vp]),
     "spec_verify": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp, c_vp, c_vp, c_vp, c_vp,
                             ctypes.POINTER(SpecSampling), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int]),

@@ -519,6 +519,8 @@ extern "C" int spec_load_weights(spec_ctx* c, const char* const* names, const vo
     return SPEC_OK;
 }
 
+extern "C" int spec_weights_copied(const spec_ctx* c) { return c && c->use_tc ? 1 : 0; }
+
 static int common_checks(spec_ctx* c) {
     if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
     if (!c->weights_ready) return set_error(SPEC_E_STATE, "weights not (fully) loaded");

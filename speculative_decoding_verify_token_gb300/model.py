@@ -45,6 +45,10 @@ class SpecModel:
         carr = (ctypes.c_char_p * len(names))(*names)
         parr = (ctypes.c_void_p * len(ptrs))(*ptrs)
         _lib.check(lib.spec_load_weights(h, carr, parr, len(names)))
+        if lib.spec_weights_copied(h):
+            # the library keeps its own tile-major copy of the GEMM matrices and reads only
+            # the embedding and the norm gains from these tensors from now on
+            self._weights = {n: t for n, t in self._weights.items() if n == "embed" or n.endswith("norm")}
         V = shape.vocab
         self.V = V
 

@@ -71,3 +71,19 @@ def test_generators_are_seeded():
     assert not np.array_equal(a["target"], synth.verify_logits_case(8, 2, 2, 300)["target"])
     assert np.array_equal(synth.prompt_tokens(1, 50, 99), synth.prompt_tokens(1, 50, 99))
     assert np.array_equal(synth.uniforms(2, (3, 4)), synth.uniforms(2, (3, 4)))
+
+
+def test_c_weight_generator_matches_torch_generator():
+    """The C generator behind the float64 oracle copies of large models gives the torch
+    generator's values bit for bit (bf16 and fp32 models, several tensors and offsets)."""
+    from synth import fastgen
+    for shape, name in ((synth.QWEN_8B, "layers.3.wk"), (synth.SMALL_BF16, "lm_head"),
+                        (synth.TINY_TARGET, "layers.1.wg"), (synth.DRAFT_0P8B, "layers.0.wo")):
+        ref = synth.model_weight(shape, name).double().numpy()
+        got = fastgen.model_weight_f64(shape, name)
+        assert got.shape == ref.shape
+        assert np.array_equal(got, ref), (shape.name, name)
+    key = synth.tensor_key(5, "x", "y")
+    ref = synth.normal_tensor(key, (3, 1000), 0.5, dtype=__import__("torch").float32).double().numpy()
+    buf = np.empty(5000)
+    assert np.array_equal(fastgen.normal_f64(key, (3, 1000), 0.5, bf16=False, out=buf), ref)
