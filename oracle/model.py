@@ -7,10 +7,12 @@ plain attention layer is rolled back by slicing off the rejected entries ([SD-Ap
 "Why this needed a patch to mlx_lm at all").
 
 For the bf16 model configurations the KV cache holds keys and values in the model's
-dtype, as the pages' bf16 runtimes do (mlx-optiq "Speculative decoding on Apple Silicon",
-section "Assistant drafter: Gemma-4", traces its verify/decode differences to bf16
-attention precision): each key and value is rounded to bfloat16 (nearest, ties to even)
-when it enters the cache.  Everything else stays float64.
+dtype: the batched-serving workload keeps them in a paged bf16 cache, and the same cache
+holds the keys of the other bf16 models (the pages' bf16 runtimes attend in bf16 too:
+mlx-optiq "Speculative decoding on Apple Silicon", section "Assistant drafter: Gemma-4").
+Each key and value is rounded to bfloat16 (nearest, ties to even) when it enters the
+cache; everything else stays float64.  kv="f64" keeps the cache in float64 as well (the
+all-float64 reading, against which the bf16 results are also reported).
 
 The decoder itself is not printed on the pages; it is the plain Llama/Qwen-style
 reading: x = E[tok]; per layer h = RMSNorm(x), q,k,v = h W_q^T, h W_k^T, h W_v^T,
@@ -125,11 +127,13 @@ class KVList:
 
 
 class Decoder:
-    """shape: synth.ModelShape; weights: callable name -> float64 array (or a dict)."""
+    """shape: synth.ModelShape; weights: callable name -> float64 array (or a dict);
+    kv: "model" (bf16 keys and values for bf16 models) or "f64"."""
 
-    def __init__(self, shape, weights):
+    def __init__(self, shape, weights, kv="model"):
+        assert kv in ("model", "f64")
         self.s = shape
-        self.kv_bf16 = shape.dtype == "bf16"     # the cache stores the model dtype
+        self.kv_bf16 = shape.dtype == "bf16" and kv == "model"     # the cache stores the model dtype
         if isinstance(weights, dict):
             cache = {}
 
@@ -144,6 +148,24 @@ class Decoder:
 
     def new_cache(self):
         return KVList(self.s.n_layers)
+
+    def append_first_layer_kv(self, tokens, cache):
+        """One-layer models: append the keys and values of `tokens` at positions
+        len(cache).. without computing their attention outputs or logits.  A layer's keys
+        and values depend only on that layer's input, which for the first layer is the
+        embedding, so this is the cache forward() would build; it lets long contexts be set
+        up without the O(T^2) attention of every prompt position."""
+        s, w = self.s, self.w
+        assert s.n_layers == 1
+        tokens = np.asarray(tokens, dtype=np.int64)
+        T = tokens.size
+        pos = len(cache) + np.arange(T)
+        h = rmsnorm(w("embed")[tokens], w("layers.0.attn_norm"), s.rms_eps)
+        k = rope((h @ w("layers.0.wk").T).reshape(T, s.n_kv_heads, s.head_dim), pos, s.rope_theta)
+        v = (h @ w("layers.0.wv").T).reshape(T, s.n_kv_heads, s.head_dim)
+        if self.kv_bf16:
+            k, v = round_bf16(k), round_bf16(v)
+        cache.append(0, k, v)
 
     def forward(self, tokens, cache, logits_rows=None):
         """Run tokens at positions len(cache).. and append their K/V to cache.

@@ -132,6 +132,49 @@ def test_bf16_shape_caches_rounded_keys():
     assert not np.array_equal(c32.k[0], om.round_bf16(c32.k[0]))
 
 
+
+def test_f64_kv_reading_keeps_unrounded_keys():
+    """kv="f64" skips the bf16 rounding of keys and values and nothing else: the cache holds
+    keys that are not all bf16 values, rounding them gives the default cache exactly, the
+    incremental forward still equals the full one, and the logits move by far less than
+    the 3e-2 logit tolerance but not by nothing."""
+    s = synth.SMALL_BF16
+    w = {n: synth.model_weight(s, n) for n in synth.weight_names(s)}
+    toks = synth.prompt_tokens(3, 9, s.vocab)
+    o16, o64 = om.Decoder(s, w), om.Decoder(s, w, kv="f64")
+    c16, c64 = o16.new_cache(), o64.new_cache()
+    l16 = o16.forward(toks, c16)
+    l64 = o64.forward(toks, c64)
+    assert not np.array_equal(c64.k[0], om.round_bf16(c64.k[0]))
+    np.testing.assert_array_equal(om.round_bf16(c64.k[0]), c16.k[0])
+    np.testing.assert_array_equal(om.round_bf16(c64.v[0]), c16.v[0])
+    d = np.max(np.abs(l16 - l64))
+    assert 0 < d < 1e-2, d
+    c = o64.new_cache()
+    inc = np.concatenate([o64.forward(toks[:4], c)] + [o64.forward([t], c) for t in toks[4:]])
+    np.testing.assert_allclose(inc, l64, rtol=1e-9, atol=1e-9)
+
+
+@pytest.mark.parametrize("kv", ["model", "f64"])
+def test_first_layer_cache_builder_equals_forward(kv):
+    """append_first_layer_kv builds the cache forward() builds on a one-layer model: the rows
+    of a verify pass after it equal the same rows of one forward over the whole sequence."""
+    import dataclasses
+    s = dataclasses.replace(synth.SMALL_BF16, n_layers=1)
+    w = {n: synth.model_weight(synth.SMALL_BF16, n) for n in synth.weight_names(s)}
+    o = om.Decoder(s, w, kv=kv)
+    toks = synth.prompt_tokens(4, 40, s.vocab)
+    full_cache = o.new_cache()
+    full = o.forward(toks, full_cache)
+    c = o.new_cache()
+    o.append_first_layer_kv(toks[:30], c)
+    o.append_first_layer_kv(toks[30:35], c)
+    rows = o.forward(toks[35:], c)
+    np.testing.assert_array_equal(c.k[0], full_cache.k[0])
+    np.testing.assert_array_equal(c.v[0], full_cache.v[0])
+    np.testing.assert_allclose(rows, full[35:], rtol=0, atol=1e-12)
+
+
 # ---- hand-worked closed forms of the layer ----------------------------------------------
 
 def test_rope_pairs_and_frequencies():

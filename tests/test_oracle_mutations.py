@@ -60,7 +60,10 @@ def model_pins():
             tm.test_single_token_layer_closed_form, tm.test_round_bf16_ties_and_library,
             lambda: tm.test_incremental_equals_full_forward(_tiny()),
             lambda: tm.test_trim_invariant(_tiny()),
-            tm.test_zero_blocks_reduce_to_embedding_readout, tm.test_bf16_shape_caches_rounded_keys]
+            tm.test_zero_blocks_reduce_to_embedding_readout, tm.test_bf16_shape_caches_rounded_keys,
+            tm.test_f64_kv_reading_keeps_unrounded_keys,
+            functools.partial(tm.test_first_layer_cache_builder_equals_forward, "model"),
+            functools.partial(tm.test_first_layer_cache_builder_equals_forward, "f64")]
 
 
 def generate_pins():
@@ -199,7 +202,8 @@ MODEL_MUTANTS = [
     ("FFN residual dropped", [("            x = x + (silu(", "            x = (silu(")]),
     ("final norm missing", [('        hf = rmsnorm(x, w("final_norm"), s.rms_eps)', "        hf = x")]),
     ("lm_head tied to the embedding", [('        return hf @ w("lm_head").T', '        return hf @ w("embed").T')]),
-    ("positions ignore the cache", [("        pos = len(cache) + np.arange(T)", "        pos = np.arange(T)")]),
+    ("positions ignore the cache",
+     [("        pos = len(cache) + np.arange(T)\n        x = w(", "        pos = np.arange(T)\n        x = w(")]),
     ("trim keeps one entry too many",
      [("                self.k[l] = self.k[l][:n]\n                self.v[l] = self.v[l][:n]",
        "                self.k[l] = self.k[l][:n + 1]\n                self.v[l] = self.v[l][:n + 1]")]),
@@ -209,6 +213,18 @@ MODEL_MUTANTS = [
      [("    return np.ldexp(np.round(np.ldexp(m, 8)), e - 8)",
        "    return np.ldexp(np.sign(m) * np.floor(np.abs(np.ldexp(m, 8)) + 0.5), e - 8)")]),
     ("bf16 cache keeps unrounded keys", [("            if self.kv_bf16:", "            if False:")]),
+    ("float64-KV reading still rounds the cache",
+     [('        self.kv_bf16 = shape.dtype == "bf16" and kv == "model"', '        self.kv_bf16 = shape.dtype == "bf16"')]),
+    ("first-layer cache builder ignores the cache length",
+     [("        pos = len(cache) + np.arange(T)\n        h = rmsnorm(", "        pos = np.arange(T)\n        h = rmsnorm(")]),
+    ("first-layer cache builder skips the attention norm",
+     [('        h = rmsnorm(w("embed")[tokens], w("layers.0.attn_norm"), s.rms_eps)', '        h = w("embed")[tokens]')]),
+    ("first-layer cache builder keeps unrounded keys",
+     [("        if self.kv_bf16:\n            k, v = round_bf16(k), round_bf16(v)\n        cache.append(0, k, v)",
+       "        cache.append(0, k, v)")]),
+    ("first-layer cache builder skips RoPE",
+     [('        k = rope((h @ w("layers.0.wk").T).reshape(T, s.n_kv_heads, s.head_dim), pos, s.rope_theta)',
+       '        k = (h @ w("layers.0.wk").T).reshape(T, s.n_kv_heads, s.head_dim)')]),
 ]
 
 GENERATE_MUTANTS = [
