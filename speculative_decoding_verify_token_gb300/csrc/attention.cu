@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnArgs a) {
     sm.Qs = sm.Vs + MMA_SPLIT * MMA_PITCH;
     sm.Qlo = sm.Qs + MMA_RT * MMA_PITCH;
     sm.Ps = sm.Qlo + MMA_RT * MMA_PITCH;
+    sm.Plo = sm.Ps + MMA_RT * MMA_PPITCH;
     sm.wmax = wmax;
     sm.wsum = wsum;
     // keys of earlier passes load before the wait for the QKV GEMM (programmatic launch)
@@ -294,7 +295,9 @@ __global__ void __launch_bounds__(128) attn_mma_multi_kernel(const AttnArgs a, i
         const int k0 = s * MMA_SPLIT;
         const int nk = min(MMA_SPLIT, Ltot - k0);
         const size_t pbase = (((size_t)b * a.hkv + g) * a.n_chunks + s) * R;
-        attn_mma_tile(a, kbuf(s), kbuf(s) + MMA_SPLIT * MMA_PITCH, Qs, Qlo, Ps, wmax, wsum, qsplit, 0, R,
+        // one row tile per item here (R <= MMA_RT), so the split's keys are dead once its
+        // scores are taken and the probabilities' lo halves go in their place
+        attn_mma_tile(a, kbuf(s), kbuf(s) + MMA_SPLIT * MMA_PITCH, Qs, Qlo, Ps, kbuf(s), wmax, wsum, qsplit, 0, R,
                       max(0, k0 - L0) * G, k0, nk, L0, G, pbase, sl2, tid, [] { __syncthreads(); });
         __syncthreads();             // this half of the buffer is refilled two splits on
     }

@@ -17,14 +17,14 @@ constexpr int MMA_RT = 64;                     // query rows per tile (4 m16 til
 constexpr int MMA_PITCH = 136;                 // bf16 row pitch of K, V, Q in smem (272 B)
 constexpr int MMA_PPITCH = 72;                 // bf16 row pitch of P (144 B)
 
-// Shared memory of one attention item: K, V, Q, Q lo [64][MMA_PITCH] and P [64][MMA_PPITCH]
-// bf16 (dynamic) and the per-warp row statistics.
+// Shared memory of one attention item: K, V, Q, Q lo [64][MMA_PITCH] and P, P lo
+// [64][MMA_PPITCH] bf16 (dynamic) and the per-warp row statistics.
 struct AttnSmem {
-    __nv_bfloat16 *Ks, *Vs, *Qs, *Qlo, *Ps;     // Qlo: lo halves of split queries
+    __nv_bfloat16 *Ks, *Vs, *Qs, *Qlo, *Ps, *Plo;     // Qlo, Plo: lo halves of split values
     float (*wmax)[MMA_RT];
     float (*wsum)[MMA_RT];
 };
-constexpr size_t MMA_SMEM = sizeof(__nv_bfloat16) * ((size_t)4 * 64 * MMA_PITCH + (size_t)MMA_RT * MMA_PPITCH);
+constexpr size_t MMA_SMEM = sizeof(__nv_bfloat16) * ((size_t)4 * 64 * MMA_PITCH + (size_t)2 * MMA_RT * MMA_PPITCH);
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
@@ -56,9 +56,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // item, in Qs / Qlo rows 0 .. nr) against the nk keys in Ks / Vs starting at key k0, and the
 // tile's per-split (max, sum, unnormalised output) for rows >= row_lo.  Each row's bits
 // depend only on the row, the keys and the split, not on the other rows of the tile.
+// The probabilities enter P V as bf16 hi + lo halves (Ps, Plo), like the split queries:
+// rounded to bf16 alone (8 significant bits) they moved the logits of one 8B-width layer
+// by up to 1e-2, which compounds over tens of layers.  Plo is written only after every
+// warp has finished reading Ks, so it may alias Ks when the tile is the item's only one.
 template <class Sync>
 __device__ __forceinline__ void attn_mma_tile(const AttnArgs& a, const __nv_bfloat16* Ks, const __nv_bfloat16* Vs,
                                               const __nv_bfloat16* Qs, const __nv_bfloat16* Qlo, __nv_bfloat16* Ps,
+                                              __nv_bfloat16* Plo,
                                               float (*wmax)[MMA_RT], float (*wsum)[MMA_RT], bool qsplit, int rt,
                                               int nr, int row_lo, int k0, int nk, int L0, int G, size_t pbase,
                                               float sl2, int tid, Sync sync) {
@@ -123,7 +128,7 @@ __device__ __forceinline__ void attn_mma_tile(const AttnArgs& a, const __nv_bflo
         }
     }
     sync();
-    // p = 2^(s - m), per-warp row sums, P to smem (bf16)
+    // p = 2^(s - m), per-warp row sums, P to smem (bf16 hi and lo)
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
         if (mt >= mtiles) continue;
@@ -139,7 +144,11 @@ __device__ __forceinline__ void attn_mma_tile(const AttnArgs& a, const __nv_bflo
                 const float p1 = exp2f(sacc[mt][nt][h * 2 + 1] - m);
                 sum += p0;
                 sum += p1;
-                *reinterpret_cast<uint32_t*>(Ps + row * MMA_PPITCH + warp * 16 + nt * 8 + 2 * tq) = pack_bf16(p0, p1);
+                const uint32_t hi = pack_bf16(p0, p1);
+                const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+                *reinterpret_cast<uint32_t*>(Ps + row * MMA_PPITCH + warp * 16 + nt * 8 + 2 * tq) = hi;
+                *reinterpret_cast<uint32_t*>(Plo + row * MMA_PPITCH + warp * 16 + nt * 8 + 2 * tq) =
+                    pack_bf16(p0 - hf.x, p1 - hf.y);
             }
             sum += __shfl_xor_sync(FULL, sum, 1);
             sum += __shfl_xor_sync(FULL, sum, 2);
@@ -171,6 +180,11 @@ __device__ __forceinline__ void attn_mma_tile(const AttnArgs& a, const __nv_bflo
                 const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
                 const int col = ks * 16 + (lane >> 4) * 8;
                 ldsm_x4(smem_u32(Ps + row * MMA_PPITCH + col), a0, a1, a2, a3);
+                mma16816(oacc[mt][0], a0, a1, a2, a3, v[0], v[1]);
+                mma16816(oacc[mt][1], a0, a1, a2, a3, v[2], v[3]);
+                mma16816(oacc[mt][2], a0, a1, a2, a3, v[4], v[5]);
+                mma16816(oacc[mt][3], a0, a1, a2, a3, v[6], v[7]);
+                ldsm_x4(smem_u32(Plo + row * MMA_PPITCH + col), a0, a1, a2, a3);
                 mma16816(oacc[mt][0], a0, a1, a2, a3, v[0], v[1]);
                 mma16816(oacc[mt][1], a0, a1, a2, a3, v[2], v[3]);
                 mma16816(oacc[mt][2], a0, a1, a2, a3, v[4], v[5]);
@@ -282,7 +296,8 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
         cp_async_wait_all();
         sync();
 
-        attn_mma_tile(a, Ks, Vs, Qs, Qlo, Ps, wmax, wsum, qsplit, rt, nr, 0, k0, nk, L0, G, pbase, sl2, tid, sync);
+        attn_mma_tile(a, Ks, Vs, Qs, Qlo, Ps, sm.Plo, wmax, wsum, qsplit, rt, nr, 0, k0, nk, L0, G, pbase, sl2, tid,
+                      sync);
     }
     return true;
 }

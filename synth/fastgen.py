@@ -69,3 +69,47 @@ def model_weight_f64(shape: ModelShape, name: str, seed: int = 0, std: float = 0
     if name.endswith("norm"):
         return np.ones(shp, dtype=np.float64)
     return normal_f64(tensor_key(seed, shape.name, name), shp, std, bf16=shape.dtype != "f32", out=out)
+
+
+class EmbedRowsF64:
+    """The embedding table of `shape` as float64 rows generated on demand (only the rows an
+    index asks for), for the oracle decoder's x = embed[tokens]."""
+
+    def __init__(self, shape: ModelShape, seed: int = 0, std: float = 0.02):
+        self.key = tensor_key(seed, shape.name, "embed")
+        self.d = shape.d_model
+        self.scale = float(np.float32(std / 131072.0))
+        self.bf16 = shape.dtype != "f32"
+
+    def __getitem__(self, idx):
+        idx = np.asarray(idx, dtype=np.int64)
+        uniq, inv = np.unique(idx.reshape(-1), return_inverse=True)
+        rows = np.empty((uniq.size, self.d), dtype=np.float64)
+        lib = _load()
+        for i, r in enumerate(uniq):
+            lib.synth_normal_f64(self.key & 0xFFFFFFFFFFFFFFFF, int(r) * self.d, self.d, self.scale,
+                                 1 if self.bf16 else 0, rows[i].ctypes.data)
+        return rows[inv].reshape(idx.shape + (self.d,))
+
+
+class WeightsF64:
+    """weights(name) -> float64 copy of gen.model_weight(shape, name, seed), generated on the
+    CPU one tensor at a time for the oracle decoder (which reads each tensor once, right
+    away).  Arrays of one shape share a buffer: a returned array stays valid only until the
+    next call for a tensor of the same shape."""
+
+    def __init__(self, shape: ModelShape, seed: int = 0):
+        self.shape, self.seed = shape, seed
+        self.embed = EmbedRowsF64(shape, seed)
+        self.bufs = {}
+
+    def __call__(self, name):
+        if name == "embed":
+            return self.embed
+        shp = weight_shape(self.shape, name)
+        if name.endswith("norm"):
+            return np.ones(shp, dtype=np.float64)
+        buf = self.bufs.get(shp)
+        if buf is None:
+            buf = self.bufs[shp] = np.empty(int(np.prod(shp)), dtype=np.float64)
+        return model_weight_f64(self.shape, name, self.seed, out=buf)

@@ -87,3 +87,18 @@ def test_c_weight_generator_matches_torch_generator():
     ref = synth.normal_tensor(key, (3, 1000), 0.5, dtype=__import__("torch").float32).double().numpy()
     buf = np.empty(5000)
     assert np.array_equal(fastgen.normal_f64(key, (3, 1000), 0.5, bf16=False, out=buf), ref)
+
+
+def test_oracle_weight_providers_match_generator():
+    """The on-demand float64 providers the oracle reads large models through give the
+    generator's values: gathered embedding rows (repeats, any order) and whole tensors
+    through a reused buffer."""
+    from synth import fastgen
+    s = synth.SMALL_BF16
+    w = fastgen.WeightsF64(s)
+    ref = synth.model_weight(s, "embed").double().numpy()
+    idx = np.array([[5, 7, 5], [4095, 0, 7]])
+    assert np.array_equal(w("embed")[idx], ref[idx])
+    for name in ("layers.1.wd", "layers.0.wo", "layers.0.wq", "lm_head"):
+        assert np.array_equal(w(name), synth.model_weight(s, name).double().numpy()), name
+    assert np.array_equal(w("layers.0.attn_norm"), np.ones(s.d_model))
