@@ -261,28 +261,24 @@ class DenseVerifyWorkload:
         self.m.profile(False)
         return prof
 
-    def roofline(self, prof, peaks):
-        g = [prof[k] for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head")]
-        kernel = "tc_gemm_kernel"
-        ms = sum(x["ms"] for x in g)
-        n = sum(x["launches"] for x in g)
-        by = sum(x["bytes"] for x in g)
-        achieved = (by / n) / (ms / n / 1e3) / 1e9
-        traffic = None
-        if kernel == "tc_gemm_kernel":
-            # DRAM bytes (read + write) of the current tc_gemm_kernel from one ncu capture of
-            # a 2-layer slice of this shape (profiles/tc_gemm_kernel-dense-8b-2layer-slice.md,
-            # --cache-control none, so that each GEMM's L2 prefetch of the next one's first
-            # weight atoms counts once): 402.1 MB per layer (QKV, O, gate/up, down) and
-            # 1227.6 MB for lm_head, scaled to the layers run; re-take it when the kernel
-            # changes
-            L = self.shape.n_layers
-            traffic = (L * 402.1e6 + 1227.6e6) / (4 * L + 1)
+    def roofline(self, prof, peaks, ms_per_step=None, profile_steps=1):
+        """The graphed verify step as the unit: its algorithmic bytes (the weights of every GEMM,
+        the KV pages read and written, the logits) over the timed step's CUDA-event time."""
+        step_bytes = sum(v["bytes"] for v in prof.values()) / profile_steps
+        achieved = step_bytes / (ms_per_step / 1e3) / 1e9
+        L = self.shape.n_layers
+        # DRAM bytes (read + write) of every kernel of one graphed verify step, from an ncu
+        # capture of a 2-layer slice of this shape (--cache-control none), scaled to L layers
+        # by the per-layer share (every layer moves the same weights); None until re-taken
+        # after a change to the kernels
+        traffic = (L * STEP_TRAFFIC_PER_LAYER + STEP_TRAFFIC_FIXED) if STEP_TRAFFIC_PER_LAYER else None
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": kernel,
-                "traffic_unit": "bytes per launch",
-                "algorithmic_bytes_per_launch": by / n, "launches_measured": n,
-                "avg_launch_us": ms / n * 1e3, "peak_source": peaks["source"]}
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": f"verify step: the graphed pass ({4 * L + 1} tc_gemm_kernel, {L} attention + "
+                          f"{L} combine, embed, 2 verify, length update)",
+                "traffic_unit": "bytes per step", "algorithmic_bytes_per_launch": step_bytes,
+                "avg_launch_us": ms_per_step * 1e3, "launch_unit": "one graphed verify step",
+                "peak_source": peaks["source"]}
 
     # end to end through the C ABI with host buffers
     def e2e(self, n):
@@ -312,54 +308,53 @@ class DenseVerifyWorkload:
         return emitted / dt, 4 + 4 * self.K + 4 * (self.K + 1), 8
 
     def oracle_sample(self, budget_s):
-        """The float64 oracle on a bounded sample of the same step: the verify pass of step 0's
-        5 tokens through 2 of the 36 layers (weights held in float64 after a first load) plus
-        final norm + lm_head, at a context of 63 tokens; the per-layer time is scaled to 36."""
-        import torch
-        from oracle import model as om
-        from oracle import verify as ov
-        s = self.shape
-        L_s = 2
-        class Rows:
-            """Embedding rows converted on demand (the oracle only indexes it)."""
-            def __init__(self, t):
-                self.t = t
+        """The float64 oracle timed on the same verify step as the GPU's (dense_oracle_step):
+        as many whole steps as fit the budget (at least one)."""
+        step, sample = dense_oracle_step(self.shape, self.K, self.alpha)
+        n, t0 = 0, time.perf_counter()
+        emitted = 0.0
+        while n == 0 or time.perf_counter() - t0 < budget_s:
+            emitted += step()
+            n += 1
+        return emitted / (time.perf_counter() - t0), f"{n} step(s): " + sample
 
-            def __getitem__(self, idx):
-                return om.to_f64(self.t[torch.as_tensor(np.asarray(idx), device=self.t.device)])
 
-        w = {"embed": Rows(self.weights["embed"])}
-        need = ["final_norm", "lm_head"] + [n for n in self.weights if n.startswith("layers.0.") or
-                                            n.startswith("layers.1.")]
-        for n in need:
-            w[n] = om.to_f64(self.weights[n])
-        import dataclasses
-        sub = dataclasses.replace(s, n_layers=L_s)
-        dec = om.Decoder(sub, w)
-        toks = [int(self.d_last[0][0])] + [int(x) for x in self.d_drafts[0][0].tolist()]
-        prefix = self.prompt[:63].cpu().numpy()
+def dense_oracle_step(shape, K, alpha):
+    """One float64 oracle verify step of the 8B workload, for the CPU baseline and the
+    reference arm: the verify pass of K + 1 tokens through all L layers at a context of 63
+    tokens (every layer uses layer 0's weights, generated once, so that the weights held on
+    the host stay at one layer's; the cost per layer is the same), the full-vocabulary
+    lm_head and the greedy rule; no prefill inside the step.  The scripted drafter's
+    decisions need the real model, so a step counts the closed-form mean of
+    (1 - alpha^(K+1)) / (1 - alpha) emitted tokens."""
+    import copy
+    from synth import fastgen
+    from oracle import model as om
+    from oracle import verify as ov
+    import synth
+    held = {}
 
-        def run():
-            cache = dec.new_cache()
-            dec.forward(prefix, cache)
-            t0 = time.perf_counter()
-            rows = dec.forward(toks, cache)
-            ov.verify_greedy(rows, toks[1:])
-            return time.perf_counter() - t0
+    def w(name):
+        base = name if not name.startswith("layers.") else "layers.0." + name.split(".", 2)[2]
+        if base not in held:
+            held[base] = fastgen.EmbedRowsF64(shape) if base == "embed" else fastgen.model_weight_f64(shape, base)
+        return held[base]
 
-        run()
-        # split the timed pass into layers and lm_head: time the lm_head part alone
-        x = np.random.default_rng(0).normal(size=(5, s.d_model))
-        t0 = time.perf_counter()
-        _ = x @ w["lm_head"].T
-        t_lm = time.perf_counter() - t0
-        t_pass = min(run() for _ in range(2))
-        t_layers = max(t_pass - t_lm, 1e-9)
-        t_step = t_layers * s.n_layers / L_s + t_lm
-        emitted_per_step = (1 - self.alpha ** (self.K + 1)) / (1 - self.alpha)
-        return emitted_per_step / t_step, (f"float64 verify pass of 5 tokens through {L_s} of {s.n_layers} layers "
-                                           f"(context 63) + lm_head, per-layer time scaled to {s.n_layers} layers; "
-                                           f"{emitted_per_step:.4f} emitted tokens per step (closed form)")
+    dec = om.Decoder(shape, w)
+    cache0 = dec.new_cache()
+    dec.forward(synth.prompt_tokens(1, 63, shape.vocab), cache0, logits_rows=np.zeros(0, dtype=np.int64))
+    toks = [int(t) for t in synth.prompt_tokens(2, K + 1, shape.vocab)]
+    per_step = (1 - alpha ** (K + 1)) / (1 - alpha)
+
+    def step():
+        cache = copy.deepcopy(cache0)
+        rows = dec.forward(toks, cache)
+        ov.verify_greedy(rows, toks[1:])
+        return per_step
+
+    return step, (f"float64 oracle verify pass of {K + 1} tokens through {shape.n_layers} layers (context 63, every "
+                  f"layer with layer 0's weights) + the {shape.vocab}-row lm_head + the greedy rule, no prefill in "
+                  f"the step; {per_step:.4f} emitted tokens per step (closed form at acceptance {alpha})")
 
 
 # ---- workload: 27B target + 0.8B draft under sampling -------------------------------------
@@ -828,8 +823,8 @@ class VerifyLogitsWorkload:
         avg = sum(prof) / len(prof)
         achieved = self.bytes_per_step() / (avg / 1e3) / 1e9
         # DRAM bytes (read + write) of both verify kernels from one ncu capture of this
-        # workload (profiles/verify_kernel-verify-logits-b64-k4.md; caches flushed per
-        # kernel): pass 1 350.09 + 5.36 MB, pass 2 4.41 MB; re-take it when they change
+        # workload (caches flushed per kernel): pass 1 350.09 + 5.36 MB, pass 2 4.41 MB;
+        # re-take it when they change
         traffic = 350.09e6 + 5.36e6 + 4.41e6 if (self.B, self.K, self.V) == (64, 4, 151936) else None
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "verify_kernel",
@@ -875,9 +870,43 @@ class VerifyLogitsWorkload:
                               "float64 numpy, one process")
 
 
+def verify_kernel_timing(dev, peaks, n=20):
+    """The standalone fused verify (B = 64, K = 4, fp32 logits of 151,936 entries) timed with
+    CUDA events on its stream: two 350 MB input sets alternate (above L2), 3 warm-up calls."""
+    import torch
+    vl = VerifyLogitsWorkload()
+    vl.setup(dev, n + 3)
+    for i in range(3):
+        vl.step(i)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(n):
+        vl.step(3 + i)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / n * 1e3
+    gbs = vl.bytes_per_step() / (us / 1e6) / 1e9
+    ok, _ = vl.check(3, n)
+    out = {"us_per_call": us, "algorithmic_bytes": vl.bytes_per_step(), "achieved_gbs": gbs,
+           "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0, "outputs_checked": ok}
+    del vl
+    torch.cuda.empty_cache()
+    return out
+
+
 WORKLOADS = {DenseVerifyWorkload.name: DenseVerifyWorkload, VerifyLogitsWorkload.name: VerifyLogitsWorkload,
              ServingWorkload.name: ServingWorkload, SamplingWorkload.name: SamplingWorkload}
 DEFAULT_WORKLOAD = DenseVerifyWorkload.name
+# DRAM bytes (read + write) of one graphed 8B verify step (see DenseVerifyWorkload.roofline),
+# from an ncu capture of a 2-layer slice with --cache-control none: per layer (the four
+# GEMMs, attention and combine: 386.8 and 386.9 MB in the two layers) and the rest of the
+# step (embed, lm_head, verify kernels, length update); in that capture the small slice's KV
+# pages stay in L2, so the full model's attention reads (about 4.3 MB per layer at a
+# context of 1.1K) are not in it.  0 = not captured for the current kernels.
+STEP_TRAFFIC_PER_LAYER = 386.9e6
+STEP_TRAFFIC_FIXED = 1247.7e6
 
 
 def run_reference(args):
@@ -1013,35 +1042,8 @@ def reference_serving_step(wl):
 
 
 def reference_dense_step(wl):
-    """One bounded oracle step of the 8B workload: the verify pass of 5 tokens through one
-    layer of the 8B shape (float64, weights drawn on the CPU from the same seeded
-    generator), counted as 1/36 of a verify step that emits the closed-form mean of
-    (1 - 0.7^5) / 0.3 tokens."""
-    import dataclasses
-    import synth
-    from oracle import model as om
-    from oracle import verify as ov
-    s = wl.shape
-    sub = dataclasses.replace(s, n_layers=1, vocab=4096)
-    names = [n for n in synth.weight_names(sub) if n.startswith("layers.0.")]
-    w = {n: om.to_f64(synth.model_weight(s, n, seed=0)) for n in names}
-    w["embed"] = om.to_f64(synth.model_weight(sub, "embed", seed=0))
-    w["final_norm"] = np.ones(s.d_model)
-    w["lm_head"] = om.to_f64(synth.model_weight(sub, "lm_head", seed=0))
-    dec = om.Decoder(sub, w)
-    prompt = synth.prompt_tokens(1, 63, sub.vocab)
-    toks = [int(t) for t in synth.prompt_tokens(2, 5, sub.vocab)]
-    per_step = (1 - wl.alpha ** (wl.K + 1)) / (1 - wl.alpha)
-
-    def step():
-        cache = dec.new_cache()
-        dec.forward(prompt, cache)
-        rows = dec.forward(toks, cache)
-        ov.verify_greedy(rows, toks[1:])
-        return per_step / s.n_layers
-
-    return step, ("float64 oracle verify pass of 5 tokens through 1 of the 36 layers of the 8B shape "
-                  "(context 63; counted as 1/36 of a step emitting the closed-form 2.7731 tokens)")
+    """The same oracle verify step as the CPU baseline of the 8B workload."""
+    return dense_oracle_step(wl.shape, wl.K, wl.alpha)
 
 
 def main():
@@ -1053,6 +1055,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-verify-kernel", action="store_true",
+                    help="skip the standalone verify-kernel timing added to the 8B workload's line")
     ap.add_argument("--profile-steps", type=int, default=10)
     ap.add_argument("--gen", type=int, default=512, help="tokens of the recorded greedy trajectory (8B workload)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the 8B shape (profiler captures only)")
@@ -1119,14 +1123,27 @@ def main():
         dec_ms = wl.decode_ms(20)
         extra["decode_ms_per_step"] = dec_ms
         extra["verify_over_decode"] = (total_ms / args.steps) / dec_ms
+        # the value counts the tokens the sampled draft lengths gave; the closed-form mean of
+        # the scripted drafter, (1 - a^(K+1)) / (1 - a), gives the expected rate
+        per_step = (1 - wl.alpha ** (wl.K + 1)) / (1 - wl.alpha)
+        extra["emitted_per_step_sampled"] = emitted / (world * args.steps)
+        extra["emitted_per_step_expected"] = per_step
+        extra["value_at_expected_emission"] = per_step * world / (total_ms / args.steps / 1e3)
     prof = wl.profile(args.profile_steps)
-    roof = wl.roofline(prof, peaks)
+    if isinstance(wl, DenseVerifyWorkload):
+        roof = wl.roofline(prof, peaks, ms_per_step=total_ms / args.steps, profile_steps=args.profile_steps)
+    else:
+        roof = wl.roofline(prof, peaks)
     if isinstance(prof, dict):
-        extra["kernel_breakdown_ms_per_step"] = {k: v["ms"] / args.profile_steps for k, v in prof.items()}
+        # an eager pass with CUDA events around every launch (no graph, no overlap between
+        # kernels): where the time goes, not the timed step
+        extra["kernel_breakdown_ms_per_step_instrumented"] = {k: v["ms"] / args.profile_steps for k, v in prof.items()}
         step_bytes = sum(v["bytes"] for v in prof.values()) / args.profile_steps
         extra["step_algorithmic_bytes"] = step_bytes
         extra["step_hbm_gbs"] = step_bytes / (total_ms / args.steps / 1e3) / 1e9
         extra["step_frac_of_8tbs"] = extra["step_hbm_gbs"] / 8000.0
+    if isinstance(wl, DenseVerifyWorkload) and not args.no_verify_kernel:
+        extra["verify_kernel_b64_k4"] = verify_kernel_timing(dev, peaks)
     e2e_val, h2d, d2h = wl.e2e(max(5, min(args.steps, 20)))
     e2e_val = e2e_val * world
     if isinstance(wl, SamplingWorkload):

@@ -113,14 +113,6 @@ int spec_verify_logits(int B, int K, int V,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
- * Sample one token from each of R rows of logits [R][V] (fp32) under the same
- * truncation, by inverse CDF over ascending token id with uniforms[r]; greedy (argmax)
- * when temperature == 0.  This is how a draft model's token is drawn from its truncated
- * distribution q ([MTP-fixes] "Truncation has to match on both sides").
- * out_tokens [R] (device); -1 for a row without a finite logit when sampling.  Workspace
- * rules as for spec_verify_logits.
- * ---------------------------------------------------------------------------------- */
-/* ------------------------------------------------------------------------------------
  * spec_verify_logits without a caller workspace, for callers that cannot allocate
  * device memory: for example code that runs while a CUDA graph is being captured (where
  * cudaMalloc is not allowed), a serving loop that must not stall on the allocator,
@@ -134,7 +126,9 @@ int spec_verify_logits(int B, int K, int V,
  * SPEC_E_RANGE.  The call allocates nothing: no cudaMalloc/cudaFree or allocating library
  * routine.  The first call on a device looks up the array's device address once
  * (cudaGetSymbolAddress, with that device current) and caches it: make that first call
- * before any stream capture.  Every call shares the one array (what must start at zero is
+ * before any stream capture.  The cached address (like the kernel attributes the
+ * library sets once per device) belongs to the device's primary context: after
+ * cudaDeviceReset on that device the library is not to be used again in the process.  Every call shares the one array (what must start at zero is
  * cleared on the stream at each call), so calls that overlap on the GPU -- on different
  * streams, or from several host threads -- race and must be serialised by the caller.
  * ---------------------------------------------------------------------------------- */
@@ -147,6 +141,14 @@ int spec_verify_logits_noalloc(int B, int K, int V,
                                int32_t* accepted_len, int32_t* next_token,
                                int32_t* out_ids, float* out_probs, int32_t* seq_status, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * Sample one token from each of R rows of logits [R][V] (fp32) under the same
+ * truncation, by inverse CDF over ascending token id with uniforms[r]; greedy (argmax)
+ * when temperature == 0.  This is how a draft model's token is drawn from its truncated
+ * distribution q ([MTP-fixes] "Truncation has to match on both sides").
+ * out_tokens [R] (device); -1 for a row without a finite logit when sampling.  Workspace
+ * rules as for spec_verify_logits.
+ * ---------------------------------------------------------------------------------- */
 size_t spec_sample_logits_workspace_bytes(int R, int V);
 
 int spec_sample_logits(int R, int V, const float* logits, const float* uniforms,

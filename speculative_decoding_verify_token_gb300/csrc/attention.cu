@@ -2,14 +2,20 @@
 //
 // For each (sequence, kv head) the T*G query rows (T positions x G = hq/hkv query heads)
 // share one pass over the sequence's KV pages.  The keys are split at fixed absolute
-// positions (SPLIT keys, a multiple of the 16-token page); one CTA per (split, kv head,
-// sequence) loads all pages of its split with 1-D bulk copies on the TMA engine (each
-// page-head block is a contiguous 16 x head_dim run) and computes, per visible row, the
-// split's max, sum and unnormalised output.  The last CTA of a (sequence, kv head) to
-// finish (atomic arrival count, no spin-wait) combines a row's splits 0..pos/SPLIT in
-// order.  Every row is computed on its own in a fixed order of operations that depends
-// only on its absolute position, so a token gets the same bits whether it is decoded
-// alone (T = 1) or verified together with K drafts (T = K + 1).
+// positions (64-key splits on the tensor-core path, a multiple of the 16-token page):
+//  * attn_mma_kernel: one CTA per (split, kv head, sequence); it copies the split's keys and
+//    values with 16-byte cp.async -- the keys of earlier passes before it waits for the QKV
+//    GEMM (programmatic launch), this pass's keys and the queries after -- and writes the
+//    split's per-row max, sum and unnormalised output (mma.sync bf16, queries and
+//    probabilities as bf16 hi + lo);
+//  * attn_mma_multi_kernel (long contexts): one CTA per run of consecutive splits, with the
+//    same per-split arithmetic and K/V double-buffered;
+//  * a combine kernel per row then reduces the row's splits 0..pos/64 in a fixed order
+//    (attn_combine128_kernel up to 512 splits, attn_combine_kernel beyond).
+// Every row is computed on its own in a fixed order of operations that depends only on
+// its absolute position, so a token gets the same bits whether it is decoded alone
+// (T = 1) or verified together with K drafts (T = K + 1).  The SIMT kernels (float32
+// models, other head dims) follow the same split / combine structure with bulk copies.
 #include <cuda_bf16.h>
 #include <cmath>
 

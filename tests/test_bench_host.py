@@ -69,3 +69,14 @@ def test_workloads_registered():
     import bench
     assert set(bench.WORKLOADS) == {"dense-8b-verify-k4", "verify-logits-b64-k4", "serving-8b-b32-k8",
                                     "sampling-27b-0p8b"}
+
+
+def test_dense_oracle_step_is_one_whole_verify_step():
+    """The CPU baseline and the reference arm time the same oracle step: K + 1 tokens through
+    every layer plus the lm_head, counted at the scripted drafter's closed-form mean."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    step, sample = bench.dense_oracle_step(synth.SMALL_BF16, 4, 0.7)
+    assert abs(step() - (1 - 0.7 ** 5) / 0.3) < 1e-12
+    assert "through 2 layers" in sample and "4096-row lm_head" in sample
