@@ -425,16 +425,10 @@ class SamplingWorkload:
         e0.record()
         if self.extra is not None:
             self.d.prefill(0, self.extra)
-        toks, rows = [], []
-        tok = self.pending
         if ud is None:
-            ud = torch.from_numpy(self.gd.random(K, dtype=np.float32)).to(dev, non_blocking=True)
-        for i in range(K):
-            tok, lg = self.d.decode([0], tok, ud[i:i + 1], self.T, self.k, self.p, want_logits=True)
-            toks.append(tok)
-            rows.append(lg)
-        drafts = torch.stack(toks, dim=1)
-        dl = torch.stack(rows, dim=1)
+            ud = torch.from_numpy(self.gd.random((1, K), dtype=np.float32)).to(dev, non_blocking=True)
+        # the draft's K tokens in one device-resident loop (spec_draft, one graph per K)
+        drafts, dl = self.d.draft([0], self.pending, K, ud.view(1, K), self.T, self.k, self.p, want_logits=True)
         if u is None:
             u = torch.from_numpy(self.g.random((1, K + 1), dtype=np.float32)).to(dev, non_blocking=True)
         e1.record()

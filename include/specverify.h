@@ -257,6 +257,22 @@ int spec_decode(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* tok
                 const spec_sampling* sampling, const float* uniforms, int32_t* next_token,
                 float* out_logits);
 
+/* Draft K tokens with this (draft) model without returning to the host between them
+ * ([SD-Apple] "The original result: Qwen3-8B": the draft's K passes are sequential, a
+ * fixed cost per round that grows with K).  Runs the kernels of K spec_decode calls back
+ * to back on the device: step i decodes row i's token and draws the next from its logits
+ * (truncated as `sampling` says, inverse CDF with uniforms[b][i]; greedy at temperature
+ * 0), which is the input of step i + 1.  The K steps are replayed from one CUDA graph per
+ * (B, K, sampling, logits wanted), captured on first use.  tokens [B] (device int32): each
+ * sequence's pending token; uniforms [B][K] (device fp32, required also when greedy);
+ * out_tokens [B][K] (device int32): the drafts d_1..d_K; out_logits [B][K][V] (device
+ * fp32, may be NULL): the logits each draft was drawn from (the draft rows of
+ * spec_verify).  KV: appends the pending token and d_1..d_{K-1} (K entries), as K
+ * spec_decode calls do; the same bits as those calls.  1 <= K <= max_k; errors as
+ * spec_verify. */
+int spec_draft(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int32_t* tokens,
+               const spec_sampling* sampling, const float* uniforms, int32_t* out_tokens, float* out_logits);
+
 /* Trim after a verify pass run with auto_trim == 0: keep accepted_len[b] + 1 of the
  * K + 1 entries it appended (device O(1) length update).  accepted_len (device int32 [B])
  * is clamped to [0, K], so a trim never reaches below the entries the pass appended. */
@@ -273,6 +289,15 @@ int spec_seq_len(spec_ctx* ctx, int seq_id, int32_t* out_len);
  * status is sticky and the context must be destroyed.  SPEC_E_CUDA on a stream error.
  * (No counterpart on the pages: the library's own failure reporting.) */
 int spec_sync(spec_ctx* ctx);
+
+/* Check of the failure path above: launch one bounded wait (the GEMM kernels' own wait
+ * helper, with a budget of budget_ms milliseconds, 1..2000) on a barrier that nothing
+ * completes.  The wait runs out, records SPEC_E_TIMEOUT in the context's device status
+ * word and the kernel returns -- no copy in flight, no tensor memory held -- so the next
+ * spec_sync returns SPEC_E_TIMEOUT and the context is spent, while the GPU and other
+ * contexts stay usable.  bf16 tensor-core contexts only (SPEC_E_STATE otherwise).
+ * (No counterpart on the pages: the library's own failure reporting.) */
+int spec_check_wait_timeout(spec_ctx* ctx, int budget_ms);
 
 /* Empty a slot and return its pages to the pool. */
 int spec_seq_reset(spec_ctx* ctx, int seq_id);

@@ -86,9 +86,12 @@ SIGNATURES = {
     "spec_decode": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_vp, ctypes.POINTER(SpecSampling), c_vp,
                             c_vp, c_vp]),
     "spec_kv_trim": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp]),
+    "spec_draft": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp, ctypes.POINTER(SpecSampling), c_vp,
+                           c_vp, c_vp]),
     "spec_seq_len": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32)]),
     "spec_seq_reset": (c_int, [c_vp, c_int]),
     "spec_sync": (c_int, [c_vp]),
+    "spec_check_wait_timeout": (c_int, [c_vp, c_int]),
     "spec_kernel_launches": (ctypes.c_longlong, [c_vp]),
     "spec_profile": (c_int, [c_vp, c_int]),
     "spec_set_option": (c_int, [c_vp, c_int, c_int]),

@@ -58,13 +58,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false when the
-// budget ran out (the caller records an error and stops using the barrier).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// budget (nanoseconds of %globaltimer) ran out; the caller records an error and stops using
+// the barrier.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long budget_ns = WAIT_BUDGET_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > WAIT_BUDGET_NS) return false;
+        if (globaltimer_ns() - t0 > budget_ns) return false;
     }
 }
 

@@ -599,6 +599,25 @@ extern "C" int spec_debug_tc_trace(unsigned long long* out) {
 }
 #endif
 
+// One bounded wait, by the GEMM kernel's wait helper, on an mbarrier that nothing
+// completes: no copy is in flight and no tensor memory is held, so when the budget runs out
+// the thread records SPEC_E_TIMEOUT in the context's device status word, exactly as a GEMM
+// wait that gave up would, and the kernel returns.
+__global__ void wait_probe_kernel(int* err, unsigned long long budget_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    if (!mbar_wait(smem_u32(&bar), 0, budget_ns)) atomicExch(err, SPEC_E_TIMEOUT);
+}
+
+int tc_wait_probe(Ctx& c, int budget_ms) {
+    if (!c.tc) return set_error(SPEC_E_STATE, "no tensor-core GEMM plan (bf16 model with all weights loaded)");
+    wait_probe_kernel<<<1, 32, 0, c.stream>>>(c.tc->err, (unsigned long long)budget_ms * 1000000ull);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : set_error(SPEC_E_CUDA, "wait_probe_kernel launch: %s", cudaGetErrorString(e));
+}
+
 int tc_error_word(Ctx& c, int* out) {
     if (!c.tc) { *out = 0; return SPEC_OK; }
     return cudaMemcpy(out, c.tc->err, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess ? SPEC_OK : SPEC_E_CUDA;

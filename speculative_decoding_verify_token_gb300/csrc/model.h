@@ -118,6 +118,15 @@ struct Ctx {
     cudaStream_t cap_stream = nullptr;     // private stream the graphs are captured on
     struct GraphEntry { int B, T; cudaGraphExec_t exec; long long kernels; };
     std::vector<GraphEntry> graphs;
+    // device-resident drafting loop (spec_draft): tokens [max_k + 1][max_batch] (row i =
+    // the input of step i), uniforms [max_k][max_batch], logits [max_k][max_batch][V], one
+    // graph per (B, K, sampling, logits wanted)
+    int* d_draft_tok = nullptr;
+    float* d_draft_u = nullptr;
+    float* d_draft_logits = nullptr;
+    int* d_draft_acc = nullptr;
+    struct DraftGraph { int B, K, top_k, want_logits; float temperature, top_p; cudaGraphExec_t exec; long long kernels; };
+    std::vector<DraftGraph> draft_graphs;
     // tensor-core GEMM
     TcGemm* tc = nullptr;
     bool use_tc = false;
@@ -132,6 +141,9 @@ void launch_rope_table(float2* table, int max_pos, int hd, double theta, cudaStr
 void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens, int B, cudaStream_t st);
 void launch_advance_len(const int* seq_ids, int* seq_len, int B, int mode, int add, const int* accepted, int K,
                         cudaStream_t st);
+// dst[c * ldd + r] = src[r * lds + c] for r < R, c < C (int32 / float32)
+void launch_transpose_i32(const int* src, int lds, int* dst, int ldd, int R, int C, cudaStream_t st);
+void launch_transpose_f32(const float* src, int lds, float* dst, int ldd, int R, int C, cudaStream_t st);
 struct EpiArgs;
 void launch_gemm_simt(const Ctx& c, const void* wa, const void* wb, const void* wc, int K, int n_pairs,
                       const void* X, const EpiArgs& e, cudaStream_t st);
@@ -147,6 +159,7 @@ void tc_destroy(Ctx& c);
 int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, int pass_M, const EpiArgs& e, cudaStream_t st);
 bool tc_supported(const Ctx& c);
 int tc_error_word(Ctx& c, int* out);          // device error word of the tensor-core GEMM (synchronous)
+int tc_wait_probe(Ctx& c, int budget_ms);     // one bounded wait that runs out (failure-path check)
 
 }  // namespace sv
 

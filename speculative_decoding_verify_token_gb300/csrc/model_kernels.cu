@@ -161,6 +161,23 @@ __global__ void advance_len_kernel(const int* __restrict__ seq_ids, int* __restr
     else seq_len[slot] -= K - a;
 }
 
+// dst[c * ldd + r] = src[r * lds + c] for r < R, c < C.
+template <typename E>
+__global__ void transpose_kernel(const E* __restrict__ src, int lds, E* __restrict__ dst, int ldd, int R, int C) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R * C) return;
+    const int r = i / C, c = i - r * C;
+    dst[(size_t)c * ldd + r] = src[(size_t)r * lds + c];
+}
+
+void launch_transpose_i32(const int* src, int lds, int* dst, int ldd, int R, int C, cudaStream_t st) {
+    transpose_kernel<int><<<(R * C + 255) / 256, 256, 0, st>>>(src, lds, dst, ldd, R, C);
+}
+
+void launch_transpose_f32(const float* src, int lds, float* dst, int ldd, int R, int C, cudaStream_t st) {
+    transpose_kernel<float><<<(R * C + 255) / 256, 256, 0, st>>>(src, lds, dst, ldd, R, C);
+}
+
 void launch_embed(const Ctx& c, int M, int T, cudaStream_t st, bool fused_norm) {
     if (c.cfg.dtype == SPEC_BF16) {
         using bf = __nv_bfloat16;

@@ -25,6 +25,7 @@ namespace sv {
 int verify_into(int B, int K, int V, const float* target, const float* draft, const int* draft_tokens,
                 const int* draft_len, const float* u, const spec_sampling* s, int* accepted, int* next, int* out_ids,
                 float* out_probs, int* status, void* ws, size_t ws_bytes, cudaStream_t st);
+int verify_prepare();
 
 static int cuda_fail(const char* what, cudaError_t e) {
     return set_error(SPEC_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -48,6 +49,8 @@ static int dalloc(Ctx& c, P** p, size_t bytes, bool zero = false) {
 static void drop_graphs(Ctx& c) {
     for (auto& g : c.graphs) cudaGraphExecDestroy(g.exec);
     c.graphs.clear();
+    for (auto& g : c.draft_graphs) cudaGraphExecDestroy(g.exec);
+    c.draft_graphs.clear();
 }
 
 static void free_all(Ctx& c) {
@@ -366,6 +369,35 @@ static int forward_graph(Ctx& c, const int* slots, int B, int T) {
     goto GraphEntryLookup;
 }
 
+// K decode steps of the draft model on the device: step i embeds row i of d_draft_tok,
+// runs the decoder pass, samples each sequence's token from its truncated distribution
+// with uniform d_draft_u[i][b] (greedy at temperature 0) into row i + 1, copies the step's
+// logits to d_draft_logits[i] when wanted, and advances the lengths by one.  Exactly the
+// kernels of K spec_decode calls, in the same order, so the drafts are the same bits.
+static int draft_steps(Ctx& c, const int* slots, int B, int K, const spec_sampling* s, bool want_logits) {
+    const int V = c.cfg.vocab;
+    int rc;
+    for (int i = 0; i < K; ++i) {
+        cudaError_t e = cudaMemcpyAsync(c.d_tokens, c.d_draft_tok + (size_t)i * c.lim.max_batch, sizeof(int) * B,
+                                        cudaMemcpyDeviceToDevice, c.stream);
+        if (e != cudaSuccess) return cuda_fail("draft token copy", e);
+        if ((rc = forward(c, slots, B, 1, c.logits, false, true)) != SPEC_OK) return rc;
+        if (want_logits) {
+            e = cudaMemcpyAsync(c.d_draft_logits + (size_t)i * c.lim.max_batch * V, c.logits, sizeof(float) * B * V,
+                                cudaMemcpyDeviceToDevice, c.stream);
+            if (e != cudaSuccess) return cuda_fail("draft logits copy", e);
+        }
+        rc = verify_into(B, 0, V, c.logits, nullptr, nullptr, nullptr, c.d_draft_u + (size_t)i * c.lim.max_batch, s,
+                         c.d_draft_acc, c.d_draft_tok + (size_t)(i + 1) * c.lim.max_batch, nullptr, nullptr,
+                         c.d_status_scratch, c.vws, c.vws_bytes, c.stream);
+        if (rc != SPEC_OK) return rc;
+        launch_advance_len(c.d_seq_ids, c.d_seq_len, B, 0, 1, nullptr, 0, c.stream);
+        c.launches += 3;
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("draft step launch", e);
+}
+
 }  // namespace sv
 
 using namespace sv;
@@ -603,6 +635,88 @@ extern "C" int spec_decode(spec_ctx* c, int B, const int32_t* seq_ids, const int
                        c->d_status_scratch, next_token, nullptr, nullptr, nullptr, out_logits, 1);
 }
 
+extern "C" int spec_draft(spec_ctx* c, int B, const int32_t* seq_ids, int K, const int32_t* tokens,
+                          const spec_sampling* sampling, const float* uniforms, int32_t* out_tokens,
+                          float* out_logits) {
+    clear_error();
+    int rc = common_checks(c);
+    if (rc != SPEC_OK) return rc;
+    if ((rc = check_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    if (K < 1 || K > c->lim.max_k) return set_error(SPEC_E_INVAL, "K=%d outside [1, %d]", K, c->lim.max_k);
+    if (!tokens || !sampling || !uniforms || !out_tokens) return set_error(SPEC_E_INVAL, "NULL required pointer");
+    const int V = c->cfg.vocab, Bm = c->lim.max_batch;
+    if (!c->d_draft_tok) {
+        if ((rc = dalloc(*c, &c->d_draft_tok, sizeof(int) * (size_t)(c->lim.max_k + 1) * Bm, true)) != SPEC_OK ||
+            (rc = dalloc(*c, &c->d_draft_u, sizeof(float) * (size_t)c->lim.max_k * Bm, true)) != SPEC_OK ||
+            (rc = dalloc(*c, &c->d_draft_logits, sizeof(float) * (size_t)c->lim.max_k * Bm * V)) != SPEC_OK ||
+            (rc = dalloc(*c, &c->d_draft_acc, sizeof(int) * (size_t)Bm)) != SPEC_OK)
+            return rc;
+    }
+    if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    if ((rc = ensure_pages(*c, seq_ids, B, K)) != SPEC_OK) return rc;
+    // inputs into the context's own buffers (a graph replays fixed addresses): the pending
+    // tokens as row 0, the uniforms [B][K] as rows [K][max_batch]
+    cudaError_t e = cudaMemcpyAsync(c->d_draft_tok, tokens, sizeof(int) * B, cudaMemcpyDeviceToDevice, c->stream);
+    if (e != cudaSuccess) return cuda_fail("token copy", e);
+    launch_transpose_f32(uniforms, K, c->d_draft_u, Bm, B, K, c->stream);
+    const bool want_logits = out_logits != nullptr;
+    const spec_sampling s = *sampling;
+    if (!c->use_graphs || c->prof_on) {
+        if ((rc = draft_steps(*c, seq_ids, B, K, &s, want_logits)) != SPEC_OK) return rc;
+    } else {
+        cudaGraphExec_t exec = nullptr;
+        for (auto& g : c->draft_graphs)
+            if (g.B == B && g.K == K && g.want_logits == (int)want_logits && g.temperature == s.temperature &&
+                g.top_k == s.top_k && g.top_p == s.top_p) {
+                exec = g.exec;
+                c->launches += g.kernels;
+                break;
+            }
+        if (!exec) {
+            if ((rc = verify_prepare()) != SPEC_OK) return set_error(SPEC_E_CUDA, "verify kernel attributes");
+            // capture on the context's private stream (the caller's may be the legacy stream)
+            cudaGraph_t graph = nullptr;
+            cudaStream_t saved = c->stream;
+            c->stream = c->cap_stream;
+            e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
+            if (e != cudaSuccess) {
+                c->stream = saved;
+                return cuda_fail("cudaStreamBeginCapture", e);
+            }
+            const long long l0 = c->launches;
+            rc = draft_steps(*c, seq_ids, B, K, &s, want_logits);
+            const long long n = c->launches - l0;
+            e = cudaStreamEndCapture(c->stream, &graph);
+            c->stream = saved;
+            if (rc != SPEC_OK) {
+                if (graph) cudaGraphDestroy(graph);
+                return rc;
+            }
+            if (e != cudaSuccess) return cuda_fail("cudaStreamEndCapture", e);
+            e = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (e != cudaSuccess) return cuda_fail("cudaGraphInstantiate", e);
+            c->draft_graphs.push_back({B, K, s.top_k, (int)want_logits, s.temperature, s.top_p, exec, n});
+        }
+        e = cudaGraphLaunch(exec, c->stream);
+        if (e != cudaSuccess) return cuda_fail("cudaGraphLaunch", e);
+    }
+    // outputs: token rows 1..K -> [B][K]; logits rows [K][max_batch][V] -> [B][K][V]
+    launch_transpose_i32(c->d_draft_tok + Bm, Bm, out_tokens, K, K, B, c->stream);
+    if (want_logits) {
+        for (int i = 0; i < K; ++i) {
+            e = cudaMemcpy2DAsync(out_logits + (size_t)i * V, sizeof(float) * (size_t)K * V,
+                                  c->d_draft_logits + (size_t)i * Bm * V, sizeof(float) * (size_t)V,
+                                  sizeof(float) * (size_t)V, B, cudaMemcpyDeviceToDevice, c->stream);
+            if (e != cudaSuccess) return cuda_fail("draft logits copy", e);
+        }
+    }
+    for (int b = 0; b < B; ++b) c->len_hi[seq_ids[b]] += K;
+    c->launches += 2;
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_draft", e);
+}
+
 extern "C" int spec_kv_trim(spec_ctx* c, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len) {
     clear_error();
     if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
@@ -636,6 +750,13 @@ extern "C" int spec_sync(spec_ctx* c) {
     const cudaError_t e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
     return device_status(*c);
+}
+
+extern "C" int spec_check_wait_timeout(spec_ctx* c, int budget_ms) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    if (budget_ms < 1 || budget_ms > 2000) return set_error(SPEC_E_INVAL, "budget_ms=%d outside [1, 2000]", budget_ms);
+    return tc_wait_probe(*c, budget_ms);
 }
 
 extern "C" int spec_seq_len(spec_ctx* c, int seq_id, int32_t* out_len) {

@@ -893,6 +893,9 @@ static int device_setup() {
     return n;
 }
 
+// Attributes of the verify kernels on the current device, set before any stream capture.
+int verify_prepare() { return device_setup() > 0 ? SPEC_OK : SPEC_E_CUDA; }
+
 static int launch_verify(VerifyParams& prm, const Plan& pl, void* ws, cudaStream_t st) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     prm.blk_next = reinterpret_cast<int*>(w + pl.off_blk);

@@ -49,15 +49,9 @@ def spec_generate(target, draft, prompt, n_new, K, seq=0, temperature=0.0, top_k
     while len(out) < n_new:
         if extra is not None:
             draft.prefill(seq, extra)
-        drafts, dlogits = [], []
-        tok = pending
-        for i in range(K):
-            ud = torch.from_numpy(gd.random(1, dtype=np.float32)).to(dev)
-            tok, lg = draft.decode([seq], tok, ud, temperature, top_k, top_p, want_logits=True)
-            drafts.append(tok)
-            dlogits.append(lg)
-        d = torch.stack(drafts, dim=1)                                    # [1, K]
-        dl = torch.stack(dlogits, dim=1) if temperature > 0 else None     # [1, K, V]
+        # the draft's K tokens in one device-resident loop (K decode steps, no host round trip)
+        ud = torch.from_numpy(gd.random((1, K), dtype=np.float32)).to(dev)
+        d, dl = draft.draft([seq], pending, K, ud, temperature, top_k, top_p, want_logits=temperature > 0)
         u = torch.from_numpy(g.random((1, K + 1), dtype=np.float32)).to(dev)
         r = target.verify([seq], pending, d, u, temperature, top_k, top_p, draft_logits=dl)
         a = int(r["accepted_len"].item())

@@ -112,6 +112,19 @@ class SpecModel:
                                         _ptr(nxt), _ptr(logits)))
         return (nxt, logits) if want_logits else nxt
 
+    def draft(self, seq_ids, tokens, K, uniforms, temperature=0.0, top_k=20, top_p=0.95, want_logits=False):
+        """K draft tokens per sequence from this model in one device-resident loop (no host
+        round trip between them); returns (drafts [B, K] int32, logits [B, K, V] or None)."""
+        B = len(seq_ids)
+        _need(tokens, torch.int32, (B,), "tokens")
+        _need(uniforms, torch.float32, (B, K), "uniforms")
+        out = torch.empty(B, K, dtype=torch.int32, device=self.device)
+        logits = torch.empty(B, K, self.V, dtype=torch.float32, device=self.device) if want_logits else None
+        s = sampling(temperature, top_k, top_p)
+        _lib.check(self.lib.spec_draft(self.h, B, _ids(seq_ids), int(K), _ptr(tokens), ctypes.byref(s), _ptr(uniforms),
+                                       _ptr(out), _ptr(logits)))
+        return out, logits
+
     def kv_trim(self, seq_ids, K, accepted_len):
         _lib.check(self.lib.spec_kv_trim(self.h, len(seq_ids), _ids(seq_ids), int(K), _ptr(accepted_len)))
 
@@ -127,6 +140,11 @@ class SpecModel:
         """Wait for the context's stream; raises SpecError (SPEC_E_TIMEOUT) if a device-side
         wait gave up since the context was created."""
         _lib.check(self.lib.spec_sync(self.h))
+
+    def check_wait_timeout(self, budget_ms=50):
+        """Run one bounded device wait that runs out (see spec_check_wait_timeout); the next
+        sync() raises SpecError(SPEC_E_TIMEOUT) and the context is spent."""
+        _lib.check(self.lib.spec_check_wait_timeout(self.h, int(budget_ms)))
 
     def launches(self):
         return int(self.lib.spec_kernel_launches(self.h))

@@ -129,6 +129,8 @@ def test_context_argument_validation(lib):
     assert lib.spec_set_option(None, _lib.SPEC_OPT_GRAPHS, 1) == _lib.SPEC_E_INVAL
     assert lib.spec_load_weights(None, None, None, 0) == _lib.SPEC_E_INVAL
     assert lib.spec_sync(None) == _lib.SPEC_E_INVAL
+    assert lib.spec_check_wait_timeout(None, 50) == _lib.SPEC_E_INVAL
+    assert lib.spec_weights_copied(None) == 0
     assert lib.spec_kernel_launches(None) == 0
     lib.spec_destroy(None)
 

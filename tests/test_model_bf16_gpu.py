@@ -137,3 +137,78 @@ def test_graphs_and_pdl_change_no_bits(lib, w):
     for outs in res[1:]:
         for a, b in zip(res[0], outs):
             assert torch.equal(a, b)
+
+
+def test_device_wait_that_runs_out_is_reported(lib, w):
+    """A bounded device wait that runs out (the GEMM kernels' wait helper on a barrier that
+    nothing completes, no copy in flight) is reported by the next sync as SPEC_E_TIMEOUT,
+    stays reported (the context is spent), and leaves the GPU usable: the kernel returned
+    after its budget and a fresh context still verifies correctly."""
+    import time
+    from speculative_decoding_verify_token_gb300 import _lib
+    m = make(lib, w, max_batch=1, max_ctx=64, max_k=4)
+    m.sync()                                     # nothing has run out yet
+    with pytest.raises(_lib.SpecError) as e:
+        m.check_wait_timeout(0)                  # budget outside [1, 2000] ms
+    assert e.value.code == _lib.SPEC_E_INVAL
+    t0 = time.perf_counter()
+    m.check_wait_timeout(50)
+    with pytest.raises(_lib.SpecError) as e:
+        m.sync()
+    assert e.value.code == _lib.SPEC_E_TIMEOUT
+    assert time.perf_counter() - t0 < 10.0
+    with pytest.raises(_lib.SpecError) as e:
+        m.sync()
+    assert e.value.code == _lib.SPEC_E_TIMEOUT
+    m.close()
+    m2 = make(lib, w, max_batch=1, max_ctx=64, max_k=4)
+    p = synth.prompt_tokens(1, 20, synth.SMALL_BF16.vocab)
+    m2.prefill(0, torch.from_numpy(p[:-1]).cuda())
+    r = m2.verify([0], torch.tensor(p[-1:], dtype=torch.int32, device="cuda"),
+                  torch.zeros(1, 4, dtype=torch.int32, device="cuda"), torch.zeros(1, 5, device="cuda"), 0.0,
+                  want_logits=True)
+    m2.sync()
+    g = ov.verify_greedy(r["logits"][0].double().cpu().numpy(), [0, 0, 0, 0])
+    assert (int(r["accepted_len"].item()), int(r["next_token"].item())) == (g["a"], g["next"])
+    m2.close()
+
+
+@pytest.mark.parametrize("temperature,graphs", [(0.0, 1), (1.0, 1), (1.0, 0)])
+def test_draft_loop_equals_per_token_decodes(lib, w, temperature, graphs):
+    """spec_draft's device-resident loop gives the drafts and draft logits of K separate
+    decode calls bit for bit (greedy and sampled, two sequences of different lengths, from a
+    graph and eagerly), leaves the same KV lengths, and a second call continues the same way."""
+    from speculative_decoding_verify_token_gb300 import _lib
+    V, K, B = synth.SMALL_BF16.vocab, 5, 2
+    prompts = [synth.prompt_tokens(60 + b, 20 + 9 * b, V) for b in range(B)]
+    u = torch.from_numpy(synth.uniforms(61, (2, B, K))).cuda()
+    res = []
+    for mode in ("loop", "calls"):
+        m = make(lib, w, max_batch=B, max_ctx=128, max_k=K)
+        m.set_option(_lib.SPEC_OPT_GRAPHS, graphs)
+        for b, p in enumerate(prompts):
+            m.prefill(b, torch.from_numpy(p[:-1]).cuda())
+        pend = torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32, device="cuda")
+        outs = []
+        for r in range(2):
+            if mode == "loop":
+                d, lg = m.draft(list(range(B)), pend, K, u[r].contiguous(), temperature, 20, 0.95, want_logits=True)
+            else:
+                toks, rows = [], []
+                tok = pend
+                for i in range(K):
+                    tok, l1 = m.decode(list(range(B)), tok, u[r, :, i].contiguous(), temperature, 20, 0.95,
+                                       want_logits=True)
+                    toks.append(tok)
+                    rows.append(l1)
+                d, lg = torch.stack(toks, 1), torch.stack(rows, 1)
+            outs.append((d.clone(), lg.clone()))
+            pend = d[:, -1].contiguous()
+        m.sync()
+        res.append((outs, [m.seq_len(b) for b in range(B)]))
+        m.close()
+    (lo, ll), (co, cl) = res
+    assert ll == cl == [len(p) - 1 + 2 * K for p in prompts]
+    for (dl_, gl), (dc, gc) in zip(lo, co):
+        assert torch.equal(dl_, dc)
+        assert torch.equal(gl, gc)
