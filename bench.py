@@ -549,11 +549,13 @@ class SamplingWorkload:
 class ServingWorkload:
     """Batched serving verify on the 8B shape: B sequences with ragged prompt lengths
     U[len_lo, len_hi] built from spans of which 40% copy an earlier window of the same
-    sequence; drafts from the native n-gram drafter (longest suffix match of 8 down to 3
-    tokens, at most K tokens, draft_len per sequence); greedy verify with auto trim.  A step
-    is one serving round: host drafting, the drafts' upload, spec_verify and the download of
-    accepted lengths and next tokens.  The verify itself is timed with CUDA events on the
-    stream (value, ms_per_step); the whole round is the end-to-end number."""
+    sequence; drafts from the n-gram drafter on the device (longest suffix match of 8 down to
+    3 tokens, at most K tokens, draft_len per sequence) over each slot's recorded tokens;
+    greedy verify with auto trim.  A step is one serving round: spec_ngram_draft_device,
+    spec_verify (pending tokens, drafts and draft lengths stay on the device between them)
+    and the download of drafts, accepted lengths, next tokens and draft lengths (the emitted
+    tokens are drafts[:accepted] + next).  Drafting + verify are timed with CUDA events on
+    the stream (value, ms_per_step); the whole round is the end-to-end number."""
     name = "serving-8b-b32-k8"
     dtype = "bf16"
     device_timed = True
@@ -574,34 +576,29 @@ class ServingWorkload:
                 "B": self.B, "K": self.K, "prompt_len": f"U[{self.len_lo}, {self.len_hi}] per sequence (seed 5)",
                 "kv_tokens_at_start": int(self.lens.sum()) if hasattr(self, "lens") else None,
                 "prompts": "spans of U[8,64] tokens, 40% copying an earlier window of the same sequence",
-                "decoding": "greedy", "drafter": "native n-gram lookup, suffix match 8..3 tokens, <= K drafted",
+                "decoding": "greedy", "drafter": "n-gram lookup on the device, suffix match 8..3 tokens, <= K drafted",
                 "kv_cache": "paged bf16, 16-token pages",
                 "l2": "inputs larger than L2 (15.1 GB of weights + the KV cache streamed per step)"}
 
     def setup(self, device, n_steps):
         import torch
         import synth
-        from speculative_decoding_verify_token_gb300 import model as M, ngram as NG
+        from speculative_decoding_verify_token_gb300 import model as M
         s, B, K = self.shape, self.B, self.K
         g = np.random.Generator(np.random.PCG64(5))
         self.lens = g.integers(self.len_lo, self.len_hi + 1, size=B)
         self.weights = synth.model_weights(s, seed=0, device=device)
         max_ctx = int(self.lens.max()) + (K + 1) * (n_steps + 64) + 64
         self.m = M.SpecModel(s, self.weights, max_batch=B, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
-        self.ctx = []
-        self.drafters = []
+        last = []
         for b in range(B):
             prompt = synth.ngram_prompt(5 + b, int(self.lens[b]), s.vocab)
             self.m.prefill(b, torch.from_numpy(prompt[:-1]).to(device))
-            d = NG.NgramDrafter(3, 8)
-            d.append(prompt)
-            self.drafters.append(d)
-            self.ctx.append(prompt)
-        self.pending = torch.tensor([int(c[-1]) for c in self.ctx], dtype=torch.int32).pin_memory()
+            last.append(int(prompt[-1]))
+        self.kv_len = self.lens.astype(np.int64) - 1        # committed tokens in each slot's cache
+        self.pending = torch.tensor(last, dtype=torch.int32, device=device)
+        self.h_out = torch.zeros(3, B, dtype=torch.int32).pin_memory()
         self.h_drafts = torch.zeros(B, K, dtype=torch.int32).pin_memory()
-        self.h_len = torch.zeros(B, dtype=torch.int32).pin_memory()
-        self.h_out = torch.zeros(2, B, dtype=torch.int32).pin_memory()
-        self.d_last = torch.empty(B, dtype=torch.int32, device=device)
         self.d_drafts = torch.empty(B, K, dtype=torch.int32, device=device)
         self.d_len = torch.empty(B, dtype=torch.int32, device=device)
         self.d_u = torch.zeros(B, K + 1, dtype=torch.float32, device=device)
@@ -618,38 +615,28 @@ class ServingWorkload:
 
     def _round(self, timed_events=True):
         import torch
-        from speculative_decoding_verify_token_gb300 import ngram as NG
         B, K = self.B, self.K
-        toks, lens = NG.draft_batch(self.drafters, K)
-        self.h_drafts.numpy()[:] = toks
-        self.h_len.numpy()[:] = lens
-        kv_read = int(sum(len(c) - 1 for c in self.ctx))
-        self.d_last.copy_(self.pending, non_blocking=True)
-        self.d_drafts.copy_(self.h_drafts, non_blocking=True)
-        self.d_len.copy_(self.h_len, non_blocking=True)
+        kv_read = int(self.kv_len.sum())
         a, b = self.ev[len(self.dev_ms) % len(self.ev)]
         a.record()
-        self.m.verify(self.seq_ids, self.d_last, self.d_drafts, self.d_u, 0.0, draft_len=self.d_len, out=self.out)
+        self.m.ngram_draft(self.seq_ids, self.pending, K, 3, 8, out=(self.d_drafts, self.d_len))
+        self.m.verify(self.seq_ids, self.pending, self.d_drafts, self.d_u, 0.0, draft_len=self.d_len, out=self.out)
         b.record()
         self.h_out[0].copy_(self.out["accepted_len"], non_blocking=True)
         self.h_out[1].copy_(self.out["next_token"], non_blocking=True)
-        st_ok = True
+        self.h_out[2].copy_(self.d_len, non_blocking=True)
+        self.h_drafts.copy_(self.d_drafts, non_blocking=True)
+        self.pending.copy_(self.out["next_token"])
         torch.cuda.current_stream().synchronize()
         self.dev_ms.append(a.elapsed_time(b))
-        acc = self.h_out[0].numpy().copy()
-        nxt = self.h_out[1].numpy().copy()
-        emitted = 0
-        for i in range(B):
-            a_i = int(acc[i])
-            if not (0 <= a_i <= int(lens[i])) or not (0 <= int(nxt[i]) < self.shape.vocab):
-                st_ok = False
-                a_i = max(0, min(a_i, int(lens[i])))
-            new = np.concatenate([toks[i, :a_i], [int(nxt[i])]]).astype(np.int32)
-            self.drafters[i].append(new)
-            self.ctx[i] = np.concatenate([self.ctx[i], new])
-            self.pending[i] = int(nxt[i])
-            emitted += a_i + 1
-        self.log.append((emitted, int(lens.sum()), int(acc.sum()), st_ok, kv_read))
+        acc = self.h_out[0].numpy().astype(np.int64)
+        nxt = self.h_out[1].numpy()
+        lens = self.h_out[2].numpy().astype(np.int64)
+        st_ok = bool(np.all((lens >= 0) & (lens <= K) & (acc >= 0) & (acc <= lens) & (nxt >= 0)
+                            & (nxt < self.shape.vocab)))
+        acc = np.clip(acc, 0, lens)
+        self.kv_len += acc + 1
+        self.log.append((int(acc.sum()) + B, int(lens.sum()), int(acc.sum()), st_ok, kv_read))
 
     def step(self, i):
         self._round()
@@ -693,8 +680,9 @@ class ServingWorkload:
                 "avg_launch_us": x["ms"] / x["launches"] * 1e3, "peak_source": peaks["source"]}
 
     def e2e(self, n):
-        """Serving rounds through the C ABI with host buffers: host drafting, the drafts'
-        upload, spec_verify, the download of the accepted lengths and next tokens."""
+        """Serving rounds through the C ABI: drafting and verify on the device, then the
+        download of the drafts, accepted lengths, next tokens and draft lengths (from which a
+        server streams out drafts[:accepted] + next); nothing is uploaded per round."""
         import torch
         torch.cuda.synchronize()
         i0 = len(self.log)
@@ -703,8 +691,7 @@ class ServingWorkload:
             self._round()
         dt = time.perf_counter() - t0
         emitted = sum(r[0] for r in self.log[i0:])
-        B, K = self.B, self.K
-        return emitted / dt, 4 * B + 4 * B * K + 4 * B, 8 * B
+        return emitted / dt, 0, 4 * self.B * (self.K + 3)
 
     def oracle_sample(self, budget_s):
         """The float64 oracle on a bounded sample: the verify pass of K+1 tokens of one

@@ -273,6 +273,22 @@ int spec_decode(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* tok
 int spec_draft(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int32_t* tokens,
                const spec_sampling* sampling, const float* uniforms, int32_t* out_tokens, float* out_logits);
 
+/* N-gram drafts on the device ([OptiQ] "N-gram lookup: any model": when the last tokens of
+ * a sequence occurred earlier in it, draft what followed).  The context of slot
+ * seq_ids[b] is its committed tokens (the positions its KV cache holds; the library
+ * records each token id as it is embedded) followed by pending[b]: the same rule as
+ * spec_ngram_draft on that context -- the longest suffix of max_match down to min_match
+ * tokens (1 <= min_match <= max_match <= SPEC_NGRAM_MAX_MATCH) with an earlier
+ * occurrence, its most recent occurrence, and the tokens that followed it.
+ * drafts [B][n_draft] (device int32, 1 <= n_draft <= 64): the draft, then pending[b] in the
+ * rows past it; draft_len [B] (device int32): min(n_draft, cap[b], tokens available), 0
+ * when nothing matches; cap [B] (device int32) may be NULL.  pending [B] device.  Feeds
+ * spec_verify (last_tokens = pending, draft_tokens = drafts with K = n_draft, draft_len)
+ * without a host round trip.  Enqueued on the context's stream. */
+int spec_ngram_draft_device(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* pending, int n_draft,
+                            int min_match, int max_match, const int32_t* cap, int32_t* drafts,
+                            int32_t* draft_len);
+
 /* Trim after a verify pass run with auto_trim == 0: keep accepted_len[b] + 1 of the
  * K + 1 entries it appended (device O(1) length update).  accepted_len (device int32 [B])
  * is clamped to [0, K], so a trim never reaches below the entries the pass appended. */

@@ -91,6 +91,7 @@ struct Ctx {
     int* d_tokens = nullptr;        // [Mmax]
     int* d_tok_seq = nullptr;
     int* d_tok_pos = nullptr;
+    int* d_tok_log = nullptr;       // [slots][max_ctx] token id at each position (n-gram context)
     int* d_seq_ids = nullptr;       // [max_batch]
     int* h_seq_ids = nullptr;       // pinned staging ring [SLOT_RING][max_batch]
     cudaEvent_t ring_ev[SLOT_RING] = {};
@@ -141,6 +142,8 @@ void launch_rope_table(float2* table, int max_pos, int hd, double theta, cudaStr
 void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens, int B, cudaStream_t st);
 void launch_advance_len(const int* seq_ids, int* seq_len, int B, int mode, int add, const int* accepted, int K,
                         cudaStream_t st);
+void launch_ngram_draft(const Ctx& c, int B, const int* pending, int n_draft, int min_match, int max_match,
+                        const int* cap, int* drafts, int* draft_len, cudaStream_t st);
 // dst[c * ldd + r] = src[r * lds + c] for r < R, c < C (int32 / float32)
 void launch_transpose_i32(const int* src, int lds, int* dst, int ldd, int R, int C, cudaStream_t st);
 void launch_transpose_f32(const float* src, int lds, float* dst, int ldd, int R, int C, cudaStream_t st);

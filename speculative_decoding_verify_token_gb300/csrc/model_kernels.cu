@@ -31,7 +31,9 @@ template <> struct Quad<__nv_bfloat16> {
 
 
 // X[m][:] = E[tok[m]][:] in fp32; token m = b*T + t belongs to slot seq_ids[b] at
-// position seq_len[slot] + t.  Ids outside [0, V) are embedded as token 0.  With Xg set
+// position seq_len[slot] + t.  Ids outside [0, V) are embedded as token 0.  The token id
+// (as given) is also recorded at tok_log[slot][position]: the slot's context for the
+// on-device n-gram drafter.  With Xg set
 // (fused RMSNorm of the tensor-core path) it also writes Xg[m] = bf16(X[m] * g) and, per
 // 128-column tile t, ssq[t][m] = sum of X[m][n]^2 over the tile (one warp per tile).
 template <typename T>
@@ -39,17 +41,19 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
                              const int* __restrict__ seq_len, int T_per_seq, const T* __restrict__ E,
                              float* __restrict__ X, int* __restrict__ tok_seq, int* __restrict__ tok_pos, int d,
                              int V, T* __restrict__ Xg, const T* __restrict__ g, float* __restrict__ ssq,
-                             int ssq_ld, size_t lo_off) {
+                             int ssq_ld, size_t lo_off, int* __restrict__ tok_log, int max_ctx) {
     pdl_launch_dependents();
     const int m = blockIdx.x;
     const int b = m / T_per_seq;
     const int t = m - b * T_per_seq;
-    int tok = tokens[m];
-    if (tok < 0 || tok >= V) tok = 0;
+    const int raw = tokens[m];
+    const int tok = (raw < 0 || raw >= V) ? 0 : raw;
     if (threadIdx.x == 0) {
         const int slot = seq_ids[b];
+        const int pos = seq_len[slot] + t;
         tok_seq[m] = slot;
-        tok_pos[m] = seq_len[slot] + t;
+        tok_pos[m] = pos;
+        if (pos < max_ctx) tok_log[(size_t)slot * max_ctx + pos] = raw;
     }
     const T* row = E + (size_t)tok * d;
     float* xr = X + (size_t)m * d;
@@ -185,11 +189,12 @@ void launch_embed(const Ctx& c, int M, int T, cudaStream_t st, bool fused_norm) 
                                             c.X, c.d_tok_seq, c.d_tok_pos, c.cfg.d_model, c.cfg.vocab,
                                             fused_norm ? static_cast<bf*>(c.Xn) : nullptr,
                                             static_cast<const bf*>(c.w.layers[0].attn_norm), c.ssq_a, c.Mmax,
-                                            c.split ? (size_t)M * c.cfg.d_model : 0);
+                                            c.split ? (size_t)M * c.cfg.d_model : 0, c.d_tok_log, c.lim.max_ctx);
     } else {
         embed_kernel<float><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T,
                                                static_cast<const float*>(c.w.embed), c.X, c.d_tok_seq, c.d_tok_pos,
-                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0, 0);
+                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0, 0, c.d_tok_log,
+                                               c.lim.max_ctx);
     }
 }
 
@@ -211,6 +216,82 @@ void launch_rope_table(float2* table, int max_pos, int hd, double theta, cudaStr
 void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens, int B, cudaStream_t st) {
     const int n = B * (K + 1);
     verify_tokens_kernel<<<(n + 255) / 256, 256, 0, st>>>(last, drafts, K, tokens, B);
+}
+
+// N-gram drafts of one sequence per CTA ("Speculative decoding on Apple Silicon"
+// (mlx-optiq docs), section "N-gram lookup: any model").  The context is the slot's
+// committed tokens tok_log[slot][0, L) (L = its length) followed by the pending token: n =
+// L + 1 tokens.  For every earlier end position e <= n - 2, l(e) = the length of the common
+// suffix of ctx[0, e] and the whole context, capped at min(max_match, n - 1); an
+// occurrence of the context's last m tokens ends at e exactly when l(e) >= m.  The longest
+// suffix with an earlier occurrence is m* = max l(e) (drafting needs m* >= min_match), and
+// its most recent occurrence is the largest e with l(e) = m*: one max-reduction of
+// (l(e), e).  The draft is ctx[e + 1, e + 1 + k), k = min(n_draft, cap, n - 1 - e); rows past
+// draft_len[b] = k hold the pending token.  The rule of spec_ngram_draft (host) and of the
+// oracle's lookup, as one scan.
+constexpr int NG_THREADS = 256;
+__global__ void __launch_bounds__(NG_THREADS) ngram_draft_kernel(const int* __restrict__ seq_ids,
+                                                               const int* __restrict__ seq_len,
+                                                               const int* __restrict__ tok_log, int max_ctx,
+                                                               const int* __restrict__ pending, int n_draft,
+                                                               int min_match, int max_match,
+                                                               const int* __restrict__ cap, int* __restrict__ drafts,
+                                                               int* __restrict__ draft_len) {
+    __shared__ int tail[SPEC_NGRAM_MAX_MATCH];
+    __shared__ unsigned long long red[NG_THREADS / 32];
+    const int b = blockIdx.x;
+    const int slot = seq_ids[b];
+    const int L = min(seq_len[slot], max_ctx);
+    const int n = L + 1;
+    const int* ctx = tok_log + (size_t)slot * max_ctx;
+    const int last = pending[b];
+    const int mcap = min(max_match, n - 1);
+    if (threadIdx.x < SPEC_NGRAM_MAX_MATCH) {
+        const int j = threadIdx.x;
+        tail[j] = j == 0 ? last : (j < n ? ctx[n - 1 - j] : 0);
+    }
+    __syncthreads();
+    // key = l << 32 | e, maximised; 0 = no occurrence of at least min_match tokens
+    unsigned long long key = 0;
+    for (int e = threadIdx.x; e <= n - 2; e += NG_THREADS) {
+        int l = 0;
+        while (l < mcap && l <= e && ctx[e - l] == tail[l]) ++l;
+        if (l >= min_match) {
+            const unsigned long long k = ((unsigned long long)l << 32) | (unsigned)e;
+            key = k > key ? k : key;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(FULL_MASK, key, o);
+        key = x > key ? x : key;
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = key;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long k = 0;
+        for (int w = 0; w < NG_THREADS / 32; ++w) k = red[w] > k ? red[w] : k;
+        red[0] = k;
+    }
+    __syncthreads();
+    key = red[0];
+    int k = 0, e = -1;
+    if (key != 0) {
+        e = (int)(key & 0xffffffffu);
+        k = min(n_draft, n - 1 - e);
+        if (cap) k = max(0, min(k, cap[b]));
+    }
+    for (int i = threadIdx.x; i < n_draft; i += NG_THREADS) {
+        const int p = e + 1 + i;
+        drafts[(size_t)b * n_draft + i] = i < k ? (p == n - 1 ? last : ctx[p]) : last;
+    }
+    if (threadIdx.x == 0) draft_len[b] = k;
+}
+
+void launch_ngram_draft(const Ctx& c, int B, const int* pending, int n_draft, int min_match, int max_match,
+                        const int* cap, int* drafts, int* draft_len, cudaStream_t st) {
+    ngram_draft_kernel<<<B, NG_THREADS, 0, st>>>(c.d_seq_ids, c.d_seq_len, c.d_tok_log, c.lim.max_ctx, pending, n_draft,
+                                                min_match, max_match, cap, drafts, draft_len);
 }
 
 void launch_advance_len(const int* seq_ids, int* seq_len, int B, int mode, int add, const int* accepted, int K,

@@ -454,6 +454,7 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
           ok(dalloc(*c, &c->d_tokens, sizeof(int) * c->Mmax, true)) &&
           ok(dalloc(*c, &c->d_tok_seq, sizeof(int) * c->Mmax, true)) &&
           ok(dalloc(*c, &c->d_tok_pos, sizeof(int) * c->Mmax, true)) &&
+          ok(dalloc(*c, &c->d_tok_log, sizeof(int) * (size_t)lim.max_batch * lim.max_ctx, true)) &&
           ok(dalloc(*c, &c->d_seq_ids, sizeof(int) * lim.max_batch, true)) &&
           ok(dalloc(*c, &c->part_o, sizeof(float) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks * m.head_dim)) &&
           ok(dalloc(*c, &c->part_ml, sizeof(float2) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks)) &&
@@ -715,6 +716,24 @@ extern "C" int spec_draft(spec_ctx* c, int B, const int32_t* seq_ids, int K, con
     c->launches += 2;
     e = cudaGetLastError();
     return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_draft", e);
+}
+
+extern "C" int spec_ngram_draft_device(spec_ctx* c, int B, const int32_t* seq_ids, const int32_t* pending,
+                                       int n_draft, int min_match, int max_match, const int32_t* cap,
+                                       int32_t* drafts, int32_t* draft_len) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    int rc = check_slots(*c, seq_ids, B);
+    if (rc != SPEC_OK) return rc;
+    if (!pending || !drafts || !draft_len) return set_error(SPEC_E_INVAL, "NULL required pointer");
+    if (n_draft < 1 || n_draft > 64 || min_match < 1 || max_match < min_match || max_match > SPEC_NGRAM_MAX_MATCH)
+        return set_error(SPEC_E_INVAL, "need 1 <= n_draft <= 64 and 1 <= min_match <= max_match <= %d",
+                         SPEC_NGRAM_MAX_MATCH);
+    if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    launch_ngram_draft(*c, B, pending, n_draft, min_match, max_match, cap, drafts, draft_len, c->stream);
+    c->launches += 1;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_ngram_draft_device", e);
 }
 
 extern "C" int spec_kv_trim(spec_ctx* c, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len) {

@@ -125,6 +125,21 @@ class SpecModel:
                                        _ptr(out), _ptr(logits)))
         return out, logits
 
+    def ngram_draft(self, seq_ids, pending, n_draft=8, min_match=3, max_match=8, cap=None, out=None):
+        """N-gram drafts on the device from each slot's committed tokens + pending [B]; returns
+        (drafts [B, n_draft] int32, draft_len [B] int32), both on the device."""
+        B = len(seq_ids)
+        _need(pending, torch.int32, (B,), "pending")
+        if cap is not None:
+            _need(cap, torch.int32, (B,), "cap")
+        if out is None:
+            out = (torch.empty(B, n_draft, dtype=torch.int32, device=self.device),
+                   torch.empty(B, dtype=torch.int32, device=self.device))
+        _lib.check(self.lib.spec_ngram_draft_device(self.h, B, _ids(seq_ids), _ptr(pending), int(n_draft),
+                                                    int(min_match), int(max_match), _ptr(cap), _ptr(out[0]),
+                                                    _ptr(out[1])))
+        return out
+
     def kv_trim(self, seq_ids, K, accepted_len):
         _lib.check(self.lib.spec_kv_trim(self.h, len(seq_ids), _ids(seq_ids), int(K), _ptr(accepted_len)))
 
