@@ -350,10 +350,11 @@ __device__ __forceinline__ void attn_combine_row_dpl(const AttnArgs& a, int r, i
                 for (int e = 0; e < DPL; ++e) o[e] = fmaf(w[u], v[u][e], o[e]);
             }
     }
-    const size_t m = (size_t)b * a.T + t;
-    T* dst = static_cast<T*>(a.o) + (m * a.hq + (size_t)g * G + hh) * a.hd + lane * DPL;
+    const int m = b * a.T + t;
+    const int col = ((g * G + hh) * a.hd) + lane * DPL;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) store_split<T>(dst + e, a.o_lo_off, o[e] / l);
+    for (int e = 0; e < DPL; ++e)
+        store_split<T>(static_cast<T*>(a.o) + act_off(m, col + e, a.hq * a.hd, a.o_sw_rows), a.o_lo_off, o[e] / l);
 }
 
 // head_dim 128 with the row's (max, sum) pairs staged in shared memory (mls: room for
@@ -400,8 +401,9 @@ __device__ __forceinline__ void attn_combine_row_128(const AttnArgs& a, int r, i
             }
     }
     __syncwarp();
-    const size_t m = (size_t)b * a.T + t;
-    T* dst = static_cast<T*>(a.o) + (m * a.hq + (size_t)g * G + hh) * 128 + lane * 4;
+    const int m = b * a.T + t;
+    // four columns inside one 16-byte chunk of the operand layout
+    T* dst = static_cast<T*>(a.o) + act_off(m, (g * G + hh) * 128 + lane * 4, a.hq * 128, a.o_sw_rows);
     store_split<T>(dst + 0, a.o_lo_off, o0 / l);
     store_split<T>(dst + 1, a.o_lo_off, o1 / l);
     store_split<T>(dst + 2, a.o_lo_off, o2 / l);

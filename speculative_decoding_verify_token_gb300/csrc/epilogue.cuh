@@ -14,6 +14,15 @@
 // W hi + W lo (about 16 significant bits of x instead of 8); the queries are split the same
 // way for the attention.  lo_off = 0 stores hi only.
 //
+// Operand layout of the tensor-core GEMM inputs (act_off): a pass of M tokens is padded to
+// Mp = act_rows(M) rows (8 up to 8 tokens, else a multiple of 16); per 64-column K atom the
+// Mp hi rows, then the Mp lo rows, of
+// 128 bytes each, every row's eight 16-byte chunks in the 128-byte swizzled order the
+// tensor cores read (chunk j of row m at position j ^ (m % 8)).  The rows of one atom are
+// then one contiguous run of global memory that lands in shared memory, by one bulk copy,
+// exactly as the MMA descriptor expects, and the lo half of an element is Mp * 64 elements
+// after its hi half.
+//
 // Fused RMSNorm (tensor-core GEMM only): RMSNorm(x) W^T = (x * g) W^T / rms(x), so a
 // residual epilogue that also writes xg = bf16(x_new * g_next) and, per 128-column tile
 // of x, the sum of x_new^2 lets the GEMM that consumes the normed row apply 1/rms(x) to
@@ -26,6 +35,18 @@
 namespace sv {
 
 enum EpiKind { EPI_QKV = 0, EPI_SWIGLU = 1, EPI_RESID = 2, EPI_STORE = 3 };
+
+// Rows of the tensor-core operand layout for a pass (or a GEMM launch) of M tokens: a
+// multiple of 8, so that a row's swizzle phase (row % 8) is the same counted from the start
+// of the hi block, of the lo block or of any launch's first row.
+__host__ __device__ __forceinline__ int act_rows(int M) { return M <= 8 ? 8 : (M + 15) & ~15; }
+
+// Element offset of row m, column n of an activation with ld columns: row-major when
+// sw_rows = 0, else the tensor-core operand layout of a pass padded to sw_rows rows.
+__host__ __device__ __forceinline__ size_t act_off(int m, int n, int ld, int sw_rows) {
+    if (sw_rows == 0) return (size_t)m * ld + n;
+    return ((size_t)(n >> 6) * 2 * sw_rows + m) * 64 + (size_t)(((((n >> 3) & 7) ^ (m & 7)) << 3) | (n & 7));
+}
 
 struct EpiArgs {
     int kind;
@@ -41,16 +62,18 @@ struct EpiArgs {
     const float2* rope;         // [max_pos][hd/2] (cos, sin)
     int hq, hkv, hd;
     // SWIGLU
-    void* h_out;                // [M][F]
+    void* h_out;                // [M][F] at act_off(m, f, F, sw_rows)
     int F;
+    int sw_rows;                // layout of h_out and xg_out (act_off); 0 = row-major
     // RESID / STORE
     float* x;                   // [M][ldx]
     int ldx;
+    int keep_last;              // STORE: 0 = every row; 1 = only the launch's last row, to row 0
     size_t lo_off;              // split activations: elements from a hi value to its lo half
     int m0;                     // token offset of this launch (rows m0 .. m0 + M - 1)
     // fused RMSNorm, producer side (RESID): xg_out = bf16(x_new * g_next), ssq_out[t][m] =
     // sum of x_new[m][n]^2 over the 128 columns n of tile t (fixed order)
-    void* xg_out;               // [M][ldx] bf16 or nullptr
+    void* xg_out;               // [M][ldx] bf16 at act_off(m, n, ldx, sw_rows), or nullptr
     const void* g_next;         // [ldx] bf16
     float* ssq_out;             // [ldx / 128][ssq_ld]
     // consumer side: accumulators of token m are scaled by 1/sqrt(sum_t ssq_in[t][row0 + m]
@@ -127,7 +150,7 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& e, int m_local, int p, f
         break;
     }
     case EPI_SWIGLU:
-        store_split<T>(static_cast<T*>(e.h_out) + (size_t)m * e.F + p, e.lo_off, silu_f(a0) * a1);
+        store_split<T>(static_cast<T*>(e.h_out) + act_off(m, p, e.F, e.sw_rows), e.lo_off, silu_f(a0) * a1);
         break;
     case EPI_RESID: {
         float* x = e.x + (size_t)m * e.ldx + 2 * p;
@@ -136,7 +159,8 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& e, int m_local, int p, f
         break;
     }
     default: {
-        float* x = e.x + (size_t)m * e.ldx + 2 * p;
+        if (e.keep_last && m_local != e.M - 1) break;
+        float* x = e.x + (size_t)(e.keep_last ? 0 : m) * e.ldx + 2 * p;
         x[0] = a0;
         x[1] = a1;
         break;

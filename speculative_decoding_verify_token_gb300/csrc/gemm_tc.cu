@@ -4,18 +4,23 @@
 // 6-150 k rows: the work is streaming the weights through HBM ("most of that pass is spent
 // moving weights through memory", "Speculative Decoding on Apple Silicon...", section
 // "How speculative decoding works").  Design:
-//  * swap-AB: a 128-row weight tile is the A operand, the tokens are the N dimension
-//    (16..256); the fp32 accumulator [128 x N] lives in tensor memory;
+//  * swap-AB: a 128-row weight tile is the A operand, the tokens' hi and lo rows are the N
+//    dimension (16..512, two MMAs above 256); the fp32 accumulator [128 x N] lives in
+//    tensor memory;
 //  * the weights are re-laid out once, when they are loaded, tile-major: every (tile, K
 //    atom) is the 16 KB A operand of one MMA atom, already in the 128-byte-swizzled order
 //    the tensor cores read, so a ring stage of n consecutive atoms of a tile is ONE
 //    contiguous bulk copy (cp.async.bulk) of n x 16 KB; a tensor-map box of 64 rows
 //    instead makes 64 separate 128-byte row requests, and issuing the boxes of a stage
 //    costs microseconds at the start of every GEMM;
-//  * the activations (the B operand, a few rows) arrive by TMA tensor loads with the
-//    128-byte swizzle; stages go into an mbarrier ring of up to 8 stages of up to four
-//    64-column K atoms; weights are loaded evict-first, activations evict-last (every CTA
-//    re-reads them);
+//  * the activations (the B operand: hi rows, then lo rows) are written by the kernels that
+//    produce them directly in the same swizzled order, K atom by K atom (the operand
+//    layout, epilogue.cuh), so a stage's B is one bulk copy as well: a tensor-map load
+//    of 16-row boxes moved about 37 GB/s per SM against 130-170 GB/s for one bulk copy of
+//    the same bytes, which at 144 tokens (36 KB of B per 16 KB weight atom) made the
+//    activations, not the weights, the limit; stages go into an mbarrier ring of up to 8
+//    stages of up to four 64-column K atoms; weights are loaded evict-first, activations
+//    evict-last (every CTA re-reads them);
 //  * warp roles: warp 0 = TMA producer, warp 1 = tcgen05.mma issuer (one thread) and TMEM
 //    owner, warps 2-5 = epilogue (tcgen05.ld of the 4 lane quarters);
 //  * persistent stream-K: the (tile, k-block) space is cut into one contiguous range per
@@ -40,8 +45,8 @@ namespace sv {
 #define TC_MAX_ATOMS 4          // most 64-element K atoms (128-byte swizzle spans) per stage
 #endif
 #ifndef TC_MIN_STAGES
-#define TC_MIN_STAGES 3         // fewest pipeline stages a launch may use
-#endif
+#define TC_MIN_STAGES 2         // fewest pipeline stages a launch may use (fewer, larger stages
+#endif                          // measured faster at 144 tokens: 2 x 104 KB over 4 x 52 KB)
 #ifndef TC_CTAS_PER_SM
 #define TC_CTAS_PER_SM 1        // resident GEMM CTAs per SM (shared memory split between them)
 #endif
@@ -51,11 +56,13 @@ constexpr int TC_SMEM_MAX = TC_CTAS_PER_SM == 1 ? 230912 : 110 * 1024;
 
 struct TcParams {
     const uint8_t* wt;        // this GEMM's tile-major weights: [n_tiles][KB] atoms of TC_ATOM_A bytes
-    CUtensorMap xmap;
+    const uint8_t* x;         // the GEMM input in the operand layout of a pass of x_rows rows
+    int x_rows;
     int gid;
     int n_tiles, KB;          // tiles; K atoms per tile (the stream-K unit)
     int ntok, M, x_row0;      // ntok = M rounded up to 16 (stride of the partial sums)
-    BRows br;                 // rows of the activation operand (split activations)
+    int x_whole;              // the launch reads all x_rows rows: a stage's B is one copy
+    BRows br;                 // rows of the activation operand (hi rows, then lo rows)
     int stages, stage_bytes;  // ring slots; bytes per slot
     int atoms;                // most atoms per stage (stages never cross a segment end)
     int hq, hkv;
@@ -85,13 +92,23 @@ __device__ __forceinline__ void load_stage_a(const TcParams& p, int tile, int kt
     bulk_g2s(a_dst, p.wt + ((size_t)tile * p.KB + kt) * TC_ATOM_A, (uint32_t)(n * TC_ATOM_A), fb, pol);
 }
 
-// The token rows (B) of one K atom at K coordinate kc, in boxes of 16 rows.
-
-__device__ __forceinline__ void load_atom_b(const TcParams& p, int kc, uint32_t b_dst, uint32_t fb, uint64_t pol) {
-    for (int t = 0; t < p.br.nr0 / 16; ++t) tma_load_2d(b_dst + t * 2048, &p.xmap, kc, p.br.b_row0 + t * 16, fb, pol);
-    if (p.br.b_row1 >= 0)
-        for (int t = 0; t < (p.br.nb - p.br.nr0) / 16; ++t)
-            tma_load_2d(b_dst + (p.br.nr0 + t * 16) * 128, &p.xmap, kc, p.br.b_row1 + t * 16, fb, pol);
+// The token rows (B) of the n K atoms kt .. kt + n - 1, already in the swizzled order the
+// MMA reads (operand layout, epilogue.cuh): per atom the launch's ntok hi rows, then its
+// ntok lo rows.  When the launch covers all rows of the pass, the atoms' blocks are
+// contiguous in global memory as in shared memory and the stage's B is one bulk copy.
+__device__ __forceinline__ void load_stage_b(const TcParams& p, int kt, int n, uint32_t b_dst, uint32_t fb,
+                                             uint64_t pol) {
+    const size_t blk = (size_t)p.x_rows * 128;                 // one atom's hi (or lo) rows
+    const uint8_t* src = p.x + (size_t)kt * 2 * blk + (size_t)p.x_row0 * 128;
+    const uint32_t rows_b = (uint32_t)p.br.rows * 128;
+    if (p.x_whole) {
+        bulk_g2s(b_dst, src, (uint32_t)n * 2 * rows_b, fb, pol);
+        return;
+    }
+    for (int at = 0; at < n; ++at) {
+        bulk_g2s(b_dst + (uint32_t)at * 2 * rows_b, src + (size_t)at * 2 * blk, rows_b, fb, pol);
+        bulk_g2s(b_dst + (uint32_t)at * 2 * rows_b + rows_b, src + (size_t)at * 2 * blk + blk, rows_b, fb, pol);
+    }
 }
 
 __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(const __grid_constant__ TcParams p) {
@@ -127,7 +144,6 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
         }
         mbar_init(smem_u32(&done_bar), 1);
         fence_barrier_init();
-        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -171,10 +187,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                     int n, tile, kt;
                     bool sf, sl;
                     w2.cur(n, tile, kt, sf, sl, sg);
-                    const uint32_t b_dst = base + (uint32_t)j * p.stage_bytes + b_off;
-                    for (int at = 0; at < n; ++at)
-                        load_atom_b(p, (kt + at) * TC_ATOM, b_dst + at * p.br.nb * TC_ATOM * 2, smem_u32(&full_bar[j]),
-                                    px);
+                    load_stage_b(p, kt, n, base + (uint32_t)j * p.stage_bytes + b_off, smem_u32(&full_bar[j]), px);
                     w2.g += n;
                     if (sl) sg = w2.g;
                 }
@@ -192,8 +205,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                 mbar_arrive_expect_tx(fb, per_atom_tx * n);
                 const uint32_t a_dst = base + (uint32_t)s * p.stage_bytes;
                 load_stage_a(p, tile, kt, n, a_dst, fb, pw);
-                for (int at = 0; at < n; ++at)
-                    load_atom_b(p, (kt + at) * TC_ATOM, a_dst + b_off + at * p.br.nb * TC_ATOM * 2, fb, px);
+                load_stage_b(p, kt, n, a_dst + b_off, fb, px);
                 w.g += n;
                 if (sl) seg0 = w.g;
             }
@@ -402,14 +414,9 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
 
 // ---- host side ------------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 struct TcGemm {
     uint8_t* wt = nullptr;                 // tile-major weights of every GEMM
     std::vector<size_t> off;               // byte offset of GEMM (layer, gid) at 4 * layer + gid; lm_head last
-    CUtensorMap xn, xo, xh;
     float* partial = nullptr;
     int* tile_cnt = nullptr;
     int* err = nullptr;
@@ -417,40 +424,10 @@ struct TcGemm {
     int grid = 0;
 };
 
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
-// bf16 row-major [rows][cols], box = 64 columns (128 B, the swizzle span) x box_rows rows.
-static int make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return set_error(SPEC_E_CUDA, "cuTensorMapEncodeTiled unavailable");
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(SPEC_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return SPEC_OK;
-}
-
 bool tc_supported(const Ctx& c) {
     const spec_model_cfg& m = c.cfg;
     return m.dtype == SPEC_BF16 && m.head_dim == 128 && m.d_model % 128 == 0 && m.vocab % 128 == 0 &&
-           m.ffn_dim % 64 == 0 && (m.n_q_heads * m.head_dim) % 64 == 0 && encode_fn();
+           m.ffn_dim % 64 == 0 && (m.n_q_heads * m.head_dim) % 64 == 0;
 }
 
 // Weight bytes, tiles and K atoms per tile of GEMM `gid` (one layer; lm_head for GEMM_LM).
@@ -543,10 +520,6 @@ int tc_create(Ctx& c) {
     }
     if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(c.stream) != cudaSuccess)
         rc = set_error(SPEC_E_CUDA, "weight re-layout failed");
-    // GEMM inputs as [2][Mmax][cols]: bf16 hi rows, then the lo remainders
-    if (rc == SPEC_OK) rc = make_map(&t->xn, c.Xn, 2 * (uint64_t)c.Mmax, d, 16);
-    if (rc == SPEC_OK) rc = make_map(&t->xo, c.O, 2 * (uint64_t)c.Mmax, qd, 16);
-    if (rc == SPEC_OK) rc = make_map(&t->xh, c.H, 2 * (uint64_t)c.Mmax, F, 16);
     t->grid = c.num_sms;
     const int max_tiles = (int)std::max<uint64_t>({V / 128, F / 64, d / 128, qd / 128 + 2 * kvd / 128});
     if (rc == SPEC_OK) {
@@ -636,7 +609,7 @@ static int gemm_grid(int n_tiles, int sms, int min_fill) {
     return 100 * g >= min_fill * sms ? g : sms;
 }
 
-static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int pass_M, const EpiArgs& e,
+static int tc_gemm_launch(Ctx& c, int gid, int layer, int x_row0, int M, int pass_M, const EpiArgs& e,
                           cudaStream_t st) {
     TcGemm* t = c.tc;
     const spec_model_cfg& m = c.cfg;
@@ -644,29 +617,31 @@ static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int 
     TcParams p{};
     const int d = m.d_model, qd = m.n_q_heads * m.head_dim, F = m.ffn_dim;
     int Kdim = d;
-    const CUtensorMap* xm = &t->xn;
-    const uint8_t* xbase = static_cast<const uint8_t*>(c.Xn);
+    p.x = static_cast<const uint8_t*>(c.Xn);
     int KB = 0;
     gemm_shape(m, gid, p.n_tiles, KB);
     p.wt = t->wt + t->off[gid == GEMM_LM ? (size_t)4 * m.n_layers : (size_t)4 * layer + gid];
     if (gid == GEMM_O) {
-        Kdim = qd; xm = &t->xo;
-        xbase = static_cast<const uint8_t*>(c.O);
+        Kdim = qd;
+        p.x = static_cast<const uint8_t*>(c.O);
     } else if (gid == GEMM_DOWN) {
-        Kdim = F; xm = &t->xh;
-        xbase = static_cast<const uint8_t*>(c.H);
+        Kdim = F;
+        p.x = static_cast<const uint8_t*>(c.H);
     }
-    const size_t off = static_cast<const uint8_t*>(X) - xbase;
-    p.x_row0 = (int)(off / ((size_t)Kdim * 2));
-    p.xmap = *xm;
+    p.x_rows = act_rows(pass_M);
+    p.x_row0 = x_row0;
     p.gid = gid;
     p.KB = Kdim / TC_ATOM;
     p.ntok = (M + 15) & ~15;
     p.M = M;
+    p.br = b_rows(M);
+    if (x_row0 % 8 != 0 || x_row0 + p.br.rows > p.x_rows)
+        return set_error(SPEC_E_RANGE, "GEMM rows [%d, %d) outside the pass's %d operand rows", x_row0,
+                         x_row0 + p.br.rows, p.x_rows);
+    p.x_whole = (x_row0 == 0 && p.br.rows == p.x_rows) ? 1 : 0;
     // the widest stage (most K atoms) that still leaves TC_MIN_STAGES ring slots; the
     // stream-K split is in atoms, so this choice changes no result bit
     const int budget = TC_SMEM_MAX - 1024 - TC_XBYTES;
-    p.br = b_rows(c.split, M, p.x_row0, pass_M);
     const int per_atom = TC_ATOM_A + p.br.nb * TC_ATOM * 2;
     p.atoms = 1;
     for (int a = TC_MAX_ATOMS; a > 1; --a)
@@ -713,10 +688,8 @@ static int tc_gemm_launch(Ctx& c, int gid, int layer, const void* X, int M, int 
 // More tokens than one launch holds run as launches over equal chunks of whole 16-token
 // groups (each streams the weights again); every token sees the same arithmetic as in a
 // single launch, so the results do not depend on the split.
-int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, int pass_M, const EpiArgs& e, cudaStream_t st) {
-    if (M <= TC_MAX_NTOK) return tc_gemm_launch(c, gid, layer, X, M, pass_M, e, st);
-    const spec_model_cfg& m = c.cfg;
-    const int Kdim = gid == GEMM_O ? m.n_q_heads * m.head_dim : (gid == GEMM_DOWN ? m.ffn_dim : m.d_model);
+int tc_gemm(Ctx& c, int gid, int layer, int x_row0, int M, int pass_M, const EpiArgs& e, cudaStream_t st) {
+    if (M <= TC_MAX_NTOK) return tc_gemm_launch(c, gid, layer, x_row0, M, pass_M, e, st);
     const int n = (M + TC_MAX_NTOK - 1) / TC_MAX_NTOK;
     int launched = 0, m0 = 0;
     for (int i = 0; i < n; ++i) {
@@ -726,8 +699,7 @@ int tc_gemm(Ctx& c, int gid, int layer, const void* X, int M, int pass_M, const 
         ec.M = chunk;
         ec.m0 = e.m0 + m0;
         if (ec.ssq_in) ec.ssq_row0 = e.ssq_row0 + m0;
-        const int r = tc_gemm_launch(c, gid, layer, static_cast<const uint8_t*>(X) + (size_t)m0 * Kdim * 2, chunk, pass_M,
-                                     ec, st);
+        const int r = tc_gemm_launch(c, gid, layer, x_row0 + m0, chunk, pass_M, ec, st);
         if (r < 0) return r;
         launched += r;
         m0 += chunk;

@@ -24,7 +24,7 @@ struct ModelWeights {
 
 struct AttnArgs {
     const void* q;            // [M][hq][hd]
-    void* o;                  // [M][hq][hd]
+    void* o;                  // [M][hq * hd] at act_off(m, col, hq * hd, o_sw_rows)
     const void* k_layer;      // [P][hkv][16][hd]
     const void* v_layer;
     const int* block_table;
@@ -41,6 +41,7 @@ struct AttnArgs {
     size_t q_lo_off;          // split activations: elements from a query (output) value to
     size_t o_lo_off;          // its bf16 lo half; 0 = not split
     int l2_ahead;             // multi-split kernel: splits prefetched into L2 ahead of the copies
+    int o_sw_rows;            // layout of o (the O GEMM's operand layout); 0 = row-major
 };
 
 struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
@@ -155,11 +156,12 @@ int attention_set_smem_limits(int hd);
 int attention_split_keys(int hd, int esize);
 
 // tcgen05 GEMM (bf16 models)
-int tc_create(Ctx& c);                       // plans + tensor maps, after weights are loaded
+int tc_create(Ctx& c);                       // tile-major weight copy + workspaces, after weights are loaded
 void tc_destroy(Ctx& c);
-// returns kernels launched, or a negative SPEC_E_* code
-// X = first row of the launch's tokens within the GEMM input of a pass of pass_M tokens
-int tc_gemm(Ctx& c, int gemm_id, int layer, const void* X, int M, int pass_M, const EpiArgs& e, cudaStream_t st);
+// returns kernels launched, or a negative SPEC_E_* code; the GEMM reads tokens [x_row0,
+// x_row0 + M) (x_row0 a multiple of 16) of its input in the operand layout of a pass of
+// pass_M tokens
+int tc_gemm(Ctx& c, int gemm_id, int layer, int x_row0, int M, int pass_M, const EpiArgs& e, cudaStream_t st);
 bool tc_supported(const Ctx& c);
 int tc_error_word(Ctx& c, int* out);          // device error word of the tensor-core GEMM (synchronous)
 int tc_wait_probe(Ctx& c, int budget_ms);     // one bounded wait that runs out (failure-path check)

@@ -34,14 +34,15 @@ template <> struct Quad<__nv_bfloat16> {
 // position seq_len[slot] + t.  Ids outside [0, V) are embedded as token 0.  The token id
 // (as given) is also recorded at tok_log[slot][position]: the slot's context for the
 // on-device n-gram drafter.  With Xg set
-// (fused RMSNorm of the tensor-core path) it also writes Xg[m] = bf16(X[m] * g) and, per
-// 128-column tile t, ssq[t][m] = sum of X[m][n]^2 over the tile (one warp per tile).
+// (fused RMSNorm of the tensor-core path) it also writes Xg[m] = bf16(X[m] * g), in the
+// GEMM operand layout act_off(m, n, d, sw_rows), and, per 128-column tile t, ssq[t][m] =
+// sum of X[m][n]^2 over the tile (one warp per tile).
 template <typename T>
 __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restrict__ seq_ids,
                              const int* __restrict__ seq_len, int T_per_seq, const T* __restrict__ E,
                              float* __restrict__ X, int* __restrict__ tok_seq, int* __restrict__ tok_pos, int d,
                              int V, T* __restrict__ Xg, const T* __restrict__ g, float* __restrict__ ssq,
-                             int ssq_ld, size_t lo_off, int* __restrict__ tok_log, int max_ctx) {
+                             int ssq_ld, size_t lo_off, int sw_rows, int* __restrict__ tok_log, int max_ctx) {
     pdl_launch_dependents();
     const int m = blockIdx.x;
     const int b = m / T_per_seq;
@@ -69,11 +70,12 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const int* __restri
         *reinterpret_cast<float4*>(xr + c) = v;
         const float4 gg = Quad<T>::load(g + c);
         const float4 y = make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w);
-        Quad<T>::store(Xg + (size_t)m * d + c, y);
+        const size_t o = act_off(m, c, d, sw_rows);      // 4 columns inside one 16-byte chunk
+        Quad<T>::store(Xg + o, y);
         if (lo_off) {      // bf16 remainder (split activations)
             const float4 h = make_float4(to_f32<T>(from_f32<T>(y.x)), to_f32<T>(from_f32<T>(y.y)),
                                          to_f32<T>(from_f32<T>(y.z)), to_f32<T>(from_f32<T>(y.w)));
-            Quad<T>::store(Xg + lo_off + (size_t)m * d + c, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
+            Quad<T>::store(Xg + lo_off + o, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
         }
         float sq = v.x * v.x;
         sq = fmaf(v.y, v.y, sq);
@@ -183,18 +185,20 @@ void launch_transpose_f32(const float* src, int lds, float* dst, int ldd, int R,
 }
 
 void launch_embed(const Ctx& c, int M, int T, cudaStream_t st, bool fused_norm) {
+    const int sw_rows = fused_norm ? act_rows(M) : 0;
     if (c.cfg.dtype == SPEC_BF16) {
         using bf = __nv_bfloat16;
         embed_kernel<bf><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T, static_cast<const bf*>(c.w.embed),
                                             c.X, c.d_tok_seq, c.d_tok_pos, c.cfg.d_model, c.cfg.vocab,
                                             fused_norm ? static_cast<bf*>(c.Xn) : nullptr,
                                             static_cast<const bf*>(c.w.layers[0].attn_norm), c.ssq_a, c.Mmax,
-                                            c.split ? (size_t)M * c.cfg.d_model : 0, c.d_tok_log, c.lim.max_ctx);
+                                            c.split ? (size_t)sw_rows * 64 : 0, sw_rows, c.d_tok_log,
+                                            c.lim.max_ctx);
     } else {
         embed_kernel<float><<<M, 256, 0, st>>>(c.d_tokens, c.d_seq_ids, c.d_seq_len, T,
                                                static_cast<const float*>(c.w.embed), c.X, c.d_tok_seq, c.d_tok_pos,
-                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0, 0, c.d_tok_log,
-                                               c.lim.max_ctx);
+                                               c.cfg.d_model, c.cfg.vocab, nullptr, nullptr, nullptr, 0, 0, 0,
+                                               c.d_tok_log, c.lim.max_ctx);
     }
 }
 

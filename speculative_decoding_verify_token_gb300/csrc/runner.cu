@@ -217,11 +217,13 @@ static inline void* layer_pool(const Ctx& c, void* pool, int l) {
     return static_cast<uint8_t*>(pool) + (size_t)l * c.layer_pool_elems * c.esize;
 }
 
+// One GEMM of the pass: on the tensor-core path over tokens [x_row0, x_row0 + e.M) of the
+// pass's pass_M tokens (operand layout, see epilogue.cuh), on the SIMT path from X.
 static int gemm(Ctx& c, int gid, int layer, const void* wa, const void* wb, const void* wc, int K, int n_pairs,
-                const void* X, const EpiArgs& e, int pass_M) {
+                const void* X, const EpiArgs& e, int pass_M, int x_row0 = 0) {
     ProfScope ps(c, gid, gemm_weight_bytes(c, gid));
     if (c.use_tc) {
-        const int n = tc_gemm(c, gid, layer, X, e.M, pass_M, e, c.stream);
+        const int n = tc_gemm(c, gid, layer, x_row0, e.M, pass_M, e, c.stream);
         if (n < 0) return n;
         c.launches += n;
         return SPEC_OK;
@@ -259,8 +261,12 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         if (!fused) return;
         e.xg_out = c.Xn; e.g_next = g; e.ssq_out = ssq; e.ssq_ld = c.Mmax;
     };
-    // split activations: the lo halves of a pass of M tokens follow its M hi rows
+    // split activations: the queries' lo halves follow the M hi rows; the GEMM operands
+    // (normed rows, attention output, SwiGLU output) are in the operand layout of act_rows(M)
+    // rows, lo halves act_rows(M) * 64 elements after the hi ones
     const size_t qlo = c.split ? (size_t)M * hq * hd : 0;
+    const int sw = c.use_tc ? act_rows(M) : 0;
+    const size_t act_lo = c.split ? (size_t)sw * 64 : 0;
     EpiArgs eq{};
     eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
     eq.tok_seq = c.d_tok_seq; eq.tok_pos = c.d_tok_pos; eq.rope = c.d_rope; eq.hq = hq; eq.hkv = hkv; eq.hd = hd;
@@ -268,17 +274,17 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     eq.lo_off = qlo;
     EpiArgs er{};
     er.kind = EPI_RESID; er.M = M; er.x = c.X; er.ldx = d;
-    er.lo_off = c.split ? (size_t)M * d : 0;
+    er.lo_off = act_lo; er.sw_rows = sw;
     EpiArgs es{};
     es.kind = EPI_SWIGLU; es.M = M; es.h_out = c.H; es.F = F;
-    es.lo_off = c.split ? (size_t)M * F : 0;
+    es.lo_off = act_lo; es.sw_rows = sw;
     norm_in(es, c.ssq_f, 0);
     AttnArgs aa{};
     aa.q = c.Q; aa.o = c.O; aa.block_table = c.d_block_table; aa.max_pages = c.max_pages; aa.seq_ids = c.d_seq_ids;
     aa.seq_len = c.d_seq_len; aa.T = T; aa.hq = hq; aa.hkv = hkv; aa.hd = hd; aa.scale = 1.0f / sqrtf((float)hd);
     aa.n_chunks = c.n_chunks; aa.part_o = c.part_o; aa.part_ml = c.part_ml;
     aa.split_keys = c.split_keys; aa.att_cnt = c.att_cnt;
-    aa.q_lo_off = qlo; aa.o_lo_off = qlo;
+    aa.q_lo_off = qlo; aa.o_lo_off = act_lo; aa.o_sw_rows = sw;
     aa.l2_ahead = c.attn_l2_ahead;
 
     int rc;
@@ -310,18 +316,27 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
         if ((rc = gemm(c, GEMM_DOWN, l, L.wd, nullptr, nullptr, F, d / 2, c.H, er, M)) != SPEC_OK) return rc;
     }
     if (logits_out != nullptr) {
-        const int rows = last_only ? 1 : M;
-        const size_t off = last_only ? (size_t)(M - 1) : 0;
-        if (!fused) {
+        EpiArgs el{};
+        el.kind = EPI_STORE; el.x = logits_out; el.ldx = m.vocab;
+        if (fused) {
+            // the last row alone: the launch covers its 16-row group (operand rows start on
+            // a multiple of 16) and stores only that group's last row
+            const int r0 = last_only ? ((M - 1) & ~15) : 0;
+            el.M = M - r0;
+            el.keep_last = last_only ? 1 : 0;
+            norm_in(el, c.ssq_a, r0);
+            if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2, c.Xn, el, M, r0)) != SPEC_OK)
+                return rc;
+        } else {
+            const int rows = last_only ? 1 : M;
+            const size_t off = last_only ? (size_t)(M - 1) : 0;
             launch_rmsnorm(c, c.X + off * d, c.w.final_norm, static_cast<uint8_t*>(c.Xn) + off * d * c.esize, rows, st);
             c.launches += 1;
+            el.M = rows;
+            if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2,
+                           static_cast<uint8_t*>(c.Xn) + off * d * c.esize, el, M)) != SPEC_OK)
+                return rc;
         }
-        EpiArgs el{};
-        el.kind = EPI_STORE; el.M = rows; el.x = logits_out; el.ldx = m.vocab;
-        norm_in(el, c.ssq_a, (int)off);
-        if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2,
-                       static_cast<uint8_t*>(c.Xn) + off * d * c.esize, el, M)) != SPEC_OK)
-            return rc;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail("decoder pass launch", e);
@@ -444,10 +459,10 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
           ok(dalloc(*c, &c->d_seq_len, sizeof(int) * lim.max_batch, true)) &&
           ok(dalloc(*c, &c->d_rope, sizeof(float2) * (size_t)lim.max_ctx * (m.head_dim / 2))) &&
           ok(dalloc(*c, &c->X, sizeof(float) * (size_t)c->Mmax * m.d_model, true)) &&
-          ok(dalloc(*c, &c->Xn, halves * c->esize * c->Mmax * m.d_model, true)) &&
+          ok(dalloc(*c, &c->Xn, halves * c->esize * act_rows(c->Mmax) * m.d_model, true)) &&
           ok(dalloc(*c, &c->Q, halves * c->esize * c->Mmax * qd, true)) &&
-          ok(dalloc(*c, &c->O, halves * c->esize * c->Mmax * qd, true)) &&
-          ok(dalloc(*c, &c->H, halves * c->esize * c->Mmax * m.ffn_dim, true)) &&
+          ok(dalloc(*c, &c->O, halves * c->esize * act_rows(c->Mmax) * qd, true)) &&
+          ok(dalloc(*c, &c->H, halves * c->esize * act_rows(c->Mmax) * m.ffn_dim, true)) &&
           ok(dalloc(*c, &c->ssq_a, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&
           ok(dalloc(*c, &c->ssq_f, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&
           ok(dalloc(*c, &c->logits, sizeof(float) * (size_t)c->Mmax * m.vocab)) &&

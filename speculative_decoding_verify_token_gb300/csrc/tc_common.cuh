@@ -24,14 +24,6 @@ constexpr int TC_XPITCH = TC_CW + 1;
 constexpr int TC_XBYTES = TC_BM * TC_XPITCH * 4;
 // ---- PTX wrappers --------------------------------------------------------------------------
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                            uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol) : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
@@ -95,13 +87,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Accumulator values of tokens c0 .. c0 + 15 in this thread's TMEM lane.  With split
-// activations the token's W x_lo product sits lo_col columns after its W x_hi product and
-// the two are added (hi + lo, in that order):
-//  * lo_col = 0: not split;
-//  * lo_col >= 16 (a multiple of 16): hi and lo in separate 16-column groups;
-//  * 1 <= lo_col <= 8 (packed, at most 8 tokens, c0 = 0): hi in columns [0, lo_col), lo in
-//    [lo_col, 2 lo_col) of the one 16-column group.
+// Accumulator values of tokens c0 .. c0 + 15 in this thread's TMEM lane: the W x_hi
+// products plus the W x_lo products lo_col columns further on (hi + lo, in that order).
+// lo_col = 8 (at most 8 tokens, c0 = 0): hi and lo share the one 16-column group.
 __device__ __forceinline__ void acc_ld16(uint32_t taddr, int c0, int lo_col, float (&v)[16]) {
     tmem_ld16(taddr + (uint32_t)c0, v);
     if (lo_col >= 16) {
@@ -109,39 +97,28 @@ __device__ __forceinline__ void acc_ld16(uint32_t taddr, int c0, int lo_col, flo
         tmem_ld16(taddr + (uint32_t)(c0 + lo_col), w);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] += w[j];
-    } else if (lo_col > 0) {
+    } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float lo = 0.0f;
-#pragma unroll
-            for (int k = 1; k <= 8; ++k)
-                if (k == lo_col) lo = v[j + k];
-            v[j] += lo;
-        }
+        for (int j = 0; j < 8; ++j) v[j] += v[j + 8];
     }
 }
 
-// Rows of the activation operand B of one launch over tokens [x_row0, x_row0 + M) of a pass
-// of pass_M tokens whose split activations hold hi rows [0, pass_M) and lo rows
-// [pass_M, 2 pass_M).
+// Rows of the activation operand B of one launch over M tokens: its rows = act_rows(M) hi
+// rows, then its rows lo rows (every K atom of the operand layout holds them in that
+// order), so the MMA's N is 2 rows, a token's lo product sits `rows` columns after its hi
+// product, and one accumulator buffer spans 2 rows TMEM columns.
 struct BRows {
-    int nb;       // rows of B (the MMA N)
-    int nr0;      // rows of the first range, from row b_row0
-    int b_row0, b_row1;   // second range (nb - nr0 rows) from b_row1, or -1
-    int lo_col;   // see acc_ld16
-    int acc_stride;       // TMEM columns per accumulator buffer
+    int rows;         // hi (and lo) rows of the launch
+    int nb;           // rows of B (the MMA N)
+    int lo_col;       // see acc_ld16
+    int acc_stride;   // TMEM columns per accumulator buffer
 };
-__host__ __device__ inline BRows b_rows(bool split, int M, int x_row0, int pass_M) {
-    const int ntok = (M + 15) & ~15;
+__host__ __device__ inline BRows b_rows(int M) {
     BRows r;
-    if (!split) {
-        r.nb = r.nr0 = ntok; r.b_row0 = x_row0; r.b_row1 = -1; r.lo_col = 0; r.acc_stride = ntok;
-    } else if (M <= 8 && x_row0 == 0 && M == pass_M) {
-        r.nb = r.nr0 = 16; r.b_row0 = 0; r.b_row1 = -1; r.lo_col = M; r.acc_stride = 16;
-    } else {
-        r.nr0 = ntok; r.nb = 2 * ntok; r.b_row0 = x_row0; r.b_row1 = pass_M + x_row0; r.lo_col = ntok;
-        r.acc_stride = 2 * ntok;
-    }
+    r.rows = act_rows(M);
+    r.nb = 2 * r.rows;
+    r.lo_col = r.rows;
+    r.acc_stride = 2 * r.rows;
     return r;
 }
 
@@ -305,7 +282,7 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
             xv.y += xs[r1 * TC_XPITCH + cc];
             *x = xv;
             const float y0 = xv.x * g.x, y1 = xv.y * g.y;
-            __nv_bfloat16* xg = static_cast<__nv_bfloat16*>(e.xg_out) + (size_t)(m + e.m0) * e.ldx + n0;
+            __nv_bfloat16* xg = static_cast<__nv_bfloat16*>(e.xg_out) + act_off(m + e.m0, n0, e.ldx, e.sw_rows);
             const __nv_bfloat162 hi = __floats2bfloat162_rn(y0, y1);
             *reinterpret_cast<__nv_bfloat162*>(xg) = hi;
             if (e.lo_off) {
