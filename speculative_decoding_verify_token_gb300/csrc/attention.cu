@@ -1,5 +1,10 @@
 // Paged causal GQA attention of a decoder pass over T new tokens per sequence.
 //
+// Passes of at most 96 query rows per (sequence, kv head) of batched contexts (max_batch >
+// 4) on the tensor-core GEMM path run the tcgen05 kernel of attn_tc.cu (512-key splits);
+// the kernels below serve small batches, longer passes (prefill chunks), other head dims
+// and float32 models.
+//
 // For each (sequence, kv head) the T*G query rows (T positions x G = hq/hkv query heads)
 // share one pass over the sequence's KV pages.  The keys are split at fixed absolute
 // positions (64-key splits on the tensor-core path, a multiple of the 16-token page):
@@ -221,7 +226,7 @@ __device__ __forceinline__ void attn_load_split(const AttnArgs& a, int slot, int
         if (key < nk) {
             const int pos = k0 + key;
             const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
-            const size_t off = (((size_t)page * a.hkv + g) * 16 + (pos & 15)) * 128 + ch * 8;
+            const size_t off = kv_off(page, g, pos & 15, ch * 8, a.hkv, 128, a.num_pages, a.kv_sw);
             cp_async16(smem_u32(Ks + key * MMA_PITCH + ch * 8), kp + off);
             cp_async16(smem_u32(Vs + key * MMA_PITCH + ch * 8), vp + off);
         } else {
@@ -232,15 +237,19 @@ __device__ __forceinline__ void attn_load_split(const AttnArgs& a, int slot, int
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Warm L2 with the K and V pages of split s (four 16-token pages of each, 4 KB apiece).
+// Warm L2 with the K and V pages of split s (four 16-token pages of each, 4 KB apiece: one
+// run, or two 2 KB halves in the tensor-core layout).
 __device__ __forceinline__ void attn_prefetch_split(const AttnArgs& a, int slot, int g, int s, int Ltot) {
     const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_layer);
     const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_layer);
     for (int pos = s * MMA_SPLIT; pos < min(Ltot, (s + 1) * MMA_SPLIT); pos += 16) {
         const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
-        const size_t off = ((size_t)page * a.hkv + g) * 16 * 128;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 4096;" :: "l"(kp + off) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 4096;" :: "l"(vp + off) : "memory");
+        for (int h = 0; h < (a.kv_sw ? 2 : 1); ++h) {
+            const size_t off = kv_off(page, g, 0, h * 64, a.hkv, 128, a.num_pages, a.kv_sw);
+            const uint32_t bytes = a.kv_sw ? 2048u : 4096u;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(kp + off), "r"(bytes) : "memory");
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(vp + off), "r"(bytes) : "memory");
+        }
     }
 }
 
@@ -358,6 +367,16 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
     const int nsplit = (max_len_after + a.split_keys - 1) / a.split_keys;
     const int G = a.hq / a.hkv;
     const dim3 cgrid((a.T * G + 3) / 4, a.hkv, B);
+    if (a.q_np > 0) {
+        // tensor-core attention and the vectorised combine, both launched early (the
+        // combine waits for the attention's partials with griddepcontrol.wait)
+        launch_attn_tc(c.use_pdl, a, nsplit, B, st);
+        if (nsplit <= COMB_MAXC)
+            launch_pdl(c.use_pdl, attn_combine128_kernel<__nv_bfloat16>, cgrid, dim3(128), 0, st, a);
+        else
+            launch_pdl(c.use_pdl, attn_combine_kernel<__nv_bfloat16>, cgrid, dim3(128), 0, st, a);
+        return 2;
+    }
     if (use_mma_path(a.hd, c.esize)) {
         // splits per CTA: one while the items fill about four waves of the GPU, more for
         // long contexts (at least ATT_MULTI_MIN), so that each CTA streams a run of keys
@@ -389,6 +408,7 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
 }
 
 int attention_set_smem_limits(int hd) {
+    if (attn_tc_set_smem_limits() != 0) return -1;
     if (cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MMA_SMEM) !=
             cudaSuccess ||
         cudaFuncSetAttribute(attn_mma_multi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

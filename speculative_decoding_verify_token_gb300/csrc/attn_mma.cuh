@@ -250,7 +250,7 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
         if (key < n_old) {
             const int pos = k0 + key;
             const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
-            const size_t off = (((size_t)page * a.hkv + g) * 16 + (pos & 15)) * 128 + ch * 8;
+            const size_t off = kv_off(page, g, pos & 15, ch * 8, a.hkv, 128, a.num_pages, a.kv_sw);
             cp_async16(smem_u32(Ks + key * MMA_PITCH + ch * 8), kp + off);
             cp_async16(smem_u32(Vs + key * MMA_PITCH + ch * 8), vp + off);
         } else if (key >= nk) {
@@ -267,7 +267,7 @@ __device__ __forceinline__ bool attn_mma_item(const AttnArgs& a, int s, int g, i
         if (key >= n_old && key < nk) {
             const int pos = k0 + key;
             const int page = a.block_table[(size_t)slot * a.max_pages + (pos >> 4)];
-            const size_t off = (((size_t)page * a.hkv + g) * 16 + (pos & 15)) * 128 + ch * 8;
+            const size_t off = kv_off(page, g, pos & 15, ch * 8, a.hkv, 128, a.num_pages, a.kv_sw);
             cp_async16(smem_u32(Ks + key * MMA_PITCH + ch * 8), kp + off);
             cp_async16(smem_u32(Vs + key * MMA_PITCH + ch * 8), vp + off);
         }

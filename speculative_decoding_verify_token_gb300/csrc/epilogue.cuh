@@ -41,6 +41,26 @@ enum EpiKind { EPI_QKV = 0, EPI_SWIGLU = 1, EPI_RESID = 2, EPI_STORE = 3 };
 // of the hi block, of the lo block or of any launch's first row.
 __host__ __device__ __forceinline__ int act_rows(int M) { return M <= 8 ? 8 : (M + 15) & ~15; }
 
+// Element offset of dimension d of key r (0..15) of KV page `page`, kv head h, in one
+// layer's K (or V) pool: row-major [page][hkv][16][hd] when sw = 0; for the tensor-core
+// attention (hd = 128) [hkv][2 halves of 64 dims][num_pages][16][64], every 128-byte key
+// row of a half in the swizzled order the MMA reads (16-byte chunk j at j ^ (r % 8)), so
+// that the keys of consecutive pages of one head and half are one contiguous run.
+__host__ __device__ __forceinline__ size_t kv_off(int page, int h, int r, int d, int hkv, int hd, int num_pages,
+                                                  int sw) {
+    if (sw == 0) return (((size_t)page * hkv + h) * 16 + r) * hd + d;
+    return ((((size_t)h * 2 + (d >> 6)) * num_pages + page) * 16 + r) * 64 +
+           (size_t)(((((d & 63) >> 3) ^ (r & 7)) << 3) | (d & 7));
+}
+
+// Element offset of dimension d of query row r (r = t * G + hh: token t, query head hh of
+// the group) of (sequence b, kv head g) in the tensor-core attention's query layout: per
+// (b, g) the hi rows then the lo rows, each as two 64-dim halves of np rows of 128 bytes
+// (swizzled as above); the lo half of a value is 2 * np * 64 elements after its hi half.
+__host__ __device__ __forceinline__ size_t q_att_off(int b, int g, int r, int d, int hkv, int np) {
+    return ((((size_t)b * hkv + g) * 4 + (d >> 6)) * np + r) * 64 + (size_t)(((((d & 63) >> 3) ^ (r & 7)) << 3) | (d & 7));
+}
+
 // Element offset of row m, column n of an activation with ld columns: row-major when
 // sw_rows = 0, else the tensor-core operand layout of a pass padded to sw_rows rows.
 __host__ __device__ __forceinline__ size_t act_off(int m, int n, int ld, int sw_rows) {
@@ -52,9 +72,11 @@ struct EpiArgs {
     int kind;
     int M;
     // QKV
-    void* q_out;                // [M][hq*hd]
-    void* k_layer;              // [P][hkv][16][hd] of this layer
+    void* q_out;                // [M][hq*hd], or the attention's query layout (q_np > 0)
+    void* k_layer;              // this layer's K pool (kv_off layout)
     void* v_layer;
+    int kv_sw, num_pages;       // KV pool layout (kv_off)
+    int q_np, q_T;              // q_np > 0: queries in q_att_off layout of q_np rows, q_T tokens per sequence
     const int* block_table;     // [slots][max_pages]
     int max_pages;
     const int* tok_seq;         // [M] slot of token m
@@ -123,16 +145,25 @@ __device__ __forceinline__ void qkv_store(const EpiArgs& e, int m, int hs, int j
         a0 = r0; a1 = r1;
     }
     if (hs < e.hq) {
-        T* q = static_cast<T*>(e.q_out) + (size_t)m * e.hq * e.hd + (size_t)hs * e.hd;
-        store_split<T>(q + j, e.lo_off, a0);
-        store_split<T>(q + j + half, e.lo_off, a1);
+        if (e.q_np > 0) {
+            const int G = e.hq / e.hkv;
+            const int b = m / e.q_T, t = m - b * e.q_T, g = hs / G, r = t * G + (hs - g * G);
+            T* q = static_cast<T*>(e.q_out);
+            const size_t lo = (size_t)2 * e.q_np * 64;
+            store_split<T>(q + q_att_off(b, g, r, j, e.hkv, e.q_np), lo, a0);
+            store_split<T>(q + q_att_off(b, g, r, j + half, e.hkv, e.q_np), lo, a1);
+        } else {
+            T* q = static_cast<T*>(e.q_out) + (size_t)m * e.hq * e.hd + (size_t)hs * e.hd;
+            store_split<T>(q + j, e.lo_off, a0);
+            store_split<T>(q + j + half, e.lo_off, a1);
+        }
     } else {
         const bool is_k = hs < e.hq + e.hkv;
         const int kvh = is_k ? hs - e.hq : hs - e.hq - e.hkv;
-        T* base = static_cast<T*>(is_k ? e.k_layer : e.v_layer) +
-                  (((size_t)page * e.hkv + kvh) * 16 + (pos & 15)) * e.hd;
-        base[j] = from_f32<T>(a0);
-        base[j + half] = from_f32<T>(a1);
+        T* base = static_cast<T*>(is_k ? e.k_layer : e.v_layer);
+        const int r = pos & 15;
+        base[kv_off(page, kvh, r, j, e.hkv, e.hd, e.num_pages, e.kv_sw)] = from_f32<T>(a0);
+        base[kv_off(page, kvh, r, j + half, e.hkv, e.hd, e.num_pages, e.kv_sw)] = from_f32<T>(a1);
     }
 }
 

@@ -591,6 +591,8 @@ int tc_wait_probe(Ctx& c, int budget_ms) {
     return e == cudaSuccess ? SPEC_OK : set_error(SPEC_E_CUDA, "wait_probe_kernel launch: %s", cudaGetErrorString(e));
 }
 
+int* tc_error_ptr(Ctx& c) { return c.tc ? c.tc->err : nullptr; }
+
 int tc_error_word(Ctx& c, int* out) {
     if (!c.tc) { *out = 0; return SPEC_OK; }
     return cudaMemcpy(out, c.tc->err, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess ? SPEC_OK : SPEC_E_CUDA;

@@ -23,9 +23,9 @@ struct ModelWeights {
 };
 
 struct AttnArgs {
-    const void* q;            // [M][hq][hd]
+    const void* q;            // [M][hq][hd], or the tensor-core attention's layout (q_np > 0)
     void* o;                  // [M][hq * hd] at act_off(m, col, hq * hd, o_sw_rows)
-    const void* k_layer;      // [P][hkv][16][hd]
+    const void* k_layer;      // this layer's K pool (kv_off layout)
     const void* v_layer;
     const int* block_table;
     int max_pages;
@@ -42,6 +42,9 @@ struct AttnArgs {
     size_t o_lo_off;          // its bf16 lo half; 0 = not split
     int l2_ahead;             // multi-split kernel: splits prefetched into L2 ahead of the copies
     int o_sw_rows;            // layout of o (the O GEMM's operand layout); 0 = row-major
+    int kv_sw, num_pages;     // KV pool layout (kv_off)
+    int q_np;                 // > 0: queries in q_att_off layout, tensor-core attention
+    int* err;                 // device status word for a wait that gave up, or nullptr
 };
 
 struct TcGemm;   // tcgen05 GEMM plans (gemm_tc.cu)
@@ -132,6 +135,7 @@ struct Ctx {
     // tensor-core GEMM
     TcGemm* tc = nullptr;
     bool use_tc = false;
+    bool att_tc = false;            // tensor-core attention for passes of <= 96 rows (max_batch > 4)
     int attn_l2_ahead = 0;                 // splits of K/V warmed in L2 ahead (long contexts)
     std::vector<void*> allocs;
 };
@@ -154,6 +158,11 @@ void launch_gemm_simt(const Ctx& c, const void* wa, const void* wb, const void* 
 int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, cudaStream_t st);
 int attention_set_smem_limits(int hd);
 int attention_split_keys(int hd, int esize);
+// tensor-core attention (attn_tc.cu): passes of up to 96 query rows per (sequence, kv head)
+int attn_tc_split_keys();                    // keys per split
+bool attn_tc_fits(int rows);
+int attn_tc_set_smem_limits();
+void launch_attn_tc(bool pdl, const AttnArgs& a, int nsplit, int B, cudaStream_t st);
 
 // tcgen05 GEMM (bf16 models)
 int tc_create(Ctx& c);                       // tile-major weight copy + workspaces, after weights are loaded
@@ -164,6 +173,7 @@ void tc_destroy(Ctx& c);
 int tc_gemm(Ctx& c, int gemm_id, int layer, int x_row0, int M, int pass_M, const EpiArgs& e, cudaStream_t st);
 bool tc_supported(const Ctx& c);
 int tc_error_word(Ctx& c, int* out);          // device error word of the tensor-core GEMM (synchronous)
+int* tc_error_ptr(Ctx& c);                    // that word's device address (nullptr without the plan)
 int tc_wait_probe(Ctx& c, int budget_ms);     // one bounded wait that runs out (failure-path check)
 
 }  // namespace sv

@@ -267,9 +267,15 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     const size_t qlo = c.split ? (size_t)M * hq * hd : 0;
     const int sw = c.use_tc ? act_rows(M) : 0;
     const size_t act_lo = c.split ? (size_t)sw * 64 : 0;
+    // the tensor-core attention (batched contexts) takes passes of up to 96 query rows per
+    // (sequence, kv head), with the queries in its own layout; the KV pool is in the
+    // swizzled layout on the tensor-core path (kv_off)
+    const bool att_tc = c.use_tc && c.att_tc && attn_tc_fits(T * (hq / hkv));
+    const int q_np = att_tc ? ((T * (hq / hkv) + 15) & ~15) : 0;
     EpiArgs eq{};
     eq.kind = EPI_QKV; eq.M = M; eq.q_out = c.Q; eq.block_table = c.d_block_table; eq.max_pages = c.max_pages;
     eq.tok_seq = c.d_tok_seq; eq.tok_pos = c.d_tok_pos; eq.rope = c.d_rope; eq.hq = hq; eq.hkv = hkv; eq.hd = hd;
+    eq.kv_sw = c.use_tc ? 1 : 0; eq.num_pages = c.num_pages; eq.q_np = q_np; eq.q_T = T;
     norm_in(eq, c.ssq_a, 0);
     eq.lo_off = qlo;
     EpiArgs er{};
@@ -283,7 +289,8 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
     aa.q = c.Q; aa.o = c.O; aa.block_table = c.d_block_table; aa.max_pages = c.max_pages; aa.seq_ids = c.d_seq_ids;
     aa.seq_len = c.d_seq_len; aa.T = T; aa.hq = hq; aa.hkv = hkv; aa.hd = hd; aa.scale = 1.0f / sqrtf((float)hd);
     aa.n_chunks = c.n_chunks; aa.part_o = c.part_o; aa.part_ml = c.part_ml;
-    aa.split_keys = c.split_keys; aa.att_cnt = c.att_cnt;
+    aa.split_keys = att_tc ? attn_tc_split_keys() : c.split_keys; aa.att_cnt = c.att_cnt;
+    aa.kv_sw = eq.kv_sw; aa.num_pages = c.num_pages; aa.q_np = q_np; aa.err = tc_error_ptr(c);
     aa.q_lo_off = qlo; aa.o_lo_off = act_lo; aa.o_sw_rows = sw;
     aa.l2_ahead = c.attn_l2_ahead;
 
@@ -446,6 +453,10 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
     c->max_pages = max_pages;
     c->w.layers.resize(m.n_layers);
     c->Mmax = std::max(lim.max_batch * (lim.max_k + 1), lim.prefill_chunk);
+    // batched contexts take the tensor-core attention (512-key splits); small batches keep
+    // the 64-key mma.sync kernel, whose short splits fill the GPU at B = 1.  The choice is
+    // fixed per context, so a token's bits never depend on the batch it shares a pass with.
+    c->att_tc = lim.max_batch > 4;
     c->split_keys = attention_split_keys(m.head_dim, c->esize);
     c->n_chunks = (lim.max_ctx + c->split_keys - 1) / c->split_keys;
     const size_t qd = (size_t)m.n_q_heads * m.head_dim;
@@ -460,7 +471,8 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
           ok(dalloc(*c, &c->d_rope, sizeof(float2) * (size_t)lim.max_ctx * (m.head_dim / 2))) &&
           ok(dalloc(*c, &c->X, sizeof(float) * (size_t)c->Mmax * m.d_model, true)) &&
           ok(dalloc(*c, &c->Xn, halves * c->esize * act_rows(c->Mmax) * m.d_model, true)) &&
-          ok(dalloc(*c, &c->Q, halves * c->esize * c->Mmax * qd, true)) &&
+          // + the padding rows of the tensor-core attention's query layout (16 per sequence and kv head)
+          ok(dalloc(*c, &c->Q, halves * c->esize * (c->Mmax * qd + (size_t)lim.max_batch * m.n_kv_heads * 16 * 128), true)) &&
           ok(dalloc(*c, &c->O, halves * c->esize * act_rows(c->Mmax) * qd, true)) &&
           ok(dalloc(*c, &c->H, halves * c->esize * act_rows(c->Mmax) * m.ffn_dim, true)) &&
           ok(dalloc(*c, &c->ssq_a, sizeof(float) * (size_t)c->Mmax * ((m.d_model + 127) / 128), true)) &&

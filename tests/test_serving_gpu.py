@@ -98,10 +98,10 @@ def test_serving_rounds(lib):
 
 
 def test_long_context_attention_bitwise(lib):
-    """32 sequences of ~1300 tokens take the multi-split attention kernel (runs of splits per
-    CTA); the same sequences alone (B=1) take one CTA per split.  Every split's arithmetic
-    is the same, as is every other stage's per-token arithmetic, so the verify rows agree
-    bit for bit."""
+    """32 sequences of ~1300 tokens verified in one pass, and the same sequences alone (B=1)
+    in a context of the same size (the attention's split length is fixed per context).
+    Every split's arithmetic is the same, as is every other stage's per-token arithmetic,
+    so the verify rows agree bit for bit."""
     model, _ = lib
     shape = dataclasses.replace(synth.QWEN_8B, n_layers=2, name="dense-8b-2l")
     w = synth.model_weights(shape, seed=0, device="cuda")
@@ -118,7 +118,7 @@ def test_long_context_attention_bitwise(lib):
     big = m.verify(list(range(B)), last, drafts, u, 0.0, want_logits=True)["logits"].cpu()
     m.close()
     for b in (0, 17):
-        one = model.SpecModel(shape, w, max_batch=1, max_ctx=1400 + K + 8, max_k=K, prefill_chunk=256)
+        one = model.SpecModel(shape, w, max_batch=B, max_ctx=1400 + K + 8, max_k=K, prefill_chunk=256)
         one.prefill(0, torch.from_numpy(prompts[b][:-1]).cuda())
         r = one.verify([0], last[b:b + 1].clone(), drafts[b:b + 1].clone(), u[b:b + 1].clone(), 0.0,
                        want_logits=True)["logits"].cpu()

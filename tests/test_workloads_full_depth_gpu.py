@@ -9,10 +9,11 @@ oracle's argmax unless the oracle's top-2 gap is below 1e-2 (token agreement cou
 teacher-forced: the oracle sees the GPU's own prefix).
 
 * Long contexts, on a one-layer slice of the 8B-class shape (full width and vocabulary):
-  nine sequences with 2,048 .. 16,384 cached tokens, where the attention runs one CTA per
-  run of at least four consecutive 64-key splits (the multi-split kernel) and the combine of
-  up to 512 splits; and one sequence of 34,000 tokens, more than 512 splits, which takes the
-  general combine.  Every sequence's K + 1 verify rows against the oracle.
+  nine sequences with 2,048 .. 16,384 cached tokens in one batched context, where the
+  tensor-core attention runs (512-key splits) with the vectorised combine; and one sequence
+  of 34,000 tokens at B = 1, where the mma.sync kernel runs one CTA per run of at least four
+  consecutive 64-key splits and more than 512 splits take the general combine.  Every
+  sequence's K + 1 verify rows against the oracle.
 * The 8B-class shape at full depth (36 layers): the 512-token plain greedy trajectory after a
   1024-token prompt, teacher-forced against ONE oracle forward of prompt + trajectory (the
   oracle generates each float64 weight tensor on the CPU when its layer needs it), and three
@@ -40,10 +41,11 @@ pytestmark = pytest.mark.gpu
 LOGIT_TOL = 3e-2
 GAP_EXCUSE = 1e-2
 K = 4
-# the attention dispatcher's thresholds: one CTA per run of splits when every CTA gets at
-# least 4 of the 64-key splits of a (kv head, sequence) at about 4 x 2 CTAs per SM; the
-# vectorised combine reads up to 512 splits
-SPLIT_KEYS, MULTI_MIN, COMBINE128_MAX = 64, 4, 512
+# the attention dispatcher's thresholds: contexts with max_batch > 4 run the tensor-core
+# kernel (512-key splits); smaller ones the mma.sync kernels (64-key splits, one CTA per run
+# of splits when every CTA gets at least 4 splits of a (kv head, sequence) at about 4 x 2
+# CTAs per SM); the vectorised combine reads up to 512 splits
+TC_MIN_BATCH, TC_SPLIT, SPLIT_KEYS, MULTI_MIN, COMBINE128_MAX = 5, 512, 64, 4, 512
 
 
 @pytest.fixture(scope="module")
@@ -69,8 +71,11 @@ def verify_long_contexts(M, shape, lens, seed):
     V = shape.vocab
     B = len(lens)
     max_ctx = max(lens) + K + 8
-    nsplit, spc = splits_per_cta(max_ctx, shape.n_kv_heads, B)
-    assert spc >= MULTI_MIN                      # the multi-split attention kernel runs
+    if B >= TC_MIN_BATCH:
+        nsplit = (max_ctx + TC_SPLIT - 1) // TC_SPLIT
+    else:
+        nsplit, spc = splits_per_cta(max_ctx, shape.n_kv_heads, B)
+        assert spc >= MULTI_MIN                  # the multi-split mma.sync kernel runs
     w = synth.model_weights(shape, seed=0, device="cuda")
     m = M.SpecModel(shape, w, max_batch=B, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
     prompts = [synth.prompt_tokens(seed + b, L + 1, V) for b, L in enumerate(lens)]
@@ -104,8 +109,9 @@ def oracle_long_context_errors(shape, prompts, drafts, got):
 
 
 def test_long_context_attention_against_oracle(model):
-    """Nine sequences of 2k-16k cached tokens: multi-split attention CTAs and the combine of
-    up to 512 splits; verify rows within 3e-2 of the oracle for every sequence."""
+    """Nine sequences of 2k-16k cached tokens (a batched context: the tensor-core attention,
+    4 to 33 splits of 512 keys per row, the vectorised combine); verify rows within 3e-2 of
+    the oracle for every sequence."""
     shape = dataclasses.replace(synth.QWEN_8B, n_layers=1)   # the 8B model's first layer
     lens = [2048, 3400, 5100, 6800, 8500, 10200, 11900, 13600, 16384]
     got, prompts, drafts, nsplit = verify_long_contexts(model, shape, lens, 300)
@@ -116,8 +122,9 @@ def test_long_context_attention_against_oracle(model):
 
 
 def test_longest_context_general_combine_against_oracle(model):
-    """One sequence of 34,000 cached tokens: more than 512 splits, so the general combine
-    runs; verify rows within 3e-2 of the oracle."""
+    """One sequence of 34,000 cached tokens (B = 1: the multi-split mma.sync kernel): more
+    than 512 splits of 64 keys, so the general combine runs; verify rows within 3e-2 of the
+    oracle."""
     shape = dataclasses.replace(synth.QWEN_8B, n_layers=1)
     got, prompts, drafts, nsplit = verify_long_contexts(model, shape, [34000], 400)
     assert nsplit > COMBINE128_MAX

@@ -182,7 +182,7 @@ def test_serving_full_shape(lib, full_weights):
       * every sequence's decision follows the greedy rule on its own verify rows;
       * every KV length grows by exactly accepted + 1;
       * the first round's rows of a short and a long sequence equal, bit for bit, the rows of
-        the same sequence verified alone (B = 1)."""
+        the same sequence verified alone (B = 1, in a context of the same size)."""
     model, _, ngram = lib
     shape = synth.QWEN_8B
     w = full_weights
@@ -226,7 +226,8 @@ def test_serving_full_shape(lib, full_weights):
     del m, out
     last0, toks0, dl0, lg0 = first
     for b in (int(np.argmin(lens)), int(np.argmax(lens))):
-        one = model.SpecModel(shape, w, max_batch=1, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
+        # a context of the same size (its attention split is fixed per context), one sequence
+        one = model.SpecModel(shape, w, max_batch=B, max_ctx=max_ctx, max_k=K, prefill_chunk=256)
         one.prefill(0, torch.from_numpy(prompts[b][:-1]).cuda())
         r1 = one.verify([0], last0[b:b + 1].clone(), toks0[b:b + 1].clone(), u[:1].clone(), 0.0,
                         draft_len=dl0[b:b + 1].clone(), want_logits=True)
