@@ -370,7 +370,7 @@ int launch_attention(const Ctx& c, const AttnArgs& a, int B, int max_len_after, 
     if (a.q_np > 0) {
         // tensor-core attention and the vectorised combine, both launched early (the
         // combine waits for the attention's partials with griddepcontrol.wait)
-        launch_attn_tc(c.use_pdl, a, nsplit, B, st);
+        launch_attn_tc(c.use_pdl, a, nsplit, B, c.num_sms > 0 ? c.num_sms : 148, st);
         if (nsplit <= COMB_MAXC)
             launch_pdl(c.use_pdl, attn_combine128_kernel<__nv_bfloat16>, cgrid, dim3(128), 0, st, a);
         else

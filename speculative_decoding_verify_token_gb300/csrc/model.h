@@ -162,7 +162,7 @@ int attention_split_keys(int hd, int esize);
 int attn_tc_split_keys();                    // keys per split
 bool attn_tc_fits(int rows);
 int attn_tc_set_smem_limits();
-void launch_attn_tc(bool pdl, const AttnArgs& a, int nsplit, int B, cudaStream_t st);
+void launch_attn_tc(bool pdl, const AttnArgs& a, int nsplit, int B, int sms, cudaStream_t st);
 
 // tcgen05 GEMM (bf16 models)
 int tc_create(Ctx& c);                       // tile-major weight copy + workspaces, after weights are loaded
