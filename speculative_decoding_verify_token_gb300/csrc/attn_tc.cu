@@ -97,8 +97,9 @@ __device__ __forceinline__ void at_fail(const AttnArgs& a) {
 }
 
 // Per row count: TMEM buffers for S and O (two while they fit, so that the scores of the
-// next item are computed while the softmax works on this one), bytes of one Q (later P)
-// buffer, ring slots of 32 KB that fit the shared memory left.
+// next item are computed while the softmax works on this one), bytes of one Q buffer (the
+// item's even P tiles go there once its scores are done; odd P tiles go to a third buffer
+// of the same size), ring slots of 32 KB that fit the shared memory left.
 template <int NP>
 struct AtCfg {
     static constexpr int SBUF = NP <= 48 ? 2 : 1;
@@ -106,11 +107,11 @@ struct AtCfg {
     static constexpr int BUFCOLS = (AT_TILES + 1) * NP;
     static constexpr int CW = SBUF * BUFCOLS;
     static constexpr uint32_t NCOLS = CW <= 128 ? 128u : (CW <= 256 ? 256u : 512u);
-    static constexpr int NS0 = (int)((232448u - 4096u - 1024u - 2u * QBYTES) / AT_SLOT_BYTES);
+    static constexpr int NS0 = (int)((232448u - 4096u - 1024u - 3u * QBYTES) / AT_SLOT_BYTES);
     static constexpr int NS = NS0 > 6 ? 6 : NS0;
     static constexpr int NK = NS / 2;                // K ring slots
     static constexpr int NV = NS - NK;               // V ring slots
-    static constexpr size_t SMEM = 1024 + 2 * (size_t)QBYTES + (size_t)NS * AT_SLOT_BYTES;
+    static constexpr size_t SMEM = 1024 + 3 * (size_t)QBYTES + (size_t)NS * AT_SLOT_BYTES;
 };
 
 // Persistent: CTA c takes items c, c + grid, ... of the (split, kv head, sequence) space
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
     extern __shared__ uint8_t at_smem[];
     __shared__ __align__(8) uint64_t k_full[C::NK], k_empty[C::NK], v_full[C::NV], v_empty[C::NV];
     __shared__ __align__(8) uint64_t q_full[2], q_free[2], s_full[C::SBUF], t_free[C::SBUF], o_full[C::SBUF];
-    __shared__ __align__(8) uint64_t p_full, p_done, done_bar;
+    __shared__ __align__(8) uint64_t p_full[2], p_done[2], done_bar;     // per P buffer (tile parity)
     __shared__ uint32_t tmem_sh;
     __shared__ volatile int abort_flag;
     __shared__ int cand_l0[AT_MAXC];      // seq_len of this CTA's k-th item's sequence, -1 = split past its end
@@ -156,10 +157,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
     }
     const uint32_t base = (smem_u32(at_smem) + 1023u) & ~1023u;
     uint8_t* gbase = at_smem + (base - smem_u32(at_smem));
-    const uint32_t ring = base + 2 * C::QBYTES;
+    const uint32_t pbuf1 = base + 2 * C::QBYTES;    // odd P tiles
+    const uint32_t ring = base + 3 * C::QBYTES;
     // zero the ring once: V rows past a split's keys are multiplied by P = 0 and must be finite
     for (int i = threadIdx.x; i < C::NS * AT_SLOT_BYTES / 16; i += AT_THREADS)
-        reinterpret_cast<uint4*>(gbase + 2 * C::QBYTES)[i] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(gbase + 3 * C::QBYTES)[i] = make_uint4(0, 0, 0, 0);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NK; ++i) {
@@ -179,8 +181,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
             mbar_init(smem_u32(&t_free[i]), 256);
             mbar_init(smem_u32(&o_full[i]), 1);
         }
-        mbar_init(smem_u32(&p_full), 256);
-        mbar_init(smem_u32(&p_done), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&p_full[i]), 256);
+            mbar_init(smem_u32(&p_done[i]), 1);
+        }
         mbar_init(smem_u32(&done_bar), 1);
         abort_flag = 0;
         fence_barrier_init();
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
             pdl_wait();
             const uint32_t id_s = idesc_bf16_m128(NP, false);
             const uint32_t id_o = idesc_bf16_m128(NP, true);
-            uint32_t sk = 0, sv = 0, pt = 0;
+            uint32_t sk = 0, sv = 0, pc0 = 0, pc1 = 0;      // P tiles consumed per buffer
             // QK queue: candidate index, item count, tile; P V queue likewise
             int qk_k = 0, qk_n = 0, qk_t = 0, qk_nt = 0;
             int pv_k = 0, pv_n = 0, pv_t = 0, pv_nt = 0;
@@ -405,10 +409,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
                 if (pv_n < qk_n) {            // P of an item exists only after its scores
                     const int buf = pv_n % C::SBUF, qb = pv_n & 1;
                     const int sl = (int)(sv % C::NV);
-                    if (mbar_test(smem_u32(&v_full[sl]), (sv / C::NV) & 1) && mbar_test(smem_u32(&p_full), pt & 1)) {
+                    const int pb = pv_t & 1;
+                    if (mbar_test(smem_u32(&v_full[sl]), (sv / C::NV) & 1) &&
+                        mbar_test(smem_u32(&p_full[pb]), (pb ? pc1 : pc0) & 1)) {
                         tc_fence_after();
                         const uint32_t vb = vring + (uint32_t)sl * AT_SLOT_BYTES;
-                        const uint32_t pbuf = base + (uint32_t)qb * C::QBYTES;
+                        const uint32_t pbuf = pb ? pbuf1 : base + (uint32_t)qb * C::QBYTES;
                         const uint32_t dcol = tmem + (uint32_t)(buf * C::BUFCOLS + AT_TILES * NP);
 #pragma unroll
                         for (int lo = 0; lo < 2; ++lo)
@@ -419,9 +425,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
                                                          (uint32_t)(ks & 3) * 32),
                                          id_o, (pv_t | lo | ks) ? 1u : 0u);
                         mma_commit(smem_u32(&v_empty[sl]));
-                        mma_commit(smem_u32(&p_done));
+                        mma_commit(smem_u32(&p_done[pb]));
                         ++sv;
-                        ++pt;
+                        if (pb) ++pc1; else ++pc0;
                         if (++pv_t == pv_nt) {
                             mma_commit(smem_u32(&o_full[buf]));
                             mma_commit(smem_u32(&q_free[qb]));
@@ -461,9 +467,32 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
         const float sl2 = a.scale * 1.4426950408889634f;
         const int atom = key >> 6, kc = key & 63;
-        uint32_t pt = 0;
+        uint32_t pw0 = 0, pw1 = 0;          // P tiles written per buffer
         int n = 0;
         bool ok = true;
+        // the output of an item is read out after the next item's maxima (its last P V has
+        // finished by then), or at once when S and O are single-buffered
+        bool o_pending = false;
+        size_t o_pbase = 0;
+        int o_buf = 0, o_n = 0;
+        auto read_out = [&]() -> bool {
+            const bool okw = !abort_flag && mbar_wait(smem_u32(&o_full[o_buf]), (uint32_t)((o_n / C::SBUF) & 1));
+            if (at_any(okw ? 0 : 1)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                float v[8];
+                tmem_ld8(tl + (uint32_t)(o_buf * C::BUFCOLS + AT_TILES * NP + r0 + ch * 8), v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (r0 + ch * 8 + e < R) a.part_o[(o_pbase + r0 + ch * 8 + e) * 128 + key] = v[e];
+            }
+            // the item's S and O columns are free for item o_n + SBUF
+            tc_fence_before();
+            mbar_arrive(smem_u32(&t_free[o_buf]));
+            o_pending = false;
+            return true;
+        };
         for (int k = 0; ok && k < ncand; ++k) {
             const int L0 = cand_l0[k];
             if (L0 < 0) continue;
@@ -521,20 +550,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
                 mrow[jj] = m == -INFINITY ? 0.0f : m;
             }
             at_bar();
-            // P = 2^(s - m) per tile, bf16 hi and lo, into the B operand of P V (in this
-            // item's query buffer: its QK MMAs are complete); row sums per thread
+            if (o_pending && !read_out()) {
+                ok = false;
+                break;
+            }
+            // P = 2^(s - m) per tile, bf16 hi and lo, into the B operand of P V: even tiles
+            // into this item's query buffer (its QK MMAs are complete), odd tiles into the
+            // third buffer, so that a tile is written while P V runs on the one before
             float lsum[HR];
 #pragma unroll
             for (int jj = 0; jj < HR; ++jj) lsum[jj] = 0.0f;
-            uint8_t* pbuf = gbase + qb * C::QBYTES;
             for (int i = 0; i < nt; ++i) {
-                if (i > 0) {
-                    okw = !abort_flag && mbar_wait(smem_u32(&p_done), (pt - 1) & 1);
+                const int pb = i & 1;
+                const uint32_t pw = pb ? pw1 : pw0;
+                if (pw > 0) {               // that buffer's previous tile must have been read
+                    okw = !abort_flag && mbar_wait(smem_u32(&p_done[pb]), (pw - 1) & 1);
                     if (at_any(okw ? 0 : 1)) {
                         ok = false;
                         break;
                     }
                 }
+                uint8_t* pbuf = gbase + (pb ? 2 * C::QBYTES : qb * C::QBYTES);
                 const int kk = i * AT_TILE + key;
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
@@ -555,8 +591,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
                 // the generic-proxy writes of P must be visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
-                mbar_arrive(smem_u32(&p_full));
-                ++pt;
+                mbar_arrive(smem_u32(&p_full[pb]));
+                if (pb) ++pw1; else ++pw0;
             }
             if (!ok) break;
             // row sums: warp butterfly, then the four lane quarters in a fixed order
@@ -573,25 +609,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
                 const float l = ((red[0][etid] + red[1][etid]) + red[2][etid]) + red[3][etid];
                 a.part_ml[pbase + etid] = make_float2(row_m[etid], l);
             }
-            okw = !abort_flag && mbar_wait(smem_u32(&o_full[buf]), (uint32_t)((n / C::SBUF) & 1));
-            if (at_any(okw ? 0 : 1)) {
+            o_pending = true;
+            o_pbase = pbase;
+            o_buf = buf;
+            o_n = n;
+            if (C::SBUF == 1 && !read_out()) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                float v[8];
-                tmem_ld8(tl + (uint32_t)(buf * C::BUFCOLS + AT_TILES * NP + r0 + ch * 8), v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (r0 + ch * 8 + e < R) a.part_o[(pbase + r0 + ch * 8 + e) * 128 + key] = v[e];
-            }
-            // this item's S and O columns are free for item n + SBUF
-            tc_fence_before();
-            mbar_arrive(smem_u32(&t_free[buf]));
             ++n;
         }
+        if (ok && o_pending && !read_out()) ok = false;
         if (!ok && etid == 0) {
             abort_flag = 1;
             at_fail(a);
