@@ -20,7 +20,7 @@ Prints one JSON line (rank 0).  Workloads:
       {1, 2, 4, 8, 16} goes beside it.
   serving-8b-b32-k8: batched verify on the 8B-class shape, B = 32 sequences with KV
       lengths uniform in [2048, 16384], n-gram drafts (K = 8 with per-sequence draft
-      lengths) from the host drafter, a KV trim after every step.
+      lengths) from the drafter on the device, a KV trim after every step.
 
 The metric is emitted tokens per second of verify steps (accepted drafts plus the
 correction or bonus token); ms_per_step is the verify-step latency; `roofline` is the
@@ -882,12 +882,12 @@ WORKLOADS = {DenseVerifyWorkload.name: DenseVerifyWorkload, VerifyLogitsWorkload
 DEFAULT_WORKLOAD = DenseVerifyWorkload.name
 # DRAM bytes (read + write) of one graphed 8B verify step (see DenseVerifyWorkload.roofline),
 # from an ncu capture of a 2-layer slice with --cache-control none: per layer (the four
-# GEMMs, attention and combine: 386.8 and 386.9 MB in the two layers) and the rest of the
+# GEMMs, attention and combine: 390.7 and 389.0 MB in the two layers) and the rest of the
 # step (embed, lm_head, verify kernels, length update); in that capture the small slice's KV
 # pages stay in L2, so the full model's attention reads (about 4.3 MB per layer at a
 # context of 1.1K) are not in it.  0 = not captured for the current kernels.
-STEP_TRAFFIC_PER_LAYER = 386.9e6
-STEP_TRAFFIC_FIXED = 1247.7e6
+STEP_TRAFFIC_PER_LAYER = 389.8e6
+STEP_TRAFFIC_FIXED = 1250.1e6
 
 
 def run_reference(args):
