@@ -239,9 +239,14 @@ int spec_prefill(spec_ctx* ctx, int seq_id, const int32_t* tokens, int n, float*
  * NULL = deterministic drafts), then, when auto_trim != 0, the trim to len + a + 1.
  * With auto_trim == 0 the K+1 entries stay and spec_kv_trim does the trim later.
  * Outputs as spec_verify_logits; out_logits (device fp32 [B][K+1][V], may be NULL)
- * receives the target logits.  Ids outside [0, V) are embedded as token 0: a pending token
- * then reads as token 0, and such a draft can never be accepted.  SPEC_E_RANGE when a sequence would exceed max_ctx, SPEC_E_NOMEM
- * when the page pool is exhausted. */
+ * receives the target logits.  Greedy (temperature 0) with out_logits NULL on a bf16
+ * model: the lm_head GEMM's epilogue keeps, per token, only each 128-row vocabulary
+ * tile's largest logit (lowest id on ties) and a merge takes the rows' argmax from those
+ * ([MTP-fixes] "Truncation has to match on both sides": the greedy rule needs the argmax
+ * alone), so the [B][K+1][V] logits are never written; the outputs are those of the
+ * full-logits path, bit for bit.  Ids outside [0, V) are embedded as token 0: a pending
+ * token then reads as token 0, and such a draft can never be accepted.  SPEC_E_RANGE when
+ * a sequence would exceed max_ctx, SPEC_E_NOMEM when the page pool is exhausted. */
 int spec_verify(spec_ctx* ctx, int B, const int32_t* seq_ids, int K,
                 const int32_t* last_tokens, const int32_t* draft_tokens, const int32_t* draft_len,
                 const float* draft_logits, const float* uniforms, const spec_sampling* sampling,

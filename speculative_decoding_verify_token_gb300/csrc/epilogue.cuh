@@ -36,6 +36,14 @@ namespace sv {
 
 enum EpiKind { EPI_QKV = 0, EPI_SWIGLU = 1, EPI_RESID = 2, EPI_STORE = 3 };
 
+// Order-preserving 64-bit key of logit v at vocabulary id: the larger key is the larger
+// value, and of equal values the lower id (the greedy argmax's tie order); -0 counts as +0.
+__device__ __forceinline__ unsigned long long amax_key(float v, int id) {
+    uint32_t u = v == 0.0f ? 0u : __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
+}
+
 // Rows of the tensor-core operand layout for a pass (or a GEMM launch) of M tokens: a
 // multiple of 8, so that a row's swizzle phase (row % 8) is the same counted from the start
 // of the hi block, of the lo block or of any launch's first row.
@@ -91,6 +99,10 @@ struct EpiArgs {
     float* x;                   // [M][ldx]
     int ldx;
     int keep_last;              // STORE: 0 = every row; 1 = only the launch's last row, to row 0
+    // STORE, tensor-core path: instead of the logits, per token m and 128-row tile t the key
+    // of the tile's largest logit at amax_out[m * amax_ld + t] (see amax_key); nullptr = store
+    unsigned long long* amax_out;
+    int amax_ld;
     size_t lo_off;              // split activations: elements from a hi value to its lo half
     int m0;                     // token offset of this launch (rows m0 .. m0 + M - 1)
     // fused RMSNorm, producer side (RESID): xg_out = bf16(x_new * g_next), ssq_out[t][m] =

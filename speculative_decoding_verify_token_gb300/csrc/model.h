@@ -96,6 +96,7 @@ struct Ctx {
     int* d_tok_seq = nullptr;
     int* d_tok_pos = nullptr;
     int* d_tok_log = nullptr;       // [slots][max_ctx] token id at each position (n-gram context)
+    unsigned long long* d_lm_amax = nullptr;   // [Mmax][vocab / 128] per-tile argmax keys (greedy, bf16)
     int* d_seq_ids = nullptr;       // [max_batch]
     int* h_seq_ids = nullptr;       // pinned staging ring [SLOT_RING][max_batch]
     cudaEvent_t ring_ev[SLOT_RING] = {};
@@ -121,7 +122,7 @@ struct Ctx {
     int l2_prefetch_atoms = 0;             // next-GEMM weight atoms per CTA warmed into L2
     int gemm_min_fill = 80;                // percent of the SMs a whole-tile GEMM split must keep busy
     cudaStream_t cap_stream = nullptr;     // private stream the graphs are captured on
-    struct GraphEntry { int B, T; cudaGraphExec_t exec; long long kernels; };
+    struct GraphEntry { int B, T; bool amax; cudaGraphExec_t exec; long long kernels; };
     std::vector<GraphEntry> graphs;
     // device-resident drafting loop (spec_draft): tokens [max_k + 1][max_batch] (row i =
     // the input of step i), uniforms [max_k][max_batch], logits [max_k][max_batch][V], one
@@ -147,6 +148,9 @@ void launch_rope_table(float2* table, int max_pos, int hd, double theta, cudaStr
 void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens, int B, cudaStream_t st);
 void launch_advance_len(const int* seq_ids, int* seq_len, int B, int mode, int add, const int* accepted, int K,
                         cudaStream_t st);
+int launch_greedy_amax(const unsigned long long* keys, int n_tiles, int B, int K, const int32_t* draft_tokens,
+                       const int32_t* draft_len, int32_t* accepted_len, int32_t* next_token, int32_t* out_ids,
+                       float* out_probs, int32_t* seq_status, cudaStream_t st);
 void launch_ngram_draft(const Ctx& c, int B, const int* pending, int n_draft, int min_match, int max_match,
                         const int* cap, int* drafts, int* draft_len, cudaStream_t st);
 // dst[c * ldd + r] = src[r * lds + c] for r < R, c < C (int32 / float32)

@@ -236,7 +236,7 @@ static int gemm(Ctx& c, int gid, int layer, const void* wa, const void* wb, cons
 // Forward of B x T tokens already in d_tokens for the slots in d_seq_ids.  logits_out gets
 // every row ([B*T][V]) or, when last_only, the last row only ([V]); nullptr = no lm_head.
 static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bool last_only,
-                   bool graph_mode = false) {
+                   bool graph_mode = false, bool lm_amax = false) {
     const spec_model_cfg& m = c.cfg;
     const int M = B * T;
     const int d = m.d_model, hd = m.head_dim, hq = m.n_q_heads, hkv = m.n_kv_heads, F = m.ffn_dim;
@@ -331,6 +331,10 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
             const int r0 = last_only ? ((M - 1) & ~15) : 0;
             el.M = M - r0;
             el.keep_last = last_only ? 1 : 0;
+            if (lm_amax && !last_only) {    // per-tile argmax keys instead of the logits
+                el.amax_out = c.d_lm_amax;
+                el.amax_ld = m.vocab / 128;
+            }
             norm_in(el, c.ssq_a, r0);
             if ((rc = gemm(c, GEMM_LM, -1, c.w.lm_head, nullptr, nullptr, d, m.vocab / 2, c.Xn, el, M, r0)) != SPEC_OK)
                 return rc;
@@ -352,10 +356,10 @@ static int forward(Ctx& c, const int* slots, int B, int T, float* logits_out, bo
 
 // The decoder pass of B x T tokens through a CUDA graph captured once per (B, T) (logits
 // to the internal buffer).  Falls back to eager launches while profiling.
-static int forward_graph(Ctx& c, const int* slots, int B, int T) {
+static int forward_graph(Ctx& c, const int* slots, int B, int T, bool lm_amax = false) {
     GraphEntryLookup:
     for (auto& g : c.graphs) {
-        if (g.B == B && g.T == T) {
+        if (g.B == B && g.T == T && g.amax == lm_amax) {
             cudaError_t e = cudaGraphLaunch(g.exec, c.stream);
             if (e != cudaSuccess) return cuda_fail("cudaGraphLaunch", e);
             c.launches += g.kernels;
@@ -373,7 +377,7 @@ static int forward_graph(Ctx& c, const int* slots, int B, int T) {
         return cuda_fail("cudaStreamBeginCapture", e);
     }
     const long long l0 = c.launches;
-    const int rc = forward(c, slots, B, T, c.logits, false, true);
+    const int rc = forward(c, slots, B, T, c.logits, false, true, lm_amax);
     const long long n = c.launches - l0;
     c.launches = l0;
     e = cudaStreamEndCapture(c.stream, &graph);
@@ -387,7 +391,7 @@ static int forward_graph(Ctx& c, const int* slots, int B, int T) {
     e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
     if (e != cudaSuccess) return cuda_fail("cudaGraphInstantiate", e);
-    c.graphs.push_back({B, T, exec, n});
+    c.graphs.push_back({B, T, lm_amax, exec, n});
     goto GraphEntryLookup;
 }
 
@@ -482,6 +486,8 @@ extern "C" int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* lim
           ok(dalloc(*c, &c->d_tok_seq, sizeof(int) * c->Mmax, true)) &&
           ok(dalloc(*c, &c->d_tok_pos, sizeof(int) * c->Mmax, true)) &&
           ok(dalloc(*c, &c->d_tok_log, sizeof(int) * (size_t)lim.max_batch * lim.max_ctx, true)) &&
+          (m.dtype != SPEC_BF16 ||
+           ok(dalloc(*c, &c->d_lm_amax, sizeof(unsigned long long) * (size_t)c->Mmax * (m.vocab / 128 + 1)))) &&
           ok(dalloc(*c, &c->d_seq_ids, sizeof(int) * lim.max_batch, true)) &&
           ok(dalloc(*c, &c->part_o, sizeof(float) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks * m.head_dim)) &&
           ok(dalloc(*c, &c->part_ml, sizeof(float2) * (size_t)c->Mmax * m.n_q_heads * c->n_chunks)) &&
@@ -625,8 +631,20 @@ extern "C" int spec_verify(spec_ctx* c, int B, const int32_t* seq_ids, int K, co
     if ((rc = ensure_pages(*c, seq_ids, B, K + 1)) != SPEC_OK) return rc;
     launch_verify_tokens(last_tokens, draft_tokens, K, c->d_tokens, B, c->stream);
     c->launches += 1;
+    // greedy without logits on the tensor-core path: the lm_head epilogue keeps only each
+    // 128-row tile's argmax key per token, the [M][V] logits are never written
+    const bool amax = c->use_tc && sampling->temperature == 0.0f && out_logits == nullptr && c->d_lm_amax;
     float* logits = out_logits ? out_logits : c->logits;
-    if (c->use_graphs && !c->prof_on) {
+    if (amax) {
+        if (c->use_graphs && !c->prof_on) rc = forward_graph(*c, seq_ids, B, K + 1, true);
+        else rc = forward(*c, seq_ids, B, K + 1, c->logits, false, false, true);
+        if (rc != SPEC_OK) return rc;
+        {
+            ProfScope psv(*c, 6, (double)B * (K + 1) * (c->cfg.vocab / 128) * 8.0);
+            rc = launch_greedy_amax(c->d_lm_amax, c->cfg.vocab / 128, B, K, draft_tokens, draft_len, accepted_len,
+                                    next_token, out_ids, out_probs, seq_status, c->stream);
+        }
+    } else if (c->use_graphs && !c->prof_on) {
         logits = c->logits;
         if ((rc = forward_graph(*c, seq_ids, B, K + 1)) != SPEC_OK) return rc;
         if (out_logits) {
@@ -637,11 +655,11 @@ extern "C" int spec_verify(spec_ctx* c, int B, const int32_t* seq_ids, int K, co
     } else if ((rc = forward(*c, seq_ids, B, K + 1, logits, false)) != SPEC_OK) {
         return rc;
     }
-    {
-    ProfScope psv(*c, 6, (double)B * (K + 1) * c->cfg.vocab * 4.0 +
-                             (draft_logits && sampling->temperature > 0 ? (double)B * K * c->cfg.vocab * 4.0 : 0.0));
-    rc = verify_into(B, K, c->cfg.vocab, logits, draft_logits, draft_tokens, draft_len, uniforms, sampling,
-                     accepted_len, next_token, out_ids, out_probs, seq_status, c->vws, c->vws_bytes, c->stream);
+    if (!amax) {
+        ProfScope psv(*c, 6, (double)B * (K + 1) * c->cfg.vocab * 4.0 +
+                                 (draft_logits && sampling->temperature > 0 ? (double)B * K * c->cfg.vocab * 4.0 : 0.0));
+        rc = verify_into(B, K, c->cfg.vocab, logits, draft_logits, draft_tokens, draft_len, uniforms, sampling,
+                         accepted_len, next_token, out_ids, out_probs, seq_status, c->vws, c->vws_bytes, c->stream);
     }
     if (rc != SPEC_OK) return rc;
     c->launches += 1;

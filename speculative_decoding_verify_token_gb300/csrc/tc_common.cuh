@@ -300,6 +300,41 @@ __device__ __forceinline__ void epi_chunk(int gid, int M, const EpiArgs& e, cons
         return;
     }
     const bool scaled = e.ssq_in != nullptr;
+    if (e.kind == EPI_STORE && e.amax_out != nullptr) {
+        // the tile's largest logit per token (lowest id on ties) instead of the logits: this
+        // thread's two adjacent rows, its warp (butterfly over keys), then the two warps of
+        // the token's parity (rows 0-63, then 64-127)
+        float v[TC_CW / 2][2];
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const int cc = half + 2 * j;
+            const float sc = (scaled && c0 + cc < M) ? inv_s[c0 + cc] : 1.0f;
+            v[j][0] = xs[r0 * TC_XPITCH + cc] * sc;
+            v[j][1] = xs[r1 * TC_XPITCH + cc] * sc;
+        }
+        epi_bar();          // every thread has its values: xs can hold the warps' keys
+        unsigned long long* wk = reinterpret_cast<unsigned long long*>(const_cast<float*>(xs));   // [4][TC_CW]
+        const int wq = (etid >> 5) & 1;
+        const int id0 = tile * TC_BM + r0;
+#pragma unroll
+        for (int j = 0; j < TC_CW / 2; ++j) {
+            const unsigned long long k0 = amax_key(v[j][0], id0), k1 = amax_key(v[j][1], id0 + 1);
+            unsigned long long k = k0 > k1 ? k0 : k1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long x = __shfl_xor_sync(FULL_MASK, k, o);
+                k = x > k ? x : k;
+            }
+            if ((etid & 31) == 0) wk[(half * 2 + wq) * TC_CW + half + 2 * j] = k;
+        }
+        epi_bar();
+        if (etid < TC_CW && c0 + etid < M) {
+            const int h = etid & 1;
+            const unsigned long long a = wk[(2 * h) * TC_CW + etid], b2 = wk[(2 * h + 1) * TC_CW + etid];
+            e.amax_out[(size_t)(e.m0 + c0 + etid) * e.amax_ld + tile] = a > b2 ? a : b2;
+        }
+        return;
+    }
     if (e.kind == EPI_QKV) {
         // the chunk's per-token inputs (position, RoPE pair, KV page) loaded together first
         int hs, jq;

@@ -1004,6 +1004,67 @@ int verify_into(int B, int K, int V, const float* target_logits, const float* dr
 
 }  // namespace sv
 
+namespace sv {
+
+// Greedy verify from the lm_head epilogue's per-tile argmax keys (amax_key, [M][n_tiles]):
+// one CTA per sequence; its warps merge each needed row's keys (the row's largest logit,
+// lowest id on ties: the argmax the top-k pass takes from the full logits), then warp 0
+// applies the greedy rule (accept drafts while they equal the row's argmax).  Outputs as
+// verify_into's greedy mode: out_ids[b][0] = next token with probability 1, the rest -1 / 0.
+constexpr int GA_WARPS = 8;
+__global__ void __launch_bounds__(GA_WARPS * 32) greedy_amax_kernel(
+    const unsigned long long* __restrict__ keys, int n_tiles, int K, const int32_t* __restrict__ draft_tokens,
+    const int32_t* __restrict__ draft_len, int32_t* accepted_len, int32_t* next_token, int32_t* out_ids,
+    float* out_probs, int32_t* seq_status) {
+    __shared__ int amax[VT_MAX_K + 1];
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int kb = K;
+    if (draft_len != nullptr) kb = min(max(draft_len[b], 0), K);
+    for (int i = warp; i <= kb; i += GA_WARPS) {
+        const unsigned long long* row = keys + (size_t)(b * (K + 1) + i) * n_tiles;
+        unsigned long long best = 0;
+        for (int t = lane; t < n_tiles; t += 32) {
+            const unsigned long long k = __ldcg(row + t);
+            best = k > best ? k : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long x = __shfl_xor_sync(FULL, best, o);
+            best = x > best ? x : best;
+        }
+        if (lane == 0) amax[i] = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    int a = 0;
+    while (a < kb && draft_tokens[(size_t)b * K + a] == amax[a]) ++a;
+    const int next = amax[a];
+    if (out_ids != nullptr) {
+        out_ids[(size_t)b * SPEC_TOPK_MAX + lane] = lane == 0 ? next : -1;
+        out_probs[(size_t)b * SPEC_TOPK_MAX + lane] = lane == 0 ? 1.0f : 0.0f;
+    }
+    if (lane == 0) {
+        accepted_len[b] = a;
+        next_token[b] = next;
+        if (seq_status) seq_status[b] = SPEC_OK;
+    }
+}
+
+int launch_greedy_amax(const unsigned long long* keys, int n_tiles, int B, int K, const int32_t* draft_tokens,
+                       const int32_t* draft_len, int32_t* accepted_len, int32_t* next_token, int32_t* out_ids,
+                       float* out_probs, int32_t* seq_status, cudaStream_t st) {
+    if (K < 0 || K > VT_MAX_K) return set_error(SPEC_E_INVAL, "K=%d outside [0, %d]", K, VT_MAX_K);
+    if ((out_ids == nullptr) != (out_probs == nullptr))
+        return set_error(SPEC_E_INVAL, "out_ids and out_probs must both be given or both be NULL");
+    greedy_amax_kernel<<<B, GA_WARPS * 32, 0, st>>>(keys, n_tiles, K, draft_tokens, draft_len, accepted_len, next_token,
+                                                   out_ids, out_probs, seq_status);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : set_error(SPEC_E_CUDA, "greedy_amax_kernel launch: %s", cudaGetErrorString(e));
+}
+
+}  // namespace sv
+
 using namespace sv;
 
 extern "C" size_t spec_verify_logits_workspace_bytes(int B, int K, int V) {

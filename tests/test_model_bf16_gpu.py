@@ -212,3 +212,53 @@ def test_draft_loop_equals_per_token_decodes(lib, w, temperature, graphs):
     for (dl_, gl), (dc, gc) in zip(lo, co):
         assert torch.equal(dl_, dc)
         assert torch.equal(gl, gc)
+
+
+@pytest.mark.parametrize("B,K", [(1, 4), (3, 7), (8, 15)])
+def test_lm_head_fused_greedy_equals_logits_path(lib, w, B, K):
+    """Greedy verify without logits keeps only each 128-row lm_head tile's argmax per token
+    ([MTP-fixes] "Truncation has to match on both sides": greedy needs the argmax alone)
+    and merges them; its decisions, tokens, output distributions and statuses equal the
+    full-logits path exactly: drafts that copy 0..K tokens of the greedy continuation, an
+    illegal id, ragged draft lengths; and single-token decode."""
+    V = synth.SMALL_BF16.vocab
+    prompts = [synth.prompt_tokens(70 + b, 23 + 11 * b, V) for b in range(B)]
+    seq = list(range(B))
+    # the greedy continuation of every prompt (fused decode on a helper context)
+    helper = make(lib, w, max_batch=B, max_ctx=256, max_k=K)
+    for b, p in enumerate(prompts):
+        helper.prefill(b, torch.from_numpy(p[:-1]).cuda())
+    tok = torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32, device="cuda")
+    cont = []
+    for _ in range(K):
+        tok = helper.decode(seq, tok)
+        cont.append(tok.clone())
+    helper.close()
+    cont = torch.stack(cont, dim=1)                                  # [B, K]
+    rng = np.random.default_rng(B * 100 + K)
+    drafts = cont.clone()
+    for b in range(B):
+        j = K if b == 0 else int(rng.integers(0, K + 1))             # first j drafts are the argmax
+        if j < K:
+            drafts[b, j] = int((int(cont[b, j]) + 1 + rng.integers(0, V - 1)) % V)
+    if B > 1:
+        drafts[1, 0] = V + 5                                         # an illegal id: rejected at once
+    dl = torch.tensor([K - (b % 3) for b in range(B)], dtype=torch.int32, device="cuda")
+    last = torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32, device="cuda")
+    u = torch.zeros(B, K + 1, dtype=torch.float32, device="cuda")
+    outs = []
+    for want in (False, True):
+        m = make(lib, w, max_batch=B, max_ctx=256, max_k=K)
+        for b, p in enumerate(prompts):
+            m.prefill(b, torch.from_numpy(p[:-1]).cuda())
+        r = m.verify(seq, last, drafts, u, 0.0, draft_len=dl, want_logits=want)
+        d = m.decode(seq, r["next_token"].clone(), want_logits=want)
+        d_tok = d[0] if want else d
+        outs.append(({k: v.cpu() for k, v in r.items() if k != "logits"}, d_tok.cpu(), [m.seq_len(b) for b in seq]))
+        m.close()
+    (fa, fd, fl), (ra, rd, rl) = outs
+    for k in ("accepted_len", "next_token", "out_ids", "out_probs", "status"):
+        assert torch.equal(fa[k], ra[k]), (k, fa[k], ra[k])
+    assert torch.equal(fd, rd)
+    assert fl == rl
+    assert int(fa["accepted_len"].sum()) > 0                         # some drafts were accepted
