@@ -291,8 +291,28 @@ int spec_draft(spec_ctx* ctx, int B, const int32_t* seq_ids, int K, const int32_
  * spec_verify (last_tokens = pending, draft_tokens = drafts with K = n_draft, draft_len)
  * without a host round trip.  Enqueued on the context's stream. */
 int spec_ngram_draft_device(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* pending, int n_draft,
-                            int min_match, int max_match, const int32_t* cap, int32_t* drafts,
+                            int min_match, int max_match, const int32_t* cap, int gated, int32_t* drafts,
                             int32_t* draft_len);
+
+/* The draft-length gate on the device ([OptiQ] "N-gram lookup: any model": the length of a
+ * step's draft follows how often recent drafts were accepted, against the timed cost of a
+ * verify pass), per sequence slot, with the rule and arithmetic of spec_ngram_gate_* (host,
+ * below): alpha = (S + 1) / (S + F + 2), S accepted draft tokens and F first rejections,
+ * both multiplied by decay every round; n = the n <= min(n_max, available) with the largest
+ * (1 + alpha + ... + alpha^n) / cost[n], the smaller n on ties.
+ * config: n_max in [0, 64], cost [n_max + 1] (HOST doubles, > 0), decay in [0, 1]; resets
+ * every slot's (S, F) to 0 (spec_seq_reset resets one slot).  Synchronous.
+ * update: one round per sequence: drafted[b], accepted[b] (device int32 [B], e.g. the
+ * draft_len given to spec_verify and its accepted_len).
+ * choose: n_out[b] (device int32 [B]) for available[b] (device int32 [B]) tokens.
+ * With gated != 0, spec_ngram_draft_device applies the gate to each sequence's available
+ * continuation (the tokens its lookup found, at most n_draft) before cap.  SPEC_E_STATE
+ * when the gate is used before config; enqueued on the context's stream. */
+int spec_ngram_gate_device_config(spec_ctx* ctx, int n_max, const double* cost, double decay);
+int spec_ngram_gate_device_update(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* drafted,
+                                  const int32_t* accepted);
+int spec_ngram_gate_device_choose(spec_ctx* ctx, int B, const int32_t* seq_ids, const int32_t* available,
+                                  int32_t* n_out);
 
 /* Trim after a verify pass run with auto_trim == 0: keep accepted_len[b] + 1 of the
  * K + 1 entries it appended (device O(1) length update).  accepted_len (device int32 [B])

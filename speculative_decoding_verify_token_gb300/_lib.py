@@ -87,7 +87,10 @@ SIGNATURES = {
                             c_vp, c_vp]),
     "spec_kv_trim": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp]),
     "spec_ngram_draft_device": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_vp, c_int, c_int, c_int, c_vp,
-                                        c_vp, c_vp]),
+                                        c_int, c_vp, c_vp]),
+    "spec_ngram_gate_device_config": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_double), ctypes.c_double]),
+    "spec_ngram_gate_device_update": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_vp, c_vp]),
+    "spec_ngram_gate_device_choose": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_vp, c_vp]),
     "spec_draft": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_vp, ctypes.POINTER(SpecSampling), c_vp,
                            c_vp, c_vp]),
     "spec_seq_len": (c_int, [c_vp, c_int, ctypes.POINTER(ctypes.c_int32)]),

@@ -97,6 +97,11 @@ struct Ctx {
     int* d_tok_pos = nullptr;
     int* d_tok_log = nullptr;       // [slots][max_ctx] token id at each position (n-gram context)
     unsigned long long* d_lm_amax = nullptr;   // [Mmax][vocab / 128] per-tile argmax keys (greedy, bf16)
+    // draft-length gate on the device: per slot (S, F); cost[0..gate_nmax]; -1 = not configured
+    double* d_gate_sf = nullptr;
+    double* d_gate_cost = nullptr;
+    double gate_decay = 0.9;
+    int gate_nmax = -1;
     int* d_seq_ids = nullptr;       // [max_batch]
     int* h_seq_ids = nullptr;       // pinned staging ring [SLOT_RING][max_batch]
     cudaEvent_t ring_ev[SLOT_RING] = {};
@@ -152,7 +157,9 @@ int launch_greedy_amax(const unsigned long long* keys, int n_tiles, int B, int K
                        const int32_t* draft_len, int32_t* accepted_len, int32_t* next_token, int32_t* out_ids,
                        float* out_probs, int32_t* seq_status, cudaStream_t st);
 void launch_ngram_draft(const Ctx& c, int B, const int* pending, int n_draft, int min_match, int max_match,
-                        const int* cap, int* drafts, int* draft_len, cudaStream_t st);
+                        const int* cap, int* drafts, int* draft_len, bool gated, cudaStream_t st);
+void launch_gate_update(const Ctx& c, int B, const int* drafted, const int* accepted, cudaStream_t st);
+void launch_gate_choose(const Ctx& c, int B, const int* available, int* n_out, cudaStream_t st);
 // dst[c * ldd + r] = src[r * lds + c] for r < R, c < C (int32 / float32)
 void launch_transpose_i32(const int* src, int lds, int* dst, int ldd, int R, int C, cudaStream_t st);
 void launch_transpose_f32(const float* src, int lds, float* dst, int ldd, int R, int C, cudaStream_t st);

@@ -222,6 +222,63 @@ void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens
     verify_tokens_kernel<<<(n + 255) / 256, 256, 0, st>>>(last, drafts, K, tokens, B);
 }
 
+// Draft-length gate ("Speculative decoding on Apple Silicon" (mlx-optiq docs), section
+// "N-gram lookup: any model"): a drafted token is accepted with probability alpha =
+// (S + 1) / (S + F + 2), S the accepted draft tokens and F the first rejections of the
+// slot's recent rounds, both decayed every round; a round of n drafts is expected to emit
+// E(n) = 1 + alpha + ... + alpha^n tokens at the timed cost cost[n], and the gate drafts the
+// n <= min(n_max, available) with the largest E(n) / cost[n], the smaller n on ties.  The
+// same double-precision arithmetic as the host gate (spec_ngram_gate_*).
+__device__ int gate_choose(double S, double F, const double* cost, int n_max, int available) {
+    const int lim = max(0, min(n_max, available));
+    const double a = (S + 1.0) / (S + F + 2.0);
+    double e = 1.0, pw = 1.0, best_v = 1.0 / cost[0];
+    int best = 0;
+    for (int n = 1; n <= lim; ++n) {
+        pw *= a;
+        e += pw;
+        const double v = e / cost[n];
+        if (v > best_v) {
+            best_v = v;
+            best = n;
+        }
+    }
+    return best;
+}
+
+__global__ void gate_update_kernel(const int* __restrict__ seq_ids, int B, double* __restrict__ sf, double decay,
+                                   const int* __restrict__ drafted, const int* __restrict__ accepted) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int slot = seq_ids[b];
+    double S = sf[2 * slot] * decay, F = sf[2 * slot + 1] * decay;
+    const int d = drafted[b], acc = accepted[b];
+    if (d > 0) {
+        S += acc;
+        if (acc < d) F += 1.0;
+    }
+    sf[2 * slot] = S;
+    sf[2 * slot + 1] = F;
+}
+
+__global__ void gate_choose_kernel(const int* __restrict__ seq_ids, int B, const double* __restrict__ sf,
+                                   const double* __restrict__ cost, int n_max, const int* __restrict__ available,
+                                   int* __restrict__ n_out) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int slot = seq_ids[b];
+    n_out[b] = gate_choose(sf[2 * slot], sf[2 * slot + 1], cost, n_max, available[b]);
+}
+
+void launch_gate_update(const Ctx& c, int B, const int* drafted, const int* accepted, cudaStream_t st) {
+    gate_update_kernel<<<(B + 127) / 128, 128, 0, st>>>(c.d_seq_ids, B, c.d_gate_sf, c.gate_decay, drafted, accepted);
+}
+
+void launch_gate_choose(const Ctx& c, int B, const int* available, int* n_out, cudaStream_t st) {
+    gate_choose_kernel<<<(B + 127) / 128, 128, 0, st>>>(c.d_seq_ids, B, c.d_gate_sf, c.d_gate_cost, c.gate_nmax,
+                                                       available, n_out);
+}
+
 // N-gram drafts of one sequence per CTA ("Speculative decoding on Apple Silicon"
 // (mlx-optiq docs), section "N-gram lookup: any model").  The context is the slot's
 // committed tokens tok_log[slot][0, L) (L = its length) followed by the pending token: n =
@@ -230,7 +287,8 @@ void launch_verify_tokens(const int* last, const int* drafts, int K, int* tokens
 // occurrence of the context's last m tokens ends at e exactly when l(e) >= m.  The longest
 // suffix with an earlier occurrence is m* = max l(e) (drafting needs m* >= min_match), and
 // its most recent occurrence is the largest e with l(e) = m*: one max-reduction of
-// (l(e), e).  The draft is ctx[e + 1, e + 1 + k), k = min(n_draft, cap, n - 1 - e); rows past
+// (l(e), e).  The draft is ctx[e + 1, e + 1 + k), k = min(n_draft, n - 1 - e), then the
+// gate's choice for those k available tokens when gate_sf is set, then cap; rows past
 // draft_len[b] = k hold the pending token.  The rule of spec_ngram_draft (host) and of the
 // oracle's lookup, as one scan.
 constexpr int NG_THREADS = 256;
@@ -240,7 +298,9 @@ __global__ void __launch_bounds__(NG_THREADS) ngram_draft_kernel(const int* __re
                                                                const int* __restrict__ pending, int n_draft,
                                                                int min_match, int max_match,
                                                                const int* __restrict__ cap, int* __restrict__ drafts,
-                                                               int* __restrict__ draft_len) {
+                                                               int* __restrict__ draft_len,
+                                                               const double* __restrict__ gate_sf,
+                                                               const double* __restrict__ gate_cost, int gate_nmax) {
     __shared__ int tail[SPEC_NGRAM_MAX_MATCH];
     __shared__ unsigned long long red[NG_THREADS / 32];
     const int b = blockIdx.x;
@@ -283,8 +343,9 @@ __global__ void __launch_bounds__(NG_THREADS) ngram_draft_kernel(const int* __re
     if (key != 0) {
         e = (int)(key & 0xffffffffu);
         k = min(n_draft, n - 1 - e);
-        if (cap) k = max(0, min(k, cap[b]));
     }
+    if (gate_sf != nullptr) k = gate_choose(gate_sf[2 * slot], gate_sf[2 * slot + 1], gate_cost, gate_nmax, k);
+    if (cap) k = max(0, min(k, cap[b]));
     for (int i = threadIdx.x; i < n_draft; i += NG_THREADS) {
         const int p = e + 1 + i;
         drafts[(size_t)b * n_draft + i] = i < k ? (p == n - 1 ? last : ctx[p]) : last;
@@ -293,9 +354,10 @@ __global__ void __launch_bounds__(NG_THREADS) ngram_draft_kernel(const int* __re
 }
 
 void launch_ngram_draft(const Ctx& c, int B, const int* pending, int n_draft, int min_match, int max_match,
-                        const int* cap, int* drafts, int* draft_len, cudaStream_t st) {
+                        const int* cap, int* drafts, int* draft_len, bool gated, cudaStream_t st) {
     ngram_draft_kernel<<<B, NG_THREADS, 0, st>>>(c.d_seq_ids, c.d_seq_len, c.d_tok_log, c.lim.max_ctx, pending, n_draft,
-                                                min_match, max_match, cap, drafts, draft_len);
+                                                min_match, max_match, cap, drafts, draft_len,
+                                                gated ? c.d_gate_sf : nullptr, c.d_gate_cost, c.gate_nmax);
 }
 
 void launch_advance_len(const int* seq_ids, int* seq_len, int B, int mode, int add, const int* accepted, int K,

@@ -10,6 +10,7 @@
 // decoding works"); the trim is the slice of a plain KV cache ("Why this needed a patch
 // to mlx_lm at all"), here an O(1) device-side length update.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <string>
 
@@ -764,7 +765,7 @@ extern "C" int spec_draft(spec_ctx* c, int B, const int32_t* seq_ids, int K, con
 }
 
 extern "C" int spec_ngram_draft_device(spec_ctx* c, int B, const int32_t* seq_ids, const int32_t* pending,
-                                       int n_draft, int min_match, int max_match, const int32_t* cap,
+                                       int n_draft, int min_match, int max_match, const int32_t* cap, int gated,
                                        int32_t* drafts, int32_t* draft_len) {
     clear_error();
     if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
@@ -774,11 +775,65 @@ extern "C" int spec_ngram_draft_device(spec_ctx* c, int B, const int32_t* seq_id
     if (n_draft < 1 || n_draft > 64 || min_match < 1 || max_match < min_match || max_match > SPEC_NGRAM_MAX_MATCH)
         return set_error(SPEC_E_INVAL, "need 1 <= n_draft <= 64 and 1 <= min_match <= max_match <= %d",
                          SPEC_NGRAM_MAX_MATCH);
+    if (gated && c->gate_nmax < 0) return set_error(SPEC_E_STATE, "the device gate is not configured");
     if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
-    launch_ngram_draft(*c, B, pending, n_draft, min_match, max_match, cap, drafts, draft_len, c->stream);
+    launch_ngram_draft(*c, B, pending, n_draft, min_match, max_match, cap, drafts, draft_len, gated != 0, c->stream);
     c->launches += 1;
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_ngram_draft_device", e);
+}
+
+extern "C" int spec_ngram_gate_device_config(spec_ctx* c, int n_max, const double* cost, double decay) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    if (n_max < 0 || n_max > 64) return set_error(SPEC_E_INVAL, "n_max=%d outside [0, 64]", n_max);
+    if (!cost) return set_error(SPEC_E_INVAL, "cost is NULL");
+    if (!(decay >= 0.0 && decay <= 1.0)) return set_error(SPEC_E_INVAL, "decay outside [0, 1]");
+    for (int n = 0; n <= n_max; ++n)
+        if (!(cost[n] > 0.0) || !std::isfinite(cost[n])) return set_error(SPEC_E_INVAL, "cost[%d] must be > 0", n);
+    if (!c->d_gate_sf) {
+        int rc = dalloc(*c, &c->d_gate_sf, sizeof(double) * 2 * (size_t)c->lim.max_batch, true);
+        if (rc == SPEC_OK) rc = dalloc(*c, &c->d_gate_cost, sizeof(double) * 65, true);
+        if (rc != SPEC_OK) return rc;
+    }
+    cudaError_t e = cudaMemcpyAsync(c->d_gate_cost, cost, sizeof(double) * (n_max + 1), cudaMemcpyHostToDevice,
+                                    c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_gate_sf, 0, sizeof(double) * 2 * (size_t)c->lim.max_batch, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail("spec_ngram_gate_device_config", e);
+    c->gate_nmax = n_max;
+    c->gate_decay = decay;
+    return SPEC_OK;
+}
+
+extern "C" int spec_ngram_gate_device_update(spec_ctx* c, int B, const int32_t* seq_ids, const int32_t* drafted,
+                                             const int32_t* accepted) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    int rc = check_slots(*c, seq_ids, B);
+    if (rc != SPEC_OK) return rc;
+    if (!drafted || !accepted) return set_error(SPEC_E_INVAL, "NULL required pointer");
+    if (c->gate_nmax < 0) return set_error(SPEC_E_STATE, "the device gate is not configured");
+    if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    launch_gate_update(*c, B, drafted, accepted, c->stream);
+    c->launches += 1;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_ngram_gate_device_update", e);
+}
+
+extern "C" int spec_ngram_gate_device_choose(spec_ctx* c, int B, const int32_t* seq_ids, const int32_t* available,
+                                             int32_t* n_out) {
+    clear_error();
+    if (!c) return set_error(SPEC_E_INVAL, "ctx is NULL");
+    int rc = check_slots(*c, seq_ids, B);
+    if (rc != SPEC_OK) return rc;
+    if (!available || !n_out) return set_error(SPEC_E_INVAL, "NULL required pointer");
+    if (c->gate_nmax < 0) return set_error(SPEC_E_STATE, "the device gate is not configured");
+    if ((rc = upload_slots(*c, seq_ids, B)) != SPEC_OK) return rc;
+    launch_gate_choose(*c, B, available, n_out, c->stream);
+    c->launches += 1;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : cuda_fail("spec_ngram_gate_device_choose", e);
 }
 
 extern "C" int spec_kv_trim(spec_ctx* c, int B, const int32_t* seq_ids, int K, const int32_t* accepted_len) {
@@ -839,6 +894,7 @@ extern "C" int spec_seq_reset(spec_ctx* c, int seq_id) {
     cudaError_t e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
     e = cudaMemset(c->d_seq_len + seq_id, 0, sizeof(int));
+    if (e == cudaSuccess && c->d_gate_sf) e = cudaMemset(c->d_gate_sf + 2 * (size_t)seq_id, 0, 2 * sizeof(double));
     if (e != cudaSuccess) return cuda_fail("cudaMemset", e);
     while (c->n_pages[seq_id] > 0) {
         --c->n_pages[seq_id];

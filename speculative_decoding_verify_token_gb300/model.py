@@ -5,6 +5,8 @@ tensors alive.  All tensors are CUDA tensors; seq_ids are host ints.
 """
 import ctypes
 
+import numpy as np
+
 import torch
 
 from . import _lib
@@ -125,9 +127,31 @@ class SpecModel:
                                        _ptr(out), _ptr(logits)))
         return out, logits
 
-    def ngram_draft(self, seq_ids, pending, n_draft=8, min_match=3, max_match=8, cap=None, out=None):
+    def gate_config(self, cost, decay=0.9):
+        """Configure the device draft-length gate: cost[n] = timed cost of a verify pass with n
+        drafts (n = 0 .. len(cost) - 1); resets every slot's acceptance record."""
+        c = np.ascontiguousarray(np.asarray(cost, dtype=np.float64))
+        _lib.check(self.lib.spec_ngram_gate_device_config(self.h, int(c.size - 1),
+                                                          c.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                                          float(decay)))
+
+    def gate_update(self, seq_ids, drafted, accepted):
+        B = len(seq_ids)
+        _need(drafted, torch.int32, (B,), "drafted")
+        _need(accepted, torch.int32, (B,), "accepted")
+        _lib.check(self.lib.spec_ngram_gate_device_update(self.h, B, _ids(seq_ids), _ptr(drafted), _ptr(accepted)))
+
+    def gate_choose(self, seq_ids, available, out=None):
+        B = len(seq_ids)
+        _need(available, torch.int32, (B,), "available")
+        out = out if out is not None else torch.empty(B, dtype=torch.int32, device=self.device)
+        _lib.check(self.lib.spec_ngram_gate_device_choose(self.h, B, _ids(seq_ids), _ptr(available), _ptr(out)))
+        return out
+
+    def ngram_draft(self, seq_ids, pending, n_draft=8, min_match=3, max_match=8, cap=None, out=None, gated=False):
         """N-gram drafts on the device from each slot's committed tokens + pending [B]; returns
-        (drafts [B, n_draft] int32, draft_len [B] int32), both on the device."""
+        (drafts [B, n_draft] int32, draft_len [B] int32), both on the device; gated: the
+        device gate picks each draft's length from the available continuation."""
         B = len(seq_ids)
         _need(pending, torch.int32, (B,), "pending")
         if cap is not None:
@@ -136,8 +160,8 @@ class SpecModel:
             out = (torch.empty(B, n_draft, dtype=torch.int32, device=self.device),
                    torch.empty(B, dtype=torch.int32, device=self.device))
         _lib.check(self.lib.spec_ngram_draft_device(self.h, B, _ids(seq_ids), _ptr(pending), int(n_draft),
-                                                    int(min_match), int(max_match), _ptr(cap), _ptr(out[0]),
-                                                    _ptr(out[1])))
+                                                    int(min_match), int(max_match), _ptr(cap), 1 if gated else 0,
+                                                    _ptr(out[0]), _ptr(out[1])))
         return out
 
     def kv_trim(self, seq_ids, K, accepted_len):

@@ -11,7 +11,11 @@ token.  Checked:
   * a per-sequence cap shortens the draft to min(cap, oracle length);
   * across greedy verify rounds fed by the device drafts (the cache trimmed to the accepted
     prefix each round), the drafts still equal the oracle's lookup on the committed tokens;
-  * the float32 path (its own embedding kernel instance) records the same context.
+  * the float32 path (its own embedding kernel instance) records the same context;
+  * the draft-length gate on the device (section "N-gram lookup: any model": the draft
+    length follows recent acceptance against the timed cost of a verify pass) chooses what
+    the oracle's DraftGate chooses over random rounds, and the gated drafter drafts that
+    many tokens of each sequence's available continuation.
 """
 import numpy as np
 import pytest
@@ -108,4 +112,50 @@ def test_device_ngram_across_verify_rounds(M):
             assert m.seq_len(b) == len(ctxs[b]) - 1
         pending = out["next_token"].clone()
     assert drafted > 0
+    m.close()
+
+
+@pytest.mark.parametrize("decay", [0.9, 0.5, 1.0])
+def test_device_gate_matches_oracle(M, decay):
+    """The draft-length gate on the device against the oracle's DraftGate, per slot, over
+    random rounds (same choice, or where the oracle's two best scores are within rounding,
+    either), then applied by the drafter to each sequence's available continuation."""
+    shape = synth.TINY_TARGET
+    B, n_max = 4, 8
+    rng = np.random.default_rng(int(decay * 10))
+    cost = np.cumsum(np.concatenate([[1.0], rng.uniform(0.02, 0.4, n_max)]))
+    w = synth.model_weights(shape, seed=0, device="cuda")
+    ctxs = [np.tile(np.array([11, 12, 13], dtype=np.int32), 12)[:34], synth.ngram_prompt(9, 200, shape.vocab),
+            synth.prompt_tokens(5, 60, shape.vocab), np.tile(np.array([40, 41, 42, 43, 44], dtype=np.int32), 9)]
+    m = M.SpecModel(shape, w, max_batch=B, max_ctx=256, max_k=8, prefill_chunk=256)
+    for b, c in enumerate(ctxs):
+        m.prefill(b, torch.from_numpy(c[:-1]).cuda())
+    m.gate_config(cost, decay)
+    refs = [og.DraftGate(cost, decay=decay) for _ in range(B)]
+    seq = list(range(B))
+
+    def same_choice(ref, avail, got):
+        e = ref.choose(avail)
+        if got != e:
+            sc = ref.scores(avail)
+            assert abs(sc[got] - sc[e]) <= 1e-12 * sc[e], (avail, got, e)
+
+    for r in range(60):
+        avail = rng.integers(0, n_max + 3, size=B).astype(np.int32)
+        n = m.gate_choose(seq, torch.from_numpy(avail).cuda()).cpu().numpy()
+        for b in range(B):
+            same_choice(refs[b], int(avail[b]), int(n[b]))
+        acc = np.array([n[b] if rng.random() < 0.5 else rng.integers(0, n[b] + 1) for b in range(B)], dtype=np.int32)
+        m.gate_update(seq, torch.from_numpy(n.astype(np.int32)).cuda(), torch.from_numpy(acc).cuda())
+        for b in range(B):
+            refs[b].update(int(n[b]), int(acc[b]))
+    # the drafter with the gate: each sequence's draft length is the gate's choice for the
+    # continuation its lookup finds, and the drafted tokens are that continuation's first ones
+    pending = torch.tensor([int(c[-1]) for c in ctxs], dtype=torch.int32, device="cuda")
+    drafts, dl = m.ngram_draft(seq, pending, 8, 3, 8, gated=True)
+    drafts, dl = drafts.cpu().numpy(), dl.cpu().numpy()
+    for b in range(B):
+        full = og.ngram_draft(ctxs[b], n_draft=8)
+        same_choice(refs[b], len(full), int(dl[b]))
+        assert [int(t) for t in drafts[b, :dl[b]]] == full[:dl[b]]
     m.close()
