@@ -199,7 +199,13 @@ typedef struct spec_ctx spec_ctx;
 /* Create a context bound to `stream` (cudaStream_t as void*): allocates the KV pool,
  * activations and workspaces on the current device.  SPEC_E_INVAL on a bad shape
  * (head_dim a multiple of 32 and <= 256, d_model <= 8192, d_model / ffn_dim / heads*head_dim multiples of 8,
- * n_q_heads a multiple of n_kv_heads), SPEC_E_NOMEM when an allocation fails. */
+ * n_q_heads a multiple of n_kv_heads), SPEC_E_NOMEM when an allocation fails.
+ * Concurrency: a tensor-core GEMM of more than 16 tokens whose tiles are shared by several
+ * CTAs has those CTAs wait for one another's partial sums (bounded: SPEC_E_TIMEOUT after
+ * 2 s), which needs all of its CTAs resident together.  The library's own launches are
+ * serialised on the context's stream, so that always holds; passes of two contexts must
+ * not run concurrently on different streams (their CTAs could hold the SMs the other's
+ * waiting CTAs need until the bound runs out). */
 int spec_create(const spec_model_cfg* cfg, const spec_ctx_limits* limits, void* stream, spec_ctx** out);
 
 /* Load the weights.  names[i] is one of "embed" [V][d], "final_norm" [d], "lm_head" [V][d],
@@ -364,6 +370,11 @@ int spec_seq_reset(spec_ctx* ctx, int seq_id);
  * always the latter).  The split sets the order of the K sums, so it changes result bits
  * (within the rounding of fp32 accumulation), the same way for every token count. */
 #define SPEC_OPT_GEMM_MIN_FILL 8
+/* SPEC_OPT_GEMM_MAX_SPLIT (0..64, default 0 = no cap): the most CTAs that share one output
+ * tile of a tensor-core GEMM with fewer tiles than SMs; with a cap the GEMM runs as that
+ * whole number of CTAs per tile (1: one CTA per tile, no fix-up), whatever share of the
+ * SMs stays busy.  Like SPEC_OPT_GEMM_MIN_FILL it sets the order of the K sums. */
+#define SPEC_OPT_GEMM_MAX_SPLIT 9
 int spec_set_option(spec_ctx* ctx, int option, int value);
 
 /* Per-kernel-class timing of the context's passes with CUDA events recorded on its

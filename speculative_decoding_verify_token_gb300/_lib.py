@@ -56,6 +56,7 @@ SPEC_OPT_GRAPHS = 1
 SPEC_OPT_PDL = 2
 SPEC_OPT_L2_PREFETCH = 3
 SPEC_OPT_GEMM_MIN_FILL = 8
+SPEC_OPT_GEMM_MAX_SPLIT = 9
 SPEC_PROF_CLASSES = 8
 PROF_CLASS_NAMES = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head", "attention",
                     "verify", "other"]

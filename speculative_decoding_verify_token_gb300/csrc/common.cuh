@@ -82,6 +82,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// Bounded wait until *cnt (written by other CTAs with release or fence + atomic) reaches
+// target, read with acquire semantics at GPU scope.  Returns false when the budget ran out.
+__device__ __forceinline__ bool wait_count_at_least(const int* cnt, int target,
+                                                    unsigned long long budget_ns = WAIT_BUDGET_NS) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= target) return true;
+        if (globaltimer_ns() - t0 > budget_ns) return false;
+        __nanosleep(32);
+    }
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

@@ -6,7 +6,7 @@
 // "How speculative decoding works").  Design:
 //  * swap-AB: a 128-row weight tile is the A operand, the tokens' hi and lo rows are the N
 //    dimension (16..512, two MMAs above 256); the fp32 accumulator [128 x N] lives in
-//    tensor memory;
+//    tensor memory, two of them while they fit its 512 columns (up to 128 tokens);
 //  * the weights are re-laid out once, when they are loaded, tile-major: every (tile, K
 //    atom) is the 16 KB A operand of one MMA atom, already in the 128-byte-swizzled order
 //    the tensor cores read, so a ring stage of n consecutive atoms of a tile is ONE
@@ -25,9 +25,12 @@
 //    owner, warps 2-5 = epilogue (tcgen05.ld of the 4 lane quarters);
 //  * persistent stream-K: the (tile, k-block) space is cut into one contiguous range per
 //    CTA; a tile shared by several CTAs is finished by the last one to arrive (atomic
-//    ticket, no spin-wait), which adds the partial sums in CTA order.  The split depends
-//    only on the weight shape and the SM count, so a token's outputs are bit-identical for
-//    every M (a decode step and a verify pass agree exactly);
+//    ticket, no spin-wait), which adds the partial sums in CTA order.  With a whole number
+//    s of CTAs per tile and more than 16 tokens, the s CTAs instead share the finishing
+//    (each takes every s-th 16-token chunk, after a bounded wait for the others' partial
+//    sums, adding them in the same order).  The split depends only on the weight shape and
+//    the SM count, so a token's outputs are bit-identical for every M (a decode step and a
+//    verify pass agree exactly);
 //  * fused epilogues (RoPE + paged KV append, SwiGLU, residual add, fp32 logits) shared
 //    with the CUDA-core GEMM, and a fused RMSNorm: the residual GEMMs also write
 //    bf16(x * g) of the next norm and per-tile sums of squares, and the GEMM reading that
@@ -72,6 +75,7 @@ struct TcParams {
     int n_ntiles, n_KB, n_atoms;       // n_atoms = 0: no prefetch
     float* partial;          // [grid][2] x ntok/16 chunks of [4][128] float4 (partial_f4)
     int* tile_cnt;           // [n_tiles], zero between launches
+    int split_s;             // CTAs per tile of a whole-tile split (grid = n_tiles x split_s), else 0
     int* err;
     EpiArgs e;
 };
@@ -79,8 +83,10 @@ struct TcParams {
 #ifdef TC_TRACE
 // Per-CTA timeline of the last launch of each GEMM kind (profiling builds only):
 // [gid][cta][0 entry, 1 set-up done, 2 first stage ready, 3 last MMA issued,
-//            4 last accumulator ready, 5 exit]
-__device__ unsigned long long g_tc_trace[5][1024][6];
+//            4 last accumulator ready, 5 exit; split fix-up: 6 partials published,
+//            7 all contributors published, 8 first own chunk done, 9 all own chunks done,
+//            10 first own chunk's sums staged]
+__device__ unsigned long long g_tc_trace[5][1024][12];
 #define TC_STAMP(i) do { if (blockIdx.x < 1024) g_tc_trace[p.gid][blockIdx.x][i] = globaltimer_ns(); } while (0)
 #else
 #define TC_STAMP(i) ((void)0)
@@ -341,6 +347,67 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM) tc_gemm_kernel(con
                     epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid, c0 == 0 ? &pre : nullptr);
                     epi_bar();
                 }
+            } else if (p.split_s > 1 && p.ntok > TC_CW) {
+                // Whole-tile split of several 16-token chunks: each of the s contributors
+                // finalizes the chunks ch with ch % s == its index.  It publishes its sums of
+                // the other chunks, waits (bounded) until all s have published, then adds the
+                // tile's sums of its own chunks in contributor order (its own from tensor
+                // memory): the additions a single finalizer makes, spread over s CTAs.
+                const int s = p.split_s, me = cta - c_lo;
+                for (int c0 = 0, ch = 0; c0 < p.ntok; c0 += TC_CW, ++ch) {
+                    if (ch % s == me) continue;
+                    float v[16];
+                    acc_ld16(taddr, c0, p.br.lo_col, v);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *partial_f4(p.partial, cta, 0, p.ntok, c0, j, row) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+                __threadfence();
+                epi_bar();
+                if (etid == 0) {
+                    atomicAdd(p.tile_cnt + tile, 1);
+                    TC_STAMP(6);
+                    last_flag = wait_count_at_least(p.tile_cnt + tile, s) ? 1 : 0;
+                    TC_STAMP(7);
+                }
+                epi_bar();
+                if (!last_flag) {
+                    if (etid == 0) atomicExch(p.err, SPEC_E_TIMEOUT);
+                } else {
+                    __threadfence();
+                    for (int c0 = me * TC_CW; c0 < p.ntok; c0 += s * TC_CW) {
+                        float acc[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
+                            float v[16];
+                            if (cc == cta) {
+                                acc_ld16(taddr, c0, p.br.lo_col, v);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float4 t4 = __ldcg(partial_f4(p.partial, cc, 0, p.ntok, c0, j, row));
+                                    v[4 * j] = t4.x; v[4 * j + 1] = t4.y; v[4 * j + 2] = t4.z; v[4 * j + 3] = t4.w;
+                                }
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] += v[j];
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) xs[row * TC_XPITCH + j] = acc[j];
+                        epi_bar();
+                        if (etid == 0 && c0 == me * TC_CW) TC_STAMP(10);
+                        epi_chunk(p.gid, p.M, p.e, xs, inv_s, red_s, tile, c0, etid, c0 == 0 ? &pre : nullptr);
+                        epi_bar();
+                        if (etid == 0 && c0 == me * TC_CW) TC_STAMP(8);
+                    }
+                }
+                if (etid == 0) TC_STAMP(9);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&acce[buf]));
+                // every contributor has passed its wait once all s have arrived a second time
+                if (etid == 0 && atomicAdd(p.tile_cnt + tile, 1) == 2 * s - 1) p.tile_cnt[tile] = 0;
             } else {
                 const int which = (s0 >= tile_k0) ? 0 : 1;
                 for (int c0 = 0; c0 < p.ntok; c0 += TC_CW) {
@@ -605,8 +672,9 @@ int tc_error_word(Ctx& c, int* out) {
 // per SM with the (tile, atom) space cut into equal ranges across tile boundaries.  The
 // choice depends only on the weight shape and the SM count, so a token's result bits do
 // not depend on how many tokens share the launch.
-static int gemm_grid(int n_tiles, int sms, int min_fill) {
+static int gemm_grid(int n_tiles, int sms, int min_fill, int max_split) {
     if (n_tiles >= sms) return sms;
+    if (max_split > 0) return n_tiles * std::min(max_split, sms / n_tiles);
     const int g = n_tiles * (sms / n_tiles);
     return 100 * g >= min_fill * sms ? g : sms;
 }
@@ -670,7 +738,9 @@ static int tc_gemm_launch(Ctx& c, int gid, int layer, int x_row0, int M, int pas
         p.n_atoms = c.l2_prefetch_atoms;
     }
     const long long T = (long long)p.n_tiles * p.KB;
-    const int grid = (int)std::min<long long>(gemm_grid(p.n_tiles, t->grid, c.gemm_min_fill), T);
+    const int grid = (int)std::min<long long>(gemm_grid(p.n_tiles, t->grid, c.gemm_min_fill, c.gemm_max_split), T);
+    // a whole number of CTAs per tile: CTA tile * s + i takes the i-th s-th of the tile's K
+    p.split_s = (p.n_tiles < grid && grid % p.n_tiles == 0) ? grid / p.n_tiles : 0;
     const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + TC_XBYTES;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -126,6 +126,7 @@ struct Ctx {
     bool use_pdl = true;
     int l2_prefetch_atoms = 0;             // next-GEMM weight atoms per CTA warmed into L2
     int gemm_min_fill = 80;                // percent of the SMs a whole-tile GEMM split must keep busy
+    int gemm_max_split = 0;                // most CTAs per output tile (0: no cap)
     cudaStream_t cap_stream = nullptr;     // private stream the graphs are captured on
     struct GraphEntry { int B, T; bool amax; cudaGraphExec_t exec; long long kernels; };
     std::vector<GraphEntry> graphs;

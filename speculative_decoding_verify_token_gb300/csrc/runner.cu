@@ -922,6 +922,10 @@ extern "C" int spec_set_option(spec_ctx* c, int option, int value) {
         if (value < 0 || value > 101) return set_error(SPEC_E_INVAL, "GEMM fill must be in [0, 101] percent");
         c->gemm_min_fill = value;
         drop_graphs(*c);
+    } else if (option == SPEC_OPT_GEMM_MAX_SPLIT) {
+        if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "GEMM split cap must be in [0, 64]");
+        c->gemm_max_split = value;
+        drop_graphs(*c);
     } else if (option == SPEC_OPT_L2_PREFETCH) {
         if (value < 0 || value > 64) return set_error(SPEC_E_INVAL, "L2 prefetch atoms must be in [0, 64]");
         c->l2_prefetch_atoms = value;

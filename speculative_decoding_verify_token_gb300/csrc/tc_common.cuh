@@ -106,7 +106,10 @@ __device__ __forceinline__ void acc_ld16(uint32_t taddr, int c0, int lo_col, flo
 // Rows of the activation operand B of one launch over M tokens: its rows = act_rows(M) hi
 // rows, then its rows lo rows (every K atom of the operand layout holds them in that
 // order), so the MMA's N is 2 rows, a token's lo product sits `rows` columns after its hi
-// product, and one accumulator buffer spans 2 rows TMEM columns.
+// product, and one accumulator buffer spans 2 rows TMEM columns.  (One MMA per K-step
+// over both halves: accumulating the lo rows into the hi rows' columns instead takes two
+// MMAs per K-step, which at 8 rows, N = 16, doubled the tensor pipe's instruction count
+// and slowed the 8-token GEMMs by a quarter.)
 struct BRows {
     int rows;         // hi (and lo) rows of the launch
     int nb;           // rows of B (the MMA N)
