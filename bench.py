@@ -889,13 +889,14 @@ WORKLOADS = {DenseVerifyWorkload.name: DenseVerifyWorkload, VerifyLogitsWorkload
              ServingWorkload.name: ServingWorkload, SamplingWorkload.name: SamplingWorkload}
 DEFAULT_WORKLOAD = DenseVerifyWorkload.name
 # DRAM bytes (read + write) of one graphed 8B verify step (see DenseVerifyWorkload.roofline),
-# from an ncu capture of a 2-layer slice with --cache-control none: per layer (the four
-# GEMMs, attention and combine: 390.7 and 389.0 MB in the two layers) and the rest of the
-# step (embed, lm_head, verify kernels, length update); in that capture the small slice's KV
-# pages stay in L2, so the full model's attention reads (about 4.3 MB per layer at a
-# context of 1.1K) are not in it.  0 = not captured for the current kernels.
-STEP_TRAFFIC_PER_LAYER = 389.8e6
-STEP_TRAFFIC_FIXED = 1250.1e6
+# from an ncu capture of a 2-layer slice with --cache-control none over two steps: per layer
+# (the four GEMMs, attention and combine: 394.8, 391.6, 388.2 and 387.9 MB) and the rest of
+# the step (embed, lm_head with its per-tile argmax keys, the greedy merge, length update:
+# 1252.0 and 1248.6 MB); in that capture the small slice's KV pages stay in L2, so the full
+# model's attention reads (about 4.3 MB per layer at a context of 1.1K) are not in it.
+# 0 = not captured for the current kernels.
+STEP_TRAFFIC_PER_LAYER = 390.6e6
+STEP_TRAFFIC_FIXED = 1250.3e6
 
 
 def run_reference(args):
